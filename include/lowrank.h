@@ -1,0 +1,181 @@
+/*
+ * lowrank.h — C ABI of liblowrank.so, the GB300 (sm_103a) implementation of the
+ * low-rank bottleneck sublayer trained by BOOST.
+ *
+ * Source of the method: "BOOST: BOttleneck-Optimized Scalable Training Framework
+ * for Low-Rank Large Language Models" (arXiv 2512.12131; abstract, and the
+ * gist.science technical summary §1-§2).  Every dense linear map W.x of the model
+ * is replaced by a low-rank pair — an r x d_in layer A followed by a d_out x r
+ * layer B (technical summary §1, §2.1) — which this library evaluates as
+ *
+ *     y = B . SiLU(A . v)                                  (one "pair")
+ *
+ * and the three system optimisations of technical summary §2.2 are built in:
+ *   - Online-RMSNorm: the RMSNorm gain is folded into A, the sum of squares of
+ *     the input row is accumulated alongside the first GEMM and the 1/rms row
+ *     scale is applied in that GEMM's epilogue (exact rewrite of RMSNorm);
+ *   - linear-layer grouping: A's that read the same input (gate/up, q/k/v)
+ *     are concatenated into one GEMM; the B's with distinct inputs run as one
+ *     batched GEMM;
+ *   - low-rank activation checkpointing: in LR_SAVE_CKPT mode only the block
+ *     input, the [T, r] bottleneck pre-activations and 1/rms are kept; the
+ *     backward recomputes the rest inside the block.
+ *
+ * Conventions for every entry point
+ *   - Matrices are dense row-major; a token is one row.  x is [T, d].  A pair's
+ *     A is [r, d_in] and its B is [d_out, r].  No biases.
+ *   - lr_dtype selects the storage and arithmetic: LR_BF16 stores every tensor
+ *     in bf16 and runs tcgen05 tensor-core GEMMs with fp32 accumulation;
+ *     LR_F32 stores fp32 and runs exact fp32 (SIMT) GEMMs.  Weight gradients and
+ *     dg are always fp32.  1/rms (s) is always fp32.
+ *   - All pointers are DEVICE pointers of the current CUDA device, 16-byte
+ *     aligned.  d, d_in, d_out, f and r must be positive multiples of 8; T >= 1.
+ *   - Ownership: the caller allocates and owns every buffer, including `saved`
+ *     and the workspace `ws` (sizes from the *_bytes queries, which need no
+ *     device).  The library allocates and frees nothing and never synchronises,
+ *     except lr_check_device_error.  Outputs must not alias inputs.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
+ *     enqueued on it, asynchronously.
+ *   - Errors: arguments are validated before any launch; on failure the call
+ *     returns a non-zero lr_status, launches nothing and leaves a message in
+ *     lr_last_error() (thread-local).  A failed launch returns LR_ERR_CUDA.
+ *     Kernels never trap: a bounded wait that runs out sets a device error
+ *     word, which lr_check_device_error reports as LR_ERR_TIMEOUT.
+ *   - Results are deterministic: the same inputs give the same bits (no atomics
+ *     in any reduction), so LR_SAVE_CKPT and LR_SAVE_FULL give bitwise-equal
+ *     gradients.
+ */
+#ifndef LOWRANK_H_
+#define LOWRANK_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LR_OK = 0,
+  LR_ERR_NULL = 1,        /* a required pointer is NULL */
+  LR_ERR_SHAPE = 2,       /* a dimension is non-positive, not a multiple of 8, or too large */
+  LR_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  LR_ERR_DTYPE = 4,       /* unknown lr_dtype or lr_mode */
+  LR_ERR_WORKSPACE = 5,   /* saved / ws buffer smaller than the size query returns */
+  LR_ERR_CUDA = 6,        /* a CUDA call or kernel launch failed */
+  LR_ERR_TIMEOUT = 7,     /* a kernel's bounded wait ran out (reported by lr_check_device_error) */
+  LR_ERR_UNSUPPORTED = 8  /* no usable device / architecture */
+} lr_status;
+
+typedef enum { LR_F32 = 0, LR_BF16 = 1 } lr_dtype;
+
+typedef enum {
+  LR_SAVE_FULL = 0, /* keep every forward intermediate for the backward */
+  LR_SAVE_CKPT = 1  /* low-rank activation checkpointing (technical summary §2.2) */
+} lr_mode;
+
+/* One low-rank pair: A [r, d_in] and B [d_out, r], storage dtype. */
+typedef struct {
+  const void* A;
+  const void* B;
+} lr_pair;
+
+/* Gradients of one pair, fp32, same shapes as the weights. */
+typedef struct {
+  float* dA;
+  float* dB;
+} lr_pair_grad;
+
+/* ------------------------------------------------------------------ MLP block
+ * Low-rank SwiGLU MLP block with a residual (the sublayer the technical summary
+ * §2.2 groups as gate/up down-projections plus a down pair):
+ *     n   = RMSNorm(x; g, eps)              s[t] = (mean_j x[t,j]^2 + eps)^(-1/2)
+ *     a   = B_gate SiLU(A_gate n)           A_gate [r,d],  B_gate [f,r]
+ *     b   = B_up   SiLU(A_up   n)           A_up   [r,d],  B_up   [f,r]
+ *     h   = SiLU(a) * b                     [T, f]
+ *     out = x + B_down SiLU(A_down h)       A_down [r,f],  B_down [d,r]
+ * Dimensions: T tokens, d model width, f MLP width, r rank.
+ *
+ * `saved` holds what the backward needs: in LR_SAVE_CKPT the pre-activations
+ * u_gate, u_up, u_down ([T, r] each, dtype) and s ([T] fp32); LR_SAVE_FULL adds
+ * the SiLU outputs and a, b, h.  Its layout is private; pass it unchanged to
+ * lr_mlp_bwd with the same dtype, mode and dimensions.  x must also be passed
+ * unchanged to the backward (checkpointing keeps the block input, not a copy).
+ */
+size_t lr_mlp_saved_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r);
+size_t lr_mlp_fwd_workspace_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r);
+size_t lr_mlp_bwd_workspace_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r);
+
+/* x [T,d], g [d] -> out [T,d]; fills `saved`. */
+lr_status lr_mlp_fwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x,
+                     const void* g, lr_pair gate, lr_pair up, lr_pair down, void* out, void* saved,
+                     size_t saved_bytes, void* ws, size_t ws_bytes, void* stream);
+
+/* dout [T,d] = dL/dout -> dx [T,d] (dtype), dg [d] fp32, and every pair's dA, dB (fp32).
+ * In LR_SAVE_CKPT the backward first re-runs the block's forward from x, s and
+ * the saved pre-activations (no other state). */
+lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x,
+                     const void* g, lr_pair gate, lr_pair up, lr_pair down, const void* saved,
+                     size_t saved_bytes, const void* dout, void* dx, float* dg, lr_pair_grad dgate,
+                     lr_pair_grad dup, lr_pair_grad ddown, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------- projection group
+ * `group` (1..3) pairs that read the same input x [T, d_in], each mapping to
+ * d_out (attention q/k/v; technical summary §2.2 grouping):
+ *     v = RMSNorm(x; g, eps) if g != NULL, else v = x
+ *     outs[i] = B_i SiLU(A_i v)            A_i [r, d_in], B_i [d_out, r]
+ * The A_i run as one stacked GEMM, the B_i as one batched GEMM.  `saved` keeps
+ * the stacked pre-activations [T, group*r], the SiLU outputs and s.
+ */
+size_t lr_proj_saved_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm);
+size_t lr_proj_fwd_workspace_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm);
+size_t lr_proj_bwd_workspace_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm);
+
+lr_status lr_proj_fwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                      const void* g, float eps, const void* x, void* const* outs, void* saved, size_t saved_bytes,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* douts[i] [T, d_out] -> dx [T, d_in] (dtype), dg [d_in] fp32 (ignored and may be NULL
+ * when g == NULL), grads[i] (fp32). */
+lr_status lr_proj_bwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                      const void* g, float eps, const void* x, const void* saved, size_t saved_bytes,
+                      const void* const* douts, void* dx, float* dg, const lr_pair_grad* grads, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/* -------------------------------------------------------------- block stack
+ * One training step of `nblocks` residual MLP blocks (as lr_mlp_fwd) and a
+ * mean-squared-error loss against `target` [T, d]:
+ *     x_0 = x, x_{l+1} = block_l(x_l), loss = mean((x_L - target)^2)
+ * then the backward through every block (in LR_SAVE_CKPT each block is
+ * re-forwarded from its saved input and bottleneck pre-activations).
+ * gs[l] is block l's gain [d]; pairs holds 3*nblocks pairs (gate, up, down of
+ * block 0, then block 1, ...); dgs[l] [d] and grads (3*nblocks) receive the fp32
+ * gradients; loss is a device fp32 scalar; dx [T,d] (dtype) may be NULL.
+ * All activations of the step live in `ws`.
+ */
+size_t lr_stack_workspace_bytes(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, int f, int r);
+
+lr_status lr_stack_step(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, int f, int r, float eps,
+                        const void* x, const void* target, const void* const* gs, const lr_pair* pairs,
+                        float* loss, void* dx, float* const* dgs, const lr_pair_grad* grads, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ status
+ * lr_last_error: message of the last failing call on this thread ("" if none).
+ * lr_check_device_error: synchronises `stream`, reads and clears the current
+ * device's error word; LR_ERR_TIMEOUT if a bounded wait ran out, LR_ERR_CUDA
+ * if the stream reports an error, else LR_OK.
+ * lr_selftest_wait_timeout: launches one kernel that waits on a barrier nothing
+ * completes, for limit_ns nanoseconds, then sets the timeout bit and returns
+ * (exercises the timeout path without any fault). */
+const char* lr_last_error(void);
+lr_status lr_check_device_error(void* stream);
+lr_status lr_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int lr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOWRANK_H_ */

@@ -1,0 +1,47 @@
+// Host-side description of one fused GEMM launch and the launchers of the two
+// GEMM engines: the tcgen05 kernel (bf16 operands) and the SIMT kernel (fp32
+// operands, exact fp32 arithmetic, no TF32).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace lr {
+
+// A matrix operand stored row-major with leading dimension `ld` (elements).
+// For operand A ([M, K] logically): K-major storage holds element (m, k) at
+// ptr[m * ld + k]; MN-major storage holds it at ptr[k * ld + m].
+// Operand B ([N, K] logically) is read the same way with n in place of m.
+struct Operand {
+  const void* ptr;
+  long long ld;
+};
+
+struct GemmCall {
+  int M, N, K;
+  int nacc;     // accumulators per tile (2: SwiGLU dual GEMM, segment s uses A[s], B[s])
+  int batches;  // independent problems of the same shape (batch b uses A[b], B[b])
+  int ksplit;   // split-K factor (EPI_F32 only): partial s goes to out0 + s * split_stride
+  bool a_mn, b_mn;
+  Operand A[kMaxBatch];
+  Operand B[kMaxBatch];
+  EpiParams ep;
+  unsigned* err;  // device error word
+  int bn;         // tcgen05 tile width chosen by the planner (128 or 256)
+};
+
+// Row-partial chunk width used by the epilogues of each engine.
+constexpr int kChunkUmma = 32;
+constexpr int kChunkSimt = 8;
+
+template <EpiKind K, int BN, int NACC, bool A_MN, bool B_MN>
+cudaError_t launch_umma(const GemmCall& g, cudaStream_t st);
+
+template <EpiKind K, int NACC>
+cudaError_t launch_simt(const GemmCall& g, cudaStream_t st);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace lr

@@ -1,0 +1,17 @@
+// tcgen05 GEMM instantiations of the forward epilogues (operands K-major).
+#include "umma_launch.cuh"
+
+namespace lr {
+#define LR_INST(K, BN, NACC, AMN, BMN) \
+  template cudaError_t launch_umma<K, BN, NACC, AMN, BMN>(const GemmCall&, cudaStream_t);
+LR_INST(EPI_NORM_SILU, 128, 1, false, false)
+LR_INST(EPI_NORM_SILU, 256, 1, false, false)
+LR_INST(EPI_SILU, 128, 1, false, false)
+LR_INST(EPI_SILU, 256, 1, false, false)
+LR_INST(EPI_STORE, 128, 1, false, false)
+LR_INST(EPI_STORE, 256, 1, false, false)
+LR_INST(EPI_RESID, 128, 1, false, false)
+LR_INST(EPI_RESID, 256, 1, false, false)
+LR_INST(EPI_SWIGLU, 128, 2, false, false)
+#undef LR_INST
+}  // namespace lr

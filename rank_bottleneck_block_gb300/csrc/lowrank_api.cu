@@ -1,0 +1,1035 @@
+// C ABI of liblowrank.so: argument validation, workspace layout and the
+// launch sequence of each entry point (declared and documented in
+// include/lowrank.h).  Every step of the path runs in this library's kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/lowrank.h"
+#include "common.cuh"
+#include "gemm.h"
+#include "small_kernels.cuh"
+
+namespace lr {
+
+// ------------------------------------------------------------------ errors
+static thread_local std::string t_last_error;
+
+static lr_status fail(lr_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+#define LR_CUDA(expr)                                                                       \
+  do {                                                                                      \
+    cudaError_t e_ = (expr);                                                                \
+    if (e_ != cudaSuccess) return fail(LR_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+#define LR_TRY(expr)                   \
+  do {                                 \
+    lr_status s_ = (expr);             \
+    if (s_ != LR_OK) return s_;        \
+  } while (0)
+
+// --------------------------------------------------------- device state
+// The device error word: kernels OR bits into it instead of trapping.
+__device__ unsigned g_device_error_word;
+
+static constexpr int kMaxDevices = 64;
+static unsigned* s_err_ptr[kMaxDevices];
+static int s_sms[kMaxDevices];
+static std::mutex s_dev_mu;
+
+static lr_status current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail(LR_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(LR_ERR_UNSUPPORTED, "device ordinal %d out of range", *dev);
+  return LR_OK;
+}
+
+// Looked up once per device with that device current; later calls reuse it.
+static lr_status device_error_word(unsigned** out) {
+  int dev;
+  LR_TRY(current_device(&dev));
+  std::lock_guard<std::mutex> lk(s_dev_mu);
+  if (!s_err_ptr[dev]) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(LR_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                  minor);
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_device_error_word);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "cudaGetSymbolAddress(error word): %s", cudaGetErrorString(e));
+    s_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = s_err_ptr[dev];
+  return LR_OK;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (!s_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    s_sms[dev] = n > 0 ? n : 1;
+  }
+  return s_sms[dev];
+}
+
+// ----------------------------------------------------------- GEMM dispatch
+struct Ctx {
+  lr_dtype dt;
+  size_t es;  // element size of the storage dtype
+  cudaStream_t st;
+  unsigned* err;
+  int sms;
+  int chunk;  // row-partial chunk width of the engine
+};
+
+static int pick_bn(const GemmCall& g, int sms) {
+  if (g.N <= 128) return 128;
+  const long long mt = (g.M + 127) / 128;
+  const long long t256 = mt * ((g.N + 255) / 256) * g.batches * std::max(1, g.ksplit);
+  const long long t128 = mt * ((g.N + 127) / 128) * g.batches * std::max(1, g.ksplit);
+  const double c256 = static_cast<double>((t256 + sms - 1) / sms);
+  const double c128 = 0.55 * static_cast<double>((t128 + sms - 1) / sms);
+  return c128 < c256 ? 128 : 256;
+}
+
+template <EpiKind K, int NACC, bool A_MN, bool B_MN>
+static cudaError_t umma_bn(const GemmCall& g, cudaStream_t st) {
+  if (g.bn == 128) return launch_umma<K, 128, NACC, A_MN, B_MN>(g, st);
+  return launch_umma<K, 256, NACC, A_MN, B_MN>(g, st);
+}
+
+static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sms) {
+  g.bn = (k == EPI_SWIGLU) ? 128 : pick_bn(g, sms);
+  const bool kk = !g.a_mn && !g.b_mn, km = !g.a_mn && g.b_mn, mm = g.a_mn && g.b_mn;
+  switch (k) {
+    case EPI_NORM_SILU: if (kk) return umma_bn<EPI_NORM_SILU, 1, false, false>(g, st); break;
+    case EPI_SILU: if (kk) return umma_bn<EPI_SILU, 1, false, false>(g, st); break;
+    case EPI_STORE:
+      if (kk) return umma_bn<EPI_STORE, 1, false, false>(g, st);
+      if (km) return umma_bn<EPI_STORE, 1, false, true>(g, st);
+      break;
+    case EPI_RESID: if (kk) return umma_bn<EPI_RESID, 1, false, false>(g, st); break;
+    case EPI_SWIGLU: if (kk && g.nacc == 2) return launch_umma<EPI_SWIGLU, 128, 2, false, false>(g, st); break;
+    case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, 1, false, true>(g, st); break;
+    case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, 1, false, true>(g, st); break;
+    case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, 1, false, true>(g, st); break;
+    case EPI_DX_NORM: if (km) return umma_bn<EPI_DX_NORM, 1, false, true>(g, st); break;
+    case EPI_F32: if (mm) return umma_bn<EPI_F32, 1, true, true>(g, st); break;
+    default: break;
+  }
+  return cudaErrorNotSupported;
+}
+
+static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
+  switch (k) {
+    case EPI_NORM_SILU: return launch_simt<EPI_NORM_SILU, 1>(g, st);
+    case EPI_SILU: return launch_simt<EPI_SILU, 1>(g, st);
+    case EPI_STORE: return launch_simt<EPI_STORE, 1>(g, st);
+    case EPI_RESID: return launch_simt<EPI_RESID, 1>(g, st);
+    case EPI_SWIGLU: return launch_simt<EPI_SWIGLU, 2>(g, st);
+    case EPI_DSILU: return launch_simt<EPI_DSILU, 1>(g, st);
+    case EPI_DSILU_NORM: return launch_simt<EPI_DSILU_NORM, 1>(g, st);
+    case EPI_SWIGLU_BWD: return launch_simt<EPI_SWIGLU_BWD, 1>(g, st);
+    case EPI_DX_NORM: return launch_simt<EPI_DX_NORM, 1>(g, st);
+    case EPI_F32: return launch_simt<EPI_F32, 1>(g, st);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+static const char* epi_name(EpiKind k) {
+  static const char* names[] = {"norm_silu", "silu", "store", "resid", "swiglu",
+                                "dsilu", "dsilu_norm", "swiglu_bwd", "dx_norm", "f32"};
+  return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
+}
+
+static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g) {
+  g.err = c.err;
+  if (g.nacc < 1) g.nacc = 1;
+  if (g.batches < 1) g.batches = 1;
+  if (g.ksplit < 1) g.ksplit = 1;
+  g.ep.M = g.M;
+  g.ep.N = g.N;
+  cudaError_t e = (c.dt == LR_BF16) ? dispatch_bf16(k, g, c.st, c.sms) : dispatch_f32(k, g, c.st);
+  if (e != cudaSuccess)
+    return fail(LR_ERR_CUDA, "GEMM %s (M=%d N=%d K=%d) launch failed: %s", epi_name(k), g.M, g.N, g.K,
+                cudaGetErrorString(e));
+  return LR_OK;
+}
+
+static GemmCall new_call(int M, int N, int K) {
+  GemmCall g;
+  memset(&g, 0, sizeof(g));
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.nacc = 1;
+  g.batches = 1;
+  g.ksplit = 1;
+  return g;
+}
+
+static inline const void* off(const void* p, size_t bytes) { return static_cast<const char*>(p) + bytes; }
+static inline void* off(void* p, size_t bytes) { return static_cast<char*>(p) + bytes; }
+
+// --------------------------------------------------- weight gradients
+// Split factor of a weight-gradient GEMM (K = tokens): enough CTAs to fill the
+// GPU, at least 8 k-blocks per split, at most 8 splits.  Device-independent upper
+// bound (used for workspace sizing): min(8, max(1, kb / 8)).
+static int wgrad_split_bound(int K) {
+  const int kb = (K + 63) / 64;
+  return std::max(1, std::min(8, kb / 8));
+}
+
+static int wgrad_split(const Ctx& c, int M, int N, int K) {
+  if (c.dt != LR_BF16) return 1;
+  const int bn = N <= 128 ? 128 : 256;
+  const long long tiles = 1LL * ((M + 127) / 128) * ((N + bn - 1) / bn);
+  int ks = static_cast<int>(std::max<long long>(1, c.sms / std::max<long long>(1, tiles)));
+  ks = std::min(ks, wgrad_split_bound(K));
+  const int kb = (K + 63) / 64;
+  const int per = (kb + ks - 1) / ks;
+  return (kb + per - 1) / per;
+}
+
+static size_t wgrad_part_bytes(lr_dtype dt, int M, int N, int K) {
+  const int ks = dt == LR_BF16 ? wgrad_split_bound(K) : 1;
+  return static_cast<size_t>(ks) * M * N * sizeof(float);
+}
+
+// dst = (A^T B) over K tokens, both operands stored [K, .] row-major (MN-major),
+// reduced over splits in a fixed order, times the optional column scale, and the
+// optional dg partial sums over row blocks.
+static lr_status wgrad(const Ctx& c, int M, int N, int K, Operand A, Operand B, WgradDst dst, int rows_each,
+                       const void* colscale, float* dgpart, float* wpart) {
+  GemmCall g = new_call(M, N, K);
+  g.a_mn = g.b_mn = true;
+  g.A[0] = A;
+  g.B[0] = B;
+  g.ksplit = wgrad_split(c, M, N, K);
+  g.ep.out0[0] = wpart;
+  g.ep.ldo0 = N;
+  g.ep.split_stride = 1LL * M * N;
+  LR_TRY(gemm(c, EPI_F32, g));
+  cudaError_t e = (c.dt == LR_BF16)
+                      ? launch_wgrad_reduce<bf16>(wpart, g.ksplit, 1LL * M * N, M, N,
+                                                  static_cast<const bf16*>(colscale), dst, rows_each, dgpart, c.st)
+                      : launch_wgrad_reduce<float>(wpart, g.ksplit, 1LL * M * N, M, N,
+                                                   static_cast<const float*>(colscale), dst, rows_each, dgpart, c.st);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "wgrad reduce: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
+// ------------------------------------------------------------ small ops
+static lr_status fold(const Ctx& c, void* out, StackSrc src, int nsrc, int rows_each, int cols, const void* g) {
+  cudaError_t e = (c.dt == LR_BF16) ? launch_fold<bf16>(static_cast<bf16*>(out), src, nsrc, rows_each, cols,
+                                                        static_cast<const bf16*>(g), c.st)
+                                    : launch_fold<float>(static_cast<float*>(out), src, nsrc, rows_each, cols,
+                                                         static_cast<const float*>(g), c.st);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "fold: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
+static lr_status rstd(const Ctx& c, const void* x, int T, int d, float eps, float* s) {
+  cudaError_t e = (c.dt == LR_BF16) ? launch_rstd<bf16>(static_cast<const bf16*>(x), T, d, eps, s, c.st)
+                                    : launch_rstd<float>(static_cast<const float*>(x), T, d, eps, s, c.st);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "rstd: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
+static lr_status silu_slab(const Ctx& c, const void* u, long long ldu, void* z, long long ldz, int T, int n) {
+  cudaError_t e = (c.dt == LR_BF16)
+                      ? launch_silu<bf16>(static_cast<const bf16*>(u), ldu, static_cast<bf16*>(z), ldz, T, n, c.st)
+                      : launch_silu<float>(static_cast<const float*>(u), ldu, static_cast<float*>(z), ldz, T, n, c.st);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "silu: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
+static lr_status dg_finalize(const Ctx& c, const float* dgpart, int nparts, int N, float* dg) {
+  cudaError_t e = launch_dg_finalize(dgpart, nparts, N, dg, c.st);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "dg: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
+// ---------------------------------------------------------------- arena
+// Bump allocator over a caller buffer; with base == nullptr it only measures.
+struct Arena {
+  char* base;
+  size_t off;
+  explicit Arena(void* b) : base(static_cast<char*>(b)), off(0) {}
+  void* take(size_t bytes) {
+    off = (off + 255) & ~size_t(255);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+  size_t size() const { return (off + 255) & ~size_t(255); }
+};
+
+static size_t esize(lr_dtype dt) { return dt == LR_BF16 ? 2 : 4; }
+static int chunk_width(lr_dtype dt) { return dt == LR_BF16 ? kChunkUmma : kChunkSimt; }
+static int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// ============================================================ MLP block
+struct MlpSaved {
+  void *u_gu, *u_d;
+  float* s;
+  void *z_gu, *z_d, *a, *b, *h;  // LR_SAVE_FULL only
+};
+
+static size_t mlp_saved_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, void* base, MlpSaved* S) {
+  (void)d;
+  const size_t es = esize(dt);
+  Arena ar(base);
+  MlpSaved tmp;
+  if (!S) S = &tmp;
+  memset(S, 0, sizeof(*S));
+  S->u_gu = ar.take(es * T * 2 * r);
+  S->u_d = ar.take(es * T * r);
+  S->s = static_cast<float*>(ar.take(sizeof(float) * T));
+  if (mode == LR_SAVE_FULL) {
+    S->z_gu = ar.take(es * T * 2 * r);
+    S->z_d = ar.take(es * T * r);
+    S->a = ar.take(es * T * f);
+    S->b = ar.take(es * T * f);
+    S->h = ar.take(es * T * f);
+  }
+  return ar.size();
+}
+
+struct MlpFwdWs {
+  void *Af, *z_gu, *z_d, *h;
+};
+
+static size_t mlp_fwd_ws_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, void* base, MlpFwdWs* W) {
+  const size_t es = esize(dt);
+  Arena ar(base);
+  MlpFwdWs tmp;
+  if (!W) W = &tmp;
+  memset(W, 0, sizeof(*W));
+  W->Af = ar.take(es * 2 * r * d);
+  if (mode == LR_SAVE_CKPT) {
+    W->z_gu = ar.take(es * T * 2 * r);
+    W->z_d = ar.take(es * T * r);
+    W->h = ar.take(es * T * f);
+  }
+  return ar.size();
+}
+
+struct MlpBwdWs {
+  void *Af, *z_gu, *z_d, *a, *b, *h;  // z/a/b/h: LR_SAVE_CKPT recompute only
+  void *du_d, *da, *db, *du_s;
+  float *rowpart, *wpart, *dgpart;
+};
+
+static size_t mlp_bwd_ws_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, void* base, MlpBwdWs* W) {
+  const size_t es = esize(dt);
+  Arena ar(base);
+  MlpBwdWs tmp;
+  if (!W) W = &tmp;
+  memset(W, 0, sizeof(*W));
+  W->Af = ar.take(es * 2 * r * d);
+  if (mode == LR_SAVE_CKPT) {
+    W->z_gu = ar.take(es * T * 2 * r);
+    W->z_d = ar.take(es * T * r);
+    W->a = ar.take(es * T * f);
+    W->b = ar.take(es * T * f);
+    W->h = ar.take(es * T * f);
+  }
+  W->du_d = ar.take(es * T * r);
+  W->da = ar.take(es * T * f);
+  W->db = ar.take(es * T * f);
+  W->du_s = ar.take(es * T * 2 * r);
+  W->rowpart = static_cast<float*>(ar.take(sizeof(float) * 2 * cdiv(r, chunk_width(dt)) * T));
+  size_t wp = std::max({wgrad_part_bytes(dt, d, r, T), wgrad_part_bytes(dt, r, f, T), wgrad_part_bytes(dt, f, r, T),
+                        wgrad_part_bytes(dt, 2 * r, d, T)});
+  W->wpart = static_cast<float*>(ar.take(wp));
+  W->dgpart = static_cast<float*>(ar.take(sizeof(float) * cdiv(2 * r, kReduceRows) * d));
+  return ar.size();
+}
+
+// The SwiGLU dual GEMM: a = z_g B_gate^T, b = z_u B_up^T, h = SiLU(a) * b.
+static lr_status swiglu_gemm(const Ctx& c, int T, int f, int r, const void* z_gu, const void* Bg, const void* Bu,
+                             void* h, void* a, void* b) {
+  GemmCall g = new_call(T, f, r);
+  g.nacc = 2;
+  g.A[0] = {z_gu, 2LL * r};
+  g.A[1] = {off(z_gu, c.es * r), 2LL * r};
+  g.B[0] = {Bg, r};
+  g.B[1] = {Bu, r};
+  g.ep.out0[0] = h;
+  g.ep.out1[0] = a;
+  g.ep.out2[0] = b;
+  g.ep.ldo0 = g.ep.ldo1 = g.ep.ldo2 = f;
+  return gemm(c, EPI_SWIGLU, g);
+}
+
+static lr_status mlp_fwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, int r, float eps, const void* x,
+                              const void* g, lr_pair gate, lr_pair up, lr_pair down, void* out, void* saved,
+                              void* ws) {
+  MlpSaved S;
+  MlpFwdWs W;
+  mlp_saved_layout(c.dt, mode, T, d, f, r, saved, &S);
+  mlp_fwd_ws_layout(c.dt, mode, T, d, f, r, ws, &W);
+  void* z_gu = mode == LR_SAVE_FULL ? S.z_gu : W.z_gu;
+  void* z_d = mode == LR_SAVE_FULL ? S.z_d : W.z_d;
+  void* h = mode == LR_SAVE_FULL ? S.h : W.h;
+
+  // Online-RMSNorm (technical summary §2.2): gain folded into the stacked [A_gate; A_up] ...
+  StackSrc src = {{gate.A, up.A, nullptr}};
+  LR_TRY(fold(c, W.Af, src, 2, r, d, g));
+  // ... 1/rms per row ...
+  LR_TRY(rstd(c, x, T, d, eps, S.s));
+  // ... applied as a row scale in the grouped gate/up GEMM's epilogue, with SiLU fused.
+  {
+    GemmCall k = new_call(T, 2 * r, d);
+    k.A[0] = {x, d};
+    k.B[0] = {W.Af, d};
+    k.ep.out0[0] = S.u_gu;
+    k.ep.out1[0] = z_gu;
+    k.ep.ldo0 = k.ep.ldo1 = 2 * r;
+    k.ep.rowscale = S.s;
+    LR_TRY(gemm(c, EPI_NORM_SILU, k));
+  }
+  // B_gate / B_up with the SwiGLU product fused.
+  LR_TRY(swiglu_gemm(c, T, f, r, z_gu, gate.B, up.B, h, mode == LR_SAVE_FULL ? S.a : nullptr,
+                     mode == LR_SAVE_FULL ? S.b : nullptr));
+  // A_down with SiLU fused.
+  {
+    GemmCall k = new_call(T, r, f);
+    k.A[0] = {h, f};
+    k.B[0] = {down.A, f};
+    k.ep.out0[0] = S.u_d;
+    k.ep.out1[0] = z_d;
+    k.ep.ldo0 = k.ep.ldo1 = r;
+    LR_TRY(gemm(c, EPI_SILU, k));
+  }
+  // B_down with the residual fused.
+  {
+    GemmCall k = new_call(T, d, r);
+    k.A[0] = {z_d, r};
+    k.B[0] = {down.B, r};
+    k.ep.out0[0] = out;
+    k.ep.ldo0 = d;
+    k.ep.aux0[0] = x;
+    k.ep.lda0 = d;
+    LR_TRY(gemm(c, EPI_RESID, k));
+  }
+  return LR_OK;
+}
+
+static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, int r, float eps, const void* x,
+                              const void* g, lr_pair gate, lr_pair up, lr_pair down, const void* saved,
+                              const void* G, void* dx, float* dg, lr_pair_grad dgate, lr_pair_grad dup,
+                              lr_pair_grad ddown, void* ws) {
+  (void)eps;
+  MlpSaved S;
+  MlpBwdWs W;
+  mlp_saved_layout(c.dt, mode, T, d, f, r, const_cast<void*>(saved), &S);
+  mlp_bwd_ws_layout(c.dt, mode, T, d, f, r, ws, &W);
+  const int ch = chunk_width(c.dt);
+
+  StackSrc src = {{gate.A, up.A, nullptr}};
+  LR_TRY(fold(c, W.Af, src, 2, r, d, g));
+
+  void *z_gu, *z_d, *a, *b, *h;
+  if (mode == LR_SAVE_CKPT) {
+    // Low-rank activation checkpointing (technical summary §2.2): re-forward inside the block
+    // from the saved [T, r] pre-activations; no other state is needed.
+    z_gu = W.z_gu;
+    z_d = W.z_d;
+    a = W.a;
+    b = W.b;
+    h = W.h;
+    LR_TRY(silu_slab(c, S.u_gu, 2 * r, z_gu, 2 * r, T, 2 * r));
+    LR_TRY(silu_slab(c, S.u_d, r, z_d, r, T, r));
+    LR_TRY(swiglu_gemm(c, T, f, r, z_gu, gate.B, up.B, h, a, b));
+  } else {
+    z_gu = S.z_gu;
+    z_d = S.z_d;
+    a = S.a;
+    b = S.b;
+    h = S.h;
+  }
+
+  // dB_down = G^T z_down
+  {
+    WgradDst dst = {{ddown.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, d, r, T, {G, d}, {z_d, r}, dst, d, nullptr, nullptr, W.wpart));
+  }
+  // du_down = (G B_down) * SiLU'(u_down)
+  {
+    GemmCall k = new_call(T, r, d);
+    k.b_mn = true;
+    k.A[0] = {G, d};
+    k.B[0] = {down.B, r};
+    k.ep.aux0[0] = S.u_d;
+    k.ep.lda0 = r;
+    k.ep.out0[0] = W.du_d;
+    k.ep.ldo0 = r;
+    LR_TRY(gemm(c, EPI_DSILU, k));
+  }
+  // dA_down = du_down^T h
+  {
+    WgradDst dst = {{ddown.dA, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, r, f, T, {W.du_d, r}, {h, f}, dst, r, nullptr, nullptr, W.wpart));
+  }
+  // dh = du_down A_down; SwiGLU backward fused: da = dh b SiLU'(a), db = dh SiLU(a)
+  {
+    GemmCall k = new_call(T, f, r);
+    k.b_mn = true;
+    k.A[0] = {W.du_d, r};
+    k.B[0] = {down.A, f};
+    k.ep.aux0[0] = a;
+    k.ep.aux1[0] = b;
+    k.ep.lda0 = k.ep.lda1 = f;
+    k.ep.out0[0] = W.da;
+    k.ep.out1[0] = W.db;
+    k.ep.ldo0 = k.ep.ldo1 = f;
+    LR_TRY(gemm(c, EPI_SWIGLU_BWD, k));
+  }
+  // dB_gate = da^T z_gate, dB_up = db^T z_up
+  {
+    WgradDst dst = {{dgate.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, f, r, T, {W.da, f}, {z_gu, 2LL * r}, dst, f, nullptr, nullptr, W.wpart));
+    WgradDst dst2 = {{dup.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, f, r, T, {W.db, f}, {off(z_gu, c.es * r), 2LL * r}, dst2, f, nullptr, nullptr, W.wpart));
+  }
+  // du_{gate,up} = (d{a,b} B) * SiLU'(u), stored pre-scaled by s; rho partials = sum du * u.
+  {
+    GemmCall k = new_call(T, r, f);
+    k.b_mn = true;
+    k.batches = 2;
+    k.A[0] = {W.da, f};
+    k.A[1] = {W.db, f};
+    k.B[0] = {gate.B, r};
+    k.B[1] = {up.B, r};
+    k.ep.aux0[0] = S.u_gu;
+    k.ep.aux0[1] = off(S.u_gu, c.es * r);
+    k.ep.lda0 = 2 * r;
+    k.ep.out0[0] = W.du_s;
+    k.ep.out0[1] = off(W.du_s, c.es * r);
+    k.ep.ldo0 = 2 * r;
+    k.ep.rowscale = S.s;
+    k.ep.rowpart = W.rowpart;
+    k.ep.rowpart_chunks = cdiv(r, ch);
+    LR_TRY(gemm(c, EPI_DSILU_NORM, k));
+  }
+  // dA'_{gate;up} = (s du)^T x; dA = dA' * g; dg_j = sum_i dA'_ij A_ij
+  {
+    WgradDst dst = {{dgate.dA, dup.dA, nullptr}, {gate.A, up.A, nullptr}};
+    LR_TRY(wgrad(c, 2 * r, d, T, {W.du_s, 2LL * r}, {x, d}, dst, r, g, W.dgpart, W.wpart));
+    LR_TRY(dg_finalize(c, W.dgpart, cdiv(2 * r, kReduceRows), d, dg));
+  }
+  // dx = G + (s du) A' - (s^2 / d) rho x  (one GEMM with K = 2r: gate and up sum inside the MMA)
+  {
+    GemmCall k = new_call(T, d, 2 * r);
+    k.b_mn = true;
+    k.A[0] = {W.du_s, 2LL * r};
+    k.B[0] = {W.Af, d};
+    k.ep.aux0[0] = G;
+    k.ep.aux1[0] = x;
+    k.ep.lda0 = k.ep.lda1 = d;
+    k.ep.rowscale = S.s;
+    k.ep.rowpart_in = W.rowpart;
+    k.ep.rowpart_in_chunks = 2 * cdiv(r, ch);
+    k.ep.coef = 1.f / static_cast<float>(d);
+    k.ep.out0[0] = dx;
+    k.ep.ldo0 = d;
+    LR_TRY(gemm(c, EPI_DX_NORM, k));
+  }
+  return LR_OK;
+}
+
+// ======================================================= projection group
+struct ProjSaved {
+  void *u, *z;
+  float* s;
+};
+
+static size_t proj_saved_layout(lr_dtype dt, int T, int r, int group, int norm, void* base, ProjSaved* S) {
+  const size_t es = esize(dt);
+  Arena ar(base);
+  ProjSaved tmp;
+  if (!S) S = &tmp;
+  S->u = ar.take(es * T * group * r);
+  S->z = ar.take(es * T * group * r);
+  S->s = norm ? static_cast<float*>(ar.take(sizeof(float) * T)) : nullptr;
+  return ar.size();
+}
+
+struct ProjWs {
+  void *Af, *du;
+  float *rowpart, *wpart, *dgpart;
+};
+
+static size_t proj_ws_layout(lr_dtype dt, bool bwd, int T, int d_in, int d_out, int r, int group, int norm,
+                             void* base, ProjWs* W) {
+  const size_t es = esize(dt);
+  Arena ar(base);
+  ProjWs tmp;
+  if (!W) W = &tmp;
+  memset(W, 0, sizeof(*W));
+  W->Af = ar.take(es * group * r * d_in);
+  if (bwd) {
+    W->du = ar.take(es * T * group * r);
+    if (norm) W->rowpart = static_cast<float*>(ar.take(sizeof(float) * group * cdiv(r, chunk_width(dt)) * T));
+    W->wpart = static_cast<float*>(
+        ar.take(std::max(wgrad_part_bytes(dt, d_out, r, T), wgrad_part_bytes(dt, group * r, d_in, T))));
+    if (norm) W->dgpart = static_cast<float*>(ar.take(sizeof(float) * cdiv(group * r, kReduceRows) * d_in));
+  }
+  return ar.size();
+}
+
+static lr_status proj_fwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                               const void* g, float eps, const void* x, void* const* outs, void* saved, void* ws) {
+  const int norm = g != nullptr;
+  ProjSaved S;
+  ProjWs W;
+  proj_saved_layout(c.dt, T, r, group, norm, saved, &S);
+  proj_ws_layout(c.dt, false, T, d_in, d_out, r, group, norm, ws, &W);
+  StackSrc src = {{nullptr, nullptr, nullptr}};
+  for (int i = 0; i < group; ++i) src.src[i] = pairs[i].A;
+  LR_TRY(fold(c, W.Af, src, group, r, d_in, g));
+  if (norm) LR_TRY(rstd(c, x, T, d_in, eps, S.s));
+  {
+    GemmCall k = new_call(T, group * r, d_in);
+    k.A[0] = {x, d_in};
+    k.B[0] = {W.Af, d_in};
+    k.ep.out0[0] = S.u;
+    k.ep.out1[0] = S.z;
+    k.ep.ldo0 = k.ep.ldo1 = 1LL * group * r;
+    k.ep.rowscale = S.s;
+    LR_TRY(gemm(c, norm ? EPI_NORM_SILU : EPI_SILU, k));
+  }
+  {
+    // The B's have distinct inputs: one batched GEMM (technical summary §2.2).
+    GemmCall k = new_call(T, d_out, r);
+    k.batches = group;
+    for (int i = 0; i < group; ++i) {
+      k.A[i] = {off(S.z, c.es * i * r), 1LL * group * r};
+      k.B[i] = {pairs[i].B, r};
+      k.ep.out0[i] = outs[i];
+    }
+    k.ep.ldo0 = d_out;
+    LR_TRY(gemm(c, EPI_STORE, k));
+  }
+  return LR_OK;
+}
+
+static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                               const void* g, const void* x, const void* saved, const void* const* douts, void* dx,
+                               float* dg, const lr_pair_grad* grads, void* ws) {
+  const int norm = g != nullptr;
+  ProjSaved S;
+  ProjWs W;
+  proj_saved_layout(c.dt, T, r, group, norm, const_cast<void*>(saved), &S);
+  proj_ws_layout(c.dt, true, T, d_in, d_out, r, group, norm, ws, &W);
+  const int ch = chunk_width(c.dt);
+  const long long ldg = 1LL * group * r;
+  StackSrc src = {{nullptr, nullptr, nullptr}};
+  for (int i = 0; i < group; ++i) src.src[i] = pairs[i].A;
+  LR_TRY(fold(c, W.Af, src, group, r, d_in, g));
+  for (int i = 0; i < group; ++i) {
+    WgradDst dst = {{grads[i].dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, d_out, r, T, {douts[i], d_out}, {off(S.z, c.es * i * r), ldg}, dst, d_out, nullptr, nullptr,
+                 W.wpart));
+  }
+  {
+    GemmCall k = new_call(T, r, d_out);
+    k.b_mn = true;
+    k.batches = group;
+    for (int i = 0; i < group; ++i) {
+      k.A[i] = {douts[i], d_out};
+      k.B[i] = {pairs[i].B, r};
+      k.ep.aux0[i] = off(S.u, c.es * i * r);
+      k.ep.out0[i] = off(W.du, c.es * i * r);
+    }
+    k.ep.lda0 = k.ep.ldo0 = ldg;
+    k.ep.rowscale = S.s;
+    k.ep.rowpart = W.rowpart;
+    k.ep.rowpart_chunks = cdiv(r, ch);
+    LR_TRY(gemm(c, norm ? EPI_DSILU_NORM : EPI_DSILU, k));
+  }
+  {
+    WgradDst dst = {{nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    for (int i = 0; i < group; ++i) {
+      dst.dst[i] = grads[i].dA;
+      dst.aw[i] = norm ? pairs[i].A : nullptr;
+    }
+    LR_TRY(wgrad(c, group * r, d_in, T, {W.du, ldg}, {x, d_in}, dst, r, g, norm ? W.dgpart : nullptr, W.wpart));
+    if (norm) LR_TRY(dg_finalize(c, W.dgpart, cdiv(group * r, kReduceRows), d_in, dg));
+  }
+  {
+    GemmCall k = new_call(T, d_in, group * r);
+    k.b_mn = true;
+    k.A[0] = {W.du, ldg};
+    k.B[0] = {W.Af, d_in};
+    k.ep.out0[0] = dx;
+    k.ep.ldo0 = d_in;
+    if (norm) {
+      k.ep.aux1[0] = x;
+      k.ep.lda1 = d_in;
+      k.ep.rowscale = S.s;
+      k.ep.rowpart_in = W.rowpart;
+      k.ep.rowpart_in_chunks = group * cdiv(r, ch);
+      k.ep.coef = 1.f / static_cast<float>(d_in);
+    }
+    LR_TRY(gemm(c, norm ? EPI_DX_NORM : EPI_STORE, k));
+  }
+  return LR_OK;
+}
+
+// ============================================================ block stack
+struct StackWs {
+  void* acts;   // x_1 .. x_L, [L][T, d]
+  void* saved;  // [L][mlp saved]
+  size_t saved_each;
+  void* scratch;  // max(mlp fwd ws, mlp bwd ws)
+  void *dy0, *dy1;
+  float* mse_part;
+};
+
+static size_t stack_ws_layout(lr_dtype dt, lr_mode mode, int L, int T, int d, int f, int r, void* base,
+                              StackWs* W) {
+  const size_t es = esize(dt);
+  Arena ar(base);
+  StackWs tmp;
+  if (!W) W = &tmp;
+  W->acts = ar.take(es * L * T * d);
+  W->saved_each = mlp_saved_layout(dt, mode, T, d, f, r, nullptr, nullptr);
+  W->saved = ar.take(W->saved_each * L);
+  W->scratch = ar.take(std::max(mlp_fwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr),
+                                mlp_bwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr)));
+  W->dy0 = ar.take(es * T * d);
+  W->dy1 = ar.take(es * T * d);
+  W->mse_part = static_cast<float*>(ar.take(sizeof(float) * kMseParts));
+  return ar.size();
+}
+
+static lr_status stack_impl(const Ctx& c, lr_mode mode, int L, int T, int d, int f, int r, float eps, const void* x,
+                            const void* target, const void* const* gs, const lr_pair* pairs, float* loss, void* dx,
+                            float* const* dgs, const lr_pair_grad* grads, void* ws) {
+  StackWs W;
+  stack_ws_layout(c.dt, mode, L, T, d, f, r, ws, &W);
+  const size_t act_bytes = c.es * T * d;
+  auto act = [&](int l) -> void* { return l == 0 ? const_cast<void*>(x) : off(W.acts, act_bytes * (l - 1)); };
+  auto sv = [&](int l) -> void* { return off(W.saved, W.saved_each * l); };
+  for (int l = 0; l < L; ++l)
+    LR_TRY(mlp_fwd_impl(c, mode, T, d, f, r, eps, act(l), gs[l], pairs[3 * l], pairs[3 * l + 1], pairs[3 * l + 2],
+                        act(l + 1), sv(l), W.scratch));
+  {
+    const long long n = 1LL * T * d;
+    cudaError_t e = (c.dt == LR_BF16)
+                        ? launch_mse<bf16>(static_cast<const bf16*>(act(L)), static_cast<const bf16*>(target), n,
+                                           static_cast<bf16*>(W.dy0), W.mse_part, kMseParts, loss, c.st)
+                        : launch_mse<float>(static_cast<const float*>(act(L)), static_cast<const float*>(target), n,
+                                            static_cast<float*>(W.dy0), W.mse_part, kMseParts, loss, c.st);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "mse: %s", cudaGetErrorString(e));
+  }
+  void* dcur = W.dy0;
+  void* dnext = W.dy1;
+  for (int l = L - 1; l >= 0; --l) {
+    void* dst = (l == 0 && dx) ? dx : dnext;
+    LR_TRY(mlp_bwd_impl(c, mode, T, d, f, r, eps, act(l), gs[l], pairs[3 * l], pairs[3 * l + 1], pairs[3 * l + 2],
+                        sv(l), dcur, dst, dgs[l], grads[3 * l], grads[3 * l + 1], grads[3 * l + 2], W.scratch));
+    std::swap(dcur, dnext);
+  }
+  return LR_OK;
+}
+
+// ============================================================ validation
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static lr_status check_ptr(const void* p, const char* name) {
+  if (!p) return fail(LR_ERR_NULL, "%s is NULL", name);
+  if (!aligned16(p)) return fail(LR_ERR_ALIGN, "%s is not 16-byte aligned", name);
+  return LR_OK;
+}
+
+static lr_status check_dim(int v, const char* name, bool mult8) {
+  if (v <= 0) return fail(LR_ERR_SHAPE, "%s = %d must be positive", name, v);
+  if (v > (1 << 24)) return fail(LR_ERR_SHAPE, "%s = %d exceeds 16777216", name, v);
+  if (mult8 && (v % 8)) return fail(LR_ERR_SHAPE, "%s = %d must be a multiple of 8", name, v);
+  return LR_OK;
+}
+
+static lr_status check_dtype(lr_dtype dt) {
+  if (dt != LR_F32 && dt != LR_BF16) return fail(LR_ERR_DTYPE, "unknown dtype %d", static_cast<int>(dt));
+  return LR_OK;
+}
+
+static lr_status check_mode(lr_mode m) {
+  if (m != LR_SAVE_FULL && m != LR_SAVE_CKPT) return fail(LR_ERR_DTYPE, "unknown mode %d", static_cast<int>(m));
+  return LR_OK;
+}
+
+static lr_status check_size(size_t have, size_t need, const char* name) {
+  if (have < need) return fail(LR_ERR_WORKSPACE, "%s has %zu bytes, needs %zu", name, have, need);
+  return LR_OK;
+}
+
+static lr_status make_ctx(lr_dtype dt, void* stream, Ctx* c) {
+  c->dt = dt;
+  c->es = esize(dt);
+  c->st = static_cast<cudaStream_t>(stream);
+  LR_TRY(device_error_word(&c->err));
+  c->sms = device_sm_count();
+  c->chunk = chunk_width(dt);
+  return LR_OK;
+}
+
+static lr_status check_mlp_dims(int T, int d, int f, int r) {
+  LR_TRY(check_dim(T, "T", false));
+  LR_TRY(check_dim(d, "d", true));
+  LR_TRY(check_dim(f, "f", true));
+  LR_TRY(check_dim(r, "r", true));
+  return LR_OK;
+}
+
+static lr_status check_proj_dims(int T, int d_in, int d_out, int r, int group) {
+  LR_TRY(check_dim(T, "T", false));
+  LR_TRY(check_dim(d_in, "d_in", true));
+  LR_TRY(check_dim(d_out, "d_out", true));
+  LR_TRY(check_dim(r, "r", true));
+  if (group < 1 || group > kMaxStack) return fail(LR_ERR_SHAPE, "group = %d must be 1..%d", group, kMaxStack);
+  return LR_OK;
+}
+
+}  // namespace lr
+
+using namespace lr;
+
+// ================================================================== C ABI
+extern "C" {
+
+int lr_version(void) { return 100; }
+
+const char* lr_last_error(void) { return t_last_error.c_str(); }
+
+size_t lr_mlp_saved_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r) {
+  if (check_dtype(dt) || check_mode(mode) || check_mlp_dims(T, d, f, r)) return 0;
+  return mlp_saved_layout(dt, mode, T, d, f, r, nullptr, nullptr);
+}
+
+size_t lr_mlp_fwd_workspace_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r) {
+  if (check_dtype(dt) || check_mode(mode) || check_mlp_dims(T, d, f, r)) return 0;
+  return mlp_fwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr);
+}
+
+size_t lr_mlp_bwd_workspace_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r) {
+  if (check_dtype(dt) || check_mode(mode) || check_mlp_dims(T, d, f, r)) return 0;
+  return mlp_bwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr);
+}
+
+static lr_status check_pair(lr_pair p, const char* name) {
+  char buf[64];
+  snprintf(buf, sizeof(buf), "%s.A", name);
+  LR_TRY(check_ptr(p.A, buf));
+  snprintf(buf, sizeof(buf), "%s.B", name);
+  return check_ptr(p.B, buf);
+}
+
+static lr_status check_grad(lr_pair_grad p, const char* name) {
+  char buf[64];
+  snprintf(buf, sizeof(buf), "%s.dA", name);
+  LR_TRY(check_ptr(p.dA, buf));
+  snprintf(buf, sizeof(buf), "%s.dB", name);
+  return check_ptr(p.dB, buf);
+}
+
+lr_status lr_mlp_fwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x, const void* g,
+                     lr_pair gate, lr_pair up, lr_pair down, void* out, void* saved, size_t saved_bytes, void* ws,
+                     size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_mode(mode));
+  LR_TRY(check_mlp_dims(T, d, f, r));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(g, "g"));
+  LR_TRY(check_pair(gate, "gate"));
+  LR_TRY(check_pair(up, "up"));
+  LR_TRY(check_pair(down, "down"));
+  LR_TRY(check_ptr(out, "out"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, mlp_saved_layout(dt, mode, T, d, f, r, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, mlp_fwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return mlp_fwd_impl(c, mode, T, d, f, r, eps, x, g, gate, up, down, out, saved, ws);
+}
+
+lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x, const void* g,
+                     lr_pair gate, lr_pair up, lr_pair down, const void* saved, size_t saved_bytes, const void* dout,
+                     void* dx, float* dg, lr_pair_grad dgate, lr_pair_grad dup, lr_pair_grad ddown, void* ws,
+                     size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_mode(mode));
+  LR_TRY(check_mlp_dims(T, d, f, r));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(g, "g"));
+  LR_TRY(check_pair(gate, "gate"));
+  LR_TRY(check_pair(up, "up"));
+  LR_TRY(check_pair(down, "down"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(dout, "dout"));
+  LR_TRY(check_ptr(dx, "dx"));
+  LR_TRY(check_ptr(dg, "dg"));
+  LR_TRY(check_grad(dgate, "dgate"));
+  LR_TRY(check_grad(dup, "dup"));
+  LR_TRY(check_grad(ddown, "ddown"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, mlp_saved_layout(dt, mode, T, d, f, r, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, mlp_bwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return mlp_bwd_impl(c, mode, T, d, f, r, eps, x, g, gate, up, down, saved, dout, dx, dg, dgate, dup, ddown, ws);
+}
+
+size_t lr_proj_saved_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm) {
+  if (check_dtype(dt) || check_proj_dims(T, d_in, d_out, r, group)) return 0;
+  return proj_saved_layout(dt, T, r, group, norm != 0, nullptr, nullptr);
+}
+
+size_t lr_proj_fwd_workspace_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm) {
+  if (check_dtype(dt) || check_proj_dims(T, d_in, d_out, r, group)) return 0;
+  return proj_ws_layout(dt, false, T, d_in, d_out, r, group, norm != 0, nullptr, nullptr);
+}
+
+size_t lr_proj_bwd_workspace_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm) {
+  if (check_dtype(dt) || check_proj_dims(T, d_in, d_out, r, group)) return 0;
+  return proj_ws_layout(dt, true, T, d_in, d_out, r, group, norm != 0, nullptr, nullptr);
+}
+
+lr_status lr_proj_fwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs, const void* g,
+                      float eps, const void* x, void* const* outs, void* saved, size_t saved_bytes, void* ws,
+                      size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_proj_dims(T, d_in, d_out, r, group));
+  if (!pairs || !outs) return fail(LR_ERR_NULL, "pairs / outs is NULL");
+  for (int i = 0; i < group; ++i) {
+    LR_TRY(check_pair(pairs[i], "pairs[i]"));
+    LR_TRY(check_ptr(outs[i], "outs[i]"));
+  }
+  if (g) LR_TRY(check_ptr(g, "g"));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, proj_saved_layout(dt, T, r, group, g != nullptr, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, proj_ws_layout(dt, false, T, d_in, d_out, r, group, g != nullptr, nullptr, nullptr),
+                    "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return proj_fwd_impl(c, T, d_in, d_out, r, group, pairs, g, eps, x, outs, saved, ws);
+}
+
+lr_status lr_proj_bwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs, const void* g,
+                      float eps, const void* x, const void* saved, size_t saved_bytes, const void* const* douts,
+                      void* dx, float* dg, const lr_pair_grad* grads, void* ws, size_t ws_bytes, void* stream) {
+  (void)eps;
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_proj_dims(T, d_in, d_out, r, group));
+  if (!pairs || !douts || !grads) return fail(LR_ERR_NULL, "pairs / douts / grads is NULL");
+  for (int i = 0; i < group; ++i) {
+    LR_TRY(check_pair(pairs[i], "pairs[i]"));
+    LR_TRY(check_ptr(douts[i], "douts[i]"));
+    LR_TRY(check_grad(grads[i], "grads[i]"));
+  }
+  if (g) {
+    LR_TRY(check_ptr(g, "g"));
+    LR_TRY(check_ptr(dg, "dg"));
+  }
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(dx, "dx"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, proj_saved_layout(dt, T, r, group, g != nullptr, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, proj_ws_layout(dt, true, T, d_in, d_out, r, group, g != nullptr, nullptr, nullptr),
+                    "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return proj_bwd_impl(c, T, d_in, d_out, r, group, pairs, g, x, saved, douts, dx, dg, grads, ws);
+}
+
+size_t lr_stack_workspace_bytes(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, int f, int r) {
+  if (check_dtype(dt) || check_mode(mode) || check_mlp_dims(T, d, f, r) || nblocks < 1) return 0;
+  return stack_ws_layout(dt, mode, nblocks, T, d, f, r, nullptr, nullptr);
+}
+
+lr_status lr_stack_step(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, int f, int r, float eps, const void* x,
+                        const void* target, const void* const* gs, const lr_pair* pairs, float* loss, void* dx,
+                        float* const* dgs, const lr_pair_grad* grads, void* ws, size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_mode(mode));
+  LR_TRY(check_mlp_dims(T, d, f, r));
+  if (nblocks < 1 || nblocks > 4096) return fail(LR_ERR_SHAPE, "nblocks = %d must be 1..4096", nblocks);
+  if (!gs || !pairs || !dgs || !grads) return fail(LR_ERR_NULL, "gs / pairs / dgs / grads is NULL");
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(target, "target"));
+  LR_TRY(check_ptr(loss, "loss"));
+  if (dx) LR_TRY(check_ptr(dx, "dx"));
+  for (int l = 0; l < nblocks; ++l) {
+    LR_TRY(check_ptr(gs[l], "gs[l]"));
+    LR_TRY(check_ptr(dgs[l], "dgs[l]"));
+    for (int k = 0; k < 3; ++k) {
+      LR_TRY(check_pair(pairs[3 * l + k], "pairs[i]"));
+      LR_TRY(check_grad(grads[3 * l + k], "grads[i]"));
+    }
+  }
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(ws_bytes, stack_ws_layout(dt, mode, nblocks, T, d, f, r, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return stack_impl(c, mode, nblocks, T, d, f, r, eps, x, target, gs, pairs, loss, dx, dgs, grads, ws);
+}
+
+lr_status lr_check_device_error(void* stream) {
+  unsigned* p = nullptr;
+  LR_TRY(device_error_word(&p));
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+  unsigned word = 0;
+  e = cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+  if (word) {
+    const unsigned zero = 0;
+    cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return fail(LR_ERR_TIMEOUT, "device error word 0x%x (1 producer, 2 mma, 4 epilogue, 8 self-test timeout)", word);
+  }
+  return LR_OK;
+}
+
+lr_status lr_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  t_last_error.clear();
+  unsigned* p = nullptr;
+  LR_TRY(device_error_word(&p));
+  if (limit_ns > 5000000000ull) return fail(LR_ERR_SHAPE, "limit_ns must be <= 5e9");
+  cudaError_t e = launch_wait_selftest(p, limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,217 @@
+#include "small_kernels.cuh"
+
+namespace lr {
+
+// ------------------------------------------------------------------ fold
+template <typename ST>
+__global__ void fold_kernel(ST* out, StackSrc src, int rows_each, int rows, int cols, const ST* g) {
+  const long long total = 1LL * rows * cols;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
+    const int r = static_cast<int>(i / cols), c = static_cast<int>(i % cols);
+    const ST* s = static_cast<const ST*>(src.src[r / rows_each]);
+    float v = static_cast<float>(s[static_cast<long long>(r % rows_each) * cols + c]);
+    if (g) v *= static_cast<float>(g[c]);
+    out[i] = static_cast<ST>(v);
+  }
+}
+
+template <typename ST>
+cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols, const ST* g, cudaStream_t st) {
+  const int rows = nsrc * rows_each;
+  const long long total = 1LL * rows * cols;
+  if (total == 0) return cudaSuccess;
+  int blocks = static_cast<int>((total + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  fold_kernel<ST><<<blocks, 256, 0, st>>>(out, src, rows_each, rows, cols, g);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ rstd
+template <typename ST>
+__global__ void rstd_kernel(const ST* x, int T, int d, float eps, float* s) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const ST* row = x + static_cast<long long>(warp) * d;
+  float ss = 0.f;
+  for (int j = lane * 8; j < d; j += 32 * 8) {
+    float v[8];
+    load8(row + j, v);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) ss = fmaf(v[t], v[t], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) s[warp] = 1.f / sqrtf(ss / static_cast<float>(d) + eps);
+}
+
+template <typename ST>
+cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + 7) / 8;
+  rstd_kernel<ST><<<blocks, 256, 0, st>>>(x, T, d, eps, s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ silu
+template <typename ST>
+__global__ void silu_kernel(const ST* u, long long ldu, ST* z, long long ldz, int T, int n) {
+  const int groups = n / 8;
+  const long long total = 1LL * T * groups;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
+    const long long t = i / groups;
+    const int c = static_cast<int>(i % groups) * 8;
+    float v[8];
+    load8(u + t * ldu + c, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = silu<ST>(v[k]);
+    store8(z + t * ldz + c, v);
+  }
+}
+
+template <typename ST>
+cudaError_t launch_silu(const ST* u, long long ldu, ST* z, long long ldz, int T, int n, cudaStream_t st) {
+  const long long total = 1LL * T * (n / 8);
+  if (total == 0) return cudaSuccess;
+  int blocks = static_cast<int>((total + 255) / 256);
+  if (blocks > 8192) blocks = 8192;
+  silu_kernel<ST><<<blocks, 256, 0, st>>>(u, ldu, z, ldz, T, n);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------- wgrad reduce
+template <typename ST>
+__global__ void wgrad_reduce_kernel(const float* part, int nsplit, long long split_stride, int M, int N,
+                                    const ST* colscale, WgradDst dst, int rows_each, float* dgpart) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const int r0 = blockIdx.y * kReduceRows;
+  const int r1 = min(M, r0 + kReduceRows);
+  const float cs = colscale ? static_cast<float>(colscale[n]) : 1.f;
+  float dga = 0.f;
+  for (int m = r0; m < r1; ++m) {
+    const long long idx = static_cast<long long>(m) * N + n;
+    float v = 0.f;
+    for (int s = 0; s < nsplit; ++s) v += part[s * split_stride + idx];
+    const int blk = m / rows_each;
+    const long long local = static_cast<long long>(m - blk * rows_each) * N + n;
+    dst.dst[blk][local] = v * cs;
+    if (dgpart) dga = fmaf(v, static_cast<float>(static_cast<const ST*>(dst.aw[blk])[local]), dga);
+  }
+  if (dgpart) dgpart[static_cast<long long>(blockIdx.y) * N + n] = dga;
+}
+
+template <typename ST>
+cudaError_t launch_wgrad_reduce(const float* part, int nsplit, long long split_stride, int M, int N,
+                                const ST* colscale, WgradDst dst, int rows_each, float* dgpart, cudaStream_t st) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  dim3 grid((N + 127) / 128, (M + kReduceRows - 1) / kReduceRows);
+  wgrad_reduce_kernel<ST><<<grid, 128, 0, st>>>(part, nsplit, split_stride, M, N, colscale, dst, rows_each, dgpart);
+  return cudaGetLastError();
+}
+
+__global__ void dg_finalize_kernel(const float* dgpart, int nparts, int N, float* dg) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  float v = 0.f;
+  for (int p = 0; p < nparts; ++p) v += dgpart[static_cast<long long>(p) * N + n];
+  dg[n] = v;
+}
+
+cudaError_t launch_dg_finalize(const float* dgpart, int nparts, int N, float* dg, cudaStream_t st) {
+  if (N == 0) return cudaSuccess;
+  dg_finalize_kernel<<<(N + 255) / 256, 256, 0, st>>>(dgpart, nparts, N, dg);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------- mse
+template <typename ST>
+__global__ void mse_kernel(const ST* y, const ST* t, long long n, ST* dy, float* partials) {
+  const float scale = 2.f / static_cast<float>(n);
+  float acc = 0.f;
+  const long long groups = n / 8;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < groups; i += 256LL * gridDim.x) {
+    float a[8], b[8], o[8];
+    load8(y + i * 8, a);
+    load8(t + i * 8, b);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float df = a[k] - b[k];
+      acc = fmaf(df, df, acc);
+      o[k] = scale * df;
+    }
+    store8(dy + i * 8, o);
+  }
+  __shared__ float red[256];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) partials[blockIdx.x] = red[0];
+}
+
+__global__ void mse_finalize_kernel(const float* partials, int nparts, long long n, float* loss) {
+  __shared__ float red[256];
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < nparts; i += 256) acc += partials[i];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = red[0] / static_cast<float>(n);
+}
+
+template <typename ST>
+cudaError_t launch_mse(const ST* y, const ST* t, long long n, ST* dy, float* partials, int nparts, float* loss,
+                       cudaStream_t st) {
+  mse_kernel<ST><<<nparts, 256, 0, st>>>(y, t, n, dy, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mse_finalize_kernel<<<1, 256, 0, st>>>(partials, nparts, n, loss);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ wait self-test
+__global__ void wait_selftest_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(1u) : "memory");
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(0u)
+        : "memory");
+    if (ok) return;  // never: nothing arrives on the barrier
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, static_cast<unsigned>(DEV_ERR_TIMEOUT_SELFTEST));
+      return;
+    }
+  }
+}
+
+cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ instantiations
+#define LR_SMALL_INST(ST)                                                                                          \
+  template cudaError_t launch_fold<ST>(ST*, StackSrc, int, int, int, const ST*, cudaStream_t);                   \
+  template cudaError_t launch_rstd<ST>(const ST*, int, int, float, float*, cudaStream_t);                        \
+  template cudaError_t launch_silu<ST>(const ST*, long long, ST*, long long, int, int, cudaStream_t);            \
+  template cudaError_t launch_wgrad_reduce<ST>(const float*, int, long long, int, int, const ST*, WgradDst, int, \
+                                               float*, cudaStream_t);                                            \
+  template cudaError_t launch_mse<ST>(const ST*, const ST*, long long, ST*, float*, int, float*, cudaStream_t);
+LR_SMALL_INST(float)
+LR_SMALL_INST(bf16)
+#undef LR_SMALL_INST
+
+}  // namespace lr

@@ -1,0 +1,405 @@
+// Persistent tcgen05 GEMM for sm_103a with fused epilogues.
+//
+//   C[M,N] = sum_k A[m,k] B[n,k]      bf16 operands, fp32 accumulator in TMEM
+//
+// Operands are staged by TMA into a ring of shared-memory stages with the
+// 128-byte swizzle; each operand is either K-major (rows contiguous in k) or
+// MN-major (rows contiguous in m / n, i.e. the transposed storage used by the
+// weight-gradient and dX = dY . W products), and the UMMA shared-memory
+// descriptors describe both natively, so no transpose kernels exist.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over output tiles):
+//   warp 0     TMA producer (one elected lane)
+//   warp 1     TMEM allocator and MMA issuer (one elected lane issues tcgen05.mma)
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused math, global stores
+// Two TMEM accumulator buffers let the epilogue of tile i overlap the
+// mainloop of tile i+1.  NACC > 1 gives each tile several accumulators fed by
+// consecutive K segments with their own operand maps (the SwiGLU dual GEMM).
+//
+// Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting role
+// sets a bit of the device error word, raises the CTA's abort flag and leaves
+// its loop; the producer then waits (bounded) for its copies still in flight,
+// the MMA warp drains its issued MMAs, and TMEM is freed before the CTA exits.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "epilogues.cuh"
+
+namespace lr {
+namespace umma {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle atom of bf16 along K
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct Maps {
+  CUtensorMap a[kMaxBatch];
+  CUtensorMap b[kMaxBatch];
+};
+
+struct Shape {
+  int M, N, K;
+  int batches, ksplit;
+  int m_tiles, n_tiles;
+  int kb_total, kb_per_split;
+  unsigned* err;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Returns false (after
+// setting `code` in the error word and the CTA abort flag) on timeout or when
+// another role of the CTA has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* err, unsigned code) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmap_prefetch(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread t of the warp receives its lane's 32 columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1 at bit 46, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, operand majors, N >> 3, M >> 4.
+template <int N_, bool A_MN, bool B_MN>
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N_ >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+template <int BN, int NACC>
+struct Config {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+  static constexpr uint32_t ACC_COLS = NACC * BN;
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS <= 32    ? 32
+                                        : 2 * ACC_COLS <= 64  ? 64
+                                        : 2 * ACC_COLS <= 128 ? 128
+                                        : 2 * ACC_COLS <= 256 ? 256
+                                                              : 512;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+  static_assert(2 * ACC_COLS <= 512, "two accumulator buffers must fit in TMEM");
+  static_assert(STAGES >= 2, "need at least two stages");
+  static_assert(BN % 64 == 0 && BN <= 256, "BN must be 64..256 in steps of 64");
+};
+
+__device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int& split, int& batch, int& mb, int& nb) {
+  const int per_batch = sh.m_tiles * sh.n_tiles;
+  const int per_split = sh.batches * per_batch;
+  split = tile / per_split;
+  int rem = tile - split * per_split;
+  batch = rem / per_batch;
+  rem -= batch * per_batch;
+  mb = rem / sh.n_tiles;
+  nb = rem - mb * sh.n_tiles;
+}
+
+template <EpiKind K, int BN, int NACC, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ Maps maps, const Shape sh, const EpiParams ep) {
+  using C = Config<BN, NACC>;
+  constexpr int STAGES = C::STAGES;
+  constexpr uint32_t IDESC = idesc_bf16<BN, A_MN, B_MN>();
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);  // one arrive per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < sh.batches || i < NACC; ++i) {
+      tmap_prefetch(&maps.a[i]);
+      tmap_prefetch(&maps.b[i]);
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = sh.ksplit * sh.batches * sh.m_tiles * sh.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int st = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int split, batch, mb, nb;
+        decode_tile(sh, tile, split, batch, mb, nb);
+        const int kb0 = split * sh.kb_per_split;
+        const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
+        const int m0 = mb * BM, n0 = nb * BN;
+        for (int s = 0; s < NACC && ok; ++s) {
+          const int set = NACC > 1 ? s : batch;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&full[st], C::STAGE_BYTES);
+            uint8_t* a_dst = sA + st * C::A_BYTES;
+            uint8_t* b_dst = sB + st * C::B_BYTES;
+            if (A_MN) {
+#pragma unroll
+              for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * 8192, &maps.a[set], &full[st], m0 + 64 * j, kb * BK);
+            } else {
+              tma_load_2d(a_dst, &maps.a[set], &full[st], kb * BK, m0);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &maps.b[set], &full[st], n0 + 64 * j, kb * BK);
+            } else {
+              tma_load_2d(b_dst, &maps.b[set], &full[st], kb * BK, n0);
+            }
+            ++issued;
+            if (++st == STAGES) {
+              st = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Wait (bounded) for the copies still in flight before the CTA may exit.
+        const long long n_back = issued < STAGES ? issued : STAGES;
+        for (long long i = 1; i <= n_back; ++i) {
+          const long long n = issued - i;
+          const int s = static_cast<int>(n % STAGES);
+          const uint32_t p = static_cast<uint32_t>((n / STAGES) & 1);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_test(&full[s], p) && global_timer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t a_base = smem_addr(sA);
+      const uint32_t b_base = smem_addr(sB);
+      int st = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        int split, batch, mb, nb;
+        decode_tile(sh, tile, split, batch, mb, nb);
+        const int kb0 = split * sh.kb_per_split;
+        const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
+        const int buf = it & 1;
+        const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
+        if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int s = 0; s < NACC && ok; ++s) {
+          const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS + s * BN;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_st = a_base + st * C::A_BYTES;
+            const uint32_t b_st = b_base + st * C::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // K-major: the 16-wide K slice sits 32 bytes further along each swizzled 128-byte row.
+              // MN-major: it is 16 rows (2 atoms of 8 rows x 128 bytes) further on.
+              const uint64_t ad = A_MN ? sdesc(a_st + kk * 2048, 8192, 1024) : sdesc(a_st + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc(b_st + kk * 2048, 8192, 1024) : sdesc(b_st + kk * 32, 16, 1024);
+              umma_f16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&empty[st]);
+            if (++st == STAGES) {
+              st = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+        if (ok) umma_commit(&tfull[buf]);
+      }
+      // Drain: all MMAs issued by this thread have completed once this barrier flips.
+      umma_commit(drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_test(drain, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      int split, batch, mb, nb;
+      decode_tile(sh, tile, split, batch, mb, nb);
+      const int buf = it & 1;
+      const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
+      if (!mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE)) break;
+      tc_fence_after();
+      const int m = mb * BM + row_in_tile;
+      const int n0 = nb * BN;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[NACC][32];
+#pragma unroll
+        for (int a = 0; a < NACC; ++a) tmem_ld32(t_row + a * BN + c * 32, v[a]);
+        tmem_ld_wait();
+        if (m < sh.M && n0 + c * 32 < sh.N) epi_apply<K, bf16, 32, NACC>(ep, batch, split, m, n0 + c * 32, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_free(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace umma
+}  // namespace lr

@@ -1,0 +1,158 @@
+"""Device-buffer plumbing around the C ABI for one MLP block, one projection
+group and one block stack.
+
+torch only allocates device memory and supplies the stream; every computation
+is a call into liblowrank.so through the ctypes binding.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional
+
+import torch
+
+from . import lowrank as L
+from .inputs import MlpShape, ProjShape
+
+_U8 = torch.uint8
+
+
+def _dt(name: str) -> int:
+    return L.LR_BF16 if name == "bf16" else L.LR_F32
+
+
+def _tdt(name: str) -> torch.dtype:
+    return torch.bfloat16 if name == "bf16" else torch.float32
+
+
+def _buf(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=_U8, device=device)
+
+
+class MlpBlock:
+    """One low-rank SwiGLU MLP block resident on the device (weights, saved set, workspaces, grads)."""
+
+    def __init__(self, shape: MlpShape, case: Dict[str, torch.Tensor], mode: int = L.LR_SAVE_CKPT,
+                 device="cuda"):
+        self.s, self.mode, self.device = shape, mode, device
+        self.dt = _dt(shape.dtype)
+        dev = {k: v.to(device) for k, v in case.items()}
+        self.t = dev
+        T, d, f, r = shape.T, shape.d, shape.f, shape.r
+        self.out = torch.empty(T, d, dtype=_tdt(shape.dtype), device=device)
+        self.dx = torch.empty_like(self.out)
+        self.saved = _buf(L.lr_mlp_saved_bytes(self.dt, mode, T, d, f, r), device)
+        self.ws_f = _buf(L.lr_mlp_fwd_workspace_bytes(self.dt, mode, T, d, f, r), device)
+        self.ws_b = _buf(L.lr_mlp_bwd_workspace_bytes(self.dt, mode, T, d, f, r), device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.dg = torch.empty(d, **f32)
+        self.grads = {}
+        for k, (ri, co) in {"gate": (r, d), "up": (r, d), "down": (r, f)}.items():
+            do = f if k != "down" else d
+            self.grads[f"dA_{k}"] = torch.empty(ri, co, **f32)
+            self.grads[f"dB_{k}"] = torch.empty(do, r, **f32)
+
+    def pairs(self):
+        t = self.t
+        return (L.pair(t["A_gate"], t["B_gate"]), L.pair(t["A_up"], t["B_up"]), L.pair(t["A_down"], t["B_down"]))
+
+    def forward(self, x: Optional[torch.Tensor] = None, stream=None):
+        s = self.s
+        x = self.t["x"] if x is None else x
+        L.lr_mlp_fwd(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, x, self.t["g"], *self.pairs(), self.out,
+                     self.saved, self.ws_f, stream)
+        return self.out
+
+    def backward(self, dout: Optional[torch.Tensor] = None, x: Optional[torch.Tensor] = None, stream=None):
+        s, gr = self.s, self.grads
+        x = self.t["x"] if x is None else x
+        dout = self.t["G"] if dout is None else dout
+        L.lr_mlp_bwd(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, x, self.t["g"], *self.pairs(), self.saved, dout,
+                     self.dx, self.dg, L.pair_grad(gr["dA_gate"], gr["dB_gate"]),
+                     L.pair_grad(gr["dA_up"], gr["dB_up"]), L.pair_grad(gr["dA_down"], gr["dB_down"]), self.ws_b,
+                     stream)
+        return self.dx
+
+    def step(self, stream=None):
+        self.forward(stream=stream)
+        self.backward(stream=stream)
+
+
+class ProjGroup:
+    """A group of low-rank pairs sharing one input, optionally behind an RMSNorm."""
+
+    def __init__(self, shape: ProjShape, case: Dict[str, object], device="cuda"):
+        self.s, self.device = shape, device
+        self.dt = _dt(shape.dtype)
+        s = shape
+        self.x = case["x"].to(device)
+        self.g = case["g"].to(device) if case["g"] is not None else None
+        self.A = [a.to(device) for a in case["A"]]
+        self.B = [b.to(device) for b in case["B"]]
+        self.G = [gg.to(device) for gg in case["G"]] if "G" in case else None
+        td = _tdt(s.dtype)
+        self.outs = [torch.empty(s.T, s.d_out, dtype=td, device=device) for _ in range(s.group)]
+        self.dx = torch.empty(s.T, s.d_in, dtype=td, device=device)
+        norm = self.g is not None
+        self.saved = _buf(L.lr_proj_saved_bytes(self.dt, s.T, s.d_in, s.d_out, s.r, s.group, norm), device)
+        self.ws_f = _buf(L.lr_proj_fwd_workspace_bytes(self.dt, s.T, s.d_in, s.d_out, s.r, s.group, norm), device)
+        self.ws_b = _buf(L.lr_proj_bwd_workspace_bytes(self.dt, s.T, s.d_in, s.d_out, s.r, s.group, norm), device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.dg = torch.empty(s.d_in, **f32) if norm else None
+        self.dA = [torch.empty(s.r, s.d_in, **f32) for _ in range(s.group)]
+        self.dB = [torch.empty(s.d_out, s.r, **f32) for _ in range(s.group)]
+
+    def pairs(self):
+        return [L.pair(a, b) for a, b in zip(self.A, self.B)]
+
+    def forward(self, stream=None):
+        s = self.s
+        L.lr_proj_fwd(self.dt, s.T, s.d_in, s.d_out, s.r, self.pairs(), self.g, s.eps, self.x, self.outs, self.saved,
+                      self.ws_f, stream)
+        return self.outs
+
+    def backward(self, stream=None):
+        s = self.s
+        L.lr_proj_bwd(self.dt, s.T, s.d_in, s.d_out, s.r, self.pairs(), self.g, s.eps, self.x, self.saved, self.G,
+                      self.dx, self.dg, [L.pair_grad(a, b) for a, b in zip(self.dA, self.dB)], self.ws_b, stream)
+        return self.dx
+
+    def step(self, stream=None):
+        self.forward(stream)
+        self.backward(stream)
+
+
+class BlockStack:
+    """A residual stack of MLP blocks trained with an MSE loss (one call per step)."""
+
+    def __init__(self, shape: MlpShape, case: Dict[str, object], mode: int = L.LR_SAVE_CKPT, device="cuda"):
+        self.s, self.mode, self.device = shape, mode, device
+        self.dt = _dt(shape.dtype)
+        s = shape
+        self.x = case["x"].to(device)
+        self.target = case["target"].to(device)
+        self.blocks: List[Dict[str, torch.Tensor]] = [{k: v.to(device) for k, v in b.items()}
+                                                      for b in case["blocks"]]
+        n = len(self.blocks)
+        self.ws = _buf(L.lr_stack_workspace_bytes(self.dt, mode, n, s.T, s.d, s.f, s.r), device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.loss = torch.zeros(1, **f32)
+        self.dx = torch.empty(s.T, s.d, dtype=_tdt(s.dtype), device=device)
+        self.dgs = [torch.empty(s.d, **f32) for _ in range(n)]
+        self.grads = []
+        for _ in range(n):
+            gr = {}
+            for k, (ri, co, do) in {"gate": (s.r, s.d, s.f), "up": (s.r, s.d, s.f), "down": (s.r, s.f, s.d)}.items():
+                gr[f"dA_{k}"] = torch.empty(ri, co, **f32)
+                gr[f"dB_{k}"] = torch.empty(do, s.r, **f32)
+            self.grads.append(gr)
+
+    def step(self, stream=None):
+        s = self.s
+        pairs, grads = [], []
+        for b, gr in zip(self.blocks, self.grads):
+            for k in ("gate", "up", "down"):
+                pairs.append(L.pair(b[f"A_{k}"], b[f"B_{k}"]))
+                grads.append(L.pair_grad(gr[f"dA_{k}"], gr[f"dB_{k}"]))
+        L.lr_stack_step(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, self.x, self.target,
+                        [b["g"] for b in self.blocks], pairs, self.loss, self.dx, self.dgs, grads, self.ws, stream)
+        return self.loss

@@ -1,0 +1,94 @@
+"""The C ABI without a GPU: the library builds, loads and exports every symbol
+include/lowrank.h declares; size queries and argument validation need no device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lowrank.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from rank_bottleneck_block_gb300 import build
+
+    build.build()
+    from rank_bottleneck_block_gb300 import lowrank
+
+    lowrank.lib()
+    return lowrank
+
+
+def declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lr_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared()
+    assert len(names) >= 15
+    lib = L.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(L.EXPORTED) == names
+
+
+def test_size_queries(L):
+    T, d, f, r = 16384, 2048, 5632, 512
+    ck = L.lr_mlp_saved_bytes(L.LR_BF16, L.LR_SAVE_CKPT, T, d, f, r)
+    full = L.lr_mlp_saved_bytes(L.LR_BF16, L.LR_SAVE_FULL, T, d, f, r)
+    # checkpoint keeps u (3r columns, bf16) and s (fp32) per token
+    assert ck == pytest.approx(T * (3 * r * 2 + 4), rel=1e-3)
+    assert full > 5 * ck
+    assert L.lr_mlp_saved_bytes(L.LR_BF16, L.LR_SAVE_CKPT, T, 2047, f, r) == 0  # d not a multiple of 8
+    assert L.lr_mlp_saved_bytes(7, 0, T, d, f, r) == 0
+    assert L.lr_stack_workspace_bytes(L.LR_BF16, 1, 24, T, d, f, r) < \
+        L.lr_stack_workspace_bytes(L.LR_BF16, 0, 24, T, d, f, r) / 3
+    assert L.lr_proj_saved_bytes(L.LR_BF16, T, 4096, 4096, 1024, 3, 1) > 0
+    assert L.lr_proj_saved_bytes(L.LR_BF16, T, 4096, 4096, 1024, 4, 1) == 0  # group > 3
+
+
+def _call_mlp_fwd(L, **over):
+    p = 0x10000  # a 16-byte aligned fake address: validation must fail before any launch
+    args = dict(dt=L.LR_BF16, mode=1, T=64, d=64, f=128, r=16, x=p, g=p, out=p, saved=p, saved_bytes=1 << 30,
+                ws=p, ws_bytes=1 << 30)
+    args.update(over)
+    pr = L.lr_pair(args.pop("A", p), p)
+    lib = L.lib()
+    return lib.lr_mlp_fwd(args["dt"], args["mode"], args["T"], args["d"], args["f"], args["r"], 1e-6, args["x"],
+                          args["g"], pr, L.lr_pair(p, p), L.lr_pair(p, p), args["out"], args["saved"],
+                          args["saved_bytes"], args["ws"], args["ws_bytes"], None)
+
+
+def test_validation_codes(L):
+    assert _call_mlp_fwd(L, x=None) == 1
+    assert _call_mlp_fwd(L, A=None) == 1
+    assert _call_mlp_fwd(L, d=60) == 2
+    assert _call_mlp_fwd(L, T=0) == 2
+    assert _call_mlp_fwd(L, x=0x10004) == 3
+    assert _call_mlp_fwd(L, dt=5) == 4
+    assert _call_mlp_fwd(L, mode=9) == 4
+    assert _call_mlp_fwd(L, ws_bytes=16) == 5
+    assert "ws" in L.lr_last_error()
+    assert _call_mlp_fwd(L, saved_bytes=16) == 5
+
+
+def test_no_device_is_reported_not_faulted(L):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert _call_mlp_fwd(L) == 8  # LR_ERR_UNSUPPORTED: validated arguments, but no device
+    assert L.lib().lr_version() == 100
+
+
+def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
+    from rank_bottleneck_block_gb300 import lowrank
+
+    monkeypatch.setattr(lowrank, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(lowrank, "_lib", None)
+    with pytest.raises(RuntimeError):
+        lowrank.lib()

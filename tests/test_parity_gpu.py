@@ -1,0 +1,276 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Metric: per tensor, max_i |gpu_i - ref_i| / max_i |ref_i| (max-relative error),
+bound 2e-2 for bf16 storage and 1e-5 for fp32.  Inputs are the seeded host
+arrays of rank_bottleneck_block_gb300.inputs; the oracle reads them widened to
+fp64, the GPU reads them as stored.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.lowrank_oracle as O
+from rank_bottleneck_block_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f32": 1e-5}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from rank_bottleneck_block_gb300 import build
+
+    build.build()
+    from rank_bottleneck_block_gb300 import lowrank as L
+
+    L.lib()
+    yield
+
+
+def maxrel(gpu, ref):
+    g = gpu.detach().float().cpu().double().numpy() if hasattr(gpu, "detach") else np.asarray(gpu)
+    ref = np.asarray(ref)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.all(np.isfinite(g))
+    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-300))
+
+
+def _sync_check():
+    from rank_bottleneck_block_gb300 import lowrank as L
+
+    torch.cuda.synchronize()
+    L.lr_check_device_error()
+
+
+def run_mlp(shape, mode, seed=0):
+    from rank_bottleneck_block_gb300.runner import MlpBlock
+
+    case = I.make_mlp_case(shape, seed)
+    blk = MlpBlock(shape, case, mode)
+    blk.forward()
+    blk.backward()
+    _sync_check()
+    return case, blk
+
+
+def check_mlp(shape, mode, seed=0):
+    case, blk = run_mlp(shape, mode, seed)
+    ref_out, saved = O.mlp_block_fwd(case["x"], case["g"], case, shape.eps, O.FULL)
+    gr = O.mlp_block_bwd(case["g"], case, saved, case["G"], shape.eps)
+    tol = TOL[shape.dtype]
+    errs = {"out": maxrel(blk.out, ref_out), "dx": maxrel(blk.dx, gr["dx"]), "dg": maxrel(blk.dg, gr["dg"])}
+    for k in ("gate", "up", "down"):
+        errs[f"dA_{k}"] = maxrel(blk.grads[f"dA_{k}"], gr[f"dA_{k}"])
+        errs[f"dB_{k}"] = maxrel(blk.grads[f"dB_{k}"], gr[f"dB_{k}"])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{shape} mode={mode}: {errs}"
+    return errs, blk
+
+
+# ------------------------------------------------------------- MLP block
+MODES = [0, 1]  # LR_SAVE_FULL, LR_SAVE_CKPT
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_mlp_tiny_f32(mode):
+    """The tiny fp32 block: T 2x64, d 256, f 688, r 64; every tensor within 1e-5."""
+    check_mlp(I.MLP_TINY_F32, mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_mlp_f32_ragged(mode):
+    check_mlp(I.MlpShape(T=77, d=72, f=200, r=24, dtype="f32"), mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("dims", [(200, 136, 328, 40), (1, 64, 64, 8), (129, 64, 128, 64), (300, 520, 264, 72)])
+def test_mlp_bf16_ragged(mode, dims):
+    """Several tiles plus ragged tails in every GEMM dimension (T, d, f, r not multiples of the tiles)."""
+    T, d, f, r = dims
+    check_mlp(I.MlpShape(T=T, d=d, f=f, r=r, dtype="bf16"), mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_mlp_bf16_medium(mode):
+    """Many tiles per GEMM and split-K weight gradients (K = T spans several splits)."""
+    check_mlp(I.MlpShape(T=2112, d=512, f=1376, r=128, dtype="bf16"), mode, seed=3)
+
+
+def test_mlp_checkpoint_bitwise_equals_full():
+    """Low-rank activation checkpointing: the re-forward reproduces the forward bit for bit,
+    so every gradient equals the no-checkpoint run exactly."""
+    shape = I.MlpShape(T=1040, d=256, f=688, r=64, dtype="bf16")
+    _, full = run_mlp(shape, 0, seed=5)
+    _, ck = run_mlp(shape, 1, seed=5)
+    assert torch.equal(full.out, ck.out)
+    assert torch.equal(full.dx, ck.dx)
+    assert torch.equal(full.dg, ck.dg)
+    for k in full.grads:
+        assert torch.equal(full.grads[k], ck.grads[k]), k
+
+
+def test_mlp_deterministic():
+    shape = I.MlpShape(T=700, d=256, f=512, r=64, dtype="bf16")
+    _, a = run_mlp(shape, 1, seed=6)
+    dx, grads = a.dx.clone(), {k: v.clone() for k, v in a.grads.items()}
+    a.forward()
+    a.backward()
+    _sync_check()
+    assert torch.equal(dx, a.dx)
+    for k in grads:
+        assert torch.equal(grads[k], a.grads[k]), k
+
+
+@pytest.mark.slow
+def test_mlp_block_full_size():
+    """The single-block workload at full size (T 16384, d 2048, f 5632, r 512, bf16) in the
+    checkpointing mode the benchmark times; the oracle computes every tensor in fp64."""
+    check_mlp(I.MLP_BLOCK_BF16, 1)
+
+
+# -------------------------------------------------------- projection group
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("group", [1, 2, 3])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_proj_group(norm, group, dtype):
+    shape = I.ProjShape(T=260, d_in=200, d_out=136, r=48, group=group, norm=norm, dtype=dtype)
+    _check_proj(shape, seed=group)
+
+
+def _check_proj(shape, seed=0):
+    from rank_bottleneck_block_gb300.runner import ProjGroup
+
+    case = I.make_proj_case(shape, seed)
+    pg = ProjGroup(shape, case)
+    pg.forward()
+    pg.backward()
+    _sync_check()
+    outs, saved = O.proj_group_fwd(case["x"], case["g"], case["A"], case["B"], shape.eps)
+    gr = O.proj_group_bwd(case["g"], case["A"], case["B"], saved, case["G"])
+    tol = TOL[shape.dtype]
+    errs = {"dx": maxrel(pg.dx, gr["dx"])}
+    if shape.norm:
+        errs["dg"] = maxrel(pg.dg, gr["dg"])
+    for i in range(shape.group):
+        errs[f"out{i}"] = maxrel(pg.outs[i], outs[i])
+        errs[f"dA{i}"] = maxrel(pg.dA[i], gr["dA"][i])
+        errs[f"dB{i}"] = maxrel(pg.dB[i], gr["dB"][i])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{shape}: {errs}"
+
+
+@pytest.mark.slow
+def test_attention_projections_full_size():
+    """q/k/v group (3 x r 1024, d 4096, RMSNorm) and the o-projection, T 16384, bf16."""
+    _check_proj(I.ATTN_PROJ_BF16, seed=0)
+    _check_proj(I.ATTN_OPROJ_BF16, seed=1)
+
+
+@pytest.mark.parametrize("idx", [0, 17, 50, 100, 143])
+def test_sweep_shapes_reduced_tokens(idx):
+    """Sweep shapes (d, r, group) at T = 640: the GEMM shapes of the grid with few tokens."""
+    s = I.sweep_shapes()[idx]
+    shape = I.ProjShape(T=640, d_in=s.d_in, d_out=s.d_out, r=s.r, group=s.group, norm=False)
+    _check_proj(shape, seed=idx)
+
+
+# ------------------------------------------------------------------ stack
+def _oracle_stack_rows(case, rows, T, eps):
+    """Forward and backward of the stack on a subset of rows (every op is row-local), with
+    the MSE gradient normalised by the full T * d."""
+    x = O.to64(case["x"])[rows]
+    t = O.to64(case["target"])[rows]
+    saves = []
+    h = x
+    for blk in case["blocks"]:
+        h, sv = O.mlp_block_fwd(h, blk["g"], blk, eps, O.FULL)
+        saves.append(sv)
+    dy = 2.0 * (h - t) / (T * h.shape[1])
+    for l in range(len(case["blocks"]) - 1, -1, -1):
+        dy = O.mlp_block_bwd(case["blocks"][l]["g"], case["blocks"][l], saves[l], dy, eps)["dx"]
+    return dy
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_stack_small(mode, dtype):
+    from rank_bottleneck_block_gb300.runner import BlockStack
+
+    shape = I.MlpShape(T=264, d=128, f=344, r=32, dtype=dtype)
+    case = I.make_stack_case(shape, blocks=3, seed=2)
+    st = BlockStack(shape, case, mode)
+    st.step()
+    _sync_check()
+    loss, grads, dx = O.stack_step(case["x"], case["target"], case["blocks"], shape.eps, O.FULL)
+    tol = TOL[dtype]
+    assert abs(st.loss.item() - loss) / abs(loss) <= tol
+    assert maxrel(st.dx, dx) <= tol
+    for l in range(3):
+        assert maxrel(st.dgs[l], grads[l]["dg"]) <= tol
+        for k in ("gate", "up", "down"):
+            assert maxrel(st.grads[l][f"dA_{k}"], grads[l][f"dA_{k}"]) <= tol, (l, k)
+            assert maxrel(st.grads[l][f"dB_{k}"], grads[l][f"dB_{k}"]) <= tol, (l, k)
+
+
+def test_stack_checkpoint_bitwise():
+    from rank_bottleneck_block_gb300.runner import BlockStack
+
+    shape = I.MlpShape(T=520, d=256, f=688, r=64, dtype="bf16")
+    case = I.make_stack_case(shape, blocks=4, seed=4)
+    a = BlockStack(shape, case, 0)
+    a.step()
+    b = BlockStack(shape, case, 1)
+    b.step()
+    _sync_check()
+    assert torch.equal(a.loss, b.loss)
+    assert torch.equal(a.dx, b.dx)
+    for l in range(4):
+        assert torch.equal(a.dgs[l], b.dgs[l])
+        for k in a.grads[l]:
+            assert torch.equal(a.grads[l][k], b.grads[l][k]), (l, k)
+
+
+@pytest.mark.slow
+def test_stack_full_size_sampled_rows():
+    """24 blocks at the single-block shape, checkpointed: dx on sampled rows vs the oracle
+    run on those rows alone, and the checkpoint saving against the no-checkpoint workspace."""
+    from rank_bottleneck_block_gb300 import lowrank as L
+    from rank_bottleneck_block_gb300.runner import BlockStack
+
+    shape = I.MLP_BLOCK_BF16
+    case = I.make_stack_case(shape, blocks=24, seed=0)
+    st = BlockStack(shape, case, 1)
+    st.step()
+    _sync_check()
+    rows = I.sample_rows(shape.T, 24).numpy()
+    ref = _oracle_stack_rows(case, rows, shape.T, shape.eps)
+    assert maxrel(st.dx[torch.from_numpy(rows).cuda()], ref) <= TOL["bf16"]
+    assert np.isfinite(st.loss.item())
+    full = L.lr_stack_workspace_bytes(L.LR_BF16, 0, 24, shape.T, shape.d, shape.f, shape.r)
+    ckpt = L.lr_stack_workspace_bytes(L.LR_BF16, 1, 24, shape.T, shape.d, shape.f, shape.r)
+    assert ckpt < full / 3
+
+
+# ------------------------------------------------------- errors / timeouts
+def test_bounded_wait_reports_timeout_and_context_survives():
+    from rank_bottleneck_block_gb300 import lowrank as L
+
+    L.lr_selftest_wait_timeout(20_000_000)  # 20 ms on a barrier nothing completes
+    with pytest.raises(L.LowRankError) as ei:
+        L.lr_check_device_error()
+    assert ei.value.status == 7
+    L.lr_check_device_error()  # the word was cleared
+    check_mlp(I.MlpShape(T=64, d=64, f=128, r=16, dtype="bf16"), 1)  # context still usable
+
+
+def test_workspace_too_small_is_rejected_before_launch():
+    from rank_bottleneck_block_gb300 import lowrank as L
+    from rank_bottleneck_block_gb300.runner import MlpBlock
+
+    shape = I.MlpShape(T=64, d=64, f=128, r=16, dtype="bf16")
+    blk = MlpBlock(shape, I.make_mlp_case(shape), 1)
+    blk.ws_f = blk.ws_f[:128]
+    with pytest.raises(L.LowRankError) as ei:
+        blk.forward()
+    assert ei.value.status == 5
