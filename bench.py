@@ -1,0 +1,351 @@
+"""Benchmark of the low-rank bottleneck sublayer on GB300.
+
+One step = forward + backward of one low-rank SwiGLU MLP block (T 16384 tokens,
+d 2048, f 5632, r 512, bf16 storage, fp32 accumulation) with low-rank activation
+checkpointing: online-RMSNorm grouped gate/up GEMM, SwiGLU dual GEMM, down pair
+with residual, and the whole backward including the re-forward of the [T, f]
+tensors from the saved [T, r] pre-activations.  Inputs are resident in HBM; L2
+is flushed (a 512 MB write) before every timed step, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--mode ckpt|full] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica on its own GPU (the path needs no exchange between GPUs): value is the
+tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "low-rank block fwd+bwd tokens/s on 1 GB300; % of per-shape roofline"
+NOMINAL = {"tflops": 2250.0, "hbm_gbs": 8000.0}
+FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d["bf16_tflops_sustained"],
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return dict(FALLBACK, source="fallback")
+
+
+# ----------------------------------------------------------------- workload
+def workload(mode: str):
+    from rank_bottleneck_block_gb300 import inputs as I
+
+    s = I.MLP_BLOCK_BF16
+    T, d, f, r = s.T, s.d, s.f, s.r
+    fwd = 2.0 * T * (2 * r * d + 2 * f * r + r * f + d * r)  # K1 (gate;up), K2 (dual), A_down, B_down
+    flops = 3.0 * fwd + (4.0 * T * r * f if mode == "ckpt" else 0.0)
+    params = 2 * r * d + 2 * f * r + r * f + d * r
+    act = 2.0 * T * d * 4  # read x and dout, write out and dx
+    saved = (3 * r * 2 + 4) * T * 2.0 if mode == "ckpt" else (3 * r * 2 * 2 + 3 * f * 2 + 4) * T * 2.0
+    nbytes = act + 2.0 * params + 4.0 * params + 2.0 * d + 4.0 * d + saved
+    cfg = {"workload": f"low-rank SwiGLU MLP block fwd+bwd, T={T} d={d} f={f} r={r}, "
+                       f"{'low-rank activation checkpointing' if mode == 'ckpt' else 'no checkpointing'}",
+           "tokens": T, "d": d, "f": f, "r": r, "mode": mode, "seed": 0,
+           "l2": "flushed before every timed step (512 MB write, outside the timed events)"}
+    return s, cfg, flops, nbytes
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_uuid=None):
+        self.p = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if dev_uuid:
+            cmd += ["-i", dev_uuid]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, smax, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ CPU baseline
+def oracle_tokens_per_s(shape, rows: int, min_seconds: float, mode: str):
+    """The fp64 oracle's fwd+bwd of the block on `rows` tokens of the workload (same d, f, r), repeated
+    until at least min_seconds; returns (tokens/s, reps, seconds)."""
+    import oracle.lowrank_oracle as O
+    from rank_bottleneck_block_gb300 import inputs as I
+
+    sub = I.MlpShape(T=rows, d=shape.d, f=shape.f, r=shape.r, dtype=shape.dtype)
+    case = I.make_mlp_case(sub, seed=0)
+    om = O.CKPT if mode == "ckpt" else O.FULL
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _, saved = O.mlp_block_fwd(case["x"], case["g"], case, sub.eps, om)
+        O.mlp_block_bwd(case["g"], case, saved, case["G"], sub.eps)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            return rows * reps / el, reps, el
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=ws)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, ws: int, seconds_max: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * ws / seconds_max
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(a, ws, rank, local):
+    import torch
+
+    from rank_bottleneck_block_gb300 import build as B
+
+    if rank == 0 or ws == 1:
+        B.build()
+    barrier(ws)
+    from rank_bottleneck_block_gb300 import inputs as I
+    from rank_bottleneck_block_gb300 import lowrank as L
+    from rank_bottleneck_block_gb300.runner import MlpBlock
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shape, cfg, flops, nbytes = workload(a.mode)
+    mode = L.LR_SAVE_CKPT if a.mode == "ckpt" else L.LR_SAVE_FULL
+    case = I.make_mlp_case(shape, seed=0)
+    blk = MlpBlock(shape, case, mode, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    for _ in range(a.warmup):
+        blk.step()
+    torch.cuda.synchronize()
+    L.lr_check_device_error()
+
+    # ------------------------------------------------ device-resident timing
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clk = ClockSampler(uuid)
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    n0 = L.lr_launch_count()
+    L.lr_profile_start()
+    for i in range(a.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        blk.step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    prof = L.lr_profile_stop()
+    launches = L.lr_launch_count() - n0
+    clocks = clk.stop()
+    L.lr_check_device_error()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    total_s = sum(step_ms) / 1e3
+    total_s_max = max_over_ranks(total_s, ws)
+    ms_per_step = total_s_max * 1e3 / a.steps
+    value = aggregate(shape.T * a.steps, ws, total_s_max)
+
+    # ------------------------------------------------ end to end (host buffers)
+    xh = case["x"].pin_memory()
+    gh = case["G"].pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(xh).pin_memory()
+    xd, gd = blk.t["x"], blk.t["G"]
+    e2e_steps = max(3, min(a.steps, 50))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        gd.copy_(gh, non_blocking=True)
+        blk.forward(xd)
+        blk.backward(gd, xd)
+        outh.copy_(blk.out, non_blocking=True)
+        dxh.copy_(blk.dx, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, ws)
+    h2d = xh.numel() * xh.element_size() + gh.numel() * gh.element_size()
+    d2h = outh.numel() * outh.element_size() + dxh.numel() * dxh.element_size()
+    e2e = {"value": aggregate(shape.T * e2e_steps, ws, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h,
+           "api": "lr_mlp_fwd + lr_mlp_bwd with x and dout copied in from pinned host memory and out, dx "
+                  "copied back, every step"}
+
+    # ------------------------------------------------ rooflines
+    pk = peaks()
+    gemms = {k: v for k, v in prof.items() if v["flops"] > 0}
+    dom_name, dom = max(gemms.items(), key=lambda kv: kv[1]["ms"])
+    achieved_tf = dom["flops"] / (dom["ms"] / 1e3) / 1e12
+    roofline = {"kernel": dom_name, "bound": "tensor", "achieved": round(achieved_tf, 1),
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved_tf / pk["bf16_tflops_sustained"], 4),
+                "peak_kind": f"bf16 dense, sustained ({pk['source']})",
+                "launches": dom["launches"], "avg_launch_us": round(1e3 * dom["ms"] / dom["launches"], 2),
+                "flops_per_launch": dom["flops"] / dom["launches"],
+                "share_of_step": round(dom["ms"] / sum(v["ms"] for v in prof.values()), 4),
+                "traffic": None}
+    ms_step_s = ms_per_step / 1e3
+    t_nom = max(flops / (NOMINAL["tflops"] * 1e12), nbytes / (NOMINAL["hbm_gbs"] * 1e9))
+    t_meas = max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+    block = {"flops_per_step": flops, "bytes_per_step": nbytes, "tflops": round(flops / ms_step_s / 1e12, 1),
+             "roofline_ms_nominal": round(t_nom * 1e3, 4), "roofline_ms_measured": round(t_meas * 1e3, 4),
+             "frac_nominal": round(t_nom / ms_step_s, 4), "frac_measured": round(t_meas / ms_step_s, 4)}
+    kernels = {k: {"launches": v["launches"], "ms_per_step": round(v["ms"] / a.steps, 4),
+                   "share": round(v["ms"] / sum(w["ms"] for w in prof.values()), 4),
+                   **({"tflops": round(v["flops"] / (v["ms"] / 1e3) / 1e12, 1)} if v["flops"] else
+                      {"gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1)})}
+               for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"])}
+
+    res = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": a.steps,
+           "warmup": a.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) "
+                                                           "weights, g=1+N(0,0.1))",
+           "config": dict(cfg, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
+           "roofline": roofline, "block_roofline": block, "e2e": e2e, "gpu_launches": int(launches),
+           "clocks": clocks, "kernels": kernels}
+    if ws == 1 and not a.no_cpu_baseline:
+        tps, reps, el = oracle_tokens_per_s(shape, a.cpu_rows, a.cpu_seconds, a.mode)
+        res["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                               "sample": f"fp64 numpy oracle fwd+bwd of the same block on {a.cpu_rows} of the "
+                                         f"{shape.T} tokens, {reps} repetition(s) in {el:.1f} s; numpy BLAS "
+                                         f"default threading"}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+# --------------------------------------------------------- reference arm
+def run_reference(a, ws, rank):
+    if rank != 0:
+        return
+    shape, cfg, _, _ = workload(a.mode)
+    budget = 90.0
+    # calibrate the oracle's per-token cost, then size each step's sample so the run stays bounded
+    tps, _, _ = oracle_tokens_per_s(shape, 64, 0.0, a.mode)
+    rows = int(budget / max(1, a.steps + a.warmup) * tps) // 8 * 8
+    rows = max(8, min(rows, 4096))
+    for _ in range(a.warmup):
+        oracle_tokens_per_s(shape, rows, 0.0, a.mode)
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        oracle_tokens_per_s(shape, rows, 0.0, a.mode)
+    el = time.perf_counter() - t0
+    value = rows * a.steps / el
+    sample = (f"fp64 numpy oracle fwd+bwd of the block on {rows} of the {shape.T} tokens per step "
+              f"(same d, f, r, seed); numpy BLAS default threading")
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(el * 1e3 / a.steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": dict(cfg, parallelism="host cores"),
+           "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--mode", choices=["ckpt", "full"], default="ckpt")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    if a.impl == "reference":
+        run_reference(a, ws, rank)
+    else:
+        run_ours(a, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -171,6 +171,23 @@ const char* lr_last_error(void);
 lr_status lr_check_device_error(void* stream);
 lr_status lr_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 
+/* ------------------------------------------------------------- profiling
+ * Instrumentation (no counterpart on the pages; it serves the measurement of
+ * the path against its roofline).
+ * lr_launch_count: kernels this library has launched in the process so far.
+ * lr_profile_start: from now on bracket every launch by two CUDA events on its
+ *   stream (clears earlier records).  lr_profile_stop: stop, synchronise the
+ *   recorded events and aggregate them per kernel name.  Then entries
+ *   0 .. lr_profile_count()-1 give each kernel's name, launches, total device
+ *   milliseconds, and algorithmic FLOPs (GEMMs: 2 M N K per accumulator and
+ *   batch entry) or bytes (memory-bound kernels) summed over its launches. */
+unsigned long long lr_launch_count(void);
+lr_status lr_profile_start(void);
+lr_status lr_profile_stop(void);
+int lr_profile_count(void);
+lr_status lr_profile_entry(int i, char* name, size_t name_len, long long* launches, double* total_ms,
+                           double* flops, double* bytes);
+
 /* Library version (major * 10000 + minor * 100 + patch). */
 int lr_version(void);
 

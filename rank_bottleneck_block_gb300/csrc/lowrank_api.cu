@@ -7,8 +7,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/lowrank.h"
 #include "common.cuh"
@@ -91,6 +93,64 @@ int device_sm_count() {
   return s_sms[dev];
 }
 
+// ------------------------------------------------------------- profiling
+// Every launch of the library increments a counter.  While profiling is on,
+// each launch is also bracketed by two CUDA events recorded on its stream,
+// tagged with the kernel's name and its algorithmic FLOPs / bytes; stopping
+// synchronises the events and aggregates per name.
+static std::atomic<unsigned long long> s_launches{0};
+
+struct ProfRec {
+  std::string name;
+  cudaEvent_t a, b;
+  double flops, bytes;
+};
+struct ProfAgg {
+  std::string name;
+  long long n;
+  double ms, flops, bytes;
+};
+static std::mutex s_prof_mu;
+static bool s_prof_on = false;
+static std::vector<ProfRec> s_prof;
+static std::vector<cudaEvent_t> s_event_pool;
+static std::vector<ProfAgg> s_prof_result;
+
+static cudaEvent_t pool_event() {
+  if (!s_event_pool.empty()) {
+    cudaEvent_t e = s_event_pool.back();
+    s_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct LaunchScope {
+  bool on;
+  ProfRec rec;
+  cudaStream_t st;
+  LaunchScope(const std::string& name, cudaStream_t s, double flops, double bytes) : on(false), st(s) {
+    s_launches.fetch_add(1, std::memory_order_relaxed);
+    std::lock_guard<std::mutex> lk(s_prof_mu);
+    if (!s_prof_on) return;
+    on = true;
+    rec.name = name;
+    rec.flops = flops;
+    rec.bytes = bytes;
+    rec.a = pool_event();
+    rec.b = pool_event();
+    cudaEventRecord(rec.a, st);
+  }
+  ~LaunchScope() {
+    if (!on) return;
+    cudaEventRecord(rec.b, st);
+    std::lock_guard<std::mutex> lk(s_prof_mu);
+    s_prof.push_back(rec);
+  }
+};
+
 // ----------------------------------------------------------- GEMM dispatch
 struct Ctx {
   lr_dtype dt;
@@ -118,7 +178,7 @@ static cudaError_t umma_bn(const GemmCall& g, cudaStream_t st) {
 }
 
 static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sms) {
-  g.bn = (k == EPI_SWIGLU) ? 128 : pick_bn(g, sms);
+  (void)sms;
   const bool kk = !g.a_mn && !g.b_mn, km = !g.a_mn && g.b_mn, mm = g.a_mn && g.b_mn;
   switch (k) {
     case EPI_NORM_SILU: if (kk) return umma_bn<EPI_NORM_SILU, 1, false, false>(g, st); break;
@@ -161,13 +221,18 @@ static const char* epi_name(EpiKind k) {
   return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
 }
 
-static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g) {
+static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes = 0) {
   g.err = c.err;
   if (g.nacc < 1) g.nacc = 1;
   if (g.batches < 1) g.batches = 1;
   if (g.ksplit < 1) g.ksplit = 1;
   g.ep.M = g.M;
   g.ep.N = g.N;
+  g.bn = (c.dt == LR_BF16) ? ((k == EPI_SWIGLU) ? 128 : pick_bn(g, c.sms)) : 0;
+  std::string name = std::string(c.dt == LR_BF16 ? "umma_" : "simt_") + epi_name(k);
+  if (g.bn) name += "_bn" + std::to_string(g.bn);
+  const double flops = 2.0 * g.M * g.N * static_cast<double>(g.K) * g.nacc * g.batches;
+  LaunchScope scope(name, c.st, flops, extra_bytes);
   cudaError_t e = (c.dt == LR_BF16) ? dispatch_bf16(k, g, c.st, c.sms) : dispatch_f32(k, g, c.st);
   if (e != cudaSuccess)
     return fail(LR_ERR_CUDA, "GEMM %s (M=%d N=%d K=%d) launch failed: %s", epi_name(k), g.M, g.N, g.K,
@@ -229,6 +294,7 @@ static lr_status wgrad(const Ctx& c, int M, int N, int K, Operand A, Operand B, 
   g.ep.ldo0 = N;
   g.ep.split_stride = 1LL * M * N;
   LR_TRY(gemm(c, EPI_F32, g));
+  LaunchScope scope("wgrad_reduce", c.st, 0, 4.0 * g.ksplit * M * N + 4.0 * M * N);
   cudaError_t e = (c.dt == LR_BF16)
                       ? launch_wgrad_reduce<bf16>(wpart, g.ksplit, 1LL * M * N, M, N,
                                                   static_cast<const bf16*>(colscale), dst, rows_each, dgpart, c.st)
@@ -240,6 +306,7 @@ static lr_status wgrad(const Ctx& c, int M, int N, int K, Operand A, Operand B, 
 
 // ------------------------------------------------------------ small ops
 static lr_status fold(const Ctx& c, void* out, StackSrc src, int nsrc, int rows_each, int cols, const void* g) {
+  LaunchScope scope("fold", c.st, 0, 2.0 * c.es * nsrc * rows_each * cols);
   cudaError_t e = (c.dt == LR_BF16) ? launch_fold<bf16>(static_cast<bf16*>(out), src, nsrc, rows_each, cols,
                                                         static_cast<const bf16*>(g), c.st)
                                     : launch_fold<float>(static_cast<float*>(out), src, nsrc, rows_each, cols,
@@ -249,6 +316,7 @@ static lr_status fold(const Ctx& c, void* out, StackSrc src, int nsrc, int rows_
 }
 
 static lr_status rstd(const Ctx& c, const void* x, int T, int d, float eps, float* s) {
+  LaunchScope scope("rstd", c.st, 0, static_cast<double>(c.es) * T * d + 4.0 * T);
   cudaError_t e = (c.dt == LR_BF16) ? launch_rstd<bf16>(static_cast<const bf16*>(x), T, d, eps, s, c.st)
                                     : launch_rstd<float>(static_cast<const float*>(x), T, d, eps, s, c.st);
   if (e != cudaSuccess) return fail(LR_ERR_CUDA, "rstd: %s", cudaGetErrorString(e));
@@ -256,6 +324,7 @@ static lr_status rstd(const Ctx& c, const void* x, int T, int d, float eps, floa
 }
 
 static lr_status silu_slab(const Ctx& c, const void* u, long long ldu, void* z, long long ldz, int T, int n) {
+  LaunchScope scope("silu", c.st, 0, 2.0 * c.es * T * n);
   cudaError_t e = (c.dt == LR_BF16)
                       ? launch_silu<bf16>(static_cast<const bf16*>(u), ldu, static_cast<bf16*>(z), ldz, T, n, c.st)
                       : launch_silu<float>(static_cast<const float*>(u), ldu, static_cast<float*>(z), ldz, T, n, c.st);
@@ -264,6 +333,7 @@ static lr_status silu_slab(const Ctx& c, const void* u, long long ldu, void* z, 
 }
 
 static lr_status dg_finalize(const Ctx& c, const float* dgpart, int nparts, int N, float* dg) {
+  LaunchScope scope("dg_finalize", c.st, 0, 4.0 * nparts * N + 4.0 * N);
   cudaError_t e = launch_dg_finalize(dgpart, nparts, N, dg, c.st);
   if (e != cudaSuccess) return fail(LR_ERR_CUDA, "dg: %s", cudaGetErrorString(e));
   return LR_OK;
@@ -738,6 +808,7 @@ static lr_status stack_impl(const Ctx& c, lr_mode mode, int L, int T, int d, int
                         act(l + 1), sv(l), W.scratch));
   {
     const long long n = 1LL * T * d;
+    LaunchScope scope("mse", c.st, 0, 3.0 * c.es * n);
     cudaError_t e = (c.dt == LR_BF16)
                         ? launch_mse<bf16>(static_cast<const bf16*>(act(L)), static_cast<const bf16*>(target), n,
                                            static_cast<bf16*>(W.dy0), W.mse_part, kMseParts, loss, c.st)
@@ -822,6 +893,64 @@ using namespace lr;
 extern "C" {
 
 int lr_version(void) { return 100; }
+
+unsigned long long lr_launch_count(void) { return s_launches.load(); }
+
+lr_status lr_profile_start(void) {
+  std::lock_guard<std::mutex> lk(s_prof_mu);
+  for (auto& r : s_prof) {
+    s_event_pool.push_back(r.a);
+    s_event_pool.push_back(r.b);
+  }
+  s_prof.clear();
+  s_prof_result.clear();
+  s_prof_on = true;
+  return LR_OK;
+}
+
+lr_status lr_profile_stop(void) {
+  std::lock_guard<std::mutex> lk(s_prof_mu);
+  s_prof_on = false;
+  s_prof_result.clear();
+  for (auto& r : s_prof) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "profile event: %s", cudaGetErrorString(e));
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    auto it = std::find_if(s_prof_result.begin(), s_prof_result.end(),
+                           [&](const ProfAgg& a) { return a.name == r.name; });
+    if (it == s_prof_result.end()) {
+      s_prof_result.push_back({r.name, 0, 0.0, 0.0, 0.0});
+      it = s_prof_result.end() - 1;
+    }
+    it->n += 1;
+    it->ms += ms;
+    it->flops += r.flops;
+    it->bytes += r.bytes;
+  }
+  return LR_OK;
+}
+
+int lr_profile_count(void) {
+  std::lock_guard<std::mutex> lk(s_prof_mu);
+  return static_cast<int>(s_prof_result.size());
+}
+
+lr_status lr_profile_entry(int i, char* name, size_t name_len, long long* launches, double* total_ms, double* flops,
+                           double* bytes) {
+  std::lock_guard<std::mutex> lk(s_prof_mu);
+  if (i < 0 || i >= static_cast<int>(s_prof_result.size())) return fail(LR_ERR_SHAPE, "profile entry %d", i);
+  const ProfAgg& a = s_prof_result[i];
+  if (name && name_len) {
+    strncpy(name, a.name.c_str(), name_len - 1);
+    name[name_len - 1] = 0;
+  }
+  if (launches) *launches = a.n;
+  if (total_ms) *total_ms = a.ms;
+  if (flops) *flops = a.flops;
+  if (bytes) *bytes = a.bytes;
+  return LR_OK;
+}
 
 const char* lr_last_error(void) { return t_last_error.c_str(); }
 

@@ -26,7 +26,8 @@ EXPORTED = [
     "lr_mlp_saved_bytes", "lr_mlp_fwd_workspace_bytes", "lr_mlp_bwd_workspace_bytes", "lr_mlp_fwd",
     "lr_mlp_bwd", "lr_proj_saved_bytes", "lr_proj_fwd_workspace_bytes", "lr_proj_bwd_workspace_bytes",
     "lr_proj_fwd", "lr_proj_bwd", "lr_stack_workspace_bytes", "lr_stack_step", "lr_last_error",
-    "lr_check_device_error", "lr_selftest_wait_timeout", "lr_version",
+    "lr_check_device_error", "lr_selftest_wait_timeout", "lr_version", "lr_launch_count",
+    "lr_profile_start", "lr_profile_stop", "lr_profile_count", "lr_profile_entry",
 ]
 
 
@@ -68,6 +69,13 @@ _SIGS = {
     "lr_check_device_error": (_I, [_P]),
     "lr_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "lr_version": (_I, []),
+    "lr_launch_count": (ctypes.c_ulonglong, []),
+    "lr_profile_start": (_I, []),
+    "lr_profile_stop": (_I, []),
+    "lr_profile_count": (_I, []),
+    "lr_profile_entry": (_I, [_I, ctypes.c_char_p, _SZ, ctypes.POINTER(ctypes.c_longlong),
+                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                              ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -219,3 +227,25 @@ def lr_check_device_error(stream=None):
 
 def lr_selftest_wait_timeout(limit_ns: int, stream=None):
     _check(lib().lr_selftest_wait_timeout(limit_ns, _stream(stream)))
+
+
+def lr_launch_count() -> int:
+    return lib().lr_launch_count()
+
+
+def lr_profile_start():
+    _check(lib().lr_profile_start())
+
+
+def lr_profile_stop():
+    """Stop profiling and return {kernel name: dict(launches, ms, flops, bytes)}."""
+    _check(lib().lr_profile_stop())
+    out = {}
+    for i in range(lib().lr_profile_count()):
+        name = ctypes.create_string_buffer(128)
+        n = ctypes.c_longlong()
+        ms, fl, by = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        _check(lib().lr_profile_entry(i, name, 128, ctypes.byref(n), ctypes.byref(ms), ctypes.byref(fl),
+                                      ctypes.byref(by)))
+        out[name.value.decode()] = dict(launches=n.value, ms=ms.value, flops=fl.value, bytes=by.value)
+    return out
