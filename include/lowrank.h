@@ -159,6 +159,35 @@ lr_status lr_stack_step(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, in
                         float* loss, void* dx, float* const* dgs, const lr_pair_grad* grads, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------- allocation-free variant
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc — code running inside a framework whose
+ * allocator owns all device memory, code under a memory budget that forbids
+ * new allocations, or code paths that must not synchronise the device (as a
+ * cudaMalloc/cudaFree can).  Such callers cannot provide `ws` for lr_proj_fwd.
+ *
+ * lr_proj_fwd_noalloc computes exactly what lr_proj_fwd computes, with the same
+ * arguments minus the workspace.  Its only scratch (the gain-folded, stacked
+ * A weights: group * r * d_in elements of the storage dtype) lives in one
+ * file-scope device array of LR_NOALLOC_SCRATCH_BYTES bytes inside this
+ * library; a call whose group * r * d_in * sizeof(dtype) exceeds it returns
+ * LR_ERR_WORKSPACE and launches nothing.  The caller still allocates the inputs,
+ * `outs` and `saved`.  The call allocates and frees nothing itself.
+ *   - Every GPU that loads the library holds the array until the process exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (each
+ *     call overwrites what it uses before reading it).  Calls that overlap on
+ *     the GPU — on different streams, or from different host threads — race
+ *     on it: serialise them.
+ *   - It returns LR_ERR_UNSUPPORTED while profiling is on (the profiler
+ *     creates CUDA events). */
+#define LR_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+lr_status lr_proj_fwd_noalloc(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                              const void* g, float eps, const void* x, void* const* outs, void* saved,
+                              size_t saved_bytes, void* stream);
+
 /* ------------------------------------------------------------------ status
  * lr_last_error: message of the last failing call on this thread ("" if none).
  * lr_check_device_error: synchronises `stream`, reads and clears the current

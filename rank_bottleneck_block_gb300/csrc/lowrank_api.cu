@@ -885,6 +885,32 @@ static lr_status check_proj_dims(int T, int d_in, int d_out, int r, int group) {
   return LR_OK;
 }
 
+// ================================================== allocation-free variant
+// Scratch of lr_proj_fwd_noalloc: the folded, stacked A' = [A_1; ...; A_group] * g
+// (the only workspace a projection-group forward needs).  It lives in a
+// file-scope device array, so every GPU that loads this library holds it until
+// the process exits, and every call shares it.
+static constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(LR_NOALLOC_SCRATCH_BYTES);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static void* s_noalloc_scratch[kMaxDevices];
+
+// The host-side name g_noalloc_scratch is only a stand-in for the array: its
+// device address is looked up once per device, with that device current.
+static lr_status noalloc_scratch(void** out) {
+  int dev;
+  LR_TRY(current_device(&dev));
+  std::lock_guard<std::mutex> lk(s_dev_mu);
+  if (!s_noalloc_scratch[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess)
+      return fail(LR_ERR_CUDA, "cudaGetSymbolAddress(no-alloc scratch): %s", cudaGetErrorString(e));
+    s_noalloc_scratch[dev] = p;
+  }
+  *out = s_noalloc_scratch[dev];
+  return LR_OK;
+}
+
 }  // namespace lr
 
 using namespace lr;
@@ -1133,6 +1159,40 @@ lr_status lr_stack_step(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, in
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
   return stack_impl(c, mode, nblocks, T, d, f, r, eps, x, target, gs, pairs, loss, dx, dgs, grads, ws);
+}
+
+lr_status lr_proj_fwd_noalloc(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                              const void* g, float eps, const void* x, void* const* outs, void* saved,
+                              size_t saved_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_proj_dims(T, d_in, d_out, r, group));
+  if (!pairs || !outs) return fail(LR_ERR_NULL, "pairs / outs is NULL");
+  for (int i = 0; i < group; ++i) {
+    LR_TRY(check_pair(pairs[i], "pairs[i]"));
+    LR_TRY(check_ptr(outs[i], "outs[i]"));
+  }
+  if (g) LR_TRY(check_ptr(g, "g"));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_size(saved_bytes, proj_saved_layout(dt, T, r, group, g != nullptr, nullptr, nullptr), "saved"));
+  const size_t need = proj_ws_layout(dt, false, T, d_in, d_out, r, group, g != nullptr, nullptr, nullptr);
+  if (need > kNoAllocScratchBytes)
+    return fail(LR_ERR_WORKSPACE,
+                "lr_proj_fwd_noalloc: group * r * d_in weights need %zu bytes of scratch, more than its fixed "
+                "%zu-byte device array; use lr_proj_fwd with a caller workspace",
+                need, kNoAllocScratchBytes);
+  {
+    std::lock_guard<std::mutex> lk(s_prof_mu);
+    if (s_prof_on)
+      return fail(LR_ERR_UNSUPPORTED,
+                  "lr_proj_fwd_noalloc does not run while profiling is on (the profiler creates CUDA events)");
+  }
+  void* scratch = nullptr;
+  LR_TRY(noalloc_scratch(&scratch));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return proj_fwd_impl(c, T, d_in, d_out, r, group, pairs, g, eps, x, outs, saved, scratch);
 }
 
 lr_status lr_check_device_error(void* stream) {

@@ -27,7 +27,7 @@ EXPORTED = [
     "lr_mlp_bwd", "lr_proj_saved_bytes", "lr_proj_fwd_workspace_bytes", "lr_proj_bwd_workspace_bytes",
     "lr_proj_fwd", "lr_proj_bwd", "lr_stack_workspace_bytes", "lr_stack_step", "lr_last_error",
     "lr_check_device_error", "lr_selftest_wait_timeout", "lr_version", "lr_launch_count",
-    "lr_profile_start", "lr_profile_stop", "lr_profile_count", "lr_profile_entry",
+    "lr_profile_start", "lr_profile_stop", "lr_profile_count", "lr_profile_entry", "lr_proj_fwd_noalloc",
 ]
 
 
@@ -62,6 +62,8 @@ _SIGS = {
                          _P, _SZ, _P]),
     "lr_proj_bwd": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, _P, _SZ, ctypes.POINTER(_P),
                          _P, _P, ctypes.POINTER(lr_pair_grad), _P, _SZ, _P]),
+    "lr_proj_fwd_noalloc": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, ctypes.POINTER(_P),
+                                 _P, _SZ, _P]),
     "lr_stack_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "lr_stack_step": (_I, [_I, _I, _I, _I, _I, _I, _I, _F, _P, _P, ctypes.POINTER(_P), ctypes.POINTER(lr_pair), _P,
                            _P, ctypes.POINTER(_P), ctypes.POINTER(lr_pair_grad), _P, _SZ, _P]),
@@ -249,3 +251,14 @@ def lr_profile_stop():
                                       ctypes.byref(by)))
         out[name.value.decode()] = dict(launches=n.value, ms=ms.value, flops=fl.value, bytes=by.value)
     return out
+
+
+LR_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def lr_proj_fwd_noalloc(dt, T, d_in, d_out, r, pairs: Sequence[lr_pair], g, eps, x, outs, saved, stream=None):
+    """lr_proj_fwd without a workspace, for callers that cannot allocate device memory: its scratch is a
+    fixed device array of LR_NOALLOC_SCRATCH_BYTES inside the library, shared by all calls (serialise them)."""
+    group = len(pairs)
+    _check(lib().lr_proj_fwd_noalloc(dt, T, d_in, d_out, r, group, _pairs(pairs), _p(g), eps, _p(x), _ptrs(outs),
+                                     _p(saved), _nbytes(saved), _stream(stream)))
