@@ -1,11 +1,12 @@
 // Fused GEMM epilogues of the low-rank bottleneck sublayer.
 //
-// One call handles one output row m and W consecutive columns n0 .. n0+W-1 of
-// one batch entry; v[a][j] is accumulator a at column n0 + j.  W is a multiple
-// of 8 and every N handled here is a multiple of 8, so each 8-column group is
-// either fully inside the output or fully outside it.  Row partial sums are
-// accumulated over the whole W-column chunk, so each chunk writes exactly one
-// partial per row (chunk index n0 / W).
+// EpiDef<K> describes one epilogue: how many accumulators it consumes (NACC),
+// how many same-shaped operand tiles it reads besides them (NAUX), how many
+// output tiles it writes (NOUT, bf16/fp32 per the storage type, or fp32 for the
+// weight-gradient partials), which per-row scalars it needs, and its math on W
+// consecutive columns of one row.  Both GEMM engines share this math; only the
+// way operand and output tiles move differs (TMA tiles through shared memory in
+// the tcgen05 kernel, direct global accesses in the SIMT kernel).
 //
 // The math follows the unfused definition of the block (BOOST technical
 // summary §2.2 states each optimisation is an exact rewrite):
@@ -13,157 +14,192 @@
 //    pre-activation is u = s * (x A'^T) with s = (mean x^2 + eps)^-1/2, and the
 //    backward is dx = s (du A') - (s^2 / d) rho x with rho = sum_i du_i u_i;
 //  * SwiGLU: h = SiLU(a) * b, da = dh b SiLU'(a), db = dh SiLU(a).
+// Values that are stored and used again are rounded to the storage type first,
+// so a re-forward from saved tensors reproduces the forward bit for bit.
 #pragma once
 
 #include "common.cuh"
 
 namespace lr {
 
-template <EpiKind K, typename ST, int W, int NACC>
-__device__ __forceinline__ void epi_apply(const EpiParams& p, int b, int split, int m, int n0,
-                                          float (&v)[NACC][W]) {
-  static_assert(W % 8 == 0, "chunk width must be a multiple of 8");
-  if constexpr (K == EPI_NORM_SILU || K == EPI_SILU) {
-    const float s = (K == EPI_NORM_SILU) ? p.rowscale[m] : 1.f;
-    ST* u_out = static_cast<ST*>(p.out0[b]) + (long long)m * p.ldo0;
-    ST* z_out = static_cast<ST*>(p.out1[b]) + (long long)m * p.ldo1;
+// Per-row inputs of an epilogue: s = 1/rms of the row, k = coef * s^2 * rho.
+struct RowIn {
+  float s;
+  float k;
+};
+
+template <EpiKind K>
+struct EpiDef;
+
+template <>
+struct EpiDef<EPI_NORM_SILU> {  // u = round(s acc), z = SiLU(u)
+  static constexpr int NACC = 1, NAUX = 0, NOUT = 2;
+  static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[1][W], const float (&)[1][W],
+                                             float (&o)[2][W], float&) {
 #pragma unroll
-    for (int j = 0; j < W; j += 8) {
-      if (n0 + j < p.N) {
-        float u[8], z[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          u[t] = Num<ST>::round(s * v[0][j + t]);
-          z[t] = silu<ST>(u[t]);
-        }
-        store8(u_out + n0 + j, u);
-        store8(z_out + n0 + j, z);
-      }
+    for (int j = 0; j < W; ++j) {
+      const float u = Num<ST>::round(ri.s * v[0][j]);
+      o[0][j] = u;
+      o[1][j] = silu<ST>(u);
     }
-  } else if constexpr (K == EPI_STORE) {
-    ST* o = static_cast<ST*>(p.out0[b]) + (long long)m * p.ldo0;
+  }
+};
+
+template <>
+struct EpiDef<EPI_SILU> {  // u = round(acc), z = SiLU(u)
+  static constexpr int NACC = 1, NAUX = 0, NOUT = 2;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&)[1][W],
+                                             float (&o)[2][W], float&) {
 #pragma unroll
-    for (int j = 0; j < W; j += 8)
-      if (n0 + j < p.N) store8(o + n0 + j, &v[0][j]);
-  } else if constexpr (K == EPI_RESID) {
-    ST* o = static_cast<ST*>(p.out0[b]) + (long long)m * p.ldo0;
-    const ST* x = static_cast<const ST*>(p.aux0[b]) + (long long)m * p.lda0;
-#pragma unroll
-    for (int j = 0; j < W; j += 8) {
-      if (n0 + j < p.N) {
-        float xv[8], o8[8];
-        load8(x + n0 + j, xv);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) o8[t] = xv[t] + v[0][j + t];
-        store8(o + n0 + j, o8);
-      }
+    for (int j = 0; j < W; ++j) {
+      const float u = Num<ST>::round(v[0][j]);
+      o[0][j] = u;
+      o[1][j] = silu<ST>(u);
     }
-  } else if constexpr (K == EPI_SWIGLU) {
-    static_assert(NACC == 2, "SwiGLU needs the gate and up accumulators");
-    ST* h_out = static_cast<ST*>(p.out0[0]) + (long long)m * p.ldo0;
-    ST* a_out = p.out1[0] ? static_cast<ST*>(p.out1[0]) + (long long)m * p.ldo1 : nullptr;
-    ST* b_out = p.out2[0] ? static_cast<ST*>(p.out2[0]) + (long long)m * p.ldo2 : nullptr;
+  }
+};
+
+template <>
+struct EpiDef<EPI_STORE> {  // out = acc
+  static constexpr int NACC = 1, NAUX = 0, NOUT = 1;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&)[1][W],
+                                             float (&o)[1][W], float&) {
 #pragma unroll
-    for (int j = 0; j < W; j += 8) {
-      if (n0 + j < p.N) {
-        float a[8], bb[8], h[8];
+    for (int j = 0; j < W; ++j) o[0][j] = v[0][j];
+  }
+};
+
+template <>
+struct EpiDef<EPI_RESID> {  // out = x + acc  (aux0 = x)
+  static constexpr int NACC = 1, NAUX = 1, NOUT = 1;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&a)[1][W],
+                                             float (&o)[1][W], float&) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          a[t] = Num<ST>::round(v[0][j + t]);
-          bb[t] = Num<ST>::round(v[1][j + t]);
-          h[t] = silu<ST>(a[t]) * bb[t];
-        }
-        store8(h_out + n0 + j, h);
-        if (a_out) store8(a_out + n0 + j, a);
-        if (b_out) store8(b_out + n0 + j, bb);
-      }
+    for (int j = 0; j < W; ++j) o[0][j] = a[0][j] + v[0][j];
+  }
+};
+
+template <>
+struct EpiDef<EPI_SWIGLU> {  // a = round(acc0), b = round(acc1), h = SiLU(a) b -> (h, a, b)
+  static constexpr int NACC = 2, NAUX = 0, NOUT = 3;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[2][W], const float (&)[1][W],
+                                             float (&o)[3][W], float&) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      const float a = Num<ST>::round(v[0][j]);
+      const float b = Num<ST>::round(v[1][j]);
+      o[0][j] = silu<ST>(a) * b;
+      o[1][j] = a;
+      o[2][j] = b;
     }
-  } else if constexpr (K == EPI_DSILU) {
-    ST* o = static_cast<ST*>(p.out0[b]) + (long long)m * p.ldo0;
-    const ST* u = static_cast<const ST*>(p.aux0[b]) + (long long)m * p.lda0;
+  }
+};
+
+template <>
+struct EpiDef<EPI_DSILU> {  // du = acc SiLU'(u)  (aux0 = u)
+  static constexpr int NACC = 1, NAUX = 1, NOUT = 1;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&a)[1][W],
+                                             float (&o)[1][W], float&) {
 #pragma unroll
-    for (int j = 0; j < W; j += 8) {
-      if (n0 + j < p.N) {
-        float uv[8], du[8];
-        load8(u + n0 + j, uv);
+    for (int j = 0; j < W; ++j) o[0][j] = v[0][j] * silu_grad<ST>(a[0][j]);
+  }
+};
+
+template <>
+struct EpiDef<EPI_DSILU_NORM> {  // du = acc SiLU'(u); out = s du; row partial += du u  (aux0 = u)
+  static constexpr int NACC = 1, NAUX = 1, NOUT = 1;
+  static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = false, ROWPART = true;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[1][W], const float (&a)[1][W],
+                                             float (&o)[1][W], float& part) {
+    float p = 0.f;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) du[t] = v[0][j + t] * silu_grad<ST>(uv[t]);
-        store8(o + n0 + j, du);
-      }
+    for (int j = 0; j < W; ++j) {
+      const float du = v[0][j] * silu_grad<ST>(a[0][j]);
+      p = fmaf(du, a[0][j], p);
+      o[0][j] = ri.s * du;
     }
-  } else if constexpr (K == EPI_DSILU_NORM) {
-    if (n0 >= p.N) return;
-    const float s = p.rowscale[m];
-    ST* o = static_cast<ST*>(p.out0[b]) + (long long)m * p.ldo0;
-    const ST* u = static_cast<const ST*>(p.aux0[b]) + (long long)m * p.lda0;
-    float part = 0.f;
+    part = p;
+  }
+};
+
+template <>
+struct EpiDef<EPI_SWIGLU_BWD> {  // dh = acc; da = dh b SiLU'(a), db = dh SiLU(a)  (aux0 = a, aux1 = b)
+  static constexpr int NACC = 1, NAUX = 2, NOUT = 2;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&a)[2][W],
+                                             float (&o)[2][W], float&) {
 #pragma unroll
-    for (int j = 0; j < W; j += 8) {
-      if (n0 + j < p.N) {
-        float uv[8], ds[8];
-        load8(u + n0 + j, uv);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float du = v[0][j + t] * silu_grad<ST>(uv[t]);
-          part = fmaf(du, uv[t], part);
-          ds[t] = s * du;
-        }
-        store8(o + n0 + j, ds);
-      }
+    for (int j = 0; j < W; ++j) {
+      const float dh = v[0][j], av = a[0][j], bv = a[1][j];
+      const float l = Num<ST>::logistic(av);
+      o[0][j] = dh * bv * (l * (1.f + av * (1.f - l)));
+      o[1][j] = dh * (av * l);
     }
-    p.rowpart[((long long)b * p.rowpart_chunks + n0 / W) * p.M + m] = part;
-  } else if constexpr (K == EPI_SWIGLU_BWD) {
-    ST* da_out = static_cast<ST*>(p.out0[b]) + (long long)m * p.ldo0;
-    ST* db_out = static_cast<ST*>(p.out1[b]) + (long long)m * p.ldo1;
-    const ST* a = static_cast<const ST*>(p.aux0[b]) + (long long)m * p.lda0;
-    const ST* bb = static_cast<const ST*>(p.aux1[b]) + (long long)m * p.lda1;
+  }
+};
+
+template <>
+struct EpiDef<EPI_DX_NORM> {  // dx = G + acc - k x  (aux0 = G, may be absent; aux1 = x)
+  static constexpr int NACC = 1, NAUX = 2, NOUT = 1;
+  static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = true, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[1][W], const float (&a)[2][W],
+                                             float (&o)[1][W], float&) {
 #pragma unroll
-    for (int j = 0; j < W; j += 8) {
-      if (n0 + j < p.N) {
-        float av[8], bv[8], da[8], db[8];
-        load8(a + n0 + j, av);
-        load8(bb + n0 + j, bv);
+    for (int j = 0; j < W; ++j) o[0][j] = a[0][j] + v[0][j] - ri.k * a[1][j];
+  }
+};
+
+template <>
+struct EpiDef<EPI_F32> {  // fp32 weight-gradient partial
+  static constexpr int NACC = 1, NAUX = 0, NOUT = 1;
+  static constexpr bool OUT_F32 = true, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&)[1][W],
+                                             float (&o)[1][W], float&) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float dh = v[0][j + t];
-          const float l = Num<ST>::logistic(av[t]);
-          da[t] = dh * bv[t] * (l * (1.f + av[t] * (1.f - l)));
-          db[t] = dh * (av[t] * l);
-        }
-        store8(da_out + n0 + j, da);
-        store8(db_out + n0 + j, db);
-      }
-    }
-  } else if constexpr (K == EPI_DX_NORM) {
+    for (int j = 0; j < W; ++j) o[0][j] = v[0][j];
+  }
+};
+
+// Per-row inputs of the epilogue for row m (0 for rows past the end).
+template <EpiKind K>
+__device__ __forceinline__ RowIn row_inputs(const EpiParams& p, int m) {
+  using D = EpiDef<K>;
+  RowIn ri{0.f, 0.f};
+  if (m >= p.M) return ri;
+  if constexpr (D::NEED_S) ri.s = p.rowscale[m];
+  if constexpr (D::NEED_RHO) {
     float rho = 0.f;
     for (int c = 0; c < p.rowpart_in_chunks; ++c) rho += p.rowpart_in[(long long)c * p.M + m];
-    const float s = p.rowscale[m];
-    const float k = p.coef * s * s * rho;
-    ST* o = static_cast<ST*>(p.out0[b]) + (long long)m * p.ldo0;
-    const ST* G = p.aux0[b] ? static_cast<const ST*>(p.aux0[b]) + (long long)m * p.lda0 : nullptr;
-    const ST* x = static_cast<const ST*>(p.aux1[b]) + (long long)m * p.lda1;
-#pragma unroll
-    for (int j = 0; j < W; j += 8) {
-      if (n0 + j < p.N) {
-        float xv[8], gv[8], o8[8];
-        load8(x + n0 + j, xv);
-        if (G) {
-          load8(G + n0 + j, gv);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 8; ++t) gv[t] = 0.f;
-        }
-#pragma unroll
-        for (int t = 0; t < 8; ++t) o8[t] = gv[t] + v[0][j + t] - k * xv[t];
-        store8(o + n0 + j, o8);
-      }
-    }
-  } else if constexpr (K == EPI_F32) {
-    float* o = static_cast<float*>(p.out0[b]) + (long long)split * p.split_stride + (long long)m * p.ldo0;
-#pragma unroll
-    for (int j = 0; j < W; j += 8)
-      if (n0 + j < p.N) store8(o + n0 + j, &v[0][j]);
+    ri.k = p.coef * ri.s * ri.s * rho;
   }
+  return ri;
+}
+
+__device__ __forceinline__ const void* epi_aux_ptr(const EpiParams& p, int a, int b) {
+  return a == 0 ? p.aux0[b] : p.aux1[b];
+}
+__device__ __forceinline__ void* epi_out_ptr(const EpiParams& p, int o, int b) {
+  return o == 0 ? p.out0[b] : (o == 1 ? p.out1[b] : p.out2[b]);
+}
+__device__ __forceinline__ long long epi_aux_ld(const EpiParams& p, int a) { return a == 0 ? p.lda0 : p.lda1; }
+__device__ __forceinline__ long long epi_out_ld(const EpiParams& p, int o) {
+  return o == 0 ? p.ldo0 : (o == 1 ? p.ldo1 : p.ldo2);
 }
 
 }  // namespace lr

@@ -32,13 +32,13 @@ struct GemmCall {
 };
 
 // Row-partial chunk width used by the epilogues of each engine.
-constexpr int kChunkUmma = 32;
+constexpr int kChunkUmma = 32;  // the tcgen05 epilogue chunk (umma::CW)
 constexpr int kChunkSimt = 8;
 
-template <EpiKind K, int BN, int NACC, bool A_MN, bool B_MN>
+template <EpiKind K, int BN, bool A_MN, bool B_MN>
 cudaError_t launch_umma(const GemmCall& g, cudaStream_t st);
 
-template <EpiKind K, int NACC>
+template <EpiKind K>
 cudaError_t launch_simt(const GemmCall& g, cudaStream_t st);
 
 // Number of SMs of the current device (cached per device).

@@ -2,16 +2,16 @@
 #include "simt_gemm.cuh"
 
 namespace lr {
-#define LR_INST(K, NACC) template cudaError_t launch_simt<K, NACC>(const GemmCall&, cudaStream_t);
-LR_INST(EPI_NORM_SILU, 1)
-LR_INST(EPI_SILU, 1)
-LR_INST(EPI_STORE, 1)
-LR_INST(EPI_RESID, 1)
-LR_INST(EPI_SWIGLU, 2)
-LR_INST(EPI_DSILU, 1)
-LR_INST(EPI_DSILU_NORM, 1)
-LR_INST(EPI_SWIGLU_BWD, 1)
-LR_INST(EPI_DX_NORM, 1)
-LR_INST(EPI_F32, 1)
+#define LR_INST(K) template cudaError_t launch_simt<K>(const GemmCall&, cudaStream_t);
+LR_INST(EPI_NORM_SILU)
+LR_INST(EPI_SILU)
+LR_INST(EPI_STORE)
+LR_INST(EPI_RESID)
+LR_INST(EPI_SWIGLU)
+LR_INST(EPI_DSILU)
+LR_INST(EPI_DSILU_NORM)
+LR_INST(EPI_SWIGLU_BWD)
+LR_INST(EPI_DX_NORM)
+LR_INST(EPI_F32)
 #undef LR_INST
 }  // namespace lr

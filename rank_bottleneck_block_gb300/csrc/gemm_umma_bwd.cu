@@ -4,19 +4,19 @@
 #include "umma_launch.cuh"
 
 namespace lr {
-#define LR_INST(K, BN, NACC, AMN, BMN) \
-  template cudaError_t launch_umma<K, BN, NACC, AMN, BMN>(const GemmCall&, cudaStream_t);
-LR_INST(EPI_DSILU, 128, 1, false, true)
-LR_INST(EPI_DSILU, 256, 1, false, true)
-LR_INST(EPI_DSILU_NORM, 128, 1, false, true)
-LR_INST(EPI_DSILU_NORM, 256, 1, false, true)
-LR_INST(EPI_SWIGLU_BWD, 128, 1, false, true)
-LR_INST(EPI_SWIGLU_BWD, 256, 1, false, true)
-LR_INST(EPI_DX_NORM, 128, 1, false, true)
-LR_INST(EPI_DX_NORM, 256, 1, false, true)
-LR_INST(EPI_STORE, 128, 1, false, true)
-LR_INST(EPI_STORE, 256, 1, false, true)
-LR_INST(EPI_F32, 128, 1, true, true)
-LR_INST(EPI_F32, 256, 1, true, true)
+#define LR_INST(K, BN, AMN, BMN) \
+  template cudaError_t launch_umma<K, BN, AMN, BMN>(const GemmCall&, cudaStream_t);
+LR_INST(EPI_DSILU, 128, false, true)
+LR_INST(EPI_DSILU, 256, false, true)
+LR_INST(EPI_DSILU_NORM, 128, false, true)
+LR_INST(EPI_DSILU_NORM, 256, false, true)
+LR_INST(EPI_SWIGLU_BWD, 128, false, true)
+LR_INST(EPI_SWIGLU_BWD, 256, false, true)
+LR_INST(EPI_DX_NORM, 128, false, true)
+LR_INST(EPI_DX_NORM, 256, false, true)
+LR_INST(EPI_STORE, 128, false, true)
+LR_INST(EPI_STORE, 256, false, true)
+LR_INST(EPI_F32, 128, true, true)
+LR_INST(EPI_F32, 256, true, true)
 #undef LR_INST
 }  // namespace lr

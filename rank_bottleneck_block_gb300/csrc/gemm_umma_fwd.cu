@@ -2,16 +2,16 @@
 #include "umma_launch.cuh"
 
 namespace lr {
-#define LR_INST(K, BN, NACC, AMN, BMN) \
-  template cudaError_t launch_umma<K, BN, NACC, AMN, BMN>(const GemmCall&, cudaStream_t);
-LR_INST(EPI_NORM_SILU, 128, 1, false, false)
-LR_INST(EPI_NORM_SILU, 256, 1, false, false)
-LR_INST(EPI_SILU, 128, 1, false, false)
-LR_INST(EPI_SILU, 256, 1, false, false)
-LR_INST(EPI_STORE, 128, 1, false, false)
-LR_INST(EPI_STORE, 256, 1, false, false)
-LR_INST(EPI_RESID, 128, 1, false, false)
-LR_INST(EPI_RESID, 256, 1, false, false)
-LR_INST(EPI_SWIGLU, 128, 2, false, false)
+#define LR_INST(K, BN, AMN, BMN) \
+  template cudaError_t launch_umma<K, BN, AMN, BMN>(const GemmCall&, cudaStream_t);
+LR_INST(EPI_NORM_SILU, 128, false, false)
+LR_INST(EPI_NORM_SILU, 256, false, false)
+LR_INST(EPI_SILU, 128, false, false)
+LR_INST(EPI_SILU, 256, false, false)
+LR_INST(EPI_STORE, 128, false, false)
+LR_INST(EPI_STORE, 256, false, false)
+LR_INST(EPI_RESID, 128, false, false)
+LR_INST(EPI_RESID, 256, false, false)
+LR_INST(EPI_SWIGLU, 128, false, false)
 #undef LR_INST
 }  // namespace lr

@@ -171,29 +171,29 @@ static int pick_bn(const GemmCall& g, int sms) {
   return c128 < c256 ? 128 : 256;
 }
 
-template <EpiKind K, int NACC, bool A_MN, bool B_MN>
+template <EpiKind K, bool A_MN, bool B_MN>
 static cudaError_t umma_bn(const GemmCall& g, cudaStream_t st) {
-  if (g.bn == 128) return launch_umma<K, 128, NACC, A_MN, B_MN>(g, st);
-  return launch_umma<K, 256, NACC, A_MN, B_MN>(g, st);
+  if (g.bn == 128) return launch_umma<K, 128, A_MN, B_MN>(g, st);
+  return launch_umma<K, 256, A_MN, B_MN>(g, st);
 }
 
 static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sms) {
   (void)sms;
   const bool kk = !g.a_mn && !g.b_mn, km = !g.a_mn && g.b_mn, mm = g.a_mn && g.b_mn;
   switch (k) {
-    case EPI_NORM_SILU: if (kk) return umma_bn<EPI_NORM_SILU, 1, false, false>(g, st); break;
-    case EPI_SILU: if (kk) return umma_bn<EPI_SILU, 1, false, false>(g, st); break;
+    case EPI_NORM_SILU: if (kk) return umma_bn<EPI_NORM_SILU, false, false>(g, st); break;
+    case EPI_SILU: if (kk) return umma_bn<EPI_SILU, false, false>(g, st); break;
     case EPI_STORE:
-      if (kk) return umma_bn<EPI_STORE, 1, false, false>(g, st);
-      if (km) return umma_bn<EPI_STORE, 1, false, true>(g, st);
+      if (kk) return umma_bn<EPI_STORE, false, false>(g, st);
+      if (km) return umma_bn<EPI_STORE, false, true>(g, st);
       break;
-    case EPI_RESID: if (kk) return umma_bn<EPI_RESID, 1, false, false>(g, st); break;
-    case EPI_SWIGLU: if (kk && g.nacc == 2) return launch_umma<EPI_SWIGLU, 128, 2, false, false>(g, st); break;
-    case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, 1, false, true>(g, st); break;
-    case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, 1, false, true>(g, st); break;
-    case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, 1, false, true>(g, st); break;
-    case EPI_DX_NORM: if (km) return umma_bn<EPI_DX_NORM, 1, false, true>(g, st); break;
-    case EPI_F32: if (mm) return umma_bn<EPI_F32, 1, true, true>(g, st); break;
+    case EPI_RESID: if (kk) return umma_bn<EPI_RESID, false, false>(g, st); break;
+    case EPI_SWIGLU: if (kk && g.nacc == 2) return launch_umma<EPI_SWIGLU, 128, false, false>(g, st); break;
+    case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, false, true>(g, st); break;
+    case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
+    case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
+    case EPI_DX_NORM: if (km) return umma_bn<EPI_DX_NORM, false, true>(g, st); break;
+    case EPI_F32: if (mm) return umma_bn<EPI_F32, true, true>(g, st); break;
     default: break;
   }
   return cudaErrorNotSupported;
@@ -201,16 +201,16 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
 
 static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
   switch (k) {
-    case EPI_NORM_SILU: return launch_simt<EPI_NORM_SILU, 1>(g, st);
-    case EPI_SILU: return launch_simt<EPI_SILU, 1>(g, st);
-    case EPI_STORE: return launch_simt<EPI_STORE, 1>(g, st);
-    case EPI_RESID: return launch_simt<EPI_RESID, 1>(g, st);
-    case EPI_SWIGLU: return launch_simt<EPI_SWIGLU, 2>(g, st);
-    case EPI_DSILU: return launch_simt<EPI_DSILU, 1>(g, st);
-    case EPI_DSILU_NORM: return launch_simt<EPI_DSILU_NORM, 1>(g, st);
-    case EPI_SWIGLU_BWD: return launch_simt<EPI_SWIGLU_BWD, 1>(g, st);
-    case EPI_DX_NORM: return launch_simt<EPI_DX_NORM, 1>(g, st);
-    case EPI_F32: return launch_simt<EPI_F32, 1>(g, st);
+    case EPI_NORM_SILU: return launch_simt<EPI_NORM_SILU>(g, st);
+    case EPI_SILU: return launch_simt<EPI_SILU>(g, st);
+    case EPI_STORE: return launch_simt<EPI_STORE>(g, st);
+    case EPI_RESID: return launch_simt<EPI_RESID>(g, st);
+    case EPI_SWIGLU: return launch_simt<EPI_SWIGLU>(g, st);
+    case EPI_DSILU: return launch_simt<EPI_DSILU>(g, st);
+    case EPI_DSILU_NORM: return launch_simt<EPI_DSILU_NORM>(g, st);
+    case EPI_SWIGLU_BWD: return launch_simt<EPI_SWIGLU_BWD>(g, st);
+    case EPI_DX_NORM: return launch_simt<EPI_DX_NORM>(g, st);
+    case EPI_F32: return launch_simt<EPI_F32>(g, st);
     default: return cudaErrorNotSupported;
   }
 }

@@ -21,8 +21,10 @@ struct Args {
   long long a_sm, a_sk, b_sn, b_sk;  // element strides along m / k and n / k
 };
 
-template <EpiKind K, int NACC>
+template <EpiKind K>
 __global__ void __launch_bounds__(256) gemm_kernel(const Args a, const EpiParams ep) {
+  using D = EpiDef<K>;
+  constexpr int NACC = D::NACC, NAUX = D::NAUX, NOUT = D::NOUT;
   __shared__ float As[TK][TM + 1];
   __shared__ float Bs[TK][TN + 1];
   const int tid = threadIdx.x;
@@ -65,14 +67,39 @@ __global__ void __launch_bounds__(256) gemm_kernel(const Args a, const EpiParams
     }
   }
   const int m = m0 + tr, n = n0 + tc * 8;
-  if (m < a.M && n < a.N) epi_apply<K, float, 8, NACC>(ep, batch, split, m, n, acc);
+  if (m >= a.M || n >= a.N) return;
+  const RowIn ri = row_inputs<K>(ep, m);
+  float av[NAUX > 0 ? NAUX : 1][8];
+#pragma unroll
+  for (int x = 0; x < NAUX; ++x) {
+    const float* p = static_cast<const float*>(epi_aux_ptr(ep, x, batch));
+    if (p) {
+      load8(p + static_cast<long long>(m) * epi_aux_ld(ep, x) + n, av[x]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) av[x][j] = 0.f;
+    }
+  }
+  float o[NOUT][8];
+  float part = 0.f;
+  D::template run<float, 8>(ri, acc, av, o, part);
+#pragma unroll
+  for (int x = 0; x < NOUT; ++x) {
+    float* p = static_cast<float*>(epi_out_ptr(ep, x, batch));
+    if (!p) continue;
+    if (D::OUT_F32) p += static_cast<long long>(split) * ep.split_stride;
+    store8(p + static_cast<long long>(m) * epi_out_ld(ep, x) + n, o[x]);
+  }
+  if constexpr (D::ROWPART)
+    ep.rowpart[(static_cast<long long>(batch) * ep.rowpart_chunks + n / 8) * ep.M + m] = part;
 }
 
 }  // namespace simt
 
-template <EpiKind K, int NACC>
+template <EpiKind K>
 cudaError_t launch_simt(const GemmCall& g, cudaStream_t st) {
   using namespace simt;
+  constexpr int NACC = EpiDef<K>::NACC;
   Args a;
   a.M = g.M;
   a.N = g.N;
@@ -93,7 +120,7 @@ cudaError_t launch_simt(const GemmCall& g, cudaStream_t st) {
   a.b_sk = g.b_mn ? g.B[0].ld : 1;
   dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, a.batches * a.ksplit);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
-  gemm_kernel<K, NACC><<<grid, 256, 0, st>>>(a, g.ep);
+  gemm_kernel<K><<<grid, 256, 0, st>>>(a, g.ep);
   return cudaGetLastError();
 }
 

@@ -1,25 +1,35 @@
-// Persistent tcgen05 GEMM for sm_103a with fused epilogues.
+// Persistent tcgen05 GEMM for sm_103a with fused, TMA-staged epilogues.
 //
 //   C[M,N] = sum_k A[m,k] B[n,k]      bf16 operands, fp32 accumulator in TMEM
 //
-// Operands are staged by TMA into a ring of shared-memory stages with the
-// 128-byte swizzle; each operand is either K-major (rows contiguous in k) or
-// MN-major (rows contiguous in m / n, i.e. the transposed storage used by the
-// weight-gradient and dX = dY . W products), and the UMMA shared-memory
-// descriptors describe both natively, so no transpose kernels exist.
+// Mainloop: operands are staged by TMA into a ring of shared-memory stages with
+// the 128-byte swizzle; each operand is K-major (rows contiguous in k) or
+// MN-major (rows contiguous in m / n: the transposed storage used by the
+// weight-gradient and dX = dY . W products), described natively by the UMMA
+// shared-memory descriptors, so no transpose kernels exist.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over output tiles):
-//   warp 0     TMA producer (one elected lane)
+// Epilogue: 8 warps in two groups of four; group g handles the 32-column
+// chunks c = g, g+2, ... of each tile.  Within a group, warp w reads TMEM lanes
+// 32 (w % 4) .. +31 with tcgen05.ld (one output row per thread), the chunk's
+// operand tiles (u, a, b, x, dout) arrive by TMA into 64-byte-swizzled shared
+// memory, the fused math runs in registers, the results go to swizzled shared
+// memory and one thread writes them to global memory with TMA bulk tensor
+// stores (rows and columns past the tensor edge are clipped by the TMA unit).
+//
+// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+//   warp 0     TMA producer of the operand ring (one elected lane)
 //   warp 1     TMEM allocator and MMA issuer (one elected lane issues tcgen05.mma)
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused math, global stores
+//   warps 2-9  epilogue
 // Two TMEM accumulator buffers let the epilogue of tile i overlap the
 // mainloop of tile i+1.  NACC > 1 gives each tile several accumulators fed by
 // consecutive K segments with their own operand maps (the SwiGLU dual GEMM).
 //
-// Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting role
-// sets a bit of the device error word, raises the CTA's abort flag and leaves
-// its loop; the producer then waits (bounded) for its copies still in flight,
-// the MMA warp drains its issued MMAs, and TMEM is freed before the CTA exits.
+// Every wait on an mbarrier is bounded: after kWaitLimitNs the waiting thread
+// sets a bit of the device error word and raises the CTA's abort flag; every
+// role then leaves its loop (epilogue groups decide together through a
+// barrier reduction), the producer waits (bounded) for its copies in flight,
+// the MMA warp drains its issued MMAs, the epilogue waits for its stores, and
+// TMEM is freed before the CTA exits.
 #pragma once
 
 #include <cuda.h>
@@ -32,12 +42,17 @@ namespace umma {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16 along K
-constexpr int kThreads = 192;
+constexpr int CW = 32;  // epilogue chunk width (columns)
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kMaxSmem = 227 * 1024;
 
 struct Maps {
   CUtensorMap a[kMaxBatch];
   CUtensorMap b[kMaxBatch];
+  CUtensorMap out[kMaxBatch][3];
+  CUtensorMap aux[kMaxBatch][2];
 };
 
 struct Shape {
@@ -104,6 +119,43 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
           smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
       : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over `nthreads` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
 }
 
 __device__ __forceinline__ void tmap_prefetch(const CUtensorMap* map) {
@@ -175,23 +227,41 @@ __host__ __device__ constexpr uint32_t idesc_bf16() {
          (static_cast<uint32_t>(N_ >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-template <int BN, int NACC>
+// Byte offset of 16-byte chunk j of row r in a swizzled staging tile with `row_bytes`
+// per row (64: the 64-byte swizzle of bf16 chunks, 128: the 128-byte swizzle of fp32 chunks).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t stage_off(int r, int j) {
+  if constexpr (ROW_BYTES == 64) return r * 64 + ((j ^ ((r >> 1) & 3)) << 4);
+  else return r * 128 + ((j ^ (r & 7)) << 4);
+}
+
+template <EpiKind K, int BN>
 struct Config {
+  using D = EpiDef<K>;
+  static constexpr int NACC = D::NACC;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+  static constexpr int OUT_ROW = CW * (D::OUT_F32 ? 4 : 2);
+  static constexpr int OUT_BUF = BM * OUT_ROW;
+  static constexpr int AUX_BUF = BM * CW * 2;
+  static constexpr int GROUP_BYTES = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;
+  static constexpr int EPI_BYTES = 2 * GROUP_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int RING_BUDGET = kMaxSmem - 1024 - EPI_BYTES - BAR_BYTES;
+  static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
   static constexpr uint32_t ACC_COLS = NACC * BN;
   static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS <= 32    ? 32
                                         : 2 * ACC_COLS <= 64  ? 64
                                         : 2 * ACC_COLS <= 128 ? 128
                                         : 2 * ACC_COLS <= 256 ? 256
                                                               : 512;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(2 * ACC_COLS <= 512, "two accumulator buffers must fit in TMEM");
   static_assert(STAGES >= 2, "need at least two stages");
   static_assert(BN % 64 == 0 && BN <= 256, "BN must be 64..256 in steps of 64");
+  static_assert((BN / CW) % 2 == 0, "both epilogue groups need the same number of chunks");
+  static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
 };
 
 __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int& split, int& batch, int& mb, int& nb) {
@@ -205,10 +275,12 @@ __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int& spli
   nb = rem - mb * sh.n_tiles;
 }
 
-template <EpiKind K, int BN, int NACC, bool A_MN, bool B_MN>
+template <EpiKind K, int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ Maps maps, const Shape sh, const EpiParams ep) {
-  using C = Config<BN, NACC>;
+  using C = Config<K, BN>;
+  using D = EpiDef<K>;
+  constexpr int NACC = D::NACC;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t IDESC = idesc_bf16<BN, A_MN, B_MN>();
 
@@ -216,12 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_BYTES);
+  uint8_t* sE = sB + STAGES * C::B_BYTES;  // epilogue staging, 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(sE + C::EPI_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* aux_full = drain + 1;  // one per epilogue group
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -234,15 +308,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);  // one arrive per epilogue warp
+      mbar_init(&tempty[i], kEpiWarps);  // one arrive per epilogue warp
+      mbar_init(&aux_full[i], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    fence_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < sh.batches || i < NACC; ++i) {
+    const int nsets = NACC > 1 ? NACC : sh.batches;
+    for (int i = 0; i < nsets; ++i) {
       tmap_prefetch(&maps.a[i]);
       tmap_prefetch(&maps.b[i]);
     }
@@ -367,30 +443,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------ epilogue warps
+    constexpr int NAUX = D::NAUX, NOUT = D::NOUT;
+    constexpr int NCH = BN / CW;
+    const int ew = warp - 2;
+    const int g = ew >> 2;   // group: chunks g, g+2, ...
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
+    const int row = q * 32 + lane;
+    const bool leader = (ew & 3) == 0 && lane == 0;
+    const int bar_id = 1 + g;
+    uint8_t* ostage = sE + g * C::GROUP_BYTES;
+    uint8_t* astage = ostage + NOUT * C::OUT_BUF;
+    uint64_t* abar = &aux_full[g];
+    uint32_t aph = 0;
+
+    auto issue_aux = [&](int t, int c) {
+      int split, batch, mb, nb;
+      decode_tile(sh, t, split, batch, mb, nb);
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int a = 0; a < NAUX; ++a)
+        if (epi_aux_ptr(ep, a, batch)) bytes += C::AUX_BUF;
+      mbar_expect_tx(abar, bytes);
+#pragma unroll
+      for (int a = 0; a < NAUX; ++a)
+        if (epi_aux_ptr(ep, a, batch))
+          tma_load_2d(astage + a * C::AUX_BUF, &maps.aux[batch][a], abar, nb * BN + c * CW, mb * BM);
+    };
+    bool aux_pending = false;  // leader: an operand-tile load is in flight on abar
+    if constexpr (NAUX > 0) {
+      if (leader && static_cast<int>(blockIdx.x) < total) {
+        issue_aux(blockIdx.x, g);
+        aux_pending = true;
+      }
+    }
+
+    bool ok = true;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
       int split, batch, mb, nb;
       decode_tile(sh, tile, split, batch, mb, nb);
       const int buf = it & 1;
       const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
-      if (!mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE)) break;
+      const int m = mb * BM + row;
+      const RowIn ri = row_inputs<K>(ep, m);
+      bool present[NOUT];
+#pragma unroll
+      for (int o = 0; o < NOUT; ++o) present[o] = epi_out_ptr(ep, o, batch) != nullptr;
+      bool aux_present[NAUX > 0 ? NAUX : 1];
+#pragma unroll
+      for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, batch) != nullptr;
+
+      ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
       tc_fence_after();
-      const int m = mb * BM + row_in_tile;
-      const int n0 = nb * BN;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[NACC][32];
+      for (int c = g; c < NCH; c += 2) {
+        if constexpr (NAUX > 0) {
+          const bool landed = mbar_wait(abar, aph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
+          ok = landed && ok;
+          if (landed) {
+            aph ^= 1u;
+            aux_pending = false;
+          }
+        }
+        float v[NACC][CW];
 #pragma unroll
-        for (int a = 0; a < NACC; ++a) tmem_ld32(t_row + a * BN + c * 32, v[a]);
+        for (int a = 0; a < NACC; ++a) tmem_ld32(t_row + a * BN + c * CW, v[a]);
         tmem_ld_wait();
-        if (m < sh.M && n0 + c * 32 < sh.N) epi_apply<K, bf16, 32, NACC>(ep, batch, split, m, n0 + c * 32, v);
+        float av[NAUX > 0 ? NAUX : 1][CW];
+#pragma unroll
+        for (int a = 0; a < NAUX; ++a) {
+          if (aux_present[a]) {
+            const uint8_t* base = astage + a * C::AUX_BUF;
+#pragma unroll
+            for (int j = 0; j < CW / 8; ++j) load8(reinterpret_cast<const bf16*>(base + stage_off<64>(row, j)), &av[a][8 * j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < CW; ++j) av[a][j] = 0.f;
+          }
+        }
+        if (leader) bulk_wait_read_all();  // this group's previous stores have left the staging tiles
+        ok = named_bar_and(bar_id, 128, ok);
+        if (!ok) break;
+        if constexpr (NAUX > 0) {
+          if (leader) {
+            int nt = tile, nc = c + 2;
+            if (nc >= NCH) {
+              nt = tile + gridDim.x;
+              nc = g;
+            }
+            if (nt < total) {
+              issue_aux(nt, nc);
+              aux_pending = true;
+            }
+          }
+        }
+        float o[NOUT][CW];
+        float part = 0.f;
+        D::template run<bf16, CW>(ri, v, av, o, part);
+#pragma unroll
+        for (int oi = 0; oi < NOUT; ++oi) {
+          if (!present[oi]) continue;
+          uint8_t* base = ostage + oi * C::OUT_BUF;
+          if constexpr (D::OUT_F32) {
+#pragma unroll
+            for (int j = 0; j < CW / 4; ++j) {
+              *reinterpret_cast<float4*>(base + stage_off<128>(row, j)) =
+                  make_float4(o[oi][4 * j], o[oi][4 * j + 1], o[oi][4 * j + 2], o[oi][4 * j + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < CW / 8; ++j) store8(reinterpret_cast<bf16*>(base + stage_off<64>(row, j)), &o[oi][8 * j]);
+          }
+        }
+        if constexpr (D::ROWPART) {
+          const int n0c = nb * BN + c * CW;
+          if (m < sh.M && n0c < sh.N)
+            ep.rowpart[(static_cast<long long>(batch) * ep.rowpart_chunks + n0c / CW) * sh.M + m] = part;
+        }
+        fence_async_smem();
+        named_bar(bar_id, 128);
+        if (leader) {
+#pragma unroll
+          for (int oi = 0; oi < NOUT; ++oi) {
+            if (!present[oi]) continue;
+            if constexpr (D::OUT_F32)
+              tma_store_3d(&maps.out[batch][oi], ostage + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM, split);
+            else
+              tma_store_2d(&maps.out[batch][oi], ostage + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM);
+          }
+          bulk_commit();
+        }
       }
+      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+    if (leader) {
+      bulk_wait_all();
+      if (aux_pending) {  // abort path: let the last operand-tile load land before the CTA exits
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test(abar, aph) && global_timer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
     }
   }
 

@@ -1,10 +1,12 @@
-// Host launcher of the tcgen05 GEMM: builds the TMA tensor maps of each
-// operand and starts a persistent grid of at most one CTA per SM.
+// Host launcher of the tcgen05 GEMM: builds the TMA tensor maps of the
+// operands, of the epilogue's operand tiles and of its outputs, and starts a
+// persistent grid of at most one CTA per SM.
 #pragma once
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "gemm.h"
@@ -26,37 +28,56 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [outer, inner] array with row pitch ld elements, 128-byte swizzle.
-inline bool encode(CUtensorMap* m, const void* ptr, long long inner, long long outer, long long ld, int box_inner,
-                   int box_outer) {
+// Tiled map over a row-major array: dims[0] is the contiguous dimension; strides in elements.
+inline bool encode(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ptr, int rank,
+                   const long long* dims, const long long* strides, const int* box, CUtensorMapSwizzle swz) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = static_cast<cuuint64_t>(dims[i]);
+    bx[i] = static_cast<cuuint32_t>(box[i]);
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = static_cast<cuuint64_t>(strides[i]) * esize;
+  CUresult r = fn(m, dt, rank, const_cast<void*>(ptr), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// bf16 [outer, inner] with row pitch ld: mainloop operand tiles, 128-byte swizzle.
+inline bool encode_operand(CUtensorMap* m, const void* ptr, long long inner, long long outer, long long ld,
+                           int box_inner, int box_outer) {
+  const long long dims[2] = {inner, outer}, strides[1] = {ld};
+  const int box[2] = {box_inner, box_outer};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// bf16 [M, N] epilogue tile map (32 columns x 128 rows, 64-byte swizzle).
+inline bool encode_epi_bf16(CUtensorMap* m, const void* ptr, long long N, long long M, long long ld) {
+  const long long dims[2] = {N, M}, strides[1] = {ld};
+  const int box[2] = {CW, BM};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// fp32 [splits, M, N] partial-output map (32 columns x 128 rows x 1 split, 128-byte swizzle).
+inline bool encode_epi_f32(CUtensorMap* m, const void* ptr, long long N, long long M, long long ld, long long splits,
+                           long long split_stride) {
+  const long long dims[3] = {N, M, splits}, strides[2] = {ld, split_stride};
+  const int box[3] = {CW, BM, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace umma
 
-template <EpiKind K, int BN, int NACC, bool A_MN, bool B_MN>
+template <EpiKind K, int BN, bool A_MN, bool B_MN>
 cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   using namespace umma;
-  using C = Config<BN, NACC>;
+  using C = Config<K, BN>;
+  using D = EpiDef<K>;
+  constexpr int NACC = D::NACC;
   Maps maps;
   memset(&maps, 0, sizeof(maps));
-  const int nsets = NACC > 1 ? NACC : g.batches;
-  for (int i = 0; i < nsets; ++i) {
-    const bool okA = A_MN ? encode(&maps.a[i], g.A[i].ptr, g.M, g.K, g.A[i].ld, 64, 64)
-                          : encode(&maps.a[i], g.A[i].ptr, g.K, g.M, g.A[i].ld, 64, BM);
-    const bool okB = B_MN ? encode(&maps.b[i], g.B[i].ptr, g.N, g.K, g.B[i].ld, 64, 64)
-                          : encode(&maps.b[i], g.B[i].ptr, g.K, g.N, g.B[i].ld, 64, BN);
-    if (!okA || !okB) return cudaErrorInvalidValue;
-  }
   Shape sh;
   sh.M = g.M;
   sh.N = g.N;
@@ -69,12 +90,40 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.kb_per_split = (sh.kb_total + ks - 1) / ks;
   sh.ksplit = (sh.kb_total + sh.kb_per_split - 1) / sh.kb_per_split;  // no empty split
   sh.err = g.err;
+
+  const int nsets = NACC > 1 ? NACC : g.batches;
+  for (int i = 0; i < nsets; ++i) {
+    const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, g.M, g.K, g.A[i].ld, 64, 64)
+                          : encode_operand(&maps.a[i], g.A[i].ptr, g.K, g.M, g.A[i].ld, 64, BM);
+    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, g.N, g.K, g.B[i].ld, 64, 64)
+                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, g.N, g.B[i].ld, 64, BN);
+    if (!okA || !okB) return cudaErrorInvalidValue;
+  }
+  const void* const* outs[3] = {g.ep.out0, g.ep.out1, g.ep.out2};
+  const long long ldo[3] = {g.ep.ldo0, g.ep.ldo1, g.ep.ldo2};
+  const void* const* auxs[2] = {g.ep.aux0, g.ep.aux1};
+  const long long lda[2] = {g.ep.lda0, g.ep.lda1};
+  for (int b = 0; b < sh.batches; ++b) {
+    for (int o = 0; o < D::NOUT; ++o) {
+      const void* p = outs[o][b];
+      if (!p) continue;
+      const bool ok = D::OUT_F32 ? encode_epi_f32(&maps.out[b][o], p, g.N, g.M, ldo[o], sh.ksplit, g.ep.split_stride)
+                                 : encode_epi_bf16(&maps.out[b][o], p, g.N, g.M, ldo[o]);
+      if (!ok) return cudaErrorInvalidValue;
+    }
+    for (int a = 0; a < D::NAUX; ++a) {
+      const void* p = auxs[a][b];
+      if (!p) continue;
+      if (!encode_epi_bf16(&maps.aux[b][a], p, g.N, g.M, lda[a])) return cudaErrorInvalidValue;
+    }
+  }
+
   const long long total = 1LL * sh.ksplit * sh.batches * sh.m_tiles * sh.n_tiles;
   if (total <= 0) return cudaSuccess;
   const int sms = device_sm_count();
   const int grid = static_cast<int>(total < sms ? total : sms);
 
-  auto kern = gemm_kernel<K, BN, NACC, A_MN, B_MN>;
+  auto kern = gemm_kernel<K, BN, A_MN, B_MN>;
   static int configured_mask = 0;  // one bit per device ordinal
   int dev = 0;
   cudaGetDevice(&dev);
