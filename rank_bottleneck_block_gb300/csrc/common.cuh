@@ -51,7 +51,9 @@ struct EpiParams {
   int rowpart_chunks;             // chunks per batch entry = ceil(N / chunk width)
   const float* rowpart_in;        // [rowpart_in_chunks][M] (read, summed in order)
   int rowpart_in_chunks;
-  float coef;                     // 1/d for the RMSNorm backward
+  float coef;                     // 1/d (RMSNorm forward statistics and backward)
+  float eps;                      // RMSNorm epsilon (forward statistics)
+  float* rowscale_out;            // s[m] written by the GEMM that computes it (online RMSNorm), or null
   long long split_stride;         // elements between split-K partial outputs
 };
 

@@ -228,7 +228,12 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   if (g.ksplit < 1) g.ksplit = 1;
   g.ep.M = g.M;
   g.ep.N = g.N;
-  g.bn = (c.dt == LR_BF16) ? ((k == EPI_SWIGLU) ? 128 : pick_bn(g, c.sms)) : 0;
+  if (c.dt == LR_BF16) {
+    if (k == EPI_SWIGLU) g.bn = 128;
+    else if (g.bn != 128 && g.bn != 256) g.bn = pick_bn(g, c.sms);
+  } else {
+    g.bn = 0;
+  }
   std::string name = std::string(c.dt == LR_BF16 ? "umma_" : "simt_") + epi_name(k);
   if (g.bn) name += "_bn" + std::to_string(g.bn);
   const double flops = 2.0 * g.M * g.N * static_cast<double>(g.K) * g.nacc * g.batches;
@@ -256,23 +261,49 @@ static inline const void* off(const void* p, size_t bytes) { return static_cast<
 static inline void* off(void* p, size_t bytes) { return static_cast<char*>(p) + bytes; }
 
 // --------------------------------------------------- weight gradients
-// Split factor of a weight-gradient GEMM (K = tokens): enough CTAs to fill the
-// GPU, at least 8 k-blocks per split, at most 8 splits.  Device-independent upper
-// bound (used for workspace sizing): min(8, max(1, kb / 8)).
+// A weight gradient is dW = X^T dY over K = tokens: a small output with a long
+// reduction.  The planner picks the tile width (128 or 256) and a split of K
+// over CTAs from a cost model: waves of persistent tiles times the per-tile
+// MMA work, plus the fp32 partial traffic of the fixed-order reduction.  At
+// most 8 splits, each at least 8 k-blocks long; the device-independent bound
+// min(8, max(1, kb / 8)) sizes the workspace.
 static int wgrad_split_bound(int K) {
   const int kb = (K + 63) / 64;
   return std::max(1, std::min(8, kb / 8));
 }
 
-static int wgrad_split(const Ctx& c, int M, int N, int K) {
-  if (c.dt != LR_BF16) return 1;
-  const int bn = N <= 128 ? 128 : 256;
-  const long long tiles = 1LL * ((M + 127) / 128) * ((N + bn - 1) / bn);
-  int ks = static_cast<int>(std::max<long long>(1, c.sms / std::max<long long>(1, tiles)));
-  ks = std::min(ks, wgrad_split_bound(K));
+struct WgradPlan {
+  int bn, ksplit;
+};
+
+static int normalise_split(int K, int ks) {
   const int kb = (K + 63) / 64;
   const int per = (kb + ks - 1) / ks;
   return (kb + per - 1) / per;
+}
+
+static WgradPlan wgrad_plan(const Ctx& c, int M, int N, int K, bool needs_pass) {
+  if (c.dt != LR_BF16) return {0, 1};
+  const double per_sm_flops = 2.25e15 / 152.0 * 0.65;  // sustained MMA rate per SM (relative units suffice)
+  const double reduce_bw = 4.0e12;                       // bytes/s of the partial reduction
+  WgradPlan best{256, 1};
+  double best_t = 1e30;
+  for (int bn : {256, 128}) {
+    const long long tiles = 1LL * ((M + 127) / 128) * ((N + bn - 1) / bn);
+    for (int ks = 1; ks <= wgrad_split_bound(K); ++ks) {
+      const int ksn = normalise_split(K, ks);
+      if (ksn != ks) continue;
+      const long long waves = (tiles * ks + c.sms - 1) / c.sms;
+      const double tile_t = 2.0 * 128 * bn * (static_cast<double>(K) / ks) / per_sm_flops * (bn == 128 ? 1.15 : 1.0);
+      double t = waves * tile_t;
+      if (ks > 1 || needs_pass) t += (static_cast<double>(ks) + 1.0) * M * N * 4.0 / reduce_bw;
+      if (t < best_t * 0.98) {
+        best_t = t;
+        best = {bn, ks};
+      }
+    }
+  }
+  return best;
 }
 
 static size_t wgrad_part_bytes(lr_dtype dt, int M, int N, int K) {
@@ -282,18 +313,24 @@ static size_t wgrad_part_bytes(lr_dtype dt, int M, int N, int K) {
 
 // dst = (A^T B) over K tokens, both operands stored [K, .] row-major (MN-major),
 // reduced over splits in a fixed order, times the optional column scale, and the
-// optional dg partial sums over row blocks.
+// optional dg partial sums over row blocks.  Without a split, a scale or dg, the
+// GEMM writes the fp32 result straight into the single destination.
 static lr_status wgrad(const Ctx& c, int M, int N, int K, Operand A, Operand B, WgradDst dst, int rows_each,
                        const void* colscale, float* dgpart, float* wpart) {
+  const bool needs_pass = colscale != nullptr || dgpart != nullptr || rows_each != M;
+  const WgradPlan plan = wgrad_plan(c, M, N, K, needs_pass);
   GemmCall g = new_call(M, N, K);
   g.a_mn = g.b_mn = true;
   g.A[0] = A;
   g.B[0] = B;
-  g.ksplit = wgrad_split(c, M, N, K);
-  g.ep.out0[0] = wpart;
+  g.bn = plan.bn;
+  g.ksplit = plan.ksplit;
+  const bool direct = !needs_pass && plan.ksplit == 1;
+  g.ep.out0[0] = direct ? static_cast<void*>(dst.dst[0]) : static_cast<void*>(wpart);
   g.ep.ldo0 = N;
   g.ep.split_stride = 1LL * M * N;
   LR_TRY(gemm(c, EPI_F32, g));
+  if (direct) return LR_OK;
   LaunchScope scope("wgrad_reduce", c.st, 0, 4.0 * g.ksplit * M * N + 4.0 * M * N);
   cudaError_t e = (c.dt == LR_BF16)
                       ? launch_wgrad_reduce<bf16>(wpart, g.ksplit, 1LL * M * N, M, N,
@@ -466,9 +503,10 @@ static lr_status mlp_fwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
   // Online-RMSNorm (technical summary §2.2): gain folded into the stacked [A_gate; A_up] ...
   StackSrc src = {{gate.A, up.A, nullptr}};
   LR_TRY(fold(c, W.Af, src, 2, r, d, g));
-  // ... 1/rms per row ...
-  LR_TRY(rstd(c, x, T, d, eps, S.s));
-  // ... applied as a row scale in the grouped gate/up GEMM's epilogue, with SiLU fused.
+  // ... the row sum of squares of x accumulated in the same pass as the grouped gate/up GEMM
+  // (tcgen05 path: statistics warps read the x tiles of the GEMM's own shared-memory ring;
+  // fp32 path: a separate row pass), and 1/rms applied as a row scale in its epilogue, SiLU fused.
+  if (c.dt != LR_BF16) LR_TRY(rstd(c, x, T, d, eps, S.s));
   {
     GemmCall k = new_call(T, 2 * r, d);
     k.A[0] = {x, d};
@@ -477,6 +515,9 @@ static lr_status mlp_fwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.out1[0] = z_gu;
     k.ep.ldo0 = k.ep.ldo1 = 2 * r;
     k.ep.rowscale = S.s;
+    k.ep.rowscale_out = S.s;
+    k.ep.coef = 1.f / static_cast<float>(d);
+    k.ep.eps = eps;
     LR_TRY(gemm(c, EPI_NORM_SILU, k));
   }
   // B_gate / B_up with the SwiGLU product fused.
@@ -679,7 +720,7 @@ static lr_status proj_fwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
   StackSrc src = {{nullptr, nullptr, nullptr}};
   for (int i = 0; i < group; ++i) src.src[i] = pairs[i].A;
   LR_TRY(fold(c, W.Af, src, group, r, d_in, g));
-  if (norm) LR_TRY(rstd(c, x, T, d_in, eps, S.s));
+  if (norm && c.dt != LR_BF16) LR_TRY(rstd(c, x, T, d_in, eps, S.s));
   {
     GemmCall k = new_call(T, group * r, d_in);
     k.A[0] = {x, d_in};
@@ -688,6 +729,9 @@ static lr_status proj_fwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
     k.ep.out1[0] = S.z;
     k.ep.ldo0 = k.ep.ldo1 = 1LL * group * r;
     k.ep.rowscale = S.s;
+    k.ep.rowscale_out = S.s;
+    k.ep.coef = 1.f / static_cast<float>(d_in);
+    k.ep.eps = eps;
     LR_TRY(gemm(c, norm ? EPI_NORM_SILU : EPI_SILU, k));
   }
   {

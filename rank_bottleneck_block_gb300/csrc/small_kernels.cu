@@ -5,23 +5,30 @@ namespace lr {
 // ------------------------------------------------------------------ fold
 template <typename ST>
 __global__ void fold_kernel(ST* out, StackSrc src, int rows_each, int rows, int cols, const ST* g) {
-  const long long total = 1LL * rows * cols;
+  const int groups = cols / 8;
+  const long long total = 1LL * rows * groups;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
-    const int r = static_cast<int>(i / cols), c = static_cast<int>(i % cols);
-    const ST* s = static_cast<const ST*>(src.src[r / rows_each]);
-    float v = static_cast<float>(s[static_cast<long long>(r % rows_each) * cols + c]);
-    if (g) v *= static_cast<float>(g[c]);
-    out[i] = static_cast<ST>(v);
+    const int r = static_cast<int>(i / groups), c = static_cast<int>(i % groups) * 8;
+    const ST* s = static_cast<const ST*>(src.src[r / rows_each]) + static_cast<long long>(r % rows_each) * cols;
+    float v[8];
+    load8(s + c, v);
+    if (g) {
+      float gv[8];
+      load8(g + c, gv);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v[t] *= gv[t];
+    }
+    store8(out + static_cast<long long>(r) * cols + c, v);
   }
 }
 
 template <typename ST>
 cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols, const ST* g, cudaStream_t st) {
   const int rows = nsrc * rows_each;
-  const long long total = 1LL * rows * cols;
+  const long long total = 1LL * rows * (cols / 8);
   if (total == 0) return cudaSuccess;
   int blocks = static_cast<int>((total + 255) / 256);
-  if (blocks > 4096) blocks = 4096;
+  if (blocks > 8192) blocks = 8192;
   fold_kernel<ST><<<blocks, 256, 0, st>>>(out, src, rows_each, rows, cols, g);
   return cudaGetLastError();
 }
@@ -80,32 +87,51 @@ cudaError_t launch_silu(const ST* u, long long ldu, ST* z, long long ldz, int T,
 }
 
 // ---------------------------------------------------------- wgrad reduce
+// One thread per 4 consecutive columns of kReduceRows rows; splits summed in order.
 template <typename ST>
 __global__ void wgrad_reduce_kernel(const float* part, int nsplit, long long split_stride, int M, int N,
                                     const ST* colscale, WgradDst dst, int rows_each, float* dgpart) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (n >= N) return;
   const int r0 = blockIdx.y * kReduceRows;
   const int r1 = min(M, r0 + kReduceRows);
-  const float cs = colscale ? static_cast<float>(colscale[n]) : 1.f;
-  float dga = 0.f;
+  float cs[4] = {1.f, 1.f, 1.f, 1.f};
+  if (colscale) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) cs[t] = static_cast<float>(colscale[n + t]);
+  }
+  float dga[4] = {0.f, 0.f, 0.f, 0.f};
   for (int m = r0; m < r1; ++m) {
     const long long idx = static_cast<long long>(m) * N + n;
-    float v = 0.f;
-    for (int s = 0; s < nsplit; ++s) v += part[s * split_stride + idx];
+    float4 v = *reinterpret_cast<const float4*>(part + idx);
+    for (int s = 1; s < nsplit; ++s) {
+      const float4 w = *reinterpret_cast<const float4*>(part + s * split_stride + idx);
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
     const int blk = m / rows_each;
     const long long local = static_cast<long long>(m - blk * rows_each) * N + n;
-    dst.dst[blk][local] = v * cs;
-    if (dgpart) dga = fmaf(v, static_cast<float>(static_cast<const ST*>(dst.aw[blk])[local]), dga);
+    *reinterpret_cast<float4*>(dst.dst[blk] + local) = make_float4(v.x * cs[0], v.y * cs[1], v.z * cs[2], v.w * cs[3]);
+    if (dgpart) {
+      const ST* aw = static_cast<const ST*>(dst.aw[blk]) + local;
+      dga[0] = fmaf(v.x, static_cast<float>(aw[0]), dga[0]);
+      dga[1] = fmaf(v.y, static_cast<float>(aw[1]), dga[1]);
+      dga[2] = fmaf(v.z, static_cast<float>(aw[2]), dga[2]);
+      dga[3] = fmaf(v.w, static_cast<float>(aw[3]), dga[3]);
+    }
   }
-  if (dgpart) dgpart[static_cast<long long>(blockIdx.y) * N + n] = dga;
+  if (dgpart)
+    *reinterpret_cast<float4*>(dgpart + static_cast<long long>(blockIdx.y) * N + n) =
+        make_float4(dga[0], dga[1], dga[2], dga[3]);
 }
 
 template <typename ST>
 cudaError_t launch_wgrad_reduce(const float* part, int nsplit, long long split_stride, int M, int N,
                                 const ST* colscale, WgradDst dst, int rows_each, float* dgpart, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
-  dim3 grid((N + 127) / 128, (M + kReduceRows - 1) / kReduceRows);
+  dim3 grid((N / 4 + 127) / 128, (M + kReduceRows - 1) / kReduceRows);
   wgrad_reduce_kernel<ST><<<grid, 128, 0, st>>>(part, nsplit, split_stride, M, N, colscale, dst, rows_each, dgpart);
   return cudaGetLastError();
 }

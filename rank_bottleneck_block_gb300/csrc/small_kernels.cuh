@@ -38,7 +38,7 @@ cudaError_t launch_silu(const ST* u, long long ldu, ST* z, long long ldz, int T,
 template <typename ST>
 cudaError_t launch_wgrad_reduce(const float* part, int nsplit, long long split_stride, int M, int N,
                                 const ST* colscale, WgradDst dst, int rows_each, float* dgpart, cudaStream_t st);
-constexpr int kReduceRows = 32;
+constexpr int kReduceRows = 8;
 
 // dg[n] = sum_p dgpart[p, n].
 cudaError_t launch_dg_finalize(const float* dgpart, int nparts, int N, float* dg, cudaStream_t st);

@@ -247,7 +247,10 @@ struct Config {
   static constexpr int AUX_BUF = BM * CW * 2;
   static constexpr int GROUP_BYTES = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;
   static constexpr int EPI_BYTES = 2 * GROUP_BYTES;
-  static constexpr int BAR_BYTES = 256;
+  // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
+  static constexpr bool STATS = (K == EPI_NORM_SILU);
+  static constexpr int THREADS = kThreads + (STATS ? 128 : 0);
+  static constexpr int BAR_BYTES = 256 + 1024;  // barriers, then s for two tiles of 128 rows
   static constexpr int RING_BUDGET = kMaxSmem - 1024 - EPI_BYTES - BAR_BYTES;
   static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
   static constexpr uint32_t ACC_COLS = NACC * BN;
@@ -276,7 +279,7 @@ __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int& spli
 }
 
 template <EpiKind K, int BN, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     gemm_kernel(const __grid_constant__ Maps maps, const Shape sh, const EpiParams ep) {
   using C = Config<K, BN>;
   using D = EpiDef<K>;
@@ -295,8 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* aux_full = drain + 1;  // one per epilogue group
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_full + 2);
+  uint64_t* sfull = aux_full + 2;   // stats -> epilogue, per TMEM buffer
+  uint64_t* sempty = sfull + 2;     // epilogue -> stats, per TMEM buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_rows = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);  // [2][BM]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -304,12 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], C::STATS ? 1 + 4 : 1);  // MMA commit (+ one arrive per stats warp)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kEpiWarps);  // one arrive per epilogue warp
       mbar_init(&aux_full[i], 1);
+      mbar_init(&sfull[i], 4);
+      mbar_init(&sempty[i], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -441,6 +449,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_test(drain, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
       }
     }
+  } else if (C::STATS && warp >= 2 + kEpiWarps) {
+    // ------------------------------------------------ online-RMSNorm statistics warps
+    // Row r of the x tile is 128 bytes per stage with its 16-byte chunks permuted by the
+    // swizzle; a sum of squares over the whole row does not depend on that order, and
+    // reading logical chunk j at physical position j ^ (r & 7) keeps the 8-thread phases
+    // of each 16-byte shared load on distinct banks.
+    const int row = (warp - 2 - kEpiWarps) * 32 + lane;
+    int st = 0;
+    uint32_t ph = 0;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      int split, batch, mb, nb;
+      decode_tile(sh, tile, split, batch, mb, nb);
+      const int kb0 = split * sh.kb_per_split;
+      const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
+      float ss = 0.f;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* a_row = sA + st * C::A_BYTES + row * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float v[8];
+          load8(reinterpret_cast<const bf16*>(a_row + ((j ^ (row & 7)) << 4)), v);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) ss = fmaf(v[t], v[t], ss);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (++st == STAGES) {
+          st = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      const float s_val = rsqrtf(ss * ep.coef + ep.eps);
+      const int m = mb * BM + row;
+      if (nb == 0 && m < sh.M && ep.rowscale_out) ep.rowscale_out[m] = s_val;
+      const int buf = it & 1;
+      const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
+      if (!mbar_wait(&sempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE)) break;
+      s_rows[buf * BM + row] = s_val;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfull[buf]);
+    }
   } else {
     // ------------------------------------------------ epilogue warps
     constexpr int NAUX = D::NAUX, NOUT = D::NOUT;
@@ -485,7 +541,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = it & 1;
       const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
       const int m = mb * BM + row;
-      const RowIn ri = row_inputs<K>(ep, m);
+      RowIn ri;
+      if constexpr (C::STATS) {
+        ri.k = 0.f;
+        ok = mbar_wait(&sfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
+        ri.s = s_rows[buf * BM + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[buf]);
+      } else {
+        ri = row_inputs<K>(ep, m);
+      }
       bool present[NOUT];
 #pragma unroll
       for (int o = 0; o < NOUT; ++o) present[o] = epi_out_ptr(ep, o, batch) != nullptr;
@@ -493,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, batch) != nullptr;
 
-      ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
+      ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
 #pragma unroll 1

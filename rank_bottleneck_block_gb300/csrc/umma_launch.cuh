@@ -132,7 +132,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
-  kern<<<grid, kThreads, C::SMEM_BYTES, st>>>(maps, sh, g.ep);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(maps, sh, g.ep);
   return cudaGetLastError();
 }
 
