@@ -294,6 +294,113 @@ def run_ours(a, ws, rank, local):
         print(json.dumps(res), flush=True)
 
 
+# ---------------------------------------------------- other workloads
+def _time_steps(step, steps, warmup, flush, stream):
+    import torch
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(s.elapsed_time(e) for s, e in evs) / steps
+
+
+def _proj_flops_bytes(T, d_in, d_out, r, group, norm):
+    f = 3.0 * 2.0 * T * r * (d_in + d_out) * group
+    params = group * r * (d_in + d_out)
+    b = 2.0 * T * d_in * 2 + 2.0 * T * d_out * group * 2  # x read, dx written; outs written, douts read
+    b += 2.0 * params + 4.0 * params + (6.0 * d_in if norm else 0.0)
+    b += (2.0 * T * group * r * 2 + (4.0 * T if norm else 0.0)) * 2  # saved u, z written and read
+    return f, b
+
+
+def _roofline(flops, nbytes, ms, pk):
+    t_nom = max(flops / (NOMINAL["tflops"] * 1e12), nbytes / (NOMINAL["hbm_gbs"] * 1e9))
+    t_meas = max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+    return {"tflops": round(flops / (ms / 1e3) / 1e12, 1), "roofline_ms_nominal": round(t_nom * 1e3, 4),
+            "frac_nominal": round(t_nom / (ms / 1e3), 4), "frac_measured": round(t_meas / (ms / 1e3), 4),
+            "bound": "tensor" if flops / (NOMINAL["tflops"] * 1e12) >= nbytes / (NOMINAL["hbm_gbs"] * 1e9) else "hbm"}
+
+
+def run_other(a):
+    """Non-default workloads (one JSON line each): attn_proj, stack, sweep."""
+    import torch
+
+    from rank_bottleneck_block_gb300 import build as B
+
+    B.build()
+    from rank_bottleneck_block_gb300 import inputs as I
+    from rank_bottleneck_block_gb300 import lowrank as L
+    from rank_bottleneck_block_gb300.runner import BlockStack, ProjGroup
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    pk = peaks()
+    if a.workload == "attn_proj":
+        qkv = ProjGroup(I.ATTN_PROJ_BF16, I.make_proj_case(I.ATTN_PROJ_BF16, seed=0, device="cuda"))
+        o = ProjGroup(I.ATTN_OPROJ_BF16, I.make_proj_case(I.ATTN_OPROJ_BF16, seed=1, device="cuda"))
+
+        def step():
+            qkv.step()
+            o.step()
+
+        ms = _time_steps(step, a.steps, a.warmup, flush, stream)
+        L.lr_check_device_error()
+        f1, b1 = _proj_flops_bytes(16384, 4096, 4096, 1024, 3, True)
+        f2, b2 = _proj_flops_bytes(16384, 4096, 4096, 1024, 1, False)
+        res = {"workload": "low-rank attention projections fwd+bwd: q/k/v group (3 pairs, r 1024, d 4096, RMSNorm) "
+                           "+ o-projection (1 pair, no norm), T 16384", "ms_per_step": round(ms, 4),
+               "tokens_per_s": round(16384 / (ms / 1e3), 1), **_roofline(f1 + f2, b1 + b2, ms, pk)}
+        print(json.dumps(res), flush=True)
+    elif a.workload == "stack":
+        shape = I.MLP_BLOCK_BF16
+        case = I.make_stack_case(shape, blocks=24, seed=0, device="cuda")
+        out = {"workload": "24 residual low-rank SwiGLU MLP blocks (T 16384, d 2048, f 5632, r 512) + MSE, one "
+                           "training step"}
+        for mode, name in ((L.LR_SAVE_CKPT, "ckpt"), (L.LR_SAVE_FULL, "full")):
+            torch.cuda.reset_peak_memory_stats(dev)
+            base = torch.cuda.memory_allocated(dev)
+            st = BlockStack(shape, case, mode, device=dev)
+            ms = _time_steps(st.step, a.steps, a.warmup, flush, stream)
+            L.lr_check_device_error()
+            peak = torch.cuda.max_memory_allocated(dev) - base
+            ws = L.lr_stack_workspace_bytes(L.LR_BF16, mode, 24, shape.T, shape.d, shape.f, shape.r)
+            fl = 24 * (3.0 * 2.0 * shape.T * (2 * shape.r * shape.d + 2 * shape.f * shape.r + shape.r * shape.f +
+                                              shape.d * shape.r) + (4.0 * shape.T * shape.r * shape.f if name == "ckpt"
+                                                                    else 0.0))
+            nb = 24 * 4.4e8
+            out[name] = {"ms_per_step": round(ms, 3), "tokens_per_s": round(shape.T / (ms / 1e3), 1),
+                         "workspace_bytes": ws, "peak_hbm_bytes": int(peak), "loss": st.loss.item(),
+                         **_roofline(fl, nb, ms, pk)}
+            del st
+            torch.cuda.empty_cache()
+        print(json.dumps(out), flush=True)
+    elif a.workload == "sweep":
+        rows = []
+        for shp in I.sweep_shapes():
+            pg = ProjGroup(shp, I.make_proj_case(shp, seed=0, device="cuda"))
+            ms = _time_steps(pg.step, a.steps, a.warmup, flush, stream)
+            L.lr_check_device_error()
+            f, b = _proj_flops_bytes(shp.T, shp.d_in, shp.d_out, shp.r, shp.group, False)
+            rows.append({"d": shp.d_in, "r": shp.r, "T": shp.T, "group": shp.group, "ms": round(ms, 4),
+                         **_roofline(f, b, ms, pk)})
+            print(json.dumps(rows[-1]), flush=True)
+            del pg
+            torch.cuda.empty_cache()
+        fr = [r["frac_nominal"] for r in rows]
+        print(json.dumps({"workload": "grouped low-rank GEMM-pair sweep, 144 shapes, fwd+bwd",
+                          "frac_nominal_min": min(fr), "frac_nominal_median": statistics.median(fr),
+                          "frac_nominal_max": max(fr), "shapes_at_or_above_0.6": sum(x >= 0.6 for x in fr)}),
+              flush=True)
+
+
 # --------------------------------------------------------- reference arm
 def run_reference(a, ws, rank):
     if rank != 0:
@@ -333,12 +440,17 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["mlp_block", "attn_proj", "stack", "sweep"], default="mlp_block",
+                    help="mlp_block is the benchmark line; the others print their own measurement lines")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_setup()
     if a.impl == "reference":
         run_reference(a, ws, rank)
+    elif a.workload != "mlp_block":
+        if rank == 0:
+            run_other(a)
     else:
         run_ours(a, ws, rank, local)
     if ws > 1:

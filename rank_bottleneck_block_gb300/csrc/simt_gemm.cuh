@@ -18,7 +18,7 @@ struct Args {
   int M, N, K, batches, ksplit, k_per_split;
   const float* A[kMaxBatch];
   const float* B[kMaxBatch];
-  long long a_sm, a_sk, b_sn, b_sk;  // element strides along m / k and n / k
+  long long a_sm[kMaxBatch], a_sk[kMaxBatch], b_sn[kMaxBatch], b_sk[kMaxBatch];  // per operand set: m / k, n / k
 };
 
 template <EpiKind K>
@@ -49,12 +49,12 @@ __global__ void __launch_bounds__(256) gemm_kernel(const Args a, const EpiParams
       for (int i = tid; i < TM * TK; i += 256) {
         const int r = i / TK, k = i % TK;
         const int m = m0 + r, kk = k0 + k;
-        As[k][r] = (m < a.M && kk < kend) ? A[m * a.a_sm + kk * a.a_sk] : 0.f;
+        As[k][r] = (m < a.M && kk < kend) ? A[m * a.a_sm[set] + kk * a.a_sk[set]] : 0.f;
       }
       for (int i = tid; i < TN * TK; i += 256) {
         const int c = i / TK, k = i % TK;
         const int n = n0 + c, kk = k0 + k;
-        Bs[k][c] = (n < a.N && kk < kend) ? B[n * a.b_sn + kk * a.b_sk] : 0.f;
+        Bs[k][c] = (n < a.N && kk < kend) ? B[n * a.b_sn[set] + kk * a.b_sk[set]] : 0.f;
       }
       __syncthreads();
 #pragma unroll
@@ -112,12 +112,11 @@ cudaError_t launch_simt(const GemmCall& g, cudaStream_t st) {
   for (int i = 0; i < nsets; ++i) {
     a.A[i] = static_cast<const float*>(g.A[i].ptr);
     a.B[i] = static_cast<const float*>(g.B[i].ptr);
+    a.a_sm[i] = g.a_mn ? 1 : g.A[i].ld;
+    a.a_sk[i] = g.a_mn ? g.A[i].ld : 1;
+    a.b_sn[i] = g.b_mn ? 1 : g.B[i].ld;
+    a.b_sk[i] = g.b_mn ? g.B[i].ld : 1;
   }
-  // All entries share one layout and leading dimension per operand.
-  a.a_sm = g.a_mn ? 1 : g.A[0].ld;
-  a.a_sk = g.a_mn ? g.A[0].ld : 1;
-  a.b_sn = g.b_mn ? 1 : g.B[0].ld;
-  a.b_sk = g.b_mn ? g.B[0].ld : 1;
   dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, a.batches * a.ksplit);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   gemm_kernel<K><<<grid, 256, 0, st>>>(a, g.ep);

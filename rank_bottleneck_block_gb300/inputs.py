@@ -12,10 +12,12 @@ shapes stand in for them):
 * RMSNorm gain ``g`` = 1 + N(0, 0.1) (0.1 is the standard deviation);
 * each low-rank pair: ``A`` [r, d_in] ~ N(0, 1/d_in), ``B`` [d_out, r] ~ N(0, 1/r)
   (N(0, 1/fan_in) for both factors);
-* draws are fp32 from one ``torch.Generator('cpu')`` per case, in a fixed
-  order (x, g, then each pair's A and B, then gradients / targets), and are then
-  rounded once to the case's storage dtype.  Both sides read the rounded values;
-  the oracle widens them exactly to fp64.
+* draws are fp32 from one ``torch.Generator`` per case, in a fixed order (x, g,
+  then each pair's A and B, then gradients / targets), and are then rounded once
+  to the case's storage dtype.  Both sides read the rounded values; the oracle
+  widens them exactly to fp64.  Parity cases draw on the CPU; timing-only
+  workloads may draw on the GPU (``device=``), which gives other values of the
+  same distribution.
 """
 from __future__ import annotations
 
@@ -92,7 +94,7 @@ def _torch_dtype(name: str) -> torch.dtype:
 
 
 def _normal(gen: torch.Generator, shape, std: float, mean: float = 0.0) -> torch.Tensor:
-    t = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    t = torch.randn(*shape, generator=gen, dtype=torch.float32, device=gen.device)
     if std != 1.0:
         t = t * std
     if mean != 0.0:
@@ -106,10 +108,10 @@ def _pair(gen: torch.Generator, r: int, d_in: int, d_out: int, dt: torch.dtype):
     return A, B
 
 
-def make_mlp_case(shape: MlpShape, seed: int = 0, with_grad: bool = True) -> Dict[str, torch.Tensor]:
+def make_mlp_case(shape: MlpShape, seed: int = 0, with_grad: bool = True, device: str = "cpu") -> Dict[str, torch.Tensor]:
     """Host tensors for one MLP block: x, g, A/B of gate, up, down, and upstream grad G."""
     dt = _torch_dtype(shape.dtype)
-    gen = torch.Generator(device="cpu")
+    gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     c: Dict[str, torch.Tensor] = {}
     c["x"] = _normal(gen, (shape.T, shape.d), 1.0).to(dt)
@@ -122,10 +124,10 @@ def make_mlp_case(shape: MlpShape, seed: int = 0, with_grad: bool = True) -> Dic
     return c
 
 
-def make_proj_case(shape: ProjShape, seed: int = 0, with_grad: bool = True) -> Dict[str, object]:
+def make_proj_case(shape: ProjShape, seed: int = 0, with_grad: bool = True, device: str = "cpu") -> Dict[str, object]:
     """Host tensors for a projection group: x, optional g, pairs, and one upstream grad per pair."""
     dt = _torch_dtype(shape.dtype)
-    gen = torch.Generator(device="cpu")
+    gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     c: Dict[str, object] = {}
     c["x"] = _normal(gen, (shape.T, shape.d_in), 1.0).to(dt)
@@ -141,10 +143,10 @@ def make_proj_case(shape: ProjShape, seed: int = 0, with_grad: bool = True) -> D
     return c
 
 
-def make_stack_case(shape: MlpShape, blocks: int, seed: int = 0) -> Dict[str, object]:
+def make_stack_case(shape: MlpShape, blocks: int, seed: int = 0, device: str = "cpu") -> Dict[str, object]:
     """Host tensors for a residual stack of MLP blocks trained against an MSE target."""
     dt = _torch_dtype(shape.dtype)
-    gen = torch.Generator(device="cpu")
+    gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     c: Dict[str, object] = {}
     c["x"] = _normal(gen, (shape.T, shape.d), 1.0).to(dt)
