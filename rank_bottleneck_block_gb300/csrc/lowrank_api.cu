@@ -161,13 +161,20 @@ struct Ctx {
   int chunk;  // row-partial chunk width of the engine
 };
 
+// Tile width of the SwiGLU dual GEMM (two accumulators: 256 fills TMEM with one buffer,
+// 128 keeps two buffers).
+static constexpr int kSwigluBn = 128;
+
+// Tile width from waves of pair tiles (256 rows, one per SM pair); a 128-wide tile costs
+// about 0.75 of a 256-wide one (its shared-memory traffic per FLOP is 1.5x higher).
 static int pick_bn(const GemmCall& g, int sms) {
   if (g.N <= 128) return 128;
-  const long long mt = (g.M + 127) / 128;
-  const long long t256 = mt * ((g.N + 255) / 256) * g.batches * std::max(1, g.ksplit);
-  const long long t128 = mt * ((g.N + 127) / 128) * g.batches * std::max(1, g.ksplit);
-  const double c256 = static_cast<double>((t256 + sms - 1) / sms);
-  const double c128 = 0.55 * static_cast<double>((t128 + sms - 1) / sms);
+  const long long slots = std::max(1, sms / 2);
+  const long long mp = (g.M + 255) / 256;
+  const long long t256 = mp * ((g.N + 255) / 256) * g.batches * std::max(1, g.ksplit);
+  const long long t128 = mp * ((g.N + 127) / 128) * g.batches * std::max(1, g.ksplit);
+  const double c256 = static_cast<double>((t256 + slots - 1) / slots);
+  const double c128 = 0.75 * static_cast<double>((t128 + slots - 1) / slots);
   return c128 < c256 ? 128 : 256;
 }
 
@@ -188,7 +195,9 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
       if (km) return umma_bn<EPI_STORE, false, true>(g, st);
       break;
     case EPI_RESID: if (kk) return umma_bn<EPI_RESID, false, false>(g, st); break;
-    case EPI_SWIGLU: if (kk && g.nacc == 2) return launch_umma<EPI_SWIGLU, 128, false, false>(g, st); break;
+    case EPI_SWIGLU:
+      if (kk && g.nacc == 2) return umma_bn<EPI_SWIGLU, false, false>(g, st);
+      break;
     case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, false, true>(g, st); break;
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
@@ -229,7 +238,7 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   g.ep.M = g.M;
   g.ep.N = g.N;
   if (c.dt == LR_BF16) {
-    if (k == EPI_SWIGLU) g.bn = 128;
+    if (k == EPI_SWIGLU) g.bn = kSwigluBn;
     else if (g.bn != 128 && g.bn != 256) g.bn = pick_bn(g, c.sms);
   } else {
     g.bn = 0;
@@ -288,13 +297,14 @@ static WgradPlan wgrad_plan(const Ctx& c, int M, int N, int K, bool needs_pass) 
   const double reduce_bw = 4.0e12;                       // bytes/s of the partial reduction
   WgradPlan best{256, 1};
   double best_t = 1e30;
+  const long long slots = std::max(1, c.sms / 2);  // SM pairs
   for (int bn : {256, 128}) {
-    const long long tiles = 1LL * ((M + 127) / 128) * ((N + bn - 1) / bn);
+    const long long tiles = 1LL * ((M + 255) / 256) * ((N + bn - 1) / bn);  // pair tiles
     for (int ks = 1; ks <= wgrad_split_bound(K); ++ks) {
       const int ksn = normalise_split(K, ks);
       if (ksn != ks) continue;
-      const long long waves = (tiles * ks + c.sms - 1) / c.sms;
-      const double tile_t = 2.0 * 128 * bn * (static_cast<double>(K) / ks) / per_sm_flops * (bn == 128 ? 1.15 : 1.0);
+      const long long waves = (tiles * ks + slots - 1) / slots;
+      const double tile_t = 2.0 * 128 * bn * (static_cast<double>(K) / ks) / per_sm_flops * (bn == 128 ? 1.33 : 1.0);
       double t = waves * tile_t;
       if (ks > 1 || needs_pass) t += (static_cast<double>(ks) + 1.0) * M * N * 4.0 / reduce_bw;
       if (t < best_t * 0.98) {

@@ -16,10 +16,18 @@
 // memory and one thread writes them to global memory with TMA bulk tensor
 // stores (rows and columns past the tensor edge are clipped by the TMA unit).
 //
-// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
-//   warp 0     TMA producer of the operand ring (one elected lane)
-//   warp 1     TMEM allocator and MMA issuer (one elected lane issues tcgen05.mma)
-//   warps 2-9  epilogue
+// CTA pairs (2-SM UMMA): the kernel runs in clusters of two CTAs on two SMs.
+// A pair tile is 256 rows x BN columns; CTA `rank` stages rows 128 rank .. +127
+// of A and half of the B tile (BN/2 rows or columns) in its own shared memory,
+// and the leader CTA issues tcgen05.mma.cta_group::2 with M = 256, which reads
+// both CTAs' operands and leaves rows 128 rank .. +127 of the accumulator in
+// each CTA's own TMEM.  Per SM this halves the B-operand traffic through shared
+// memory (the mainloop's limit with one CTA per tile) and the B stage size.
+//
+// Warp roles (320 threads per CTA, one CTA per SM, persistent over pair tiles):
+//   warp 0     TMA producer of the CTA's half of the operand ring (one lane)
+//   warp 1     TMEM allocator; in the leader CTA also the MMA issuer (one lane)
+//   warps 2-9  epilogue of the CTA's 128 rows
 // Two TMEM accumulator buffers let the epilogue of tile i overlap the
 // mainloop of tile i+1.  NACC > 1 gives each tile several accumulators fed by
 // consecutive K segments with their own operand maps (the SwiGLU dual GEMM).
@@ -59,6 +67,7 @@ struct Shape {
   int M, N, K;
   int batches, ksplit;
   int m_tiles, n_tiles;
+  int m_pairs;  // pair tiles along M: the CTAs of a cluster take m-tiles 2p and 2p + 1
   int kb_total, kb_per_split;
   unsigned* err;
 };
@@ -121,6 +130,33 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Shared::cluster address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+// A TMA load into this CTA's shared memory whose byte count completes on an mbarrier of
+// either CTA of the pair (`bar_cluster` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -165,14 +201,15 @@ __device__ __forceinline__ void tmap_prefetch(const CUtensorMap* map) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Both CTAs of the pair allocate together and receive the same TMEM address.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(ncols)
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(ncols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -180,14 +217,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
+// Arrive on the mbarrier at this offset in every CTA of ctamask once the issued MMAs complete.
+__device__ __forceinline__ void umma_commit(uint64_t* bar, uint16_t ctamask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(ctamask)
+      : "memory");
 }
 
 // 32 lanes x 32 consecutive fp32 columns: thread t of the warp receives its lane's 32 columns.
@@ -220,11 +261,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;
 }
 
-// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, operand majors, N >> 3, M >> 4.
+// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, operand majors, N >> 3, M >> 4
+// (M = 256: the pair's two 128-row halves).
 template <int N_, bool A_MN, bool B_MN>
 __host__ __device__ constexpr uint32_t idesc_bf16() {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N_ >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>(N_ >> 3) << 17) | (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 }
 
 // Byte offset of 16-byte chunk j of row r in a swizzled staging tile with `row_bytes`
@@ -240,7 +282,7 @@ struct Config {
   using D = EpiDef<K>;
   static constexpr int NACC = D::NACC;
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's half of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int OUT_ROW = CW * (D::OUT_F32 ? 4 : 2);
   static constexpr int OUT_BUF = BM * OUT_ROW;
@@ -250,32 +292,37 @@ struct Config {
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
   static constexpr bool STATS = (K == EPI_NORM_SILU);
   static constexpr int THREADS = kThreads + (STATS ? 128 : 0);
-  static constexpr int BAR_BYTES = 256 + 1024;  // barriers, then s for two tiles of 128 rows
+  static constexpr int BAR_BYTES = 512 + 1024;  // barriers, then s for two tiles of 128 rows
   static constexpr int RING_BUDGET = kMaxSmem - 1024 - EPI_BYTES - BAR_BYTES;
   static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
   static constexpr uint32_t ACC_COLS = NACC * BN;
-  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS <= 32    ? 32
-                                        : 2 * ACC_COLS <= 64  ? 64
-                                        : 2 * ACC_COLS <= 128 ? 128
-                                        : 2 * ACC_COLS <= 256 ? 256
-                                                              : 512;
+  // Two accumulator buffers when they fit in the 512 TMEM columns, else one.
+  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
+  static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS <= 32    ? 32
+                                        : NBUF * ACC_COLS <= 64  ? 64
+                                        : NBUF * ACC_COLS <= 128 ? 128
+                                        : NBUF * ACC_COLS <= 256 ? 256
+                                                                 : 512;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-  static_assert(2 * ACC_COLS <= 512, "two accumulator buffers must fit in TMEM");
+  static_assert(NBUF * ACC_COLS <= 512, "accumulator buffers must fit in TMEM");
   static_assert(STAGES >= 2, "need at least two stages");
-  static_assert(BN % 64 == 0 && BN <= 256, "BN must be 64..256 in steps of 64");
+  static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256 (each CTA stages BN/2, whole 64-column chunks)");
   static_assert((BN / CW) % 2 == 0, "both epilogue groups need the same number of chunks");
   static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
 };
 
-__device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int& split, int& batch, int& mb, int& nb) {
-  const int per_batch = sh.m_tiles * sh.n_tiles;
+// Pair-tile index -> (split, batch, this CTA's m-tile, n-tile); n runs fastest.
+__device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
+                                            int& nb) {
+  const int per_batch = sh.m_pairs * sh.n_tiles;
   const int per_split = sh.batches * per_batch;
   split = tile / per_split;
   int rem = tile - split * per_split;
   batch = rem / per_batch;
   rem -= batch * per_batch;
-  mb = rem / sh.n_tiles;
-  nb = rem - mb * sh.n_tiles;
+  const int mp = rem / sh.n_tiles;
+  nb = rem - mp * sh.n_tiles;
+  mb = 2 * mp + rank;
 }
 
 template <EpiKind K, int BN, bool A_MN, bool B_MN>
@@ -294,7 +341,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   uint8_t* sE = sB + STAGES * C::B_BYTES;  // epilogue staging, 1024-aligned
   uint64_t* full = reinterpret_cast<uint64_t*>(sE + C::EPI_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* consumed = empty + STAGES;  // MMA done with a stage (statistics warps may read it)
+  uint64_t* tfull = consumed + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* aux_full = drain + 1;  // one per epilogue group
@@ -302,19 +350,20 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   uint64_t* sempty = sfull + 2;     // epilogue -> stats, per TMEM buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_rows = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);  // [2][BM]
+  float* s_rows = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [2][BM]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], C::STATS ? 1 + 4 : 1);  // MMA commit (+ one arrive per stats warp)
+      mbar_init(&full[i], 1);                  // leader: its producer's expect_tx (+ both CTAs' bytes)
+      mbar_init(&empty[i], C::STATS ? 4 : 1);  // MMA commit, or the statistics warps after it
+      mbar_init(&consumed[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiWarps);  // one arrive per epilogue warp
+      mbar_init(&tempty[i], 2 * kEpiWarps);  // leader: one arrive per epilogue warp of both CTAs
       mbar_init(&aux_full[i], 1);
       mbar_init(&sfull[i], 4);
       mbar_init(&sempty[i], kEpiWarps);
@@ -331,13 +380,18 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       tmap_prefetch(&maps.b[i]);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  __syncwarp();
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);  // both CTAs: one joint allocation
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before either touches the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total = sh.ksplit * sh.batches * sh.m_tiles * sh.n_tiles;
+  const int rank = static_cast<int>(blockIdx.x & 1);  // 0: leader (issues the MMAs)
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int ncl = static_cast<int>(gridDim.x >> 1);
+  constexpr uint16_t kBoth = 0x3;
+  const int total = sh.ksplit * sh.batches * sh.m_pairs * sh.n_tiles;  // pair tiles
 
   if (warp == 0) {
     if (lane == 0) {
@@ -346,9 +400,9 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = cid; tile < total && ok; tile += ncl) {
         int split, batch, mb, nb;
-        decode_tile(sh, tile, split, batch, mb, nb);
+        decode_tile(sh, tile, rank, split, batch, mb, nb);
         const int kb0 = split * sh.kb_per_split;
         const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
         const int m0 = mb * BM, n0 = nb * BN;
@@ -359,20 +413,25 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               ok = false;
               break;
             }
-            mbar_expect_tx(&full[st], C::STAGE_BYTES);
+            // The leader's full barrier counts the bytes of both CTAs' halves of the stage.
+            if (rank == 0) mbar_expect_tx(&full[st], 2 * C::STAGE_BYTES);
+            const uint32_t fbar = mapa(smem_addr(&full[st]), 0);
             uint8_t* a_dst = sA + st * C::A_BYTES;
             uint8_t* b_dst = sB + st * C::B_BYTES;
             if (A_MN) {
 #pragma unroll
-              for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * 8192, &maps.a[set], &full[st], m0 + 64 * j, kb * BK);
+              for (int j = 0; j < BM / 64; ++j)
+                tma_load_2d_pair(a_dst + j * 8192, &maps.a[set], fbar, m0 + 64 * j, kb * BK);
             } else {
-              tma_load_2d(a_dst, &maps.a[set], &full[st], kb * BK, m0);
+              tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK, m0);
             }
+            const int nb0 = n0 + rank * (BN / 2);  // this CTA's half of the B tile
             if (B_MN) {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &maps.b[set], &full[st], n0 + 64 * j, kb * BK);
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j, kb * BK);
             } else {
-              tma_load_2d(b_dst, &maps.b[set], &full[st], kb * BK, n0);
+              tma_load_2d_pair(b_dst, &maps.b[set], fbar, kb * BK, nb0);
             }
             ++issued;
             if (++st == STAGES) {
@@ -382,8 +441,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // Wait (bounded) for the copies still in flight before the CTA may exit.
+      if (!ok && rank == 0) {
+        // Wait (bounded) for the pair's copies still in flight before the CTAs may exit.
         const long long n_back = issued < STAGES ? issued : STAGES;
         for (long long i = 1; i <= n_back; ++i) {
           const long long n = issued - i;
@@ -396,21 +455,21 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------ MMA issuer (leader CTA)
       const uint32_t a_base = smem_addr(sA);
       const uint32_t b_base = smem_addr(sB);
       int st = 0;
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
         int split, batch, mb, nb;
-        decode_tile(sh, tile, split, batch, mb, nb);
+        decode_tile(sh, tile, rank, split, batch, mb, nb);
         const int kb0 = split * sh.kb_per_split;
         const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
-        const int buf = it & 1;
-        const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
+        const int buf = C::NBUF == 2 ? (it & 1) : 0;
+        const uint32_t tph = static_cast<uint32_t>(C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1));
         if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
           ok = false;
           break;
@@ -434,17 +493,18 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               const uint64_t bd = B_MN ? sdesc(b_st + kk * 2048, 8192, 1024) : sdesc(b_st + kk * 32, 16, 1024);
               umma_f16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
             }
-            umma_commit(&empty[st]);
+            // Both CTAs' halves of the stage are free once these MMAs complete.
+            umma_commit(C::STATS ? &consumed[st] : &empty[st], kBoth);
             if (++st == STAGES) {
               st = 0;
               ph ^= 1u;
             }
           }
         }
-        if (ok) umma_commit(&tfull[buf]);
+        if (ok) umma_commit(&tfull[buf], kBoth);
       }
       // Drain: all MMAs issued by this thread have completed once this barrier flips.
-      umma_commit(drain);
+      umma_commit(drain, 0x1);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_test(drain, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
       }
@@ -460,14 +520,16 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     uint32_t ph = 0;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+    for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
-      decode_tile(sh, tile, split, batch, mb, nb);
+      decode_tile(sh, tile, rank, split, batch, mb, nb);
       const int kb0 = split * sh.kb_per_split;
       const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
       float ss = 0.f;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(&full[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE)) {
+        // The MMAs have read the stage of both CTAs (so it has landed); it is refilled only
+        // after these warps arrive on `empty`.
+        if (!mbar_wait(&consumed[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE)) {
           ok = false;
           break;
         }
@@ -514,7 +576,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 
     auto issue_aux = [&](int t, int c) {
       int split, batch, mb, nb;
-      decode_tile(sh, t, split, batch, mb, nb);
+      decode_tile(sh, t, rank, split, batch, mb, nb);
       uint32_t bytes = 0;
 #pragma unroll
       for (int a = 0; a < NAUX; ++a)
@@ -527,27 +589,29 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     };
     bool aux_pending = false;  // leader: an operand-tile load is in flight on abar
     if constexpr (NAUX > 0) {
-      if (leader && static_cast<int>(blockIdx.x) < total) {
-        issue_aux(blockIdx.x, g);
+      if (leader && cid < total) {
+        issue_aux(cid, g);
         aux_pending = true;
       }
     }
 
     bool ok = true;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+    for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
-      decode_tile(sh, tile, split, batch, mb, nb);
-      const int buf = it & 1;
-      const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
+      decode_tile(sh, tile, rank, split, batch, mb, nb);
+      const int buf = C::NBUF == 2 ? (it & 1) : 0;
+      const uint32_t tph = static_cast<uint32_t>(C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1));
+      const int sbuf = it & 1;  // statistics double buffer (independent of TMEM)
+      const uint32_t sph = static_cast<uint32_t>((it >> 1) & 1);
       const int m = mb * BM + row;
       RowIn ri;
       if constexpr (C::STATS) {
         ri.k = 0.f;
-        ok = mbar_wait(&sfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
-        ri.s = s_rows[buf * BM + row];
+        ok = mbar_wait(&sfull[sbuf], sph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
+        ri.s = s_rows[sbuf * BM + row];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sempty[buf]);
+        if (lane == 0) mbar_arrive(&sempty[sbuf]);
       } else {
         ri = row_inputs<K>(ep, m);
       }
@@ -594,7 +658,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           if (leader) {
             int nt = tile, nc = c + 2;
             if (nc >= NCH) {
-              nt = tile + gridDim.x;
+              nt = tile + ncl;
               nc = g;
             }
             if (nt < total) {
@@ -643,7 +707,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       if (!ok) break;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[buf]), 0));  // the leader's MMA reuses it
     }
     if (leader) {
       bulk_wait_all();
@@ -655,7 +719,9 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     }
   }
 
-  __syncthreads();
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while the other may still use its memory or barriers
   if (warp == 1) {
     tc_fence_after();
     tmem_free(tmem_base, C::TMEM_COLS);

@@ -85,6 +85,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.batches = NACC > 1 ? 1 : g.batches;
   sh.m_tiles = (g.M + BM - 1) / BM;
   sh.n_tiles = (g.N + BN - 1) / BN;
+  sh.m_pairs = (sh.m_tiles + 1) / 2;
   sh.kb_total = (g.K + BK - 1) / BK;
   const int ks = g.ksplit < 1 ? 1 : g.ksplit;
   sh.kb_per_split = (sh.kb_total + ks - 1) / ks;
@@ -95,8 +96,9 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   for (int i = 0; i < nsets; ++i) {
     const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, g.M, g.K, g.A[i].ld, 64, 64)
                           : encode_operand(&maps.a[i], g.A[i].ptr, g.K, g.M, g.A[i].ld, 64, BM);
+    // Each CTA of a pair stages half of the B tile: BN/2 rows (K-major) or 64-column chunks (MN-major).
     const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, g.N, g.K, g.B[i].ld, 64, 64)
-                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, g.N, g.B[i].ld, 64, BN);
+                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, g.N, g.B[i].ld, 64, BN / 2);
     if (!okA || !okB) return cudaErrorInvalidValue;
   }
   const void* const* outs[3] = {g.ep.out0, g.ep.out1, g.ep.out2};
@@ -118,21 +120,46 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
     }
   }
 
-  const long long total = 1LL * sh.ksplit * sh.batches * sh.m_tiles * sh.n_tiles;
+  const long long total = 1LL * sh.ksplit * sh.batches * sh.m_pairs * sh.n_tiles;  // pair tiles
   if (total <= 0) return cudaSuccess;
-  const int sms = device_sm_count();
-  const int grid = static_cast<int>(total < sms ? total : sms);
 
   auto kern = gemm_kernel<K, BN, A_MN, B_MN>;
-  static int configured_mask = 0;  // one bit per device ordinal
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;  // a CTA pair on two SMs
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+
+  // Per device, once: the shared-memory opt-in and how many pairs can be resident at once.
+  static int configured_mask = 0;
+  static int max_pairs[32];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+  if (dev < 0 || dev >= 32) return cudaErrorInvalidDevice;
+  if (!(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = device_sm_count() / 2;
+    }
+    max_pairs[dev] = n;
     __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(maps, sh, g.ep);
+  const long long pairs = total < max_pairs[dev] ? total : max_pairs[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, sh, g.ep);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
