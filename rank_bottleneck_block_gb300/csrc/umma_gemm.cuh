@@ -287,7 +287,13 @@ struct Config {
   static constexpr int OUT_ROW = CW * (D::OUT_F32 ? 4 : 2);
   static constexpr int OUT_BUF = BM * OUT_ROW;
   static constexpr int AUX_BUF = BM * CW * 2;
-  static constexpr int GROUP_BYTES = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;
+  static constexpr int GROUP_SET = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;  // one chunk's staging
+  // Epilogues that read operand tiles get two staging sets per group (operand tiles two
+  // chunks ahead, output tiles in ping-pong) when the operand ring still keeps three
+  // stages; the others keep one set and a deeper ring.
+  static constexpr int EB =
+      D::NAUX > 0 && (kMaxSmem - 1024 - 2 * 2 * GROUP_SET - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3 ? 2 : 1;
+  static constexpr int GROUP_BYTES = EB * GROUP_SET;
   static constexpr int EPI_BYTES = 2 * GROUP_BYTES;
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
   static constexpr bool STATS = (K == EPI_NORM_SILU);
@@ -345,8 +351,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   uint64_t* tfull = consumed + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* aux_full = drain + 1;  // one per epilogue group
-  uint64_t* sfull = aux_full + 2;   // stats -> epilogue, per TMEM buffer
+  uint64_t* aux_full = drain + 1;  // per epilogue group and staging set
+  uint64_t* sfull = aux_full + 4;   // stats -> epilogue, per TMEM buffer
   uint64_t* sempty = sfull + 2;     // epilogue -> stats, per TMEM buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -364,7 +370,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 2 * kEpiWarps);  // leader: one arrive per epilogue warp of both CTAs
-      mbar_init(&aux_full[i], 1);
+      mbar_init(&aux_full[2 * i], 1);
+      mbar_init(&aux_full[2 * i + 1], 1);
       mbar_init(&sfull[i], 4);
       mbar_init(&sempty[i], kEpiWarps);
     }
@@ -563,40 +570,56 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     // ------------------------------------------------ epilogue warps
     constexpr int NAUX = D::NAUX, NOUT = D::NOUT;
     constexpr int NCH = BN / CW;
+    constexpr int EB = C::EB;
     const int ew = warp - 2;
     const int g = ew >> 2;   // group: chunks g, g+2, ...
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const bool leader = (ew & 3) == 0 && lane == 0;
     const int bar_id = 1 + g;
-    uint8_t* ostage = sE + g * C::GROUP_BYTES;
-    uint8_t* astage = ostage + NOUT * C::OUT_BUF;
-    uint64_t* abar = &aux_full[g];
-    uint32_t aph = 0;
+    uint8_t* gstage = sE + g * C::GROUP_BYTES;  // EB sets of [NOUT output tiles | NAUX operand tiles]
+    auto ostage = [&](int b) { return gstage + b * C::GROUP_SET; };
+    auto astage = [&](int b) { return gstage + b * C::GROUP_SET + NOUT * C::OUT_BUF; };
+    uint64_t* abar = &aux_full[2 * g];
+    uint32_t aph = 0u;      // bit b: phase parity of abar[b]
+    uint32_t pending = 0u;  // leader, bit b: an operand-tile load is in flight on abar[b]
 
-    auto issue_aux = [&](int t, int c) {
+    // The group's chunk sequence: (tile, c) for c = g, g+2, ... of each of this CTA's tiles.
+    auto next_chunk = [&](int& t, int& c) {
+      c += 2;
+      if (c >= NCH) {
+        t += ncl;
+        c = g;
+      }
+    };
+    auto issue_aux = [&](int t, int c, int b) {
       int split, batch, mb, nb;
       decode_tile(sh, t, rank, split, batch, mb, nb);
       uint32_t bytes = 0;
 #pragma unroll
       for (int a = 0; a < NAUX; ++a)
         if (epi_aux_ptr(ep, a, batch)) bytes += C::AUX_BUF;
-      mbar_expect_tx(abar, bytes);
+      mbar_expect_tx(&abar[b], bytes);
 #pragma unroll
       for (int a = 0; a < NAUX; ++a)
         if (epi_aux_ptr(ep, a, batch))
-          tma_load_2d(astage + a * C::AUX_BUF, &maps.aux[batch][a], abar, nb * BN + c * CW, mb * BM);
+          tma_load_2d(astage(b) + a * C::AUX_BUF, &maps.aux[batch][a], &abar[b], nb * BN + c * CW, mb * BM);
+      pending |= 1u << b;
     };
-    bool aux_pending = false;  // leader: an operand-tile load is in flight on abar
+    // Prefetch cursor: the next chunk whose operand tiles are not yet requested.
+    int pf_t = cid, pf_c = g;
     if constexpr (NAUX > 0) {
-      if (leader && cid < total) {
-        issue_aux(cid, g);
-        aux_pending = true;
+      if (leader) {
+        for (int b = 0; b < EB && pf_t < total; ++b) {
+          issue_aux(pf_t, pf_c, b);
+          next_chunk(pf_t, pf_c);
+        }
       }
     }
 
     bool ok = true;
     int it = 0;
+    int qi = 0;  // index of the group's current chunk in its sequence
     for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
       decode_tile(sh, tile, rank, split, batch, mb, nb);
@@ -626,13 +649,14 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
 #pragma unroll 1
-      for (int c = g; c < NCH; c += 2) {
+      for (int c = g; c < NCH; c += 2, ++qi) {
+        const int b = EB == 2 ? (qi & 1) : 0;
         if constexpr (NAUX > 0) {
-          const bool landed = mbar_wait(abar, aph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
+          const bool landed = mbar_wait(&abar[b], (aph >> b) & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
           ok = landed && ok;
           if (landed) {
-            aph ^= 1u;
-            aux_pending = false;
+            aph ^= 1u << b;
+            pending &= ~(1u << b);
           }
         }
         float v[NACC][CW];
@@ -643,7 +667,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
         for (int a = 0; a < NAUX; ++a) {
           if (aux_present[a]) {
-            const uint8_t* base = astage + a * C::AUX_BUF;
+            const uint8_t* base = astage(b) + a * C::AUX_BUF;
 #pragma unroll
             for (int j = 0; j < CW / 8; ++j) load8(reinterpret_cast<const bf16*>(base + stage_off<64>(row, j)), &av[a][8 * j]);
           } else {
@@ -651,20 +675,17 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
             for (int j = 0; j < CW; ++j) av[a][j] = 0.f;
           }
         }
-        if (leader) bulk_wait_read_all();  // this group's previous stores have left the staging tiles
+        // The stores that last used this output set have finished reading it.
+        if (leader) {
+          if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          else bulk_wait_read_all();
+        }
         ok = named_bar_and(bar_id, 128, ok);
         if (!ok) break;
         if constexpr (NAUX > 0) {
-          if (leader) {
-            int nt = tile, nc = c + 2;
-            if (nc >= NCH) {
-              nt = tile + ncl;
-              nc = g;
-            }
-            if (nt < total) {
-              issue_aux(nt, nc);
-              aux_pending = true;
-            }
+          if (leader && pf_t < total) {  // refill the operand set this chunk has just released
+            issue_aux(pf_t, pf_c, b);
+            next_chunk(pf_t, pf_c);
           }
         }
         float o[NOUT][CW];
@@ -673,7 +694,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
         for (int oi = 0; oi < NOUT; ++oi) {
           if (!present[oi]) continue;
-          uint8_t* base = ostage + oi * C::OUT_BUF;
+          uint8_t* base = ostage(b) + oi * C::OUT_BUF;
           if constexpr (D::OUT_F32) {
 #pragma unroll
             for (int j = 0; j < CW / 4; ++j) {
@@ -697,9 +718,9 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           for (int oi = 0; oi < NOUT; ++oi) {
             if (!present[oi]) continue;
             if constexpr (D::OUT_F32)
-              tma_store_3d(&maps.out[batch][oi], ostage + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM, split);
+              tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM, split);
             else
-              tma_store_2d(&maps.out[batch][oi], ostage + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM);
+              tma_store_2d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM);
           }
           bulk_commit();
         }
@@ -711,9 +732,10 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     }
     if (leader) {
       bulk_wait_all();
-      if (aux_pending) {  // abort path: let the last operand-tile load land before the CTA exits
+      for (int b = 0; b < 2; ++b) {  // abort path: let operand-tile loads in flight land before the CTA exits
+        if (!((pending >> b) & 1u)) continue;
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_test(abar, aph) && global_timer_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_test(&abar[b], (aph >> b) & 1u) && global_timer_ns() - t0 < kWaitLimitNs) {
         }
       }
     }
