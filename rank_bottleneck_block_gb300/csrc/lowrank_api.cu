@@ -370,11 +370,9 @@ static lr_status rstd(const Ctx& c, const void* x, int T, int d, float eps, floa
   return LR_OK;
 }
 
-static lr_status silu_slab(const Ctx& c, const void* u, long long ldu, void* z, long long ldz, int T, int n) {
-  LaunchScope scope("silu", c.st, 0, 2.0 * c.es * T * n);
-  cudaError_t e = (c.dt == LR_BF16)
-                      ? launch_silu<bf16>(static_cast<const bf16*>(u), ldu, static_cast<bf16*>(z), ldz, T, n, c.st)
-                      : launch_silu<float>(static_cast<const float*>(u), ldu, static_cast<float*>(z), ldz, T, n, c.st);
+static lr_status silu_slabs(const Ctx& c, SiluSlab a, SiluSlab b, int T) {
+  LaunchScope scope("silu", c.st, 0, 2.0 * c.es * T * (a.n + b.n));
+  cudaError_t e = (c.dt == LR_BF16) ? launch_silu<bf16>(a, b, T, c.st) : launch_silu<float>(a, b, T, c.st);
   if (e != cudaSuccess) return fail(LR_ERR_CUDA, "silu: %s", cudaGetErrorString(e));
   return LR_OK;
 }
@@ -580,8 +578,7 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     a = W.a;
     b = W.b;
     h = W.h;
-    LR_TRY(silu_slab(c, S.u_gu, 2 * r, z_gu, 2 * r, T, 2 * r));
-    LR_TRY(silu_slab(c, S.u_d, r, z_d, r, T, r));
+    LR_TRY(silu_slabs(c, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, r}, T));
     LR_TRY(swiglu_gemm(c, T, f, r, z_gu, gate.B, up.B, h, a, b));
   } else {
     z_gu = S.z_gu;

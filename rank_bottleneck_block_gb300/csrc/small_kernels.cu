@@ -62,64 +62,80 @@ cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStre
 
 // ------------------------------------------------------------------ silu
 template <typename ST>
-__global__ void silu_kernel(const ST* u, long long ldu, ST* z, long long ldz, int T, int n) {
-  const int groups = n / 8;
-  const long long total = 1LL * T * groups;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
-    const long long t = i / groups;
-    const int c = static_cast<int>(i % groups) * 8;
+__global__ void silu_kernel(SiluSlab a, SiluSlab b, int T) {
+  const long long ga = 1LL * T * (a.n / 8), gb = 1LL * T * (b.n / 8);
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < ga + gb; i += 256LL * gridDim.x) {
+    const bool first = i < ga;
+    const SiluSlab& sl = first ? a : b;
+    const long long k = first ? i : i - ga;
+    const int groups = sl.n / 8;
+    const long long t = k / groups;
+    const int c = static_cast<int>(k % groups) * 8;
     float v[8];
-    load8(u + t * ldu + c, v);
+    load8(static_cast<const ST*>(sl.u) + t * sl.ldu + c, v);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = silu<ST>(v[k]);
-    store8(z + t * ldz + c, v);
+    for (int q = 0; q < 8; ++q) v[q] = silu<ST>(v[q]);
+    store8(static_cast<ST*>(sl.z) + t * sl.ldz + c, v);
   }
 }
 
 template <typename ST>
-cudaError_t launch_silu(const ST* u, long long ldu, ST* z, long long ldz, int T, int n, cudaStream_t st) {
-  const long long total = 1LL * T * (n / 8);
+cudaError_t launch_silu(SiluSlab a, SiluSlab b, int T, cudaStream_t st) {
+  const long long total = 1LL * T * (a.n / 8 + b.n / 8);
   if (total == 0) return cudaSuccess;
   int blocks = static_cast<int>((total + 255) / 256);
   if (blocks > 8192) blocks = 8192;
-  silu_kernel<ST><<<blocks, 256, 0, st>>>(u, ldu, z, ldz, T, n);
+  silu_kernel<ST><<<blocks, 256, 0, st>>>(a, b, T);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------- wgrad reduce
-// One thread per 4 consecutive columns of kReduceRows rows; splits summed in order.
+// One thread per 4 consecutive columns of kReduceRows rows; splits summed in order.  The
+// row loop is unrolled so the loads of all rows and splits are in flight together.
 template <typename ST>
 __global__ void wgrad_reduce_kernel(const float* part, int nsplit, long long split_stride, int M, int N,
                                     const ST* colscale, WgradDst dst, int rows_each, float* dgpart) {
   const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (n >= N) return;
   const int r0 = blockIdx.y * kReduceRows;
-  const int r1 = min(M, r0 + kReduceRows);
   float cs[4] = {1.f, 1.f, 1.f, 1.f};
   if (colscale) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) cs[t] = static_cast<float>(colscale[n + t]);
   }
-  float dga[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int m = r0; m < r1; ++m) {
-    const long long idx = static_cast<long long>(m) * N + n;
-    float4 v = *reinterpret_cast<const float4*>(part + idx);
-    for (int s = 1; s < nsplit; ++s) {
-      const float4 w = *reinterpret_cast<const float4*>(part + s * split_stride + idx);
-      v.x += w.x;
-      v.y += w.y;
-      v.z += w.z;
-      v.w += w.w;
+  float4 v[kReduceRows];
+#pragma unroll
+  for (int i = 0; i < kReduceRows; ++i) {
+    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r0 + i < M) v[i] = *reinterpret_cast<const float4*>(part + static_cast<long long>(r0 + i) * N + n);
+  }
+  for (int s = 1; s < nsplit; ++s) {
+#pragma unroll
+    for (int i = 0; i < kReduceRows; ++i) {
+      if (r0 + i < M) {
+        const float4 w = *reinterpret_cast<const float4*>(part + s * split_stride + static_cast<long long>(r0 + i) * N + n);
+        v[i].x += w.x;
+        v[i].y += w.y;
+        v[i].z += w.z;
+        v[i].w += w.w;
+      }
     }
+  }
+  float dga[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kReduceRows; ++i) {
+    const int m = r0 + i;
+    if (m >= M) break;
     const int blk = m / rows_each;
     const long long local = static_cast<long long>(m - blk * rows_each) * N + n;
-    *reinterpret_cast<float4*>(dst.dst[blk] + local) = make_float4(v.x * cs[0], v.y * cs[1], v.z * cs[2], v.w * cs[3]);
+    *reinterpret_cast<float4*>(dst.dst[blk] + local) =
+        make_float4(v[i].x * cs[0], v[i].y * cs[1], v[i].z * cs[2], v[i].w * cs[3]);
     if (dgpart) {
       const ST* aw = static_cast<const ST*>(dst.aw[blk]) + local;
-      dga[0] = fmaf(v.x, static_cast<float>(aw[0]), dga[0]);
-      dga[1] = fmaf(v.y, static_cast<float>(aw[1]), dga[1]);
-      dga[2] = fmaf(v.z, static_cast<float>(aw[2]), dga[2]);
-      dga[3] = fmaf(v.w, static_cast<float>(aw[3]), dga[3]);
+      dga[0] = fmaf(v[i].x, static_cast<float>(aw[0]), dga[0]);
+      dga[1] = fmaf(v[i].y, static_cast<float>(aw[1]), dga[1]);
+      dga[2] = fmaf(v[i].z, static_cast<float>(aw[2]), dga[2]);
+      dga[3] = fmaf(v[i].w, static_cast<float>(aw[3]), dga[3]);
     }
   }
   if (dgpart)
@@ -136,17 +152,27 @@ cudaError_t launch_wgrad_reduce(const float* part, int nsplit, long long split_s
   return cudaGetLastError();
 }
 
+// 32 columns per block; the 8 thread rows each sum every 8th partial, then the 8 sums are
+// added in a fixed order.
 __global__ void dg_finalize_kernel(const float* dgpart, int nparts, int N, float* dg) {
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= N) return;
+  __shared__ float red[8][33];
+  const int n = blockIdx.x * 32 + threadIdx.x;
   float v = 0.f;
-  for (int p = 0; p < nparts; ++p) v += dgpart[static_cast<long long>(p) * N + n];
-  dg[n] = v;
+  if (n < N)
+    for (int p = threadIdx.y; p < nparts; p += 8) v += dgpart[static_cast<long long>(p) * N + n];
+  red[threadIdx.y][threadIdx.x] = v;
+  __syncthreads();
+  if (threadIdx.y == 0 && n < N) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][threadIdx.x];
+    dg[n] = t;
+  }
 }
 
 cudaError_t launch_dg_finalize(const float* dgpart, int nparts, int N, float* dg, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
-  dg_finalize_kernel<<<(N + 255) / 256, 256, 0, st>>>(dgpart, nparts, N, dg);
+  dg_finalize_kernel<<<(N + 31) / 32, dim3(32, 8), 0, st>>>(dgpart, nparts, N, dg);
   return cudaGetLastError();
 }
 
@@ -232,7 +258,7 @@ cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, cud
 #define LR_SMALL_INST(ST)                                                                                          \
   template cudaError_t launch_fold<ST>(ST*, StackSrc, int, int, int, const ST*, cudaStream_t);                   \
   template cudaError_t launch_rstd<ST>(const ST*, int, int, float, float*, cudaStream_t);                        \
-  template cudaError_t launch_silu<ST>(const ST*, long long, ST*, long long, int, int, cudaStream_t);            \
+  template cudaError_t launch_silu<ST>(SiluSlab, SiluSlab, int, cudaStream_t);                                  \
   template cudaError_t launch_wgrad_reduce<ST>(const float*, int, long long, int, int, const ST*, WgradDst, int, \
                                                float*, cudaStream_t);                                            \
   template cudaError_t launch_mse<ST>(const ST*, const ST*, long long, ST*, float*, int, float*, cudaStream_t);

@@ -29,9 +29,17 @@ cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols
 template <typename ST>
 cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st);
 
-// z[t, c0 + j] = SiLU(u[t, j]) for a [T, n] slab (u and z with their own leading dimensions).
+// z[t, j] = SiLU(u[t, j]) for two [T, n] slabs in one launch (u and z with their own leading
+// dimensions; a slab with n = 0 is skipped).
+struct SiluSlab {
+  const void* u;
+  long long ldu;
+  void* z;
+  long long ldz;
+  int n;
+};
 template <typename ST>
-cudaError_t launch_silu(const ST* u, long long ldu, ST* z, long long ldz, int T, int n, cudaStream_t st);
+cudaError_t launch_silu(SiluSlab a, SiluSlab b, int T, cudaStream_t st);
 
 // dst = sum over splits of part (fixed order) times the optional column scale;
 // dgpart[row_block, n] = sum over the block's rows of (unscaled sum) * aw.

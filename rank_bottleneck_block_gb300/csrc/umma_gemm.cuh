@@ -171,6 +171,41 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 
+// Explicit 16-byte shared-memory accesses for the staging tiles (their swizzled layout is
+// bank-conflict free only when each thread moves whole 16-byte chunks).
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t& x, uint32_t& y, uint32_t& z, uint32_t& w) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void unpack_bf16x2(uint32_t w, float& a, float& b) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  a = f.x;
+  b = f.y;
+}
+
+// Eight bf16 values at a shared address <-> eight floats.
+__device__ __forceinline__ void sts_bf16x8(uint32_t addr, const float* v) {
+  sts128(addr, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+__device__ __forceinline__ void lds_bf16x8(uint32_t addr, float* v) {
+  uint32_t w0, w1, w2, w3;
+  lds128(addr, w0, w1, w2, w3);
+  unpack_bf16x2(w0, v[0], v[1]);
+  unpack_bf16x2(w1, v[2], v[3]);
+  unpack_bf16x2(w2, v[4], v[5]);
+  unpack_bf16x2(w3, v[6], v[7]);
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -544,7 +579,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           float v[8];
-          load8(reinterpret_cast<const bf16*>(a_row + ((j ^ (row & 7)) << 4)), v);
+          lds_bf16x8(smem_addr(a_row) + ((j ^ (row & 7)) << 4), v);
 #pragma unroll
           for (int t = 0; t < 8; ++t) ss = fmaf(v[t], v[t], ss);
         }
@@ -669,7 +704,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           if (aux_present[a]) {
             const uint8_t* base = astage(b) + a * C::AUX_BUF;
 #pragma unroll
-            for (int j = 0; j < CW / 8; ++j) load8(reinterpret_cast<const bf16*>(base + stage_off<64>(row, j)), &av[a][8 * j]);
+            for (int j = 0; j < CW / 8; ++j) lds_bf16x8(smem_addr(base) + stage_off<64>(row, j), &av[a][8 * j]);
           } else {
 #pragma unroll
             for (int j = 0; j < CW; ++j) av[a][j] = 0.f;
@@ -698,12 +733,13 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           if constexpr (D::OUT_F32) {
 #pragma unroll
             for (int j = 0; j < CW / 4; ++j) {
-              *reinterpret_cast<float4*>(base + stage_off<128>(row, j)) =
-                  make_float4(o[oi][4 * j], o[oi][4 * j + 1], o[oi][4 * j + 2], o[oi][4 * j + 3]);
+              sts128(smem_addr(base) + stage_off<128>(row, j), __float_as_uint(o[oi][4 * j]),
+                     __float_as_uint(o[oi][4 * j + 1]), __float_as_uint(o[oi][4 * j + 2]),
+                     __float_as_uint(o[oi][4 * j + 3]));
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < CW / 8; ++j) store8(reinterpret_cast<bf16*>(base + stage_off<64>(row, j)), &o[oi][8 * j]);
+            for (int j = 0; j < CW / 8; ++j) sts_bf16x8(smem_addr(base) + stage_off<64>(row, j), &o[oi][8 * j]);
           }
         }
         if constexpr (D::ROWPART) {
