@@ -194,6 +194,21 @@ def run_ours(a, ws, rank, local):
     torch.cuda.synchronize()
     L.lr_check_device_error()
 
+    # ------------------------------------------------ per-kernel pass (untimed)
+    # Events around every launch break the overlap of each kernel's start with the
+    # previous kernel's tail, so the per-kernel table comes from a pass of its own and
+    # the timed steps carry events around the dominant kernel only.
+    prof_steps = max(3, min(a.steps, 20))
+    L.lr_profile_filter(None)
+    L.lr_profile_start()
+    for i in range(prof_steps):
+        flush.fill_(i & 0xFF)
+        blk.step()
+    torch.cuda.synchronize()
+    prof_all = L.lr_profile_stop()
+    gemms = {k: v for k, v in prof_all.items() if v["flops"] > 0}
+    dom_name = max(gemms.items(), key=lambda kv: kv[1]["ms"])[0]
+
     # ------------------------------------------------ device-resident timing
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
     uuid = None
@@ -206,6 +221,7 @@ def run_ours(a, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     n0 = L.lr_launch_count()
+    L.lr_profile_filter(dom_name)
     L.lr_profile_start()
     for i in range(a.steps):
         flush.fill_(i & 0xFF)
@@ -215,6 +231,7 @@ def run_ours(a, ws, rank, local):
     torch.cuda.synchronize()
     barrier(ws)
     prof = L.lr_profile_stop()
+    L.lr_profile_filter(None)
     launches = L.lr_launch_count() - n0
     clocks = clk.stop()
     L.lr_check_device_error()
@@ -254,8 +271,7 @@ def run_ours(a, ws, rank, local):
 
     # ------------------------------------------------ rooflines
     pk = peaks()
-    gemms = {k: v for k, v in prof.items() if v["flops"] > 0}
-    dom_name, dom = max(gemms.items(), key=lambda kv: kv[1]["ms"])
+    dom = prof[dom_name]
     achieved_tf = dom["flops"] / (dom["ms"] / 1e3) / 1e12
     roofline = {"kernel": dom_name, "bound": "tensor", "achieved": round(achieved_tf, 1),
                 "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
@@ -263,7 +279,7 @@ def run_ours(a, ws, rank, local):
                 "peak_kind": f"bf16 dense, sustained ({pk['source']})",
                 "launches": dom["launches"], "avg_launch_us": round(1e3 * dom["ms"] / dom["launches"], 2),
                 "flops_per_launch": dom["flops"] / dom["launches"],
-                "share_of_step": round(dom["ms"] / sum(v["ms"] for v in prof.values()), 4),
+                "share_of_step": round(dom["ms"] / a.steps / ms_per_step, 4),
                 "traffic": None}
     ms_step_s = ms_per_step / 1e3
     t_nom = max(flops / (NOMINAL["tflops"] * 1e12), nbytes / (NOMINAL["hbm_gbs"] * 1e9))
@@ -271,11 +287,13 @@ def run_ours(a, ws, rank, local):
     block = {"flops_per_step": flops, "bytes_per_step": nbytes, "tflops": round(flops / ms_step_s / 1e12, 1),
              "roofline_ms_nominal": round(t_nom * 1e3, 4), "roofline_ms_measured": round(t_meas * 1e3, 4),
              "frac_nominal": round(t_nom / ms_step_s, 4), "frac_measured": round(t_meas / ms_step_s, 4)}
-    kernels = {k: {"launches": v["launches"], "ms_per_step": round(v["ms"] / a.steps, 4),
-                   "share": round(v["ms"] / sum(w["ms"] for w in prof.values()), 4),
+    kernels = {k: {"launches": v["launches"], "ms_per_step": round(v["ms"] / prof_steps, 4),
+                   "share": round(v["ms"] / sum(w["ms"] for w in prof_all.values()), 4),
                    **({"tflops": round(v["flops"] / (v["ms"] / 1e3) / 1e12, 1)} if v["flops"] else
                       {"gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1)})}
-               for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"])}
+               for k, v in sorted(prof_all.items(), key=lambda kv: -kv[1]["ms"])}
+    kernels["_pass"] = (f"{prof_steps} untimed steps with events around every launch (they serialise "
+                        f"launches, so the sum exceeds the timed step)")
 
     res = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": a.steps,
            "warmup": a.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -433,7 +451,7 @@ def run_reference(a, ws, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--mode", choices=["ckpt", "full"], default="ckpt")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")

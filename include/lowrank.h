@@ -209,10 +209,16 @@ lr_status lr_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
  *   recorded events and aggregate them per kernel name.  Then entries
  *   0 .. lr_profile_count()-1 give each kernel's name, launches, total device
  *   milliseconds, and algorithmic FLOPs (GEMMs: 2 M N K per accumulator and
- *   batch entry) or bytes (memory-bound kernels) summed over its launches. */
+ *   batch entry) or bytes (memory-bound kernels) summed over its launches.
+ * lr_profile_filter: record only launches whose kernel name starts with
+ *   `prefix` (NULL or "" records all; the setting outlives start/stop).  Events
+ *   between two launches end the overlap of the second one's start with the
+ *   first one's tail, so a step timed under the profiler runs a little slower
+ *   than one timed with events around the step alone. */
 unsigned long long lr_launch_count(void);
 lr_status lr_profile_start(void);
 lr_status lr_profile_stop(void);
+lr_status lr_profile_filter(const char* prefix);
 int lr_profile_count(void);
 lr_status lr_profile_entry(int i, char* name, size_t name_len, long long* launches, double* total_ms,
                            double* flops, double* bytes);

@@ -11,6 +11,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <utility>
 
 namespace lr {
 
@@ -132,6 +136,47 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// --------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialisation: it may start (and run its prologue) while the kernel before it
+// in the stream is still finishing.  pdl_wait() returns once that kernel has
+// completed and its memory operations are visible; every thread calls it before
+// its first global-memory access and before any early return (so a grid never
+// completes ahead of its predecessor and the ordering stays transitive).
+// pdl_trigger() lets the next kernel be scheduled once every CTA of this grid has
+// called it or exited; it does not release any memory ordering.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Programmatic dependent launch is on unless the environment sets LR_PDL=0 (read once).
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("LR_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+// Launches kern<<<grid, block, smem, st>>>(args...) with the programmatic-serialisation attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace lr

@@ -112,6 +112,7 @@ struct ProfAgg {
 };
 static std::mutex s_prof_mu;
 static bool s_prof_on = false;
+static std::string s_prof_filter;  // record only kernels whose name starts with this (empty: all)
 static std::vector<ProfRec> s_prof;
 static std::vector<cudaEvent_t> s_event_pool;
 static std::vector<ProfAgg> s_prof_result;
@@ -135,6 +136,7 @@ struct LaunchScope {
     s_launches.fetch_add(1, std::memory_order_relaxed);
     std::lock_guard<std::mutex> lk(s_prof_mu);
     if (!s_prof_on) return;
+    if (!s_prof_filter.empty() && name.compare(0, s_prof_filter.size(), s_prof_filter) != 0) return;
     on = true;
     rec.name = name;
     rec.flops = flops;
@@ -982,6 +984,12 @@ lr_status lr_profile_start(void) {
   s_prof.clear();
   s_prof_result.clear();
   s_prof_on = true;
+  return LR_OK;
+}
+
+lr_status lr_profile_filter(const char* prefix) {
+  std::lock_guard<std::mutex> lk(s_prof_mu);
+  s_prof_filter = prefix ? prefix : "";
   return LR_OK;
 }
 

@@ -23,6 +23,8 @@ struct Args {
 
 template <EpiKind K>
 __global__ void __launch_bounds__(256) gemm_kernel(const Args a, const EpiParams ep) {
+  pdl_wait();
+  pdl_trigger();
   using D = EpiDef<K>;
   constexpr int NACC = D::NACC, NAUX = D::NAUX, NOUT = D::NOUT;
   __shared__ float As[TK][TM + 1];
@@ -119,8 +121,7 @@ cudaError_t launch_simt(const GemmCall& g, cudaStream_t st) {
   }
   dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, a.batches * a.ksplit);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
-  gemm_kernel<K><<<grid, 256, 0, st>>>(a, g.ep);
-  return cudaGetLastError();
+  return launch_pdl(gemm_kernel<K>, grid, dim3(256), 0, st, a, g.ep);
 }
 
 }  // namespace lr

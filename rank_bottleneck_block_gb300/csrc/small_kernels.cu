@@ -5,6 +5,8 @@ namespace lr {
 // ------------------------------------------------------------------ fold
 template <typename ST>
 __global__ void fold_kernel(ST* out, StackSrc src, int rows_each, int rows, int cols, const ST* g) {
+  pdl_wait();
+  pdl_trigger();
   const int groups = cols / 8;
   const long long total = 1LL * rows * groups;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
@@ -29,13 +31,14 @@ cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols
   if (total == 0) return cudaSuccess;
   int blocks = static_cast<int>((total + 255) / 256);
   if (blocks > 8192) blocks = 8192;
-  fold_kernel<ST><<<blocks, 256, 0, st>>>(out, src, rows_each, rows, cols, g);
-  return cudaGetLastError();
+  return launch_pdl(fold_kernel<ST>, dim3(blocks), dim3(256), 0, st, out, src, rows_each, rows, cols, g);
 }
 
 // ------------------------------------------------------------------ rstd
 template <typename ST>
 __global__ void rstd_kernel(const ST* x, int T, int d, float eps, float* s) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -56,13 +59,14 @@ template <typename ST>
 cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int blocks = (T + 7) / 8;
-  rstd_kernel<ST><<<blocks, 256, 0, st>>>(x, T, d, eps, s);
-  return cudaGetLastError();
+  return launch_pdl(rstd_kernel<ST>, dim3(blocks), dim3(256), 0, st, x, T, d, eps, s);
 }
 
 // ------------------------------------------------------------------ silu
 template <typename ST>
 __global__ void silu_kernel(SiluSlab a, SiluSlab b, int T) {
+  pdl_wait();
+  pdl_trigger();
   const long long ga = 1LL * T * (a.n / 8), gb = 1LL * T * (b.n / 8);
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < ga + gb; i += 256LL * gridDim.x) {
     const bool first = i < ga;
@@ -85,8 +89,7 @@ cudaError_t launch_silu(SiluSlab a, SiluSlab b, int T, cudaStream_t st) {
   if (total == 0) return cudaSuccess;
   int blocks = static_cast<int>((total + 255) / 256);
   if (blocks > 8192) blocks = 8192;
-  silu_kernel<ST><<<blocks, 256, 0, st>>>(a, b, T);
-  return cudaGetLastError();
+  return launch_pdl(silu_kernel<ST>, dim3(blocks), dim3(256), 0, st, a, b, T);
 }
 
 // ---------------------------------------------------------- wgrad reduce
@@ -95,6 +98,8 @@ cudaError_t launch_silu(SiluSlab a, SiluSlab b, int T, cudaStream_t st) {
 template <typename ST>
 __global__ void wgrad_reduce_kernel(const float* part, int nsplit, long long split_stride, int M, int N,
                                     const ST* colscale, WgradDst dst, int rows_each, float* dgpart) {
+  pdl_wait();
+  pdl_trigger();
   const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (n >= N) return;
   const int r0 = blockIdx.y * kReduceRows;
@@ -148,13 +153,15 @@ cudaError_t launch_wgrad_reduce(const float* part, int nsplit, long long split_s
                                 const ST* colscale, WgradDst dst, int rows_each, float* dgpart, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   dim3 grid((N / 4 + 127) / 128, (M + kReduceRows - 1) / kReduceRows);
-  wgrad_reduce_kernel<ST><<<grid, 128, 0, st>>>(part, nsplit, split_stride, M, N, colscale, dst, rows_each, dgpart);
-  return cudaGetLastError();
+  return launch_pdl(wgrad_reduce_kernel<ST>, grid, dim3(128), 0, st, part, nsplit, split_stride, M, N, colscale, dst,
+                    rows_each, dgpart);
 }
 
 // 32 columns per block; the 8 thread rows each sum every 8th partial, then the 8 sums are
 // added in a fixed order.
 __global__ void dg_finalize_kernel(const float* dgpart, int nparts, int N, float* dg) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8][33];
   const int n = blockIdx.x * 32 + threadIdx.x;
   float v = 0.f;
@@ -172,13 +179,14 @@ __global__ void dg_finalize_kernel(const float* dgpart, int nparts, int N, float
 
 cudaError_t launch_dg_finalize(const float* dgpart, int nparts, int N, float* dg, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
-  dg_finalize_kernel<<<(N + 31) / 32, dim3(32, 8), 0, st>>>(dgpart, nparts, N, dg);
-  return cudaGetLastError();
+  return launch_pdl(dg_finalize_kernel, dim3((N + 31) / 32), dim3(32, 8), 0, st, dgpart, nparts, N, dg);
 }
 
 // ------------------------------------------------------------------- mse
 template <typename ST>
 __global__ void mse_kernel(const ST* y, const ST* t, long long n, ST* dy, float* partials) {
+  pdl_wait();
+  pdl_trigger();
   const float scale = 2.f / static_cast<float>(n);
   float acc = 0.f;
   const long long groups = n / 8;
@@ -205,6 +213,8 @@ __global__ void mse_kernel(const ST* y, const ST* t, long long n, ST* dy, float*
 }
 
 __global__ void mse_finalize_kernel(const float* partials, int nparts, long long n, float* loss) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[256];
   float acc = 0.f;
   for (int i = threadIdx.x; i < nparts; i += 256) acc += partials[i];
@@ -220,15 +230,15 @@ __global__ void mse_finalize_kernel(const float* partials, int nparts, long long
 template <typename ST>
 cudaError_t launch_mse(const ST* y, const ST* t, long long n, ST* dy, float* partials, int nparts, float* loss,
                        cudaStream_t st) {
-  mse_kernel<ST><<<nparts, 256, 0, st>>>(y, t, n, dy, partials);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(mse_kernel<ST>, dim3(nparts), dim3(256), 0, st, y, t, n, dy, partials);
   if (e != cudaSuccess) return e;
-  mse_finalize_kernel<<<1, 256, 0, st>>>(partials, nparts, n, loss);
-  return cudaGetLastError();
+  return launch_pdl(mse_finalize_kernel, dim3(1), dim3(256), 0, st, partials, nparts, n, loss);
 }
 
 // ------------------------------------------------------ wait self-test
 __global__ void wait_selftest_kernel(unsigned* err, unsigned long long limit_ns) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint64_t bar;
   if (threadIdx.x != 0) return;
   const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
@@ -250,8 +260,7 @@ __global__ void wait_selftest_kernel(unsigned* err, unsigned long long limit_ns)
 }
 
 cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t st) {
-  wait_selftest_kernel<<<1, 32, 0, st>>>(err, limit_ns);
-  return cudaGetLastError();
+  return launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, st, err, limit_ns);
 }
 
 // ------------------------------------------------------ instantiations

@@ -428,6 +428,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   cluster_sync();  // both CTAs' barriers and TMEM exist before either touches the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above touches no global memory; it overlaps the previous kernel's tail.
+  pdl_wait();
 
   const int rank = static_cast<int>(blockIdx.x & 1);  // 0: leader (issues the MMAs)
   const int cid = static_cast<int>(blockIdx.x >> 1);
@@ -483,6 +485,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           }
         }
       }
+      pdl_trigger();  // every load of this CTA is issued: the next kernel may be scheduled
       if (!ok && rank == 0) {
         // Wait (bounded) for the pair's copies still in flight before the CTAs may exit.
         const long long n_back = issued < STAGES ? issued : STAGES;

@@ -126,11 +126,13 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   auto kern = gemm_kernel<K, BN, A_MN, B_MN>;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;  // a CTA pair on two SMs
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
@@ -158,6 +160,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   }
   const long long pairs = total < max_pairs[dev] ? total : max_pairs[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, sh, g.ep);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

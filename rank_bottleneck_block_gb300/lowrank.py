@@ -27,7 +27,8 @@ EXPORTED = [
     "lr_mlp_bwd", "lr_proj_saved_bytes", "lr_proj_fwd_workspace_bytes", "lr_proj_bwd_workspace_bytes",
     "lr_proj_fwd", "lr_proj_bwd", "lr_stack_workspace_bytes", "lr_stack_step", "lr_last_error",
     "lr_check_device_error", "lr_selftest_wait_timeout", "lr_version", "lr_launch_count",
-    "lr_profile_start", "lr_profile_stop", "lr_profile_count", "lr_profile_entry", "lr_proj_fwd_noalloc",
+    "lr_profile_start", "lr_profile_stop", "lr_profile_filter", "lr_profile_count", "lr_profile_entry",
+    "lr_proj_fwd_noalloc",
 ]
 
 
@@ -74,6 +75,7 @@ _SIGS = {
     "lr_launch_count": (ctypes.c_ulonglong, []),
     "lr_profile_start": (_I, []),
     "lr_profile_stop": (_I, []),
+    "lr_profile_filter": (_I, [ctypes.c_char_p]),
     "lr_profile_count": (_I, []),
     "lr_profile_entry": (_I, [_I, ctypes.c_char_p, _SZ, ctypes.POINTER(ctypes.c_longlong),
                               ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
@@ -237,6 +239,11 @@ def lr_launch_count() -> int:
 
 def lr_profile_start():
     _check(lib().lr_profile_start())
+
+
+def lr_profile_filter(prefix=None):
+    """Record only launches whose kernel name starts with `prefix` (None: all)."""
+    _check(lib().lr_profile_filter(prefix.encode() if prefix else None))
 
 
 def lr_profile_stop():
