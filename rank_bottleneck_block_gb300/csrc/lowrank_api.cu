@@ -165,7 +165,7 @@ struct Ctx {
 
 // Tile width of the SwiGLU dual GEMM (two accumulators: 256 fills TMEM with one buffer,
 // 128 keeps two buffers).
-static constexpr int kSwigluBn = 128;
+static constexpr int kSwigluBn = 256;
 
 // Tile width from waves of pair tiles (256 rows, one per SM pair); a 128-wide tile costs
 // about 0.75 of a 256-wide one (its shared-memory traffic per FLOP is 1.5x higher).

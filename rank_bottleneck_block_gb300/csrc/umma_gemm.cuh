@@ -323,11 +323,21 @@ struct Config {
   static constexpr int OUT_BUF = BM * OUT_ROW;
   static constexpr int AUX_BUF = BM * CW * 2;
   static constexpr int GROUP_SET = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;  // one chunk's staging
-  // Epilogues that read operand tiles get two staging sets per group (operand tiles two
-  // chunks ahead, output tiles in ping-pong) when the operand ring still keeps three
-  // stages; the others keep one set and a deeper ring.
+  static constexpr uint32_t ACC_COLS = NACC * BN;
+  // Two accumulator buffers when they fit in the 512 TMEM columns, else one.
+  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
+  // SwiGLU with 256-wide accumulators (a and b fill TMEM): the two accumulators complete
+  // and are released separately.  The epilogue first moves round(a) into registers (packed
+  // bf16, exact), which frees a's columns for the next tile while b still accumulates;
+  // then it consumes b, so the next tile's b accumulation overlaps the h math and stores.
+  static constexpr bool SPLIT = (K == EPI_SWIGLU) && NBUF == 1;
+  // Epilogues that read operand tiles, and the split SwiGLU, get two staging sets per group
+  // (operand tiles two chunks ahead, output tiles in ping-pong) when the operand ring still
+  // keeps three stages; the others keep one set and a deeper ring.
   static constexpr int EB =
-      D::NAUX > 0 && (kMaxSmem - 1024 - 2 * 2 * GROUP_SET - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3 ? 2 : 1;
+      (D::NAUX > 0 || SPLIT) && (kMaxSmem - 1024 - 2 * 2 * GROUP_SET - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3
+          ? 2
+          : 1;
   static constexpr int GROUP_BYTES = EB * GROUP_SET;
   static constexpr int EPI_BYTES = 2 * GROUP_BYTES;
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
@@ -336,9 +346,6 @@ struct Config {
   static constexpr int BAR_BYTES = 512 + 1024;  // barriers, then s for two tiles of 128 rows
   static constexpr int RING_BUDGET = kMaxSmem - 1024 - EPI_BYTES - BAR_BYTES;
   static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
-  static constexpr uint32_t ACC_COLS = NACC * BN;
-  // Two accumulator buffers when they fit in the 512 TMEM columns, else one.
-  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS <= 32    ? 32
                                         : NBUF * ACC_COLS <= 64  ? 64
                                         : NBUF * ACC_COLS <= 128 ? 128
@@ -515,12 +522,21 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
         const int buf = C::NBUF == 2 ? (it & 1) : 0;
         const uint32_t tph = static_cast<uint32_t>(C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1));
-        if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
-          ok = false;
-          break;
+        if (!C::SPLIT) {
+          if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
         for (int s = 0; s < NACC && ok; ++s) {
+          if (C::SPLIT) {  // accumulator s has its own full / empty barrier pair
+            if (!mbar_wait(&tempty[s], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS + s * BN;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
@@ -545,8 +561,9 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               ph ^= 1u;
             }
           }
+          if (C::SPLIT && ok) umma_commit(&tfull[s], kBoth);
         }
-        if (ok) umma_commit(&tfull[buf], kBoth);
+        if (!C::SPLIT && ok) umma_commit(&tfull[buf], kBoth);
       }
       // Drain: all MMAs issued by this thread have completed once this barrier flips.
       umma_commit(drain, 0x1);
@@ -683,91 +700,184 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
       for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, batch) != nullptr;
 
-      ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
-#pragma unroll 1
-      for (int c = g; c < NCH; c += 2, ++qi) {
-        const int b = EB == 2 ? (qi & 1) : 0;
-        if constexpr (NAUX > 0) {
-          const bool landed = mbar_wait(&abar[b], (aph >> b) & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
-          ok = landed && ok;
-          if (landed) {
-            aph ^= 1u << b;
-            pending &= ~(1u << b);
-          }
-        }
-        float v[NACC][CW];
+      if constexpr (C::SPLIT) {
+        // Phase 1: round(a) of this group's chunks into registers (bf16 pairs: exact, since
+        // a is stored rounded), optionally stored; then a's TMEM columns are released.
+        constexpr int NC = NCH / 2;
+        uint32_t apk[NC][CW / 2];
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        ok = mbar_wait(&tfull[0], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        tc_fence_after();
 #pragma unroll
-        for (int a = 0; a < NACC; ++a) tmem_ld32(t_row + a * BN + c * CW, v[a]);
-        tmem_ld_wait();
-        float av[NAUX > 0 ? NAUX : 1][CW];
+        for (int ci = 0; ci < NC; ++ci) {
+          const int c = g + 2 * ci;
+          float v[CW];
+          tmem_ld32(t_row + c * CW, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int a = 0; a < NAUX; ++a) {
-          if (aux_present[a]) {
-            const uint8_t* base = astage(b) + a * C::AUX_BUF;
-#pragma unroll
-            for (int j = 0; j < CW / 8; ++j) lds_bf16x8(smem_addr(base) + stage_off<64>(row, j), &av[a][8 * j]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < CW; ++j) av[a][j] = 0.f;
-          }
-        }
-        // The stores that last used this output set have finished reading it.
-        if (leader) {
-          if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          else bulk_wait_read_all();
-        }
-        ok = named_bar_and(bar_id, 128, ok);
-        if (!ok) break;
-        if constexpr (NAUX > 0) {
-          if (leader && pf_t < total) {  // refill the operand set this chunk has just released
-            issue_aux(pf_t, pf_c, b);
-            next_chunk(pf_t, pf_c);
-          }
-        }
-        float o[NOUT][CW];
-        float part = 0.f;
-        D::template run<bf16, CW>(ri, v, av, o, part);
-#pragma unroll
-        for (int oi = 0; oi < NOUT; ++oi) {
-          if (!present[oi]) continue;
-          uint8_t* base = ostage(b) + oi * C::OUT_BUF;
-          if constexpr (D::OUT_F32) {
-#pragma unroll
-            for (int j = 0; j < CW / 4; ++j) {
-              sts128(smem_addr(base) + stage_off<128>(row, j), __float_as_uint(o[oi][4 * j]),
-                     __float_as_uint(o[oi][4 * j + 1]), __float_as_uint(o[oi][4 * j + 2]),
-                     __float_as_uint(o[oi][4 * j + 3]));
+          for (int j = 0; j < CW / 2; ++j) apk[ci][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+          if (present[1]) {
+            const int b = EB == 2 ? (qi & 1) : 0;
+            if (leader) {
+              if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+              else bulk_wait_read_all();
             }
-          } else {
+            ok = named_bar_and(bar_id, 128, ok);
+            if (!ok) break;
+            const uint32_t base = smem_addr(ostage(b) + C::OUT_BUF);
 #pragma unroll
-            for (int j = 0; j < CW / 8; ++j) sts_bf16x8(smem_addr(base) + stage_off<64>(row, j), &o[oi][8 * j]);
+            for (int j = 0; j < CW / 8; ++j)
+              sts128(base + stage_off<64>(row, j), apk[ci][4 * j], apk[ci][4 * j + 1], apk[ci][4 * j + 2],
+                     apk[ci][4 * j + 3]);
+            fence_async_smem();
+            named_bar(bar_id, 128);
+            if (leader) {
+              tma_store_2d(&maps.out[batch][1], ostage(b) + C::OUT_BUF, nb * BN + c * CW, mb * BM);
+              bulk_commit();
+            }
+            ++qi;
           }
         }
-        if constexpr (D::ROWPART) {
-          const int n0c = nb * BN + c * CW;
-          if (m < sh.M && n0c < sh.N)
-            ep.rowpart[(static_cast<long long>(batch) * ep.rowpart_chunks + n0c / CW) * sh.M + m] = part;
-        }
-        fence_async_smem();
-        named_bar(bar_id, 128);
-        if (leader) {
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[0]), 0));
+        // Phase 2: b, h = SiLU(a) b; outputs h and (optionally) b.
+        ok = mbar_wait(&tfull[1], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        tc_fence_after();
 #pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+          const int c = g + 2 * ci;
+          const int b = EB == 2 ? (qi & 1) : 0;
+          float v[CW];
+          tmem_ld32(t_row + BN + c * CW, v);
+          tmem_ld_wait();
+          if (leader) {
+            if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            else bulk_wait_read_all();
+          }
+          ok = named_bar_and(bar_id, 128, ok);
+          if (!ok) break;
+          uint32_t bpk[CW / 2];  // round(b), packed; v becomes h = SiLU(a) b
+#pragma unroll
+          for (int j = 0; j < CW / 2; ++j) {
+            float a0, a1, b0, b1;
+            unpack_bf16x2(apk[ci][j], a0, a1);
+            bpk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+            unpack_bf16x2(bpk[j], b0, b1);
+            v[2 * j] = silu<bf16>(a0) * b0;
+            v[2 * j + 1] = silu<bf16>(a1) * b1;
+          }
+          const uint32_t hbase = smem_addr(ostage(b));
+#pragma unroll
+          for (int j = 0; j < CW / 8; ++j) sts_bf16x8(hbase + stage_off<64>(row, j), &v[8 * j]);
+          if (present[2]) {
+            const uint32_t bbase = smem_addr(ostage(b) + 2 * C::OUT_BUF);
+#pragma unroll
+            for (int j = 0; j < CW / 8; ++j)
+              sts128(bbase + stage_off<64>(row, j), bpk[4 * j], bpk[4 * j + 1], bpk[4 * j + 2], bpk[4 * j + 3]);
+          }
+          fence_async_smem();
+          named_bar(bar_id, 128);
+          if (leader) {
+            if (present[0]) tma_store_2d(&maps.out[batch][0], ostage(b), nb * BN + c * CW, mb * BM);
+            if (present[2])
+              tma_store_2d(&maps.out[batch][2], ostage(b) + 2 * C::OUT_BUF, nb * BN + c * CW, mb * BM);
+            bulk_commit();
+          }
+          ++qi;
+        }
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[1]), 0));
+      } else {
+        ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
+  #pragma unroll 1
+        for (int c = g; c < NCH; c += 2, ++qi) {
+          const int b = EB == 2 ? (qi & 1) : 0;
+          if constexpr (NAUX > 0) {
+            const bool landed = mbar_wait(&abar[b], (aph >> b) & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
+            ok = landed && ok;
+            if (landed) {
+              aph ^= 1u << b;
+              pending &= ~(1u << b);
+            }
+          }
+          float v[NACC][CW];
+  #pragma unroll
+          for (int a = 0; a < NACC; ++a) tmem_ld32(t_row + a * BN + c * CW, v[a]);
+          tmem_ld_wait();
+          float av[NAUX > 0 ? NAUX : 1][CW];
+  #pragma unroll
+          for (int a = 0; a < NAUX; ++a) {
+            if (aux_present[a]) {
+              const uint8_t* base = astage(b) + a * C::AUX_BUF;
+  #pragma unroll
+              for (int j = 0; j < CW / 8; ++j) lds_bf16x8(smem_addr(base) + stage_off<64>(row, j), &av[a][8 * j]);
+            } else {
+  #pragma unroll
+              for (int j = 0; j < CW; ++j) av[a][j] = 0.f;
+            }
+          }
+          // The stores that last used this output set have finished reading it.
+          if (leader) {
+            if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            else bulk_wait_read_all();
+          }
+          ok = named_bar_and(bar_id, 128, ok);
+          if (!ok) break;
+          if constexpr (NAUX > 0) {
+            if (leader && pf_t < total) {  // refill the operand set this chunk has just released
+              issue_aux(pf_t, pf_c, b);
+              next_chunk(pf_t, pf_c);
+            }
+          }
+          float o[NOUT][CW];
+          float part = 0.f;
+          D::template run<bf16, CW>(ri, v, av, o, part);
+  #pragma unroll
           for (int oi = 0; oi < NOUT; ++oi) {
             if (!present[oi]) continue;
-            if constexpr (D::OUT_F32)
-              tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM, split);
-            else
-              tma_store_2d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM);
+            uint8_t* base = ostage(b) + oi * C::OUT_BUF;
+            if constexpr (D::OUT_F32) {
+  #pragma unroll
+              for (int j = 0; j < CW / 4; ++j) {
+                sts128(smem_addr(base) + stage_off<128>(row, j), __float_as_uint(o[oi][4 * j]),
+                       __float_as_uint(o[oi][4 * j + 1]), __float_as_uint(o[oi][4 * j + 2]),
+                       __float_as_uint(o[oi][4 * j + 3]));
+              }
+            } else {
+  #pragma unroll
+              for (int j = 0; j < CW / 8; ++j) sts_bf16x8(smem_addr(base) + stage_off<64>(row, j), &o[oi][8 * j]);
+            }
           }
-          bulk_commit();
+          if constexpr (D::ROWPART) {
+            const int n0c = nb * BN + c * CW;
+            if (m < sh.M && n0c < sh.N)
+              ep.rowpart[(static_cast<long long>(batch) * ep.rowpart_chunks + n0c / CW) * sh.M + m] = part;
+          }
+          fence_async_smem();
+          named_bar(bar_id, 128);
+          if (leader) {
+  #pragma unroll
+            for (int oi = 0; oi < NOUT; ++oi) {
+              if (!present[oi]) continue;
+              if constexpr (D::OUT_F32)
+                tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM, split);
+              else
+                tma_store_2d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM);
+            }
+            bulk_commit();
+          }
         }
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[buf]), 0));  // the leader's MMA reuses it
       }
-      if (!ok) break;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[buf]), 0));  // the leader's MMA reuses it
     }
     if (leader) {
       bulk_wait_all();
