@@ -51,6 +51,7 @@ namespace umma {
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16 along K
 constexpr int CW = 32;  // epilogue chunk width (columns)
+constexpr int ER = 32;  // rows of an epilogue staging tile: one warp's TMEM lane quarter
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -211,24 +212,6 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void named_bar(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Barrier over `nthreads` threads that also ANDs a predicate across them.
-__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(out)
-      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
-      : "memory");
-  return out != 0;
-}
-
 __device__ __forceinline__ void tmap_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -320,9 +303,9 @@ struct Config {
   static constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's half of the B tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int OUT_ROW = CW * (D::OUT_F32 ? 4 : 2);
-  static constexpr int OUT_BUF = BM * OUT_ROW;
-  static constexpr int AUX_BUF = BM * CW * 2;
-  static constexpr int GROUP_SET = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;  // one chunk's staging
+  static constexpr int OUT_BUF = ER * OUT_ROW;  // one warp's rows of a chunk
+  static constexpr int AUX_BUF = ER * CW * 2;
+  static constexpr int WARP_SET = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;  // one chunk's staging
   static constexpr uint32_t ACC_COLS = NACC * BN;
   // Two accumulator buffers when they fit in the 512 TMEM columns, else one.
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
@@ -331,15 +314,16 @@ struct Config {
   // bf16, exact), which frees a's columns for the next tile while b still accumulates;
   // then it consumes b, so the next tile's b accumulation overlaps the h math and stores.
   static constexpr bool SPLIT = (K == EPI_SWIGLU) && NBUF == 1;
-  // Epilogues that read operand tiles, and the split SwiGLU, get two staging sets per group
+  // Epilogues that read operand tiles, and the split SwiGLU, get two staging sets per warp
   // (operand tiles two chunks ahead, output tiles in ping-pong) when the operand ring still
   // keeps three stages; the others keep one set and a deeper ring.
   static constexpr int EB =
-      (D::NAUX > 0 || SPLIT) && (kMaxSmem - 1024 - 2 * 2 * GROUP_SET - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3
+      (D::NAUX > 0 || SPLIT) &&
+              (kMaxSmem - 1024 - kEpiWarps * 2 * WARP_SET - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3
           ? 2
           : 1;
-  static constexpr int GROUP_BYTES = EB * GROUP_SET;
-  static constexpr int EPI_BYTES = 2 * GROUP_BYTES;
+  static constexpr int WARP_BYTES = EB * WARP_SET;
+  static constexpr int EPI_BYTES = kEpiWarps * WARP_BYTES;
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
   static constexpr bool STATS = (K == EPI_NORM_SILU);
   static constexpr int THREADS = kThreads + (STATS ? 128 : 0);
@@ -355,7 +339,8 @@ struct Config {
   static_assert(NBUF * ACC_COLS <= 512, "accumulator buffers must fit in TMEM");
   static_assert(STAGES >= 2, "need at least two stages");
   static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256 (each CTA stages BN/2, whole 64-column chunks)");
-  static_assert((BN / CW) % 2 == 0, "both epilogue groups need the same number of chunks");
+  static_assert((BN / CW) % 2 == 0, "both epilogue warps of a lane quarter need the same number of chunks");
+  static_assert(WARP_SET % 1024 == 0 || (WARP_SET % 512 == 0 && !D::OUT_F32), "staging tiles keep swizzle alignment");
   static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
 };
 
@@ -393,8 +378,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   uint64_t* tfull = consumed + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* aux_full = drain + 1;  // per epilogue group and staging set
-  uint64_t* sfull = aux_full + 4;   // stats -> epilogue, per TMEM buffer
+  uint64_t* aux_full = drain + 1;             // per epilogue warp and staging set
+  uint64_t* sfull = aux_full + 2 * kEpiWarps;  // stats -> epilogue, per TMEM buffer
   uint64_t* sempty = sfull + 2;     // epilogue -> stats, per TMEM buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -412,12 +397,11 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 2 * kEpiWarps);  // leader: one arrive per epilogue warp of both CTAs
-      mbar_init(&aux_full[2 * i], 1);
-      mbar_init(&aux_full[2 * i + 1], 1);
       mbar_init(&sfull[i], 4);
       mbar_init(&sempty[i], kEpiWarps);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&aux_full[i], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
@@ -623,23 +607,26 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------ epilogue warps
+    // Each epilogue warp is an independent unit: warp (g, q) owns TMEM lane quarter q (rows
+    // 32 q .. 32 q + 31 of the CTA's tile) and the chunks c = g, g+2, ... of each tile.  Its
+    // lane 0 loads the chunk's operand tiles and stores its output tiles (32 x 32 boxes)
+    // through the warp's own staging sets; the warp synchronises only with itself.
     constexpr int NAUX = D::NAUX, NOUT = D::NOUT;
     constexpr int NCH = BN / CW;
     constexpr int EB = C::EB;
     const int ew = warp - 2;
-    const int g = ew >> 2;   // group: chunks g, g+2, ...
+    const int g = ew >> 2;   // chunk parity
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    const bool leader = (ew & 3) == 0 && lane == 0;
-    const int bar_id = 1 + g;
-    uint8_t* gstage = sE + g * C::GROUP_BYTES;  // EB sets of [NOUT output tiles | NAUX operand tiles]
-    auto ostage = [&](int b) { return gstage + b * C::GROUP_SET; };
-    auto astage = [&](int b) { return gstage + b * C::GROUP_SET + NOUT * C::OUT_BUF; };
-    uint64_t* abar = &aux_full[2 * g];
+    const bool leader = lane == 0;
+    uint8_t* wstage = sE + ew * C::WARP_BYTES;  // EB sets of [NOUT output tiles | NAUX operand tiles]
+    auto ostage = [&](int b) { return wstage + b * C::WARP_SET; };
+    auto astage = [&](int b) { return wstage + b * C::WARP_SET + NOUT * C::OUT_BUF; };
+    uint64_t* abar = &aux_full[2 * ew];
     uint32_t aph = 0u;      // bit b: phase parity of abar[b]
-    uint32_t pending = 0u;  // leader, bit b: an operand-tile load is in flight on abar[b]
+    uint32_t pending = 0u;  // lane 0, bit b: an operand-tile load is in flight on abar[b]
 
-    // The group's chunk sequence: (tile, c) for c = g, g+2, ... of each of this CTA's tiles.
+    // The warp's chunk sequence: (tile, c) for c = g, g+2, ... of each of this CTA's tiles.
     auto next_chunk = [&](int& t, int& c) {
       c += 2;
       if (c >= NCH) {
@@ -658,8 +645,16 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
       for (int a = 0; a < NAUX; ++a)
         if (epi_aux_ptr(ep, a, batch))
-          tma_load_2d(astage(b) + a * C::AUX_BUF, &maps.aux[batch][a], &abar[b], nb * BN + c * CW, mb * BM);
+          tma_load_2d(astage(b) + a * C::AUX_BUF, &maps.aux[batch][a], &abar[b], nb * BN + c * CW,
+                      mb * BM + q * ER);
       pending |= 1u << b;
+    };
+    // Lane 0: the stores that last used output set b have finished reading it.
+    auto wait_set_free = [&]() {
+      if (leader) {
+        if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        else bulk_wait_read_all();
+      }
     };
     // Prefetch cursor: the next chunk whose operand tiles are not yet requested.
     int pf_t = cid, pf_c = g;
@@ -674,7 +669,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 
     bool ok = true;
     int it = 0;
-    int qi = 0;  // index of the group's current chunk in its sequence
+    int qi = 0;  // index of the warp's current chunk in its sequence
     for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
       decode_tile(sh, tile, rank, split, batch, mb, nb);
@@ -683,6 +678,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       const int sbuf = it & 1;  // statistics double buffer (independent of TMEM)
       const uint32_t sph = static_cast<uint32_t>((it >> 1) & 1);
       const int m = mb * BM + row;
+      const int r0 = mb * BM + q * ER;  // first row of this warp's boxes
       RowIn ri;
       if constexpr (C::STATS) {
         ri.k = 0.f;
@@ -701,7 +697,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, batch) != nullptr;
 
       if constexpr (C::SPLIT) {
-        // Phase 1: round(a) of this group's chunks into registers (bf16 pairs: exact, since
+        // Phase 1: round(a) of this warp's chunks into registers (bf16 pairs: exact, since
         // a is stored rounded), optionally stored; then a's TMEM columns are released.
         constexpr int NC = NCH / 2;
         uint32_t apk[NC][CW / 2];
@@ -718,21 +714,18 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           for (int j = 0; j < CW / 2; ++j) apk[ci][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
           if (present[1]) {
             const int b = EB == 2 ? (qi & 1) : 0;
-            if (leader) {
-              if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-              else bulk_wait_read_all();
-            }
-            ok = named_bar_and(bar_id, 128, ok);
+            wait_set_free();
+            ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const uint32_t base = smem_addr(ostage(b) + C::OUT_BUF);
 #pragma unroll
             for (int j = 0; j < CW / 8; ++j)
-              sts128(base + stage_off<64>(row, j), apk[ci][4 * j], apk[ci][4 * j + 1], apk[ci][4 * j + 2],
+              sts128(base + stage_off<64>(lane, j), apk[ci][4 * j], apk[ci][4 * j + 1], apk[ci][4 * j + 2],
                      apk[ci][4 * j + 3]);
             fence_async_smem();
-            named_bar(bar_id, 128);
+            __syncwarp();
             if (leader) {
-              tma_store_2d(&maps.out[batch][1], ostage(b) + C::OUT_BUF, nb * BN + c * CW, mb * BM);
+              tma_store_2d(&maps.out[batch][1], ostage(b) + C::OUT_BUF, nb * BN + c * CW, r0);
               bulk_commit();
             }
             ++qi;
@@ -752,11 +745,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           float v[CW];
           tmem_ld32(t_row + BN + c * CW, v);
           tmem_ld_wait();
-          if (leader) {
-            if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            else bulk_wait_read_all();
-          }
-          ok = named_bar_and(bar_id, 128, ok);
+          wait_set_free();
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           uint32_t bpk[CW / 2];  // round(b), packed; v becomes h = SiLU(a) b
 #pragma unroll
@@ -770,19 +760,18 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           }
           const uint32_t hbase = smem_addr(ostage(b));
 #pragma unroll
-          for (int j = 0; j < CW / 8; ++j) sts_bf16x8(hbase + stage_off<64>(row, j), &v[8 * j]);
+          for (int j = 0; j < CW / 8; ++j) sts_bf16x8(hbase + stage_off<64>(lane, j), &v[8 * j]);
           if (present[2]) {
             const uint32_t bbase = smem_addr(ostage(b) + 2 * C::OUT_BUF);
 #pragma unroll
             for (int j = 0; j < CW / 8; ++j)
-              sts128(bbase + stage_off<64>(row, j), bpk[4 * j], bpk[4 * j + 1], bpk[4 * j + 2], bpk[4 * j + 3]);
+              sts128(bbase + stage_off<64>(lane, j), bpk[4 * j], bpk[4 * j + 1], bpk[4 * j + 2], bpk[4 * j + 3]);
           }
           fence_async_smem();
-          named_bar(bar_id, 128);
+          __syncwarp();
           if (leader) {
-            if (present[0]) tma_store_2d(&maps.out[batch][0], ostage(b), nb * BN + c * CW, mb * BM);
-            if (present[2])
-              tma_store_2d(&maps.out[batch][2], ostage(b) + 2 * C::OUT_BUF, nb * BN + c * CW, mb * BM);
+            if (present[0]) tma_store_2d(&maps.out[batch][0], ostage(b), nb * BN + c * CW, r0);
+            if (present[2]) tma_store_2d(&maps.out[batch][2], ostage(b) + 2 * C::OUT_BUF, nb * BN + c * CW, r0);
             bulk_commit();
           }
           ++qi;
@@ -795,7 +784,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         tc_fence_after();
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
-  #pragma unroll 1
+#pragma unroll 1
         for (int c = g; c < NCH; c += 2, ++qi) {
           const int b = EB == 2 ? (qi & 1) : 0;
           if constexpr (NAUX > 0) {
@@ -807,27 +796,23 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
             }
           }
           float v[NACC][CW];
-  #pragma unroll
+#pragma unroll
           for (int a = 0; a < NACC; ++a) tmem_ld32(t_row + a * BN + c * CW, v[a]);
           tmem_ld_wait();
           float av[NAUX > 0 ? NAUX : 1][CW];
-  #pragma unroll
+#pragma unroll
           for (int a = 0; a < NAUX; ++a) {
             if (aux_present[a]) {
               const uint8_t* base = astage(b) + a * C::AUX_BUF;
-  #pragma unroll
-              for (int j = 0; j < CW / 8; ++j) lds_bf16x8(smem_addr(base) + stage_off<64>(row, j), &av[a][8 * j]);
+#pragma unroll
+              for (int j = 0; j < CW / 8; ++j) lds_bf16x8(smem_addr(base) + stage_off<64>(lane, j), &av[a][8 * j]);
             } else {
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < CW; ++j) av[a][j] = 0.f;
             }
           }
-          // The stores that last used this output set have finished reading it.
-          if (leader) {
-            if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            else bulk_wait_read_all();
-          }
-          ok = named_bar_and(bar_id, 128, ok);
+          wait_set_free();
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           if constexpr (NAUX > 0) {
             if (leader && pf_t < total) {  // refill the operand set this chunk has just released
@@ -838,20 +823,20 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           float o[NOUT][CW];
           float part = 0.f;
           D::template run<bf16, CW>(ri, v, av, o, part);
-  #pragma unroll
+#pragma unroll
           for (int oi = 0; oi < NOUT; ++oi) {
             if (!present[oi]) continue;
             uint8_t* base = ostage(b) + oi * C::OUT_BUF;
             if constexpr (D::OUT_F32) {
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < CW / 4; ++j) {
-                sts128(smem_addr(base) + stage_off<128>(row, j), __float_as_uint(o[oi][4 * j]),
+                sts128(smem_addr(base) + stage_off<128>(lane, j), __float_as_uint(o[oi][4 * j]),
                        __float_as_uint(o[oi][4 * j + 1]), __float_as_uint(o[oi][4 * j + 2]),
                        __float_as_uint(o[oi][4 * j + 3]));
               }
             } else {
-  #pragma unroll
-              for (int j = 0; j < CW / 8; ++j) sts_bf16x8(smem_addr(base) + stage_off<64>(row, j), &o[oi][8 * j]);
+#pragma unroll
+              for (int j = 0; j < CW / 8; ++j) sts_bf16x8(smem_addr(base) + stage_off<64>(lane, j), &o[oi][8 * j]);
             }
           }
           if constexpr (D::ROWPART) {
@@ -860,15 +845,15 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               ep.rowpart[(static_cast<long long>(batch) * ep.rowpart_chunks + n0c / CW) * sh.M + m] = part;
           }
           fence_async_smem();
-          named_bar(bar_id, 128);
+          __syncwarp();
           if (leader) {
-  #pragma unroll
+#pragma unroll
             for (int oi = 0; oi < NOUT; ++oi) {
               if (!present[oi]) continue;
               if constexpr (D::OUT_F32)
-                tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM, split);
+                tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split);
               else
-                tma_store_2d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, mb * BM);
+                tma_store_2d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0);
             }
             bulk_commit();
           }

@@ -53,18 +53,18 @@ inline bool encode_operand(CUtensorMap* m, const void* ptr, long long inner, lon
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// bf16 [M, N] epilogue tile map (32 columns x 128 rows, 64-byte swizzle).
+// bf16 [M, N] epilogue tile map (32 columns x 32 rows: one warp's rows, 64-byte swizzle).
 inline bool encode_epi_bf16(CUtensorMap* m, const void* ptr, long long N, long long M, long long ld) {
   const long long dims[2] = {N, M}, strides[1] = {ld};
-  const int box[2] = {CW, BM};
+  const int box[2] = {CW, ER};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// fp32 [splits, M, N] partial-output map (32 columns x 128 rows x 1 split, 128-byte swizzle).
+// fp32 [splits, M, N] partial-output map (32 columns x 32 rows x 1 split, 128-byte swizzle).
 inline bool encode_epi_f32(CUtensorMap* m, const void* ptr, long long N, long long M, long long ld, long long splits,
                            long long split_stride) {
   const long long dims[3] = {N, M, splits}, strides[2] = {ld, split_stride};
-  const int box[3] = {CW, BM, 1};
+  const int box[3] = {CW, ER, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
