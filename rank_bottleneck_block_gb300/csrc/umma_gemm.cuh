@@ -265,6 +265,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 16 consecutive fp32 columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
@@ -742,30 +755,32 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         for (int ci = 0; ci < NC; ++ci) {
           const int c = g + 2 * ci;
           const int b = EB == 2 ? (qi & 1) : 0;
-          float v[CW];
-          tmem_ld32(t_row + BN + c * CW, v);
-          tmem_ld_wait();
           wait_set_free();
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          uint32_t bpk[CW / 2];  // round(b), packed; v becomes h = SiLU(a) b
-#pragma unroll
-          for (int j = 0; j < CW / 2; ++j) {
-            float a0, a1, b0, b1;
-            unpack_bf16x2(apk[ci][j], a0, a1);
-            bpk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-            unpack_bf16x2(bpk[j], b0, b1);
-            v[2 * j] = silu<bf16>(a0) * b0;
-            v[2 * j + 1] = silu<bf16>(a1) * b1;
-          }
           const uint32_t hbase = smem_addr(ostage(b));
+          const uint32_t bbase = smem_addr(ostage(b) + 2 * C::OUT_BUF);
 #pragma unroll
-          for (int j = 0; j < CW / 8; ++j) sts_bf16x8(hbase + stage_off<64>(lane, j), &v[8 * j]);
-          if (present[2]) {
-            const uint32_t bbase = smem_addr(ostage(b) + 2 * C::OUT_BUF);
+          for (int hh = 0; hh < 2; ++hh) {  // two halves of 16 columns keep the live registers down
+            float v[CW / 2];
+            tmem_ld16(t_row + BN + c * CW + hh * (CW / 2), v);
+            tmem_ld_wait();
+            uint32_t bpk[CW / 4];  // round(b), packed; v becomes h = SiLU(a) b
 #pragma unroll
-            for (int j = 0; j < CW / 8; ++j)
-              sts128(bbase + stage_off<64>(lane, j), bpk[4 * j], bpk[4 * j + 1], bpk[4 * j + 2], bpk[4 * j + 3]);
+            for (int j = 0; j < CW / 4; ++j) {
+              float a0, a1, b0, b1;
+              unpack_bf16x2(apk[ci][hh * (CW / 4) + j], a0, a1);
+              bpk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+              unpack_bf16x2(bpk[j], b0, b1);
+              v[2 * j] = silu<bf16>(a0) * b0;
+              v[2 * j + 1] = silu<bf16>(a1) * b1;
+            }
+            sts_bf16x8(hbase + stage_off<64>(lane, 2 * hh), &v[0]);
+            sts_bf16x8(hbase + stage_off<64>(lane, 2 * hh + 1), &v[8]);
+            if (present[2]) {
+              sts128(bbase + stage_off<64>(lane, 2 * hh), bpk[0], bpk[1], bpk[2], bpk[3]);
+              sts128(bbase + stage_off<64>(lane, 2 * hh + 1), bpk[4], bpk[5], bpk[6], bpk[7]);
+            }
           }
           fence_async_smem();
           __syncwarp();
