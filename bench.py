@@ -31,6 +31,34 @@ NOMINAL = {"tflops": 2250.0, "hbm_gbs": 8000.0}
 FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, averaged over the launches of
+# one step) from an ncu capture of the named kernel.  A figure holds only for the kernel sources it was
+# taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
+TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
+NCU_TRAFFIC = {
+    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * (182.678272e6 + 562.732032e6),
+                          "sources_sha256": "2441a17e0632d0e3b51799380063af9b383a9865bb17d66b11e821eb0191d96b",
+                          "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
+}
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "rank_bottleneck_block_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel: str):
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec is None or rec["sources_sha256"] != kernel_sources_sha256():
+        return None, "no ncu capture of the current kernel sources"
+    return rec["bytes_per_launch"], rec["profile"]
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -242,32 +270,31 @@ def run_ours(a, ws, rank, local):
     value = aggregate(shape.T * a.steps, ws, total_s_max)
 
     # ------------------------------------------------ end to end (host buffers)
+    # Inputs x and dout come from pinned host memory and out, dx go back every step; the
+    # copies of neighbouring steps run on two copy streams and overlap the compute.
+    from rank_bottleneck_block_gb300.runner import HostPipeline
+
     xh = case["x"].pin_memory()
     gh = case["G"].pin_memory()
     outh = torch.empty_like(xh).pin_memory()
     dxh = torch.empty_like(xh).pin_memory()
-    xd, gd = blk.t["x"], blk.t["G"]
-    e2e_steps = max(3, min(a.steps, 50))
+    pipe = HostPipeline(blk)
+    pipe.run([xh], [gh], outh, dxh, 3, stream)  # warm-up of the copy path
+    e2e_steps = max(3, min(a.steps, 200))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     ev0.record(stream)
-    for _ in range(e2e_steps):
-        xd.copy_(xh, non_blocking=True)
-        gd.copy_(gh, non_blocking=True)
-        blk.forward(xd)
-        blk.backward(gd, xd)
-        outh.copy_(blk.out, non_blocking=True)
-        dxh.copy_(blk.dx, non_blocking=True)
+    pipe.run([xh], [gh], outh, dxh, e2e_steps, stream)
     ev1.record(stream)
     torch.cuda.synchronize()
+    L.lr_check_device_error()
     e2e_s = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, ws)
-    h2d = xh.numel() * xh.element_size() + gh.numel() * gh.element_size()
-    d2h = outh.numel() * outh.element_size() + dxh.numel() * dxh.element_size()
+    h2d, d2h = pipe.bytes_per_step()
     e2e = {"value": aggregate(shape.T * e2e_steps, ws, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h,
-           "api": "lr_mlp_fwd + lr_mlp_bwd with x and dout copied in from pinned host memory and out, dx "
-                  "copied back, every step"}
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "api": "lr_mlp_fwd + lr_mlp_bwd on device copies of pinned host x and dout, out and dx copied back, "
+                  "every step; copies on two side streams overlap the neighbouring steps' compute"}
 
     # ------------------------------------------------ rooflines
     pk = peaks()
@@ -281,6 +308,11 @@ def run_ours(a, ws, rank, local):
                 "flops_per_launch": dom["flops"] / dom["launches"],
                 "share_of_step": round(dom["ms"] / a.steps / ms_per_step, 4),
                 "traffic": None}
+    traffic, tsrc = ncu_traffic(dom_name)
+    roofline["traffic"] = traffic
+    roofline["traffic_source"] = tsrc
+    if traffic:
+        roofline["traffic_gbs"] = round(traffic / (dom["ms"] / dom["launches"] / 1e3) / 1e9, 1)
     ms_step_s = ms_per_step / 1e3
     t_nom = max(flops / (NOMINAL["tflops"] * 1e12), nbytes / (NOMINAL["hbm_gbs"] * 1e9))
     t_meas = max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))

@@ -55,26 +55,85 @@ class MlpBlock:
         t = self.t
         return (L.pair(t["A_gate"], t["B_gate"]), L.pair(t["A_up"], t["B_up"]), L.pair(t["A_down"], t["B_down"]))
 
-    def forward(self, x: Optional[torch.Tensor] = None, stream=None):
+    def forward(self, x: Optional[torch.Tensor] = None, stream=None, out: Optional[torch.Tensor] = None):
         s = self.s
         x = self.t["x"] if x is None else x
-        L.lr_mlp_fwd(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, x, self.t["g"], *self.pairs(), self.out,
+        out = self.out if out is None else out
+        L.lr_mlp_fwd(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, x, self.t["g"], *self.pairs(), out,
                      self.saved, self.ws_f, stream)
-        return self.out
+        return out
 
-    def backward(self, dout: Optional[torch.Tensor] = None, x: Optional[torch.Tensor] = None, stream=None):
+    def backward(self, dout: Optional[torch.Tensor] = None, x: Optional[torch.Tensor] = None, stream=None,
+                 dx: Optional[torch.Tensor] = None):
         s, gr = self.s, self.grads
         x = self.t["x"] if x is None else x
         dout = self.t["G"] if dout is None else dout
+        dx = self.dx if dx is None else dx
         L.lr_mlp_bwd(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, x, self.t["g"], *self.pairs(), self.saved, dout,
-                     self.dx, self.dg, L.pair_grad(gr["dA_gate"], gr["dB_gate"]),
+                     dx, self.dg, L.pair_grad(gr["dA_gate"], gr["dB_gate"]),
                      L.pair_grad(gr["dA_up"], gr["dB_up"]), L.pair_grad(gr["dA_down"], gr["dB_down"]), self.ws_b,
                      stream)
-        return self.dx
+        return dx
 
     def step(self, stream=None):
         self.forward(stream=stream)
         self.backward(stream=stream)
+
+
+class HostPipeline:
+    """fwd + bwd of an MlpBlock over batches that live in (pinned) host memory.
+
+    Step i copies x_i and dout_i to the device on a copy stream, runs the block on the
+    compute stream and copies out_i and dx_i back on a second copy stream; with two device
+    buffer sets the copies of steps i+1 and i-1 overlap the compute of step i.
+    """
+
+    def __init__(self, blk: MlpBlock):
+        self.blk = blk
+        s, dev = blk.s, blk.device
+        td = _tdt(s.dtype)
+        self.x = [torch.empty(s.T, s.d, dtype=td, device=dev) for _ in range(2)]
+        self.G = [torch.empty(s.T, s.d, dtype=td, device=dev) for _ in range(2)]
+        self.out = [torch.empty(s.T, s.d, dtype=td, device=dev) for _ in range(2)]
+        self.dx = [torch.empty(s.T, s.d, dtype=td, device=dev) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the set copied in
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]  # compute of the set finished
+        self.ev_read = [torch.cuda.Event() for _ in range(2)]  # results of the set copied out
+
+    def bytes_per_step(self):
+        e = self.x[0].element_size() * self.x[0].numel()
+        return 2 * e, 2 * e  # (host -> device: x, dout), (device -> host: out, dx)
+
+    def run(self, xh: List[torch.Tensor], gh: List[torch.Tensor], outh: torch.Tensor, dxh: torch.Tensor,
+            steps: int, stream=None):
+        """Runs `steps` steps on batches xh[i % len], gh[i % len]; results land in outh, dxh."""
+        blk = self.blk
+        comp = stream if stream is not None else torch.cuda.current_stream(blk.device)
+        self.h2d.wait_stream(comp)
+        self.d2h.wait_stream(comp)
+        for i in range(steps):
+            b = i % 2
+            with torch.cuda.stream(self.h2d):
+                if i >= 2:
+                    self.h2d.wait_event(self.ev_done[b])  # step i-2 no longer reads this input set
+                self.x[b].copy_(xh[i % len(xh)], non_blocking=True)
+                self.G[b].copy_(gh[i % len(gh)], non_blocking=True)
+                self.ev_in[b].record(self.h2d)
+            comp.wait_event(self.ev_in[b])
+            if i >= 2:
+                comp.wait_event(self.ev_read[b])  # step i-2's results have been copied out of this set
+            blk.forward(self.x[b], stream=comp.cuda_stream, out=self.out[b])
+            blk.backward(self.G[b], self.x[b], stream=comp.cuda_stream, dx=self.dx[b])
+            self.ev_done[b].record(comp)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.ev_done[b])
+                outh.copy_(self.out[b], non_blocking=True)
+                dxh.copy_(self.dx[b], non_blocking=True)
+                self.ev_read[b].record(self.d2h)
+        comp.wait_stream(self.d2h)
+        comp.wait_stream(self.h2d)
 
 
 class ProjGroup:
