@@ -68,11 +68,9 @@ struct Num;
 template <>
 struct Num<bf16> {
   static __device__ __forceinline__ float round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
-  // logistic(u) = 1 / (1 + e^-u); the fast intrinsic is accurate far beyond bf16 storage precision.
-  static __device__ __forceinline__ float logistic(float u) {
-    u = fmaxf(u, -80.f);
-    return __fdividef(1.f, 1.f + __expf(-u));
-  }
+  // logistic(u) = 1 / (1 + e^-u); the fast intrinsics are accurate far beyond bf16 storage
+  // precision.  For u below about -88 e^-u overflows to +inf and the quotient is exactly 0.
+  static __device__ __forceinline__ float logistic(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
 };
 
 template <>

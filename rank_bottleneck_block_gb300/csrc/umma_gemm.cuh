@@ -318,7 +318,7 @@ struct Config {
   static constexpr int OUT_ROW = CW * (D::OUT_F32 ? 4 : 2);
   static constexpr int OUT_BUF = ER * OUT_ROW;  // one warp's rows of a chunk
   static constexpr int AUX_BUF = ER * CW * 2;
-  static constexpr int WARP_SET = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;  // one chunk's staging
+  static constexpr int WARP_SET_BASE = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;  // one chunk's staging
   static constexpr uint32_t ACC_COLS = NACC * BN;
   // Two accumulator buffers when they fit in the 512 TMEM columns, else one.
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
@@ -330,12 +330,16 @@ struct Config {
   // Epilogues that read operand tiles, and the split SwiGLU, get two staging sets per warp
   // (operand tiles two chunks ahead, output tiles in ping-pong) when the operand ring still
   // keeps three stages; the others keep one set and a deeper ring.
+  // Split SwiGLU: the staging sets hold the h and b tiles of a chunk; round(a) of the warp's
+  // chunks waits for phase 2 in a buffer of its own (the a tiles, TMA-stored from there).
+  static constexpr int WARP_SET = SPLIT ? 2 * OUT_BUF : WARP_SET_BASE;
+  static constexpr int ABUF = SPLIT ? (BN / CW / 2) * OUT_BUF : 0;  // per warp
   static constexpr int EB =
       (D::NAUX > 0 || SPLIT) &&
-              (kMaxSmem - 1024 - kEpiWarps * 2 * WARP_SET - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3
+              (kMaxSmem - 1024 - kEpiWarps * (2 * WARP_SET + ABUF) - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3
           ? 2
           : 1;
-  static constexpr int WARP_BYTES = EB * WARP_SET;
+  static constexpr int WARP_BYTES = EB * WARP_SET + ABUF;
   static constexpr int EPI_BYTES = kEpiWarps * WARP_BYTES;
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
   static constexpr bool STATS = (K == EPI_NORM_SILU);
@@ -710,47 +714,56 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, batch) != nullptr;
 
       if constexpr (C::SPLIT) {
-        // Phase 1: round(a) of this warp's chunks into registers (bf16 pairs: exact, since
-        // a is stored rounded), optionally stored; then a's TMEM columns are released.
+        // Phase 1: round(a) of this warp's chunks into its a tiles in shared memory (exact:
+        // a is stored rounded), optionally TMA-stored from there; then a's TMEM columns are
+        // released, so the next tile's a accumulation overlaps the rest of this epilogue.
         constexpr int NC = NCH / 2;
-        uint32_t apk[NC][CW / 2];
+        uint8_t* abuf = wstage + EB * C::WARP_SET;  // NC tiles of 32 rows x 32 columns
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         ok = mbar_wait(&tfull[0], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         tc_fence_after();
+        if (present[1] && leader) bulk_wait_read_all();  // the previous tile's a stores have read abuf
+        __syncwarp();
 #pragma unroll
         for (int ci = 0; ci < NC; ++ci) {
           const int c = g + 2 * ci;
           float v[CW];
           tmem_ld32(t_row + c * CW, v);
           tmem_ld_wait();
+          const uint32_t base = smem_addr(abuf + ci * C::OUT_BUF);
 #pragma unroll
-          for (int j = 0; j < CW / 2; ++j) apk[ci][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-          if (present[1]) {
-            const int b = EB == 2 ? (qi & 1) : 0;
-            wait_set_free();
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            const uint32_t base = smem_addr(ostage(b) + C::OUT_BUF);
+          for (int j = 0; j < CW / 8; ++j) sts_bf16x8(base + stage_off<64>(lane, j), &v[8 * j]);
+        }
+        if (present[1]) {
+          fence_async_smem();
+          __syncwarp();
+          if (leader) {
 #pragma unroll
-            for (int j = 0; j < CW / 8; ++j)
-              sts128(base + stage_off<64>(lane, j), apk[ci][4 * j], apk[ci][4 * j + 1], apk[ci][4 * j + 2],
-                     apk[ci][4 * j + 3]);
-            fence_async_smem();
-            __syncwarp();
-            if (leader) {
-              tma_store_2d(&maps.out[batch][1], ostage(b) + C::OUT_BUF, nb * BN + c * CW, r0);
-              bulk_commit();
-            }
-            ++qi;
+            for (int ci = 0; ci < NC; ++ci)
+              tma_store_2d(&maps.out[batch][1], abuf + ci * C::OUT_BUF, nb * BN + (g + 2 * ci) * CW, r0);
+            bulk_commit();
           }
         }
-        if (!ok) break;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[0]), 0));
-        // Phase 2: b, h = SiLU(a) b; outputs h and (optionally) b.
+        // Phase 2a: round(b) of this warp's chunks into registers (packed bf16, exact); then b's
+        // columns are released and the next tile's b accumulation overlaps the h math and stores.
+        uint32_t bpk[NC][CW / 2];
         ok = mbar_wait(&tfull[1], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         tc_fence_after();
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+          float v[CW];
+          tmem_ld32(t_row + BN + (g + 2 * ci) * CW, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CW / 2; ++j) bpk[ci][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[1]), 0));
+        // Phase 2b: h = SiLU(a) b; outputs h and (optionally) b.
 #pragma unroll
         for (int ci = 0; ci < NC; ++ci) {
           const int c = g + 2 * ci;
@@ -758,43 +771,35 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           wait_set_free();
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
+          const uint32_t abase = smem_addr(abuf + ci * C::OUT_BUF);
           const uint32_t hbase = smem_addr(ostage(b));
-          const uint32_t bbase = smem_addr(ostage(b) + 2 * C::OUT_BUF);
+          const uint32_t bbase = smem_addr(ostage(b) + C::OUT_BUF);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {  // two halves of 16 columns keep the live registers down
-            float v[CW / 2];
-            tmem_ld16(t_row + BN + c * CW + hh * (CW / 2), v);
-            tmem_ld_wait();
-            uint32_t bpk[CW / 4];  // round(b), packed; v becomes h = SiLU(a) b
+          for (int j = 0; j < CW / 8; ++j) {
+            float av[8], hv[8];
+            lds_bf16x8(abase + stage_off<64>(lane, j), av);
 #pragma unroll
-            for (int j = 0; j < CW / 4; ++j) {
-              float a0, a1, b0, b1;
-              unpack_bf16x2(apk[ci][hh * (CW / 4) + j], a0, a1);
-              bpk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-              unpack_bf16x2(bpk[j], b0, b1);
-              v[2 * j] = silu<bf16>(a0) * b0;
-              v[2 * j + 1] = silu<bf16>(a1) * b1;
+            for (int t = 0; t < 4; ++t) {
+              float b0, b1;
+              unpack_bf16x2(bpk[ci][4 * j + t], b0, b1);
+              hv[2 * t] = silu<bf16>(av[2 * t]) * b0;
+              hv[2 * t + 1] = silu<bf16>(av[2 * t + 1]) * b1;
             }
-            sts_bf16x8(hbase + stage_off<64>(lane, 2 * hh), &v[0]);
-            sts_bf16x8(hbase + stage_off<64>(lane, 2 * hh + 1), &v[8]);
-            if (present[2]) {
-              sts128(bbase + stage_off<64>(lane, 2 * hh), bpk[0], bpk[1], bpk[2], bpk[3]);
-              sts128(bbase + stage_off<64>(lane, 2 * hh + 1), bpk[4], bpk[5], bpk[6], bpk[7]);
-            }
+            sts_bf16x8(hbase + stage_off<64>(lane, j), hv);
+            if (present[2])
+              sts128(bbase + stage_off<64>(lane, j), bpk[ci][4 * j], bpk[ci][4 * j + 1], bpk[ci][4 * j + 2],
+                     bpk[ci][4 * j + 3]);
           }
           fence_async_smem();
           __syncwarp();
           if (leader) {
             if (present[0]) tma_store_2d(&maps.out[batch][0], ostage(b), nb * BN + c * CW, r0);
-            if (present[2]) tma_store_2d(&maps.out[batch][2], ostage(b) + 2 * C::OUT_BUF, nb * BN + c * CW, r0);
+            if (present[2]) tma_store_2d(&maps.out[batch][2], ostage(b) + C::OUT_BUF, nb * BN + c * CW, r0);
             bulk_commit();
           }
           ++qi;
         }
         if (!ok) break;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[1]), 0));
       } else {
         ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         tc_fence_after();
