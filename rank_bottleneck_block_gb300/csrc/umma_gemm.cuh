@@ -52,6 +52,13 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16 along K
 constexpr int CW = 32;  // epilogue chunk width (columns)
 constexpr int ER = 32;  // rows of an epilogue staging tile: one warp's TMEM lane quarter
+constexpr int kMaxAuxSets = 4;  // operand-tile staging sets per epilogue warp, at most
+
+// Operand-tile sets per epilogue warp: how many chunks ahead the operand loads run.  The
+// residual GEMM (K = r, one [T, d] operand streamed from HBM) gains from four; for the others
+// the shared memory is worth more as operand-ring stages (measured: the SwiGLU backward with
+// three sets and two stages, and the dz_down GEMM with three sets, were slower).
+__host__ __device__ constexpr int aux_sets(EpiKind k) { return k == EPI_RESID ? 4 : 2; }
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -318,33 +325,28 @@ struct Config {
   static constexpr int OUT_ROW = CW * (D::OUT_F32 ? 4 : 2);
   static constexpr int OUT_BUF = ER * OUT_ROW;  // one warp's rows of a chunk
   static constexpr int AUX_BUF = ER * CW * 2;
-  static constexpr int WARP_SET_BASE = D::NOUT * OUT_BUF + D::NAUX * AUX_BUF;  // one chunk's staging
   static constexpr uint32_t ACC_COLS = NACC * BN;
   // Two accumulator buffers when they fit in the 512 TMEM columns, else one.
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
-  // SwiGLU with 256-wide accumulators (a and b fill TMEM): the two accumulators complete
-  // and are released separately.  The epilogue first moves round(a) into registers (packed
-  // bf16, exact), which frees a's columns for the next tile while b still accumulates;
-  // then it consumes b, so the next tile's b accumulation overlaps the h math and stores.
+  // SwiGLU with 256-wide accumulators (a and b fill TMEM): the two accumulators complete and
+  // are released separately.  Phase 1 stages round(a) in shared memory (exact: a is stored
+  // rounded) and frees a's columns for the next tile while b still accumulates; phase 2 moves
+  // round(b) into registers, frees b's columns, then computes h.
   static constexpr bool SPLIT = (K == EPI_SWIGLU) && NBUF == 1;
-  // Epilogues that read operand tiles, and the split SwiGLU, get two staging sets per warp
-  // (operand tiles two chunks ahead, output tiles in ping-pong) when the operand ring still
-  // keeps three stages; the others keep one set and a deeper ring.
-  // Split SwiGLU: the staging sets hold the h and b tiles of a chunk; round(a) of the warp's
-  // chunks waits for phase 2 in a buffer of its own (the a tiles, TMA-stored from there).
-  static constexpr int WARP_SET = SPLIT ? 2 * OUT_BUF : WARP_SET_BASE;
-  static constexpr int ABUF = SPLIT ? (BN / CW / 2) * OUT_BUF : 0;  // per warp
-  static constexpr int EB =
-      (D::NAUX > 0 || SPLIT) &&
-              (kMaxSmem - 1024 - kEpiWarps * (2 * WARP_SET + ABUF) - (512 + 1024)) / (A_BYTES + B_BYTES) >= 3
-          ? 2
-          : 1;
-  static constexpr int WARP_BYTES = EB * WARP_SET + ABUF;
+  // Staging per epilogue warp: NO output sets of NOUT tiles (ping-pong when stores would
+  // otherwise stall the next chunk), NA operand sets of NAUX tiles (loads NA chunks ahead),
+  // and for the split SwiGLU the round(a) tiles of the warp's chunks.
+  static constexpr int OSET = (SPLIT ? 2 : D::NOUT) * OUT_BUF;
+  static constexpr int ASET = D::NAUX * AUX_BUF;
+  static constexpr int ABUF = SPLIT ? (BN / CW / 2) * OUT_BUF : 0;
+  static constexpr int NO = (D::NAUX > 0 || SPLIT) ? 2 : 1;
+  static constexpr int NA = D::NAUX > 0 ? aux_sets(K) : 0;
+  static constexpr int WARP_BYTES = NO * OSET + NA * ASET + ABUF;
   static constexpr int EPI_BYTES = kEpiWarps * WARP_BYTES;
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
   static constexpr bool STATS = (K == EPI_NORM_SILU);
   static constexpr int THREADS = kThreads + (STATS ? 128 : 0);
-  static constexpr int BAR_BYTES = 512 + 1024;  // barriers, then s for two tiles of 128 rows
+  static constexpr int BAR_BYTES = 1024 + 1024;  // barriers, then s for two tiles of 128 rows
   static constexpr int RING_BUDGET = kMaxSmem - 1024 - EPI_BYTES - BAR_BYTES;
   static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS <= 32    ? 32
@@ -357,7 +359,10 @@ struct Config {
   static_assert(STAGES >= 2, "need at least two stages");
   static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256 (each CTA stages BN/2, whole 64-column chunks)");
   static_assert((BN / CW) % 2 == 0, "both epilogue warps of a lane quarter need the same number of chunks");
-  static_assert(WARP_SET % 1024 == 0 || (WARP_SET % 512 == 0 && !D::OUT_F32), "staging tiles keep swizzle alignment");
+  static_assert(OSET % 1024 == 0 || (OSET % 512 == 0 && !D::OUT_F32), "staging tiles keep swizzle alignment");
+  static_assert(ASET % 512 == 0 && ABUF % 512 == 0, "staging tiles keep swizzle alignment");
+  static_assert(NA <= kMaxAuxSets, "operand-tile barriers per warp");
+  static_assert(3 * 8 + 2 + 2 + 1 + kMaxAuxSets * kEpiWarps + 2 + 2 <= 127, "barriers, TMEM slot and flag fit");
   static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
 };
 
@@ -395,12 +400,12 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   uint64_t* tfull = consumed + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* aux_full = drain + 1;             // per epilogue warp and staging set
-  uint64_t* sfull = aux_full + 2 * kEpiWarps;  // stats -> epilogue, per TMEM buffer
+  uint64_t* aux_full = drain + 1;                       // per epilogue warp and operand set
+  uint64_t* sfull = aux_full + kMaxAuxSets * kEpiWarps;  // stats -> epilogue, per TMEM buffer
   uint64_t* sempty = sfull + 2;     // epilogue -> stats, per TMEM buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_rows = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [2][BM]
+  float* s_rows = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 1024);  // [2][BM]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       mbar_init(&sempty[i], kEpiWarps);
     }
     mbar_init(drain, 1);
-    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&aux_full[i], 1);
+    for (int i = 0; i < kMaxAuxSets * kEpiWarps; ++i) mbar_init(&aux_full[i], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
@@ -630,16 +635,16 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     // through the warp's own staging sets; the warp synchronises only with itself.
     constexpr int NAUX = D::NAUX, NOUT = D::NOUT;
     constexpr int NCH = BN / CW;
-    constexpr int EB = C::EB;
+    constexpr int NO = C::NO, NA = C::NA;
     const int ew = warp - 2;
     const int g = ew >> 2;   // chunk parity
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const bool leader = lane == 0;
-    uint8_t* wstage = sE + ew * C::WARP_BYTES;  // EB sets of [NOUT output tiles | NAUX operand tiles]
-    auto ostage = [&](int b) { return wstage + b * C::WARP_SET; };
-    auto astage = [&](int b) { return wstage + b * C::WARP_SET + NOUT * C::OUT_BUF; };
-    uint64_t* abar = &aux_full[2 * ew];
+    uint8_t* wstage = sE + ew * C::WARP_BYTES;  // NO output sets | NA operand sets | round(a) tiles
+    auto ostage = [&](int b) { return wstage + b * C::OSET; };
+    auto astage = [&](int b) { return wstage + NO * C::OSET + b * C::ASET; };
+    uint64_t* abar = &aux_full[kMaxAuxSets * ew];
     uint32_t aph = 0u;      // bit b: phase parity of abar[b]
     uint32_t pending = 0u;  // lane 0, bit b: an operand-tile load is in flight on abar[b]
 
@@ -669,15 +674,14 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     // Lane 0: the stores that last used output set b have finished reading it.
     auto wait_set_free = [&]() {
       if (leader) {
-        if constexpr (EB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        else bulk_wait_read_all();
+        asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(NO - 1) : "memory");
       }
     };
     // Prefetch cursor: the next chunk whose operand tiles are not yet requested.
     int pf_t = cid, pf_c = g;
     if constexpr (NAUX > 0) {
       if (leader) {
-        for (int b = 0; b < EB && pf_t < total; ++b) {
+        for (int b = 0; b < NA && pf_t < total; ++b) {
           issue_aux(pf_t, pf_c, b);
           next_chunk(pf_t, pf_c);
         }
@@ -718,7 +722,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         // a is stored rounded), optionally TMA-stored from there; then a's TMEM columns are
         // released, so the next tile's a accumulation overlaps the rest of this epilogue.
         constexpr int NC = NCH / 2;
-        uint8_t* abuf = wstage + EB * C::WARP_SET;  // NC tiles of 32 rows x 32 columns
+        uint8_t* abuf = wstage + NO * C::OSET + NA * C::ASET;  // NC tiles of 32 rows x 32 columns
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         ok = mbar_wait(&tfull[0], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         tc_fence_after();
@@ -767,7 +771,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
         for (int ci = 0; ci < NC; ++ci) {
           const int c = g + 2 * ci;
-          const int b = EB == 2 ? (qi & 1) : 0;
+          const int b = qi % NO;
           wait_set_free();
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
@@ -806,13 +810,14 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
 #pragma unroll 1
         for (int c = g; c < NCH; c += 2, ++qi) {
-          const int b = EB == 2 ? (qi & 1) : 0;
+          const int b = qi % NO;  // output set
+          const int ba = NA > 0 ? qi % NA : 0;  // operand set
           if constexpr (NAUX > 0) {
-            const bool landed = mbar_wait(&abar[b], (aph >> b) & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
+            const bool landed = mbar_wait(&abar[ba], (aph >> ba) & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
             ok = landed && ok;
             if (landed) {
-              aph ^= 1u << b;
-              pending &= ~(1u << b);
+              aph ^= 1u << ba;
+              pending &= ~(1u << ba);
             }
           }
           float v[NACC][CW];
@@ -823,7 +828,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
           for (int a = 0; a < NAUX; ++a) {
             if (aux_present[a]) {
-              const uint8_t* base = astage(b) + a * C::AUX_BUF;
+              const uint8_t* base = astage(ba) + a * C::AUX_BUF;
 #pragma unroll
               for (int j = 0; j < CW / 8; ++j) lds_bf16x8(smem_addr(base) + stage_off<64>(lane, j), &av[a][8 * j]);
             } else {
@@ -836,7 +841,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           if (!ok) break;
           if constexpr (NAUX > 0) {
             if (leader && pf_t < total) {  // refill the operand set this chunk has just released
-              issue_aux(pf_t, pf_c, b);
+              issue_aux(pf_t, pf_c, ba);
               next_chunk(pf_t, pf_c);
             }
           }
@@ -886,7 +891,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     }
     if (leader) {
       bulk_wait_all();
-      for (int b = 0; b < 2; ++b) {  // abort path: let operand-tile loads in flight land before the CTA exits
+      for (int b = 0; b < NA; ++b) {  // abort path: let operand-tile loads in flight land before the CTA exits
         if (!((pending >> b) & 1u)) continue;
         const uint64_t t0 = global_timer_ns();
         while (!mbar_test(&abar[b], (aph >> b) & 1u) && global_timer_ns() - t0 < kWaitLimitNs) {
