@@ -59,7 +59,7 @@ typedef enum {
   LR_ERR_NULL = 1,        /* a required pointer is NULL */
   LR_ERR_SHAPE = 2,       /* a dimension is non-positive, not a multiple of 8, or too large */
   LR_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
-  LR_ERR_DTYPE = 4,       /* unknown lr_dtype or lr_mode */
+  LR_ERR_DTYPE = 4,       /* unknown lr_dtype, lr_mode or lr_act */
   LR_ERR_WORKSPACE = 5,   /* saved / ws buffer smaller than the size query returns */
   LR_ERR_CUDA = 6,        /* a CUDA call or kernel launch failed */
   LR_ERR_TIMEOUT = 7,     /* a kernel's bounded wait ran out (reported by lr_check_device_error) */
@@ -72,6 +72,12 @@ typedef enum {
   LR_SAVE_FULL = 0, /* keep every forward intermediate for the backward */
   LR_SAVE_CKPT = 1  /* low-rank activation checkpointing (technical summary §2.2) */
 } lr_mode;
+
+/* The activation sigma between a pair's A and B.  The pages name no sigma: SiLU is the
+ * reading used throughout; identity is the plain factorisation W = B A (the SVD-style
+ * low-rank variant the technical summary lists).  The SwiGLU product of the MLP block
+ * keeps its SiLU in both. */
+typedef enum { LR_ACT_SILU = 0, LR_ACT_IDENTITY = 1 } lr_act;
 
 /* One low-rank pair: A [r, d_in] and B [d_out, r], storage dtype. */
 typedef struct {
@@ -89,16 +95,16 @@ typedef struct {
  * Low-rank SwiGLU MLP block with a residual (the sublayer the technical summary
  * §2.2 groups as gate/up down-projections plus a down pair):
  *     n   = RMSNorm(x; g, eps)              s[t] = (mean_j x[t,j]^2 + eps)^(-1/2)
- *     a   = B_gate SiLU(A_gate n)           A_gate [r,d],  B_gate [f,r]
- *     b   = B_up   SiLU(A_up   n)           A_up   [r,d],  B_up   [f,r]
+ *     a   = B_gate sigma(A_gate n)          A_gate [r,d],  B_gate [f,r]
+ *     b   = B_up   sigma(A_up   n)          A_up   [r,d],  B_up   [f,r]
  *     h   = SiLU(a) * b                     [T, f]
- *     out = x + B_down SiLU(A_down h)       A_down [r,f],  B_down [d,r]
- * Dimensions: T tokens, d model width, f MLP width, r rank.
+ *     out = x + B_down sigma(A_down h)      A_down [r,f],  B_down [d,r]
+ * Dimensions: T tokens, d model width, f MLP width, r rank; sigma per `act`.
  *
  * `saved` holds what the backward needs: in LR_SAVE_CKPT the pre-activations
  * u_gate, u_up, u_down ([T, r] each, dtype) and s ([T] fp32); LR_SAVE_FULL adds
- * the SiLU outputs and a, b, h.  Its layout is private; pass it unchanged to
- * lr_mlp_bwd with the same dtype, mode and dimensions.  x must also be passed
+ * the sigma outputs and a, b, h.  Its layout is private; pass it unchanged to
+ * lr_mlp_bwd with the same dtype, mode, act and dimensions.  x must also be passed
  * unchanged to the backward (checkpointing keeps the block input, not a copy).
  */
 size_t lr_mlp_saved_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r);
@@ -106,14 +112,14 @@ size_t lr_mlp_fwd_workspace_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f
 size_t lr_mlp_bwd_workspace_bytes(lr_dtype dt, lr_mode mode, int T, int d, int f, int r);
 
 /* x [T,d], g [d] -> out [T,d]; fills `saved`. */
-lr_status lr_mlp_fwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x,
+lr_status lr_mlp_fwd(lr_dtype dt, lr_mode mode, lr_act act, int T, int d, int f, int r, float eps, const void* x,
                      const void* g, lr_pair gate, lr_pair up, lr_pair down, void* out, void* saved,
                      size_t saved_bytes, void* ws, size_t ws_bytes, void* stream);
 
 /* dout [T,d] = dL/dout -> dx [T,d] (dtype), dg [d] fp32, and every pair's dA, dB (fp32).
  * In LR_SAVE_CKPT the backward first re-runs the block's forward from x, s and
  * the saved pre-activations (no other state). */
-lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x,
+lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, lr_act act, int T, int d, int f, int r, float eps, const void* x,
                      const void* g, lr_pair gate, lr_pair up, lr_pair down, const void* saved,
                      size_t saved_bytes, const void* dout, void* dx, float* dg, lr_pair_grad dgate,
                      lr_pair_grad dup, lr_pair_grad ddown, void* ws, size_t ws_bytes, void* stream);
@@ -122,27 +128,27 @@ lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, floa
  * `group` (1..3) pairs that read the same input x [T, d_in], each mapping to
  * d_out (attention q/k/v; technical summary §2.2 grouping):
  *     v = RMSNorm(x; g, eps) if g != NULL, else v = x
- *     outs[i] = B_i SiLU(A_i v)            A_i [r, d_in], B_i [d_out, r]
+ *     outs[i] = B_i sigma(A_i v)           A_i [r, d_in], B_i [d_out, r]; sigma per `act`
  * The A_i run as one stacked GEMM, the B_i as one batched GEMM.  `saved` keeps
- * the stacked pre-activations [T, group*r], the SiLU outputs and s.
+ * the stacked pre-activations [T, group*r], the sigma outputs and s.
  */
 size_t lr_proj_saved_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm);
 size_t lr_proj_fwd_workspace_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm);
 size_t lr_proj_bwd_workspace_bytes(lr_dtype dt, int T, int d_in, int d_out, int r, int group, int norm);
 
-lr_status lr_proj_fwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+lr_status lr_proj_fwd(lr_dtype dt, lr_act act, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
                       const void* g, float eps, const void* x, void* const* outs, void* saved, size_t saved_bytes,
                       void* ws, size_t ws_bytes, void* stream);
 
 /* douts[i] [T, d_out] -> dx [T, d_in] (dtype), dg [d_in] fp32 (ignored and may be NULL
  * when g == NULL), grads[i] (fp32). */
-lr_status lr_proj_bwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+lr_status lr_proj_bwd(lr_dtype dt, lr_act act, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
                       const void* g, float eps, const void* x, const void* saved, size_t saved_bytes,
                       const void* const* douts, void* dx, float* dg, const lr_pair_grad* grads, void* ws,
                       size_t ws_bytes, void* stream);
 
 /* -------------------------------------------------------------- block stack
- * One training step of `nblocks` residual MLP blocks (as lr_mlp_fwd) and a
+ * One training step of `nblocks` residual MLP blocks (as lr_mlp_fwd, sigma = SiLU) and a
  * mean-squared-error loss against `target` [T, d]:
  *     x_0 = x, x_{l+1} = block_l(x_l), loss = mean((x_L - target)^2)
  * then the backward through every block (in LR_SAVE_CKPT each block is
@@ -166,7 +172,7 @@ lr_status lr_stack_step(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, in
  * new allocations, or code paths that must not synchronise the device (as a
  * cudaMalloc/cudaFree can).  Such callers cannot provide `ws` for lr_proj_fwd.
  *
- * lr_proj_fwd_noalloc computes exactly what lr_proj_fwd computes, with the same
+ * lr_proj_fwd_noalloc computes exactly what lr_proj_fwd (act = LR_ACT_SILU) computes, with the same
  * arguments minus the workspace.  Its only scratch (the gain-folded, stacked
  * A weights: group * r * d_in elements of the storage dtype) lives in one
  * file-scope device array of LR_NOALLOC_SCRATCH_BYTES bytes inside this

@@ -59,6 +59,7 @@ struct EpiParams {
   float eps;                      // RMSNorm epsilon (forward statistics)
   float* rowscale_out;            // s[m] written by the GEMM that computes it (online RMSNorm), or null
   long long split_stride;         // elements between split-K partial outputs
+  int act;                        // pair activation sigma: 0 SiLU, 1 identity
 };
 
 // ---------------------------------------------------------------- numerics

@@ -22,17 +22,29 @@
 
 namespace lr {
 
-// Per-row inputs of an epilogue: s = 1/rms of the row, k = coef * s^2 * rho.
+// Per-row inputs of an epilogue: s = 1/rms of the row, k = coef * s^2 * rho, and the pair
+// activation (0 SiLU, 1 identity; uniform over the launch).
 struct RowIn {
   float s;
   float k;
+  int act;
 };
+
+// The pair activation sigma and its derivative.
+template <typename ST>
+__device__ __forceinline__ float pair_act(int act, float u) {
+  return act ? u : silu<ST>(u);
+}
+template <typename ST>
+__device__ __forceinline__ float pair_act_grad(int act, float u) {
+  return act ? 1.f : silu_grad<ST>(u);
+}
 
 template <EpiKind K>
 struct EpiDef;
 
 template <>
-struct EpiDef<EPI_NORM_SILU> {  // u = round(s acc), z = SiLU(u)
+struct EpiDef<EPI_NORM_SILU> {  // u = round(s acc), z = sigma(u)
   static constexpr int NACC = 1, NAUX = 0, NOUT = 2;
   static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = false, ROWPART = false;
   template <typename ST, int W>
@@ -42,23 +54,23 @@ struct EpiDef<EPI_NORM_SILU> {  // u = round(s acc), z = SiLU(u)
     for (int j = 0; j < W; ++j) {
       const float u = Num<ST>::round(ri.s * v[0][j]);
       o[0][j] = u;
-      o[1][j] = silu<ST>(u);
+      o[1][j] = pair_act<ST>(ri.act, u);
     }
   }
 };
 
 template <>
-struct EpiDef<EPI_SILU> {  // u = round(acc), z = SiLU(u)
+struct EpiDef<EPI_SILU> {  // u = round(acc), z = sigma(u)
   static constexpr int NACC = 1, NAUX = 0, NOUT = 2;
   static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
   template <typename ST, int W>
-  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&)[1][W],
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[1][W], const float (&)[1][W],
                                              float (&o)[2][W], float&) {
 #pragma unroll
     for (int j = 0; j < W; ++j) {
       const float u = Num<ST>::round(v[0][j]);
       o[0][j] = u;
-      o[1][j] = silu<ST>(u);
+      o[1][j] = pair_act<ST>(ri.act, u);
     }
   }
 };
@@ -106,19 +118,19 @@ struct EpiDef<EPI_SWIGLU> {  // a = round(acc0), b = round(acc1), h = SiLU(a) b 
 };
 
 template <>
-struct EpiDef<EPI_DSILU> {  // du = acc SiLU'(u)  (aux0 = u)
+struct EpiDef<EPI_DSILU> {  // du = acc sigma'(u)  (aux0 = u)
   static constexpr int NACC = 1, NAUX = 1, NOUT = 1;
   static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
   template <typename ST, int W>
-  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&a)[1][W],
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[1][W], const float (&a)[1][W],
                                              float (&o)[1][W], float&) {
 #pragma unroll
-    for (int j = 0; j < W; ++j) o[0][j] = v[0][j] * silu_grad<ST>(a[0][j]);
+    for (int j = 0; j < W; ++j) o[0][j] = v[0][j] * pair_act_grad<ST>(ri.act, a[0][j]);
   }
 };
 
 template <>
-struct EpiDef<EPI_DSILU_NORM> {  // du = acc SiLU'(u); out = s du; row partial += du u  (aux0 = u)
+struct EpiDef<EPI_DSILU_NORM> {  // du = acc sigma'(u); out = s du; row partial += du u  (aux0 = u)
   static constexpr int NACC = 1, NAUX = 1, NOUT = 1;
   static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = false, ROWPART = true;
   template <typename ST, int W>
@@ -127,7 +139,7 @@ struct EpiDef<EPI_DSILU_NORM> {  // du = acc SiLU'(u); out = s du; row partial +
     float p = 0.f;
 #pragma unroll
     for (int j = 0; j < W; ++j) {
-      const float du = v[0][j] * silu_grad<ST>(a[0][j]);
+      const float du = v[0][j] * pair_act_grad<ST>(ri.act, a[0][j]);
       p = fmaf(du, a[0][j], p);
       o[0][j] = ri.s * du;
     }
@@ -180,7 +192,7 @@ struct EpiDef<EPI_F32> {  // fp32 weight-gradient partial
 template <EpiKind K>
 __device__ __forceinline__ RowIn row_inputs(const EpiParams& p, int m) {
   using D = EpiDef<K>;
-  RowIn ri{0.f, 0.f};
+  RowIn ri{0.f, 0.f, p.act};
   if (m >= p.M) return ri;
   if constexpr (D::NEED_S) ri.s = p.rowscale[m];
   if constexpr (D::NEED_RHO) {

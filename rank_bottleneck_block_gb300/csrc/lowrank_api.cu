@@ -156,6 +156,7 @@ struct LaunchScope {
 // ----------------------------------------------------------- GEMM dispatch
 struct Ctx {
   lr_dtype dt;
+  int act;    // pair activation: 0 SiLU, 1 identity
   size_t es;  // element size of the storage dtype
   cudaStream_t st;
   unsigned* err;
@@ -239,6 +240,7 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   if (g.ksplit < 1) g.ksplit = 1;
   g.ep.M = g.M;
   g.ep.N = g.N;
+  g.ep.act = c.act;
   if (c.dt == LR_BF16) {
     if (k == EPI_SWIGLU) g.bn = kSwigluBn;
     else if (g.bn != 128 && g.bn != 256) g.bn = pick_bn(g, c.sms);
@@ -580,7 +582,12 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     a = W.a;
     b = W.b;
     h = W.h;
-    LR_TRY(silu_slabs(c, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, r}, T));
+    if (c.act) {  // sigma = identity: z is u itself
+      z_gu = S.u_gu;
+      z_d = S.u_d;
+    } else {
+      LR_TRY(silu_slabs(c, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, r}, T));
+    }
     LR_TRY(swiglu_gemm(c, T, f, r, z_gu, gate.B, up.B, h, a, b));
   } else {
     z_gu = S.z_gu;
@@ -906,13 +913,19 @@ static lr_status check_mode(lr_mode m) {
   return LR_OK;
 }
 
+static lr_status check_act(lr_act a) {
+  if (a != LR_ACT_SILU && a != LR_ACT_IDENTITY) return fail(LR_ERR_DTYPE, "unknown act %d", static_cast<int>(a));
+  return LR_OK;
+}
+
 static lr_status check_size(size_t have, size_t need, const char* name) {
   if (have < need) return fail(LR_ERR_WORKSPACE, "%s has %zu bytes, needs %zu", name, have, need);
   return LR_OK;
 }
 
-static lr_status make_ctx(lr_dtype dt, void* stream, Ctx* c) {
+static lr_status make_ctx(lr_dtype dt, void* stream, Ctx* c, lr_act act = LR_ACT_SILU) {
   c->dt = dt;
+  c->act = act == LR_ACT_IDENTITY ? 1 : 0;
   c->es = esize(dt);
   c->st = static_cast<cudaStream_t>(stream);
   LR_TRY(device_error_word(&c->err));
@@ -1070,12 +1083,13 @@ static lr_status check_grad(lr_pair_grad p, const char* name) {
   return check_ptr(p.dB, buf);
 }
 
-lr_status lr_mlp_fwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x, const void* g,
-                     lr_pair gate, lr_pair up, lr_pair down, void* out, void* saved, size_t saved_bytes, void* ws,
-                     size_t ws_bytes, void* stream) {
+lr_status lr_mlp_fwd(lr_dtype dt, lr_mode mode, lr_act act, int T, int d, int f, int r, float eps, const void* x,
+                     const void* g, lr_pair gate, lr_pair up, lr_pair down, void* out, void* saved,
+                     size_t saved_bytes, void* ws, size_t ws_bytes, void* stream) {
   t_last_error.clear();
   LR_TRY(check_dtype(dt));
   LR_TRY(check_mode(mode));
+  LR_TRY(check_act(act));
   LR_TRY(check_mlp_dims(T, d, f, r));
   LR_TRY(check_ptr(x, "x"));
   LR_TRY(check_ptr(g, "g"));
@@ -1088,17 +1102,18 @@ lr_status lr_mlp_fwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, floa
   LR_TRY(check_size(saved_bytes, mlp_saved_layout(dt, mode, T, d, f, r, nullptr, nullptr), "saved"));
   LR_TRY(check_size(ws_bytes, mlp_fwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr), "ws"));
   Ctx c;
-  LR_TRY(make_ctx(dt, stream, &c));
+  LR_TRY(make_ctx(dt, stream, &c, act));
   return mlp_fwd_impl(c, mode, T, d, f, r, eps, x, g, gate, up, down, out, saved, ws);
 }
 
-lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, float eps, const void* x, const void* g,
-                     lr_pair gate, lr_pair up, lr_pair down, const void* saved, size_t saved_bytes, const void* dout,
-                     void* dx, float* dg, lr_pair_grad dgate, lr_pair_grad dup, lr_pair_grad ddown, void* ws,
-                     size_t ws_bytes, void* stream) {
+lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, lr_act act, int T, int d, int f, int r, float eps, const void* x,
+                     const void* g, lr_pair gate, lr_pair up, lr_pair down, const void* saved, size_t saved_bytes,
+                     const void* dout, void* dx, float* dg, lr_pair_grad dgate, lr_pair_grad dup, lr_pair_grad ddown,
+                     void* ws, size_t ws_bytes, void* stream) {
   t_last_error.clear();
   LR_TRY(check_dtype(dt));
   LR_TRY(check_mode(mode));
+  LR_TRY(check_act(act));
   LR_TRY(check_mlp_dims(T, d, f, r));
   LR_TRY(check_ptr(x, "x"));
   LR_TRY(check_ptr(g, "g"));
@@ -1116,7 +1131,7 @@ lr_status lr_mlp_bwd(lr_dtype dt, lr_mode mode, int T, int d, int f, int r, floa
   LR_TRY(check_size(saved_bytes, mlp_saved_layout(dt, mode, T, d, f, r, nullptr, nullptr), "saved"));
   LR_TRY(check_size(ws_bytes, mlp_bwd_ws_layout(dt, mode, T, d, f, r, nullptr, nullptr), "ws"));
   Ctx c;
-  LR_TRY(make_ctx(dt, stream, &c));
+  LR_TRY(make_ctx(dt, stream, &c, act));
   return mlp_bwd_impl(c, mode, T, d, f, r, eps, x, g, gate, up, down, saved, dout, dx, dg, dgate, dup, ddown, ws);
 }
 
@@ -1135,11 +1150,12 @@ size_t lr_proj_bwd_workspace_bytes(lr_dtype dt, int T, int d_in, int d_out, int 
   return proj_ws_layout(dt, true, T, d_in, d_out, r, group, norm != 0, nullptr, nullptr);
 }
 
-lr_status lr_proj_fwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs, const void* g,
-                      float eps, const void* x, void* const* outs, void* saved, size_t saved_bytes, void* ws,
-                      size_t ws_bytes, void* stream) {
+lr_status lr_proj_fwd(lr_dtype dt, lr_act act, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                      const void* g, float eps, const void* x, void* const* outs, void* saved, size_t saved_bytes,
+                      void* ws, size_t ws_bytes, void* stream) {
   t_last_error.clear();
   LR_TRY(check_dtype(dt));
+  LR_TRY(check_act(act));
   LR_TRY(check_proj_dims(T, d_in, d_out, r, group));
   if (!pairs || !outs) return fail(LR_ERR_NULL, "pairs / outs is NULL");
   for (int i = 0; i < group; ++i) {
@@ -1154,16 +1170,18 @@ lr_status lr_proj_fwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group,
   LR_TRY(check_size(ws_bytes, proj_ws_layout(dt, false, T, d_in, d_out, r, group, g != nullptr, nullptr, nullptr),
                     "ws"));
   Ctx c;
-  LR_TRY(make_ctx(dt, stream, &c));
+  LR_TRY(make_ctx(dt, stream, &c, act));
   return proj_fwd_impl(c, T, d_in, d_out, r, group, pairs, g, eps, x, outs, saved, ws);
 }
 
-lr_status lr_proj_bwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs, const void* g,
-                      float eps, const void* x, const void* saved, size_t saved_bytes, const void* const* douts,
-                      void* dx, float* dg, const lr_pair_grad* grads, void* ws, size_t ws_bytes, void* stream) {
+lr_status lr_proj_bwd(lr_dtype dt, lr_act act, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
+                      const void* g, float eps, const void* x, const void* saved, size_t saved_bytes,
+                      const void* const* douts, void* dx, float* dg, const lr_pair_grad* grads, void* ws,
+                      size_t ws_bytes, void* stream) {
   (void)eps;
   t_last_error.clear();
   LR_TRY(check_dtype(dt));
+  LR_TRY(check_act(act));
   LR_TRY(check_proj_dims(T, d_in, d_out, r, group));
   if (!pairs || !douts || !grads) return fail(LR_ERR_NULL, "pairs / douts / grads is NULL");
   for (int i = 0; i < group; ++i) {
@@ -1183,7 +1201,7 @@ lr_status lr_proj_bwd(lr_dtype dt, int T, int d_in, int d_out, int r, int group,
   LR_TRY(check_size(ws_bytes, proj_ws_layout(dt, true, T, d_in, d_out, r, group, g != nullptr, nullptr, nullptr),
                     "ws"));
   Ctx c;
-  LR_TRY(make_ctx(dt, stream, &c));
+  LR_TRY(make_ctx(dt, stream, &c, act));
   return proj_bwd_impl(c, T, d_in, d_out, r, group, pairs, g, x, saved, douts, dx, dg, grads, ws);
 }
 

@@ -703,6 +703,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       RowIn ri;
       if constexpr (C::STATS) {
         ri.k = 0.f;
+        ri.act = ep.act;
         ok = mbar_wait(&sfull[sbuf], sph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE);
         ri.s = s_rows[sbuf * BM + row];
         __syncwarp();

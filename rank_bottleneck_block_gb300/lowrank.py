@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(PKG, "liblowrank.so")
 
 LR_F32, LR_BF16 = 0, 1
 LR_SAVE_FULL, LR_SAVE_CKPT = 0, 1
+LR_ACT_SILU, LR_ACT_IDENTITY = 0, 1
 STATUS = {
     0: "LR_OK", 1: "LR_ERR_NULL", 2: "LR_ERR_SHAPE", 3: "LR_ERR_ALIGN", 4: "LR_ERR_DTYPE",
     5: "LR_ERR_WORKSPACE", 6: "LR_ERR_CUDA", 7: "LR_ERR_TIMEOUT", 8: "LR_ERR_UNSUPPORTED",
@@ -53,15 +54,17 @@ _SIGS = {
     "lr_mlp_saved_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "lr_mlp_fwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "lr_mlp_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
-    "lr_mlp_fwd": (_I, [_I, _I, _I, _I, _I, _I, _F, _P, _P, lr_pair, lr_pair, lr_pair, _P, _P, _SZ, _P, _SZ, _P]),
-    "lr_mlp_bwd": (_I, [_I, _I, _I, _I, _I, _I, _F, _P, _P, lr_pair, lr_pair, lr_pair, _P, _SZ, _P, _P, _P,
+    "lr_mlp_fwd": (_I, [_I, _I, _I, _I, _I, _I, _I, _F, _P, _P, lr_pair, lr_pair, lr_pair, _P, _P, _SZ, _P, _SZ,
+                        _P]),
+    "lr_mlp_bwd": (_I, [_I, _I, _I, _I, _I, _I, _I, _F, _P, _P, lr_pair, lr_pair, lr_pair, _P, _SZ, _P, _P, _P,
                         lr_pair_grad, lr_pair_grad, lr_pair_grad, _P, _SZ, _P]),
     "lr_proj_saved_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "lr_proj_fwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "lr_proj_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
-    "lr_proj_fwd": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, ctypes.POINTER(_P), _P, _SZ,
-                         _P, _SZ, _P]),
-    "lr_proj_bwd": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, _P, _SZ, ctypes.POINTER(_P),
+    "lr_proj_fwd": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, ctypes.POINTER(_P), _P,
+                         _SZ, _P, _SZ, _P]),
+    "lr_proj_bwd": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, _P, _SZ,
+                         ctypes.POINTER(_P),
                          _P, _P, ctypes.POINTER(lr_pair_grad), _P, _SZ, _P]),
     "lr_proj_fwd_noalloc": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, ctypes.POINTER(_P),
                                  _P, _SZ, _P]),
@@ -165,15 +168,18 @@ def lr_mlp_bwd_workspace_bytes(dt, mode, T, d, f, r) -> int:
     return lib().lr_mlp_bwd_workspace_bytes(dt, mode, T, d, f, r)
 
 
-def lr_mlp_fwd(dt, mode, T, d, f, r, eps, x, g, gate, up, down, out, saved, ws, stream=None):
-    _check(lib().lr_mlp_fwd(dt, mode, T, d, f, r, eps, _p(x), _p(g), gate, up, down, _p(out), _p(saved),
+def lr_mlp_fwd(dt, mode, T, d, f, r, eps, x, g, gate, up, down, out, saved, ws, stream=None, act=None):
+    act = LR_ACT_SILU if act is None else act
+    _check(lib().lr_mlp_fwd(dt, mode, act, T, d, f, r, eps, _p(x), _p(g), gate, up, down, _p(out), _p(saved),
                             _nbytes(saved), _p(ws), _nbytes(ws), _stream(stream)))
 
 
 def lr_mlp_bwd(dt, mode, T, d, f, r, eps, x, g, gate, up, down, saved, dout, dx, dg, dgate, dup, ddown, ws,
-               stream=None):
-    _check(lib().lr_mlp_bwd(dt, mode, T, d, f, r, eps, _p(x), _p(g), gate, up, down, _p(saved), _nbytes(saved),
-                            _p(dout), _p(dx), _p(dg), dgate, dup, ddown, _p(ws), _nbytes(ws), _stream(stream)))
+               stream=None, act=None):
+    act = LR_ACT_SILU if act is None else act
+    _check(lib().lr_mlp_bwd(dt, mode, act, T, d, f, r, eps, _p(x), _p(g), gate, up, down, _p(saved),
+                            _nbytes(saved), _p(dout), _p(dx), _p(dg), dgate, dup, ddown, _p(ws), _nbytes(ws),
+                            _stream(stream)))
 
 
 def lr_proj_saved_bytes(dt, T, d_in, d_out, r, group, norm) -> int:
@@ -197,17 +203,20 @@ def _ptrs(ts):
     return (ctypes.c_void_p * len(ts))(*[_p(t) for t in ts])
 
 
-def lr_proj_fwd(dt, T, d_in, d_out, r, pairs: Sequence[lr_pair], g, eps, x, outs, saved, ws, stream=None):
+def lr_proj_fwd(dt, T, d_in, d_out, r, pairs: Sequence[lr_pair], g, eps, x, outs, saved, ws, stream=None,
+                act=None):
+    act = LR_ACT_SILU if act is None else act
     group = len(pairs)
-    _check(lib().lr_proj_fwd(dt, T, d_in, d_out, r, group, _pairs(pairs), _p(g), eps, _p(x), _ptrs(outs), _p(saved),
-                             _nbytes(saved), _p(ws), _nbytes(ws), _stream(stream)))
+    _check(lib().lr_proj_fwd(dt, act, T, d_in, d_out, r, group, _pairs(pairs), _p(g), eps, _p(x), _ptrs(outs),
+                             _p(saved), _nbytes(saved), _p(ws), _nbytes(ws), _stream(stream)))
 
 
 def lr_proj_bwd(dt, T, d_in, d_out, r, pairs: Sequence[lr_pair], g, eps, x, saved, douts, dx, dg,
-                grads: Sequence[lr_pair_grad], ws, stream=None):
+                grads: Sequence[lr_pair_grad], ws, stream=None, act=None):
+    act = LR_ACT_SILU if act is None else act
     group = len(pairs)
     garr = (lr_pair_grad * group)(*grads)
-    _check(lib().lr_proj_bwd(dt, T, d_in, d_out, r, group, _pairs(pairs), _p(g), eps, _p(x), _p(saved),
+    _check(lib().lr_proj_bwd(dt, act, T, d_in, d_out, r, group, _pairs(pairs), _p(g), eps, _p(x), _p(saved),
                              _nbytes(saved), _ptrs(douts), _p(dx), _p(dg), garr, _p(ws), _nbytes(ws),
                              _stream(stream)))
 

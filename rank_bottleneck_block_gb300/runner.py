@@ -32,8 +32,8 @@ class MlpBlock:
     """One low-rank SwiGLU MLP block resident on the device (weights, saved set, workspaces, grads)."""
 
     def __init__(self, shape: MlpShape, case: Dict[str, torch.Tensor], mode: int = L.LR_SAVE_CKPT,
-                 device="cuda"):
-        self.s, self.mode, self.device = shape, mode, device
+                 device="cuda", act: int = L.LR_ACT_SILU):
+        self.s, self.mode, self.device, self.act = shape, mode, device, act
         self.dt = _dt(shape.dtype)
         dev = {k: v.to(device) for k, v in case.items()}
         self.t = dev
@@ -60,7 +60,7 @@ class MlpBlock:
         x = self.t["x"] if x is None else x
         out = self.out if out is None else out
         L.lr_mlp_fwd(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, x, self.t["g"], *self.pairs(), out,
-                     self.saved, self.ws_f, stream)
+                     self.saved, self.ws_f, stream, act=self.act)
         return out
 
     def backward(self, dout: Optional[torch.Tensor] = None, x: Optional[torch.Tensor] = None, stream=None,
@@ -72,7 +72,7 @@ class MlpBlock:
         L.lr_mlp_bwd(self.dt, self.mode, s.T, s.d, s.f, s.r, s.eps, x, self.t["g"], *self.pairs(), self.saved, dout,
                      dx, self.dg, L.pair_grad(gr["dA_gate"], gr["dB_gate"]),
                      L.pair_grad(gr["dA_up"], gr["dB_up"]), L.pair_grad(gr["dA_down"], gr["dB_down"]), self.ws_b,
-                     stream)
+                     stream, act=self.act)
         return dx
 
     def step(self, stream=None):
@@ -139,8 +139,8 @@ class HostPipeline:
 class ProjGroup:
     """A group of low-rank pairs sharing one input, optionally behind an RMSNorm."""
 
-    def __init__(self, shape: ProjShape, case: Dict[str, object], device="cuda"):
-        self.s, self.device = shape, device
+    def __init__(self, shape: ProjShape, case: Dict[str, object], device="cuda", act: int = L.LR_ACT_SILU):
+        self.s, self.device, self.act = shape, device, act
         self.dt = _dt(shape.dtype)
         s = shape
         self.x = case["x"].to(device)
@@ -166,13 +166,14 @@ class ProjGroup:
     def forward(self, stream=None):
         s = self.s
         L.lr_proj_fwd(self.dt, s.T, s.d_in, s.d_out, s.r, self.pairs(), self.g, s.eps, self.x, self.outs, self.saved,
-                      self.ws_f, stream)
+                      self.ws_f, stream, act=self.act)
         return self.outs
 
     def backward(self, stream=None):
         s = self.s
         L.lr_proj_bwd(self.dt, s.T, s.d_in, s.d_out, s.r, self.pairs(), self.g, s.eps, self.x, self.saved, self.G,
-                      self.dx, self.dg, [L.pair_grad(a, b) for a, b in zip(self.dA, self.dB)], self.ws_b, stream)
+                      self.dx, self.dg, [L.pair_grad(a, b) for a, b in zip(self.dA, self.dB)], self.ws_b, stream,
+                      act=self.act)
         return self.dx
 
     def step(self, stream=None):

@@ -53,12 +53,13 @@ def test_size_queries(L):
 
 def _call_mlp_fwd(L, **over):
     p = 0x10000  # a 16-byte aligned fake address: validation must fail before any launch
-    args = dict(dt=L.LR_BF16, mode=1, T=64, d=64, f=128, r=16, x=p, g=p, out=p, saved=p, saved_bytes=1 << 30,
-                ws=p, ws_bytes=1 << 30)
+    args = dict(dt=L.LR_BF16, mode=1, act=0, T=64, d=64, f=128, r=16, x=p, g=p, out=p, saved=p,
+                saved_bytes=1 << 30, ws=p, ws_bytes=1 << 30)
     args.update(over)
     pr = L.lr_pair(args.pop("A", p), p)
     lib = L.lib()
-    return lib.lr_mlp_fwd(args["dt"], args["mode"], args["T"], args["d"], args["f"], args["r"], 1e-6, args["x"],
+    return lib.lr_mlp_fwd(args["dt"], args["mode"], args["act"], args["T"], args["d"], args["f"], args["r"], 1e-6,
+                          args["x"],
                           args["g"], pr, L.lr_pair(p, p), L.lr_pair(p, p), args["out"], args["saved"],
                           args["saved_bytes"], args["ws"], args["ws_bytes"], None)
 
@@ -71,6 +72,7 @@ def test_validation_codes(L):
     assert _call_mlp_fwd(L, x=0x10004) == 3
     assert _call_mlp_fwd(L, dt=5) == 4
     assert _call_mlp_fwd(L, mode=9) == 4
+    assert _call_mlp_fwd(L, act=2) == 4
     assert _call_mlp_fwd(L, ws_bytes=16) == 5
     assert "ws" in L.lr_last_error()
     assert _call_mlp_fwd(L, saved_bytes=16) == 5

@@ -43,28 +43,31 @@ def _sync_check():
     L.lr_check_device_error()
 
 
-def run_mlp(shape, mode, seed=0):
+ACT_NAMES = {0: "silu", 1: "identity"}
+
+
+def run_mlp(shape, mode, seed=0, act=0):
     from rank_bottleneck_block_gb300.runner import MlpBlock
 
     case = I.make_mlp_case(shape, seed)
-    blk = MlpBlock(shape, case, mode)
+    blk = MlpBlock(shape, case, mode, act=act)
     blk.forward()
     blk.backward()
     _sync_check()
     return case, blk
 
 
-def check_mlp(shape, mode, seed=0):
-    case, blk = run_mlp(shape, mode, seed)
-    ref_out, saved = O.mlp_block_fwd(case["x"], case["g"], case, shape.eps, O.FULL)
-    gr = O.mlp_block_bwd(case["g"], case, saved, case["G"], shape.eps)
+def check_mlp(shape, mode, seed=0, act=0):
+    case, blk = run_mlp(shape, mode, seed, act)
+    ref_out, saved = O.mlp_block_fwd(case["x"], case["g"], case, shape.eps, O.FULL, act=ACT_NAMES[act])
+    gr = O.mlp_block_bwd(case["g"], case, saved, case["G"], shape.eps, act=ACT_NAMES[act])
     tol = TOL[shape.dtype]
     errs = {"out": maxrel(blk.out, ref_out), "dx": maxrel(blk.dx, gr["dx"]), "dg": maxrel(blk.dg, gr["dg"])}
     for k in ("gate", "up", "down"):
         errs[f"dA_{k}"] = maxrel(blk.grads[f"dA_{k}"], gr[f"dA_{k}"])
         errs[f"dB_{k}"] = maxrel(blk.grads[f"dB_{k}"], gr[f"dB_{k}"])
     bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, f"{shape} mode={mode}: {errs}"
+    assert not bad, f"{shape} mode={mode} act={act}: {errs}"
     return errs, blk
 
 
@@ -167,16 +170,16 @@ def test_proj_group(norm, group, dtype):
     _check_proj(shape, seed=group)
 
 
-def _check_proj(shape, seed=0):
+def _check_proj(shape, seed=0, act=0):
     from rank_bottleneck_block_gb300.runner import ProjGroup
 
     case = I.make_proj_case(shape, seed)
-    pg = ProjGroup(shape, case)
+    pg = ProjGroup(shape, case, act=act)
     pg.forward()
     pg.backward()
     _sync_check()
-    outs, saved = O.proj_group_fwd(case["x"], case["g"], case["A"], case["B"], shape.eps)
-    gr = O.proj_group_bwd(case["g"], case["A"], case["B"], saved, case["G"])
+    outs, saved = O.proj_group_fwd(case["x"], case["g"], case["A"], case["B"], shape.eps, act=ACT_NAMES[act])
+    gr = O.proj_group_bwd(case["g"], case["A"], case["B"], saved, case["G"], act=ACT_NAMES[act])
     tol = TOL[shape.dtype]
     errs = {"dx": maxrel(pg.dx, gr["dx"])}
     if shape.norm:
@@ -187,6 +190,35 @@ def _check_proj(shape, seed=0):
         errs[f"dB{i}"] = maxrel(pg.dB[i], gr["dB"][i])
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{shape}: {errs}"
+
+
+# ------------------------------------------- sigma = identity (plain W = B A)
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("dims", [(200, 136, 328, 40), (129, 64, 128, 64)])
+def test_mlp_identity_bf16(mode, dims):
+    T, d, f, r = dims
+    check_mlp(I.MlpShape(T=T, d=d, f=f, r=r, dtype="bf16"), mode, seed=21, act=1)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_mlp_identity_f32(mode):
+    check_mlp(I.MLP_TINY_F32, mode, seed=22, act=1)
+
+
+def test_mlp_identity_checkpoint_bitwise_equals_full():
+    shape = I.MlpShape(T=520, d=256, f=688, r=64, dtype="bf16")
+    _, full = run_mlp(shape, 0, seed=23, act=1)
+    _, ck = run_mlp(shape, 1, seed=23, act=1)
+    assert torch.equal(full.dx, ck.dx)
+    for k in full.grads:
+        assert torch.equal(full.grads[k], ck.grads[k]), k
+
+
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_proj_group_identity(norm, dtype):
+    shape = I.ProjShape(T=260, d_in=200, d_out=136, r=48, group=3, norm=norm, dtype=dtype)
+    _check_proj(shape, seed=24, act=1)
 
 
 @pytest.mark.slow
