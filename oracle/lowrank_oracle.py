@@ -251,6 +251,44 @@ def mlp_block_bwd(g, W: Dict[str, np.ndarray], saved, G, eps: float = 1e-6, act:
 
 
 # ---------------------------------------------------------------------------
+# Dense (full-rank) SwiGLU MLP block, the map the low-rank block replaces
+# (technical summary §1: each dense W is replaced by a pair; the pages compare
+# BOOST with full-rank training):
+#   n = RMSNorm(x); a = n W_gate^T; b = n W_up^T; h = SiLU(a) * b; out = x + h W_down^T
+# ---------------------------------------------------------------------------
+_DENSE_KEYS = ("W_gate", "W_up", "W_down")
+
+
+def dense_mlp_fwd(x, g, W: Dict[str, np.ndarray], eps: float = 1e-6):
+    """Forward of the dense block. Returns (out, saved) with every intermediate kept."""
+    x, g = to64(x), to64(g)
+    W = {k: to64(W[k]) for k in _DENSE_KEYS}
+    n, s = rmsnorm(x, g, eps)
+    a = n @ W["W_gate"].T
+    b = n @ W["W_up"].T
+    h = silu(a) * b
+    out = x + h @ W["W_down"].T
+    return out, dict(x=x, n=n, s=s, a=a, b=b, h=h)
+
+
+def dense_mlp_bwd(g, W: Dict[str, np.ndarray], saved, G):
+    """Backward of the dense block given dL/dout = G. Returns dict with dx, dg, dW_gate, dW_up, dW_down."""
+    g = to64(g)
+    W = {k: to64(W[k]) for k in _DENSE_KEYS}
+    G = to64(G)
+    S = saved
+    dW_down = G.T @ S["h"]
+    dh = G @ W["W_down"]
+    da = dh * S["b"] * silu_grad(S["a"])
+    db = dh * silu(S["a"])
+    dW_gate = da.T @ S["n"]
+    dW_up = db.T @ S["n"]
+    dn = da @ W["W_gate"] + db @ W["W_up"]
+    dx_n, dg = rmsnorm_bwd(S["x"], g, S["s"], dn)
+    return dict(dx=G + dx_n, dg=dg, dW_gate=dW_gate, dW_up=dW_up, dW_down=dW_down)
+
+
+# ---------------------------------------------------------------------------
 # Projection group: pairs that read the same input (q/k/v), optionally behind
 # one RMSNorm; technical summary §2.2 "linear-layer grouping" concatenates
 # their A weights, which is exact, so the oracle runs them one by one.

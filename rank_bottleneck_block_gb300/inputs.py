@@ -124,6 +124,23 @@ def make_mlp_case(shape: MlpShape, seed: int = 0, with_grad: bool = True, device
     return c
 
 
+def make_dense_case(shape: MlpShape, seed: int = 0, with_grad: bool = True, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """Host tensors for the dense (full-rank) MLP block of the same d, f: x, g, W_gate, W_up [f, d],
+    W_down [d, f] (N(0, 1/fan_in)) and upstream grad G.  shape.r is not used."""
+    dt = _torch_dtype(shape.dtype)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    c: Dict[str, torch.Tensor] = {}
+    c["x"] = _normal(gen, (shape.T, shape.d), 1.0).to(dt)
+    c["g"] = _normal(gen, (shape.d,), 0.1, mean=1.0).to(dt)
+    c["W_gate"] = _normal(gen, (shape.f, shape.d), shape.d ** -0.5).to(dt)
+    c["W_up"] = _normal(gen, (shape.f, shape.d), shape.d ** -0.5).to(dt)
+    c["W_down"] = _normal(gen, (shape.d, shape.f), shape.f ** -0.5).to(dt)
+    if with_grad:
+        c["G"] = _normal(gen, (shape.T, shape.d), 1.0).to(dt)
+    return c
+
+
 def make_proj_case(shape: ProjShape, seed: int = 0, with_grad: bool = True, device: str = "cpu") -> Dict[str, object]:
     """Host tensors for a projection group: x, optional g, pairs, and one upstream grad per pair."""
     dt = _torch_dtype(shape.dtype)

@@ -276,6 +276,67 @@ def test_backward_matches_autograd_moderate_size():
         assert rel(gr[f"dB_{k}"], tW[f"B_{k}"].grad.numpy()) < 1e-12
 
 
+# ------------------------------------------------------- dense (full-rank) block
+def tiny_dense(seed, T=5, d=16, f=24):
+    R = rng(seed)
+    x = R.standard_normal((T, d))
+    g = 1.0 + 0.1 * R.standard_normal(d)
+    W = {"W_gate": R.standard_normal((f, d)) / np.sqrt(d), "W_up": R.standard_normal((f, d)) / np.sqrt(d),
+         "W_down": R.standard_normal((d, f)) / np.sqrt(f)}
+    G = R.standard_normal((T, d))
+    return x, g, W, G
+
+
+def test_dense_block_finite_differences():
+    x, g, W, G = tiny_dense(31)
+
+    def loss():
+        out, _ = O.dense_mlp_fwd(x, g, W, 1e-6)
+        return float(np.sum(out * G))
+
+    _, saved = O.dense_mlp_fwd(x, g, W, 1e-6)
+    gr = O.dense_mlp_bwd(g, W, saved, G)
+    _fd_check(loss, {"x": x, "g": g, **W}, {"x": gr["dx"], "g": gr["dg"], "W_gate": gr["dW_gate"],
+                                            "W_up": gr["dW_up"], "W_down": gr["dW_down"]})
+
+
+def test_dense_block_is_the_lowrank_block_with_identity_factors():
+    """r = d, A_gate = A_up = I, B = W, A_down = W_down, B_down = I and sigma = identity turn the
+    low-rank block into the dense one: outputs and every gradient agree."""
+    x, g, W, G = tiny_dense(32, T=6, d=16, f=24)
+    d = x.shape[1]
+    I_d = np.eye(d)
+    L = {"A_gate": I_d, "B_gate": W["W_gate"], "A_up": I_d, "B_up": W["W_up"], "A_down": W["W_down"],
+         "B_down": I_d}
+    out_l, sv_l = O.mlp_block_fwd(x, g, L, 1e-6, O.FULL, act="identity")
+    gr_l = O.mlp_block_bwd(g, L, sv_l, G, 1e-6, act="identity")
+    out_d, sv_d = O.dense_mlp_fwd(x, g, W, 1e-6)
+    gr_d = O.dense_mlp_bwd(g, W, sv_d, G)
+    assert rel(out_d, out_l) < 1e-13
+    assert rel(gr_d["dx"], gr_l["dx"]) < 1e-12
+    assert rel(gr_d["dg"], gr_l["dg"]) < 1e-12
+    assert rel(gr_d["dW_gate"], gr_l["dB_gate"]) < 1e-12
+    assert rel(gr_d["dW_up"], gr_l["dB_up"]) < 1e-12
+    assert rel(gr_d["dW_down"], gr_l["dA_down"]) < 1e-12
+
+
+def test_dense_block_matches_autograd():
+    x, g, W, G = tiny_dense(33, T=48, d=64, f=96)
+    _, saved = O.dense_mlp_fwd(x, g, W, 1e-6)
+    gr = O.dense_mlp_bwd(g, W, saved, G)
+    tx = torch.from_numpy(x.copy()).requires_grad_()
+    tg = torch.from_numpy(g.copy()).requires_grad_()
+    tW = {k: torch.from_numpy(v.copy()).requires_grad_() for k, v in W.items()}
+    F = torch.nn.functional
+    n = F.rms_norm(tx, (x.shape[1],), tg, eps=1e-6)
+    out = tx + (F.silu(n @ tW["W_gate"].T) * (n @ tW["W_up"].T)) @ tW["W_down"].T
+    (out * torch.from_numpy(G)).sum().backward()
+    assert rel(gr["dx"], tx.grad.numpy()) < 1e-12
+    assert rel(gr["dg"], tg.grad.numpy()) < 1e-12
+    for k in W:
+        assert rel(gr[f"d{k}"], tW[k].grad.numpy()) < 1e-12, k
+
+
 def test_folded_backward_forms_match_explicit():
     """The folded forms a fused implementation uses (gain inside A, 1/rms as a row scale,
     rho = sum_i du_i u_i) agree with the oracle's explicit RMSNorm backward."""
