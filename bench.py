@@ -379,7 +379,7 @@ def _roofline(flops, nbytes, ms, pk):
 
 
 def run_other(a):
-    """Non-default workloads (one JSON line each): attn_proj, stack, sweep."""
+    """Non-default workloads (one JSON line each): attn_proj, stack, sweep, dense."""
     import torch
 
     from rank_bottleneck_block_gb300 import build as B
@@ -387,7 +387,7 @@ def run_other(a):
     B.build()
     from rank_bottleneck_block_gb300 import inputs as I
     from rank_bottleneck_block_gb300 import lowrank as L
-    from rank_bottleneck_block_gb300.runner import BlockStack, ProjGroup
+    from rank_bottleneck_block_gb300.runner import BlockStack, DenseBlock, MlpBlock, ProjGroup
 
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
@@ -432,6 +432,28 @@ def run_other(a):
             del st
             torch.cuda.empty_cache()
         print(json.dumps(out), flush=True)
+    elif a.workload == "dense":
+        # The low-rank block against the full-rank block it replaces, same d, f, T, same kernels, one box.
+        shape = I.MLP_BLOCK_BF16
+        T, d, f, r = shape.T, shape.d, shape.f, shape.r
+        res = {"workload": f"low-rank vs dense SwiGLU MLP block fwd+bwd, T={T} d={d} f={f} (low-rank r={r}), bf16"}
+        lr_blk = MlpBlock(shape, I.make_mlp_case(shape, seed=0, device="cuda"), L.LR_SAVE_CKPT, device=dev)
+        ms_lr = _time_steps(lr_blk.step, a.steps, a.warmup, flush, stream)
+        L.lr_check_device_error()
+        _, _, fl_lr, nb_lr = workload("ckpt")
+        res["lowrank_ckpt"] = {"ms_per_step": round(ms_lr, 4), "tokens_per_s": round(T / (ms_lr / 1e3), 1),
+                               "params": 2 * r * d + 2 * f * r + r * f + d * r, **_roofline(fl_lr, nb_lr, ms_lr, pk)}
+        del lr_blk
+        torch.cuda.empty_cache()
+        dn = DenseBlock(shape, I.make_dense_case(shape, seed=0, device="cuda"), device=dev)
+        ms_dn = _time_steps(dn.step, a.steps, a.warmup, flush, stream)
+        L.lr_check_device_error()
+        fl_dn = 18.0 * T * d * f  # fwd 6 T d f, bwd twice that
+        nb_dn = 2.0 * T * d * 4 + 3 * d * f * (2 + 4) + 3.0 * T * f * 2 * 2 + 2.0 * d * 6
+        res["dense"] = {"ms_per_step": round(ms_dn, 4), "tokens_per_s": round(T / (ms_dn / 1e3), 1),
+                        "params": 3 * d * f, **_roofline(fl_dn, nb_dn, ms_dn, pk)}
+        res["lowrank_speedup"] = round(ms_dn / ms_lr, 3)
+        print(json.dumps(res), flush=True)
     elif a.workload == "sweep":
         rows = []
         for shp in I.sweep_shapes():
@@ -490,7 +512,7 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["mlp_block", "attn_proj", "stack", "sweep"], default="mlp_block",
+    ap.add_argument("--workload", choices=["mlp_block", "attn_proj", "stack", "sweep", "dense"], default="mlp_block",
                     help="mlp_block is the benchmark line; the others print their own measurement lines")
     a = ap.parse_args(argv)
     if a.warmup < 3:

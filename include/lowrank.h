@@ -147,6 +147,34 @@ lr_status lr_proj_bwd(lr_dtype dt, lr_act act, int T, int d_in, int d_out, int r
                       const void* const* douts, void* dx, float* dg, const lr_pair_grad* grads, void* ws,
                       size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------- dense MLP block
+ * The full-rank block that the low-rank MLP block replaces (the pages compare
+ * BOOST against full-rank training; this is the same-device reference point):
+ *     n   = RMSNorm(x; g, eps)
+ *     a   = W_gate n,  b = W_up n           W_gate, W_up [f, d]
+ *     h   = SiLU(a) * b                     [T, f]
+ *     out = x + W_down h                    W_down [d, f]
+ * It runs on the same kernels as the low-rank block: gate/up as one
+ * dual-accumulator GEMM with the gain folded into the weights and 1/rms applied
+ * as a row scale (s from a row pass), the SwiGLU product and its backward fused
+ * into the GEMM epilogues.  `saved` keeps a, b, h (dtype) and s (fp32); there
+ * is no checkpointing mode.  Same conventions and errors as the MLP block.
+ */
+size_t lr_dense_saved_bytes(lr_dtype dt, int T, int d, int f);
+size_t lr_dense_fwd_workspace_bytes(lr_dtype dt, int T, int d, int f);
+size_t lr_dense_bwd_workspace_bytes(lr_dtype dt, int T, int d, int f);
+
+/* x [T,d], g [d] -> out [T,d]; fills `saved`. */
+lr_status lr_dense_fwd(lr_dtype dt, int T, int d, int f, float eps, const void* x, const void* g,
+                       const void* W_gate, const void* W_up, const void* W_down, void* out, void* saved,
+                       size_t saved_bytes, void* ws, size_t ws_bytes, void* stream);
+
+/* dout [T,d] -> dx [T,d] (dtype), dg [d], dW_gate, dW_up [f,d], dW_down [d,f] (fp32). */
+lr_status lr_dense_bwd(lr_dtype dt, int T, int d, int f, float eps, const void* x, const void* g,
+                       const void* W_gate, const void* W_up, const void* W_down, const void* saved,
+                       size_t saved_bytes, const void* dout, void* dx, float* dg, float* dW_gate, float* dW_up,
+                       float* dW_down, void* ws, size_t ws_bytes, void* stream);
+
 /* -------------------------------------------------------------- block stack
  * One training step of `nblocks` residual MLP blocks (as lr_mlp_fwd, sigma = SiLU) and a
  * mean-squared-error loss against `target` [T, d]:

@@ -34,7 +34,10 @@ enum EpiKind : int {
   EPI_SWIGLU_BWD = 7, // dh = acc; a = aux0, b = aux1: out0 = dh b SiLU'(a), out1 = dh SiLU(a)
   EPI_DX_NORM = 8,    // out0 = aux0 (optional) + acc - coef s[m]^2 rho[m] aux1[m,n], rho = sum of rowpart_in
   EPI_F32 = 9,        // fp32 out0 (+ split * split_stride): weight-gradient partials
-  EPI_COUNT = 10
+  EPI_NORM_SWIGLU = 10,     // dense gate/up: a = round(s acc0), b = round(s acc1), h = SiLU(a) b -> (h, a, b)
+  EPI_SWIGLU_BWD_NORM = 11, // dense: dh = acc; da, db as SWIGLU_BWD; out0 = s da, out1 = s db;
+                            //        rowpart = sum (da a + db b)
+  EPI_COUNT = 12
 };
 
 constexpr int kMaxBatch = 4;

@@ -177,6 +177,46 @@ struct EpiDef<EPI_DX_NORM> {  // dx = G + acc - k x  (aux0 = G, may be absent; a
 };
 
 template <>
+struct EpiDef<EPI_NORM_SWIGLU> {  // a = round(s acc0), b = round(s acc1), h = SiLU(a) b -> (h, a, b)
+  static constexpr int NACC = 2, NAUX = 0, NOUT = 3;
+  static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[2][W], const float (&)[1][W],
+                                             float (&o)[3][W], float&) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      const float a = Num<ST>::round(ri.s * v[0][j]);
+      const float b = Num<ST>::round(ri.s * v[1][j]);
+      o[0][j] = silu<ST>(a) * b;
+      o[1][j] = a;
+      o[2][j] = b;
+    }
+  }
+};
+
+template <>
+struct EpiDef<EPI_SWIGLU_BWD_NORM> {  // dh = acc; da, db; out = s da, s db; part = sum da a + db b (aux a, b)
+  static constexpr int NACC = 1, NAUX = 2, NOUT = 2;
+  static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = false, ROWPART = true;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[1][W], const float (&a)[2][W],
+                                             float (&o)[2][W], float& part) {
+    float p = 0.f;
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      const float dh = v[0][j], av = a[0][j], bv = a[1][j];
+      const float l = Num<ST>::logistic(av);
+      const float da = dh * bv * (l * (1.f + av * (1.f - l)));
+      const float db = dh * (av * l);
+      p = fmaf(da, av, fmaf(db, bv, p));
+      o[0][j] = ri.s * da;
+      o[1][j] = ri.s * db;
+    }
+    part = p;
+  }
+};
+
+template <>
 struct EpiDef<EPI_F32> {  // fp32 weight-gradient partial
   static constexpr int NACC = 1, NAUX = 0, NOUT = 1;
   static constexpr bool OUT_F32 = true, NEED_S = false, NEED_RHO = false, ROWPART = false;

@@ -13,5 +13,7 @@ LR_INST(EPI_DSILU_NORM)
 LR_INST(EPI_SWIGLU_BWD)
 LR_INST(EPI_DX_NORM)
 LR_INST(EPI_F32)
+LR_INST(EPI_NORM_SWIGLU)
+LR_INST(EPI_SWIGLU_BWD_NORM)
 #undef LR_INST
 }  // namespace lr

@@ -12,6 +12,8 @@ LR_INST(EPI_DSILU_NORM, 128, false, true)
 LR_INST(EPI_DSILU_NORM, 256, false, true)
 LR_INST(EPI_SWIGLU_BWD, 128, false, true)
 LR_INST(EPI_SWIGLU_BWD, 256, false, true)
+LR_INST(EPI_SWIGLU_BWD_NORM, 128, false, true)
+LR_INST(EPI_SWIGLU_BWD_NORM, 256, false, true)
 LR_INST(EPI_DX_NORM, 128, false, true)
 LR_INST(EPI_DX_NORM, 256, false, true)
 LR_INST(EPI_STORE, 128, false, true)

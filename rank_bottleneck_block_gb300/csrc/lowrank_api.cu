@@ -201,6 +201,10 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_SWIGLU:
       if (kk && g.nacc == 2) return umma_bn<EPI_SWIGLU, false, false>(g, st);
       break;
+    case EPI_NORM_SWIGLU:
+      if (kk && g.nacc == 2) return launch_umma<EPI_NORM_SWIGLU, 256, false, false>(g, st);
+      break;
+    case EPI_SWIGLU_BWD_NORM: if (km) return umma_bn<EPI_SWIGLU_BWD_NORM, false, true>(g, st); break;
     case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, false, true>(g, st); break;
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
@@ -223,13 +227,15 @@ static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
     case EPI_SWIGLU_BWD: return launch_simt<EPI_SWIGLU_BWD>(g, st);
     case EPI_DX_NORM: return launch_simt<EPI_DX_NORM>(g, st);
     case EPI_F32: return launch_simt<EPI_F32>(g, st);
+    case EPI_NORM_SWIGLU: return launch_simt<EPI_NORM_SWIGLU>(g, st);
+    case EPI_SWIGLU_BWD_NORM: return launch_simt<EPI_SWIGLU_BWD_NORM>(g, st);
     default: return cudaErrorNotSupported;
   }
 }
 
 static const char* epi_name(EpiKind k) {
-  static const char* names[] = {"norm_silu", "silu", "store", "resid", "swiglu",
-                                "dsilu", "dsilu_norm", "swiglu_bwd", "dx_norm", "f32"};
+  static const char* names[] = {"norm_silu", "silu",       "store",  "resid",       "swiglu",        "dsilu",
+                                "dsilu_norm", "swiglu_bwd", "dx_norm", "f32", "norm_swiglu", "swiglu_bwd_norm"};
   return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
 }
 
@@ -243,6 +249,7 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   g.ep.act = c.act;
   if (c.dt == LR_BF16) {
     if (k == EPI_SWIGLU) g.bn = kSwigluBn;
+    else if (k == EPI_NORM_SWIGLU) g.bn = 256;  // the split-phase dual-accumulator kernel
     else if (g.bn != 128 && g.bn != 256) g.bn = pick_bn(g, c.sms);
   } else {
     g.bn = 0;
@@ -678,6 +685,147 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.rowscale = S.s;
     k.ep.rowpart_in = W.rowpart;
     k.ep.rowpart_in_chunks = 2 * cdiv(r, ch);
+    k.ep.coef = 1.f / static_cast<float>(d);
+    k.ep.out0[0] = dx;
+    k.ep.ldo0 = d;
+    LR_TRY(gemm(c, EPI_DX_NORM, k));
+  }
+  return LR_OK;
+}
+
+// ====================================================== dense MLP block
+// The full-rank SwiGLU MLP block the low-rank block replaces, on the same kernels, for a
+// same-device comparison: n = RMSNorm(x), a = W_gate n, b = W_up n, h = SiLU(a) b,
+// out = x + W_down h.  RMSNorm is folded the same way (W' = W * g, 1/rms as a row scale;
+// the statistics come from a row pass), gate and up are one dual-accumulator GEMM with the
+// SwiGLU product fused, and the backward mirrors the low-rank one with the pairs replaced by
+// single matrices: dh = dout W_down with the SwiGLU backward, 1/rms scaling and rho partials
+// fused; dW = (s du)^T x with the gain unfold and dg; dx in one GEMM with K = 2f.
+struct DenseSaved {
+  void *a, *b, *h;
+  float* s;
+};
+
+static size_t dense_saved_layout(lr_dtype dt, int T, int f, void* base, DenseSaved* S) {
+  const size_t es = esize(dt);
+  Arena ar(base);
+  DenseSaved tmp;
+  if (!S) S = &tmp;
+  S->a = ar.take(es * T * f);
+  S->b = ar.take(es * T * f);
+  S->h = ar.take(es * T * f);
+  S->s = static_cast<float*>(ar.take(sizeof(float) * T));
+  return ar.size();
+}
+
+struct DenseWs {
+  void *Wf, *du_s;
+  float *rowpart, *wpart, *dgpart;
+};
+
+static size_t dense_ws_layout(lr_dtype dt, bool bwd, int T, int d, int f, void* base, DenseWs* W) {
+  const size_t es = esize(dt);
+  Arena ar(base);
+  DenseWs tmp;
+  if (!W) W = &tmp;
+  memset(W, 0, sizeof(*W));
+  W->Wf = ar.take(es * 2 * f * d);
+  if (bwd) {
+    W->du_s = ar.take(es * T * 2 * f);
+    W->rowpart = static_cast<float*>(ar.take(sizeof(float) * cdiv(f, chunk_width(dt)) * T));
+    W->wpart = static_cast<float*>(
+        ar.take(std::max(wgrad_part_bytes(dt, d, f, T), wgrad_part_bytes(dt, 2 * f, d, T))));
+    W->dgpart = static_cast<float*>(ar.take(sizeof(float) * cdiv(2 * f, kReduceRows) * d));
+  }
+  return ar.size();
+}
+
+static lr_status dense_fwd_impl(const Ctx& c, int T, int d, int f, float eps, const void* x, const void* g,
+                                const void* Wg, const void* Wu, const void* Wd, void* out, void* saved, void* ws) {
+  DenseSaved S;
+  DenseWs W;
+  dense_saved_layout(c.dt, T, f, saved, &S);
+  dense_ws_layout(c.dt, false, T, d, f, ws, &W);
+  StackSrc src = {{Wg, Wu, nullptr}};
+  LR_TRY(fold(c, W.Wf, src, 2, f, d, g));
+  LR_TRY(rstd(c, x, T, d, eps, S.s));
+  {
+    GemmCall k = new_call(T, f, d);
+    k.nacc = 2;
+    k.A[0] = {x, d};
+    k.A[1] = {x, d};
+    k.B[0] = {W.Wf, d};
+    k.B[1] = {off(W.Wf, c.es * f * d), d};
+    k.ep.out0[0] = S.h;
+    k.ep.out1[0] = S.a;
+    k.ep.out2[0] = S.b;
+    k.ep.ldo0 = k.ep.ldo1 = k.ep.ldo2 = f;
+    k.ep.rowscale = S.s;
+    LR_TRY(gemm(c, EPI_NORM_SWIGLU, k));
+  }
+  {
+    GemmCall k = new_call(T, d, f);
+    k.A[0] = {S.h, f};
+    k.B[0] = {Wd, f};
+    k.ep.out0[0] = out;
+    k.ep.ldo0 = d;
+    k.ep.aux0[0] = x;
+    k.ep.lda0 = d;
+    LR_TRY(gemm(c, EPI_RESID, k));
+  }
+  return LR_OK;
+}
+
+static lr_status dense_bwd_impl(const Ctx& c, int T, int d, int f, const void* x, const void* g, const void* Wg,
+                                const void* Wu, const void* Wd, const void* saved, const void* G, void* dx, float* dg,
+                                float* dWg, float* dWu, float* dWd, void* ws) {
+  DenseSaved S;
+  DenseWs W;
+  dense_saved_layout(c.dt, T, f, const_cast<void*>(saved), &S);
+  dense_ws_layout(c.dt, true, T, d, f, ws, &W);
+  const int ch = chunk_width(c.dt);
+  StackSrc src = {{Wg, Wu, nullptr}};
+  LR_TRY(fold(c, W.Wf, src, 2, f, d, g));
+  // dh = dout W_down; da = dh b SiLU'(a), db = dh SiLU(a); du_s = s [da | db]; rho partials
+  {
+    GemmCall k = new_call(T, f, d);
+    k.b_mn = true;
+    k.A[0] = {G, d};
+    k.B[0] = {Wd, f};
+    k.ep.aux0[0] = S.a;
+    k.ep.aux1[0] = S.b;
+    k.ep.lda0 = k.ep.lda1 = f;
+    k.ep.out0[0] = W.du_s;
+    k.ep.out1[0] = off(W.du_s, c.es * f);
+    k.ep.ldo0 = k.ep.ldo1 = 2LL * f;
+    k.ep.rowscale = S.s;
+    k.ep.rowpart = W.rowpart;
+    k.ep.rowpart_chunks = cdiv(f, ch);
+    LR_TRY(gemm(c, EPI_SWIGLU_BWD_NORM, k));
+  }
+  // dW_down = dout^T h
+  {
+    WgradDst dst = {{dWd, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, d, f, T, {G, d}, {S.h, f}, dst, d, nullptr, nullptr, W.wpart));
+  }
+  // dW'_{gate;up} = (s du)^T x; dW = dW' * g; dg_j = sum_i dW'_ij W_ij
+  {
+    WgradDst dst = {{dWg, dWu, nullptr}, {Wg, Wu, nullptr}};
+    LR_TRY(wgrad(c, 2 * f, d, T, {W.du_s, 2LL * f}, {x, d}, dst, f, g, W.dgpart, W.wpart));
+    LR_TRY(dg_finalize(c, W.dgpart, cdiv(2 * f, kReduceRows), d, dg));
+  }
+  // dx = dout + (s du) W' - (s^2 / d) rho x
+  {
+    GemmCall k = new_call(T, d, 2 * f);
+    k.b_mn = true;
+    k.A[0] = {W.du_s, 2LL * f};
+    k.B[0] = {W.Wf, d};
+    k.ep.aux0[0] = G;
+    k.ep.aux1[0] = x;
+    k.ep.lda0 = k.ep.lda1 = d;
+    k.ep.rowscale = S.s;
+    k.ep.rowpart_in = W.rowpart;
+    k.ep.rowpart_in_chunks = cdiv(f, ch);
     k.ep.coef = 1.f / static_cast<float>(d);
     k.ep.out0[0] = dx;
     k.ep.ldo0 = d;
@@ -1203,6 +1351,70 @@ lr_status lr_proj_bwd(lr_dtype dt, lr_act act, int T, int d_in, int d_out, int r
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c, act));
   return proj_bwd_impl(c, T, d_in, d_out, r, group, pairs, g, x, saved, douts, dx, dg, grads, ws);
+}
+
+size_t lr_dense_saved_bytes(lr_dtype dt, int T, int d, int f) {
+  if (check_dtype(dt) || check_dim(T, "T", false) || check_dim(d, "d", true) || check_dim(f, "f", true)) return 0;
+  return dense_saved_layout(dt, T, f, nullptr, nullptr);
+}
+
+size_t lr_dense_fwd_workspace_bytes(lr_dtype dt, int T, int d, int f) {
+  if (check_dtype(dt) || check_dim(T, "T", false) || check_dim(d, "d", true) || check_dim(f, "f", true)) return 0;
+  return dense_ws_layout(dt, false, T, d, f, nullptr, nullptr);
+}
+
+size_t lr_dense_bwd_workspace_bytes(lr_dtype dt, int T, int d, int f) {
+  if (check_dtype(dt) || check_dim(T, "T", false) || check_dim(d, "d", true) || check_dim(f, "f", true)) return 0;
+  return dense_ws_layout(dt, true, T, d, f, nullptr, nullptr);
+}
+
+lr_status lr_dense_fwd(lr_dtype dt, int T, int d, int f, float eps, const void* x, const void* g, const void* W_gate,
+                       const void* W_up, const void* W_down, void* out, void* saved, size_t saved_bytes, void* ws,
+                       size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_mlp_dims(T, d, f, 8));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(g, "g"));
+  LR_TRY(check_ptr(W_gate, "W_gate"));
+  LR_TRY(check_ptr(W_up, "W_up"));
+  LR_TRY(check_ptr(W_down, "W_down"));
+  LR_TRY(check_ptr(out, "out"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, dense_saved_layout(dt, T, f, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, dense_ws_layout(dt, false, T, d, f, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return dense_fwd_impl(c, T, d, f, eps, x, g, W_gate, W_up, W_down, out, saved, ws);
+}
+
+lr_status lr_dense_bwd(lr_dtype dt, int T, int d, int f, float eps, const void* x, const void* g, const void* W_gate,
+                       const void* W_up, const void* W_down, const void* saved, size_t saved_bytes, const void* dout,
+                       void* dx, float* dg, float* dW_gate, float* dW_up, float* dW_down, void* ws, size_t ws_bytes,
+                       void* stream) {
+  (void)eps;
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_mlp_dims(T, d, f, 8));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(g, "g"));
+  LR_TRY(check_ptr(W_gate, "W_gate"));
+  LR_TRY(check_ptr(W_up, "W_up"));
+  LR_TRY(check_ptr(W_down, "W_down"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(dout, "dout"));
+  LR_TRY(check_ptr(dx, "dx"));
+  LR_TRY(check_ptr(dg, "dg"));
+  LR_TRY(check_ptr(dW_gate, "dW_gate"));
+  LR_TRY(check_ptr(dW_up, "dW_up"));
+  LR_TRY(check_ptr(dW_down, "dW_down"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, dense_saved_layout(dt, T, f, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, dense_ws_layout(dt, true, T, d, f, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return dense_bwd_impl(c, T, d, f, x, g, W_gate, W_up, W_down, saved, dout, dx, dg, dW_gate, dW_up, dW_down, ws);
 }
 
 size_t lr_stack_workspace_bytes(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, int f, int r) {

@@ -332,7 +332,7 @@ struct Config {
   // are released separately.  Phase 1 stages round(a) in shared memory (exact: a is stored
   // rounded) and frees a's columns for the next tile while b still accumulates; phase 2 moves
   // round(b) into registers, frees b's columns, then computes h.
-  static constexpr bool SPLIT = (K == EPI_SWIGLU) && NBUF == 1;
+  static constexpr bool SPLIT = (K == EPI_SWIGLU || K == EPI_NORM_SWIGLU) && NBUF == 1;
   // Staging per epilogue warp: NO output sets of NOUT tiles (ping-pong when stores would
   // otherwise stall the next chunk), NA operand sets of NAUX tiles (loads NA chunks ahead),
   // and for the split SwiGLU the round(a) tiles of the warp's chunks.
@@ -735,6 +735,10 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           float v[CW];
           tmem_ld32(t_row + c * CW, v);
           tmem_ld_wait();
+          if constexpr (D::NEED_S) {  // dense gate/up: the 1/rms row scale of the normalised input
+#pragma unroll
+            for (int j = 0; j < CW; ++j) v[j] *= ri.s;
+          }
           const uint32_t base = smem_addr(abuf + ci * C::OUT_BUF);
 #pragma unroll
           for (int j = 0; j < CW / 8; ++j) sts_bf16x8(base + stage_off<64>(lane, j), &v[8 * j]);
@@ -762,6 +766,10 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           float v[CW];
           tmem_ld32(t_row + BN + (g + 2 * ci) * CW, v);
           tmem_ld_wait();
+          if constexpr (D::NEED_S) {
+#pragma unroll
+            for (int j = 0; j < CW; ++j) v[j] *= ri.s;
+          }
 #pragma unroll
           for (int j = 0; j < CW / 2; ++j) bpk[ci][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
         }

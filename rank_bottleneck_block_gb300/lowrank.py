@@ -29,7 +29,8 @@ EXPORTED = [
     "lr_proj_fwd", "lr_proj_bwd", "lr_stack_workspace_bytes", "lr_stack_step", "lr_last_error",
     "lr_check_device_error", "lr_selftest_wait_timeout", "lr_version", "lr_launch_count",
     "lr_profile_start", "lr_profile_stop", "lr_profile_filter", "lr_profile_count", "lr_profile_entry",
-    "lr_proj_fwd_noalloc",
+    "lr_proj_fwd_noalloc", "lr_dense_saved_bytes", "lr_dense_fwd_workspace_bytes", "lr_dense_bwd_workspace_bytes",
+    "lr_dense_fwd", "lr_dense_bwd",
 ]
 
 
@@ -69,6 +70,11 @@ _SIGS = {
     "lr_proj_fwd_noalloc": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _F, _P, ctypes.POINTER(_P),
                                  _P, _SZ, _P]),
     "lr_stack_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "lr_dense_saved_bytes": (_SZ, [_I, _I, _I, _I]),
+    "lr_dense_fwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "lr_dense_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "lr_dense_fwd": (_I, [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P]),
+    "lr_dense_bwd": (_I, [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "lr_stack_step": (_I, [_I, _I, _I, _I, _I, _I, _I, _F, _P, _P, ctypes.POINTER(_P), ctypes.POINTER(lr_pair), _P,
                            _P, ctypes.POINTER(_P), ctypes.POINTER(lr_pair_grad), _P, _SZ, _P]),
     "lr_last_error": (ctypes.c_char_p, []),
@@ -219,6 +225,29 @@ def lr_proj_bwd(dt, T, d_in, d_out, r, pairs: Sequence[lr_pair], g, eps, x, save
     _check(lib().lr_proj_bwd(dt, act, T, d_in, d_out, r, group, _pairs(pairs), _p(g), eps, _p(x), _p(saved),
                              _nbytes(saved), _ptrs(douts), _p(dx), _p(dg), garr, _p(ws), _nbytes(ws),
                              _stream(stream)))
+
+
+def lr_dense_saved_bytes(dt, T, d, f) -> int:
+    return lib().lr_dense_saved_bytes(dt, T, d, f)
+
+
+def lr_dense_fwd_workspace_bytes(dt, T, d, f) -> int:
+    return lib().lr_dense_fwd_workspace_bytes(dt, T, d, f)
+
+
+def lr_dense_bwd_workspace_bytes(dt, T, d, f) -> int:
+    return lib().lr_dense_bwd_workspace_bytes(dt, T, d, f)
+
+
+def lr_dense_fwd(dt, T, d, f, eps, x, g, Wg, Wu, Wd, out, saved, ws, stream=None):
+    _check(lib().lr_dense_fwd(dt, T, d, f, eps, _p(x), _p(g), _p(Wg), _p(Wu), _p(Wd), _p(out), _p(saved),
+                              _nbytes(saved), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def lr_dense_bwd(dt, T, d, f, eps, x, g, Wg, Wu, Wd, saved, dout, dx, dg, dWg, dWu, dWd, ws, stream=None):
+    _check(lib().lr_dense_bwd(dt, T, d, f, eps, _p(x), _p(g), _p(Wg), _p(Wu), _p(Wd), _p(saved), _nbytes(saved),
+                              _p(dout), _p(dx), _p(dg), _p(dWg), _p(dWu), _p(dWd), _p(ws), _nbytes(ws),
+                              _stream(stream)))
 
 
 def lr_stack_workspace_bytes(dt, mode, nblocks, T, d, f, r) -> int:

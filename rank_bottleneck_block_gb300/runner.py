@@ -80,6 +80,45 @@ class MlpBlock:
         self.backward(stream=stream)
 
 
+class DenseBlock:
+    """The full-rank SwiGLU MLP block of the same d, f, resident on the device: the reference point
+    the low-rank block is compared with."""
+
+    def __init__(self, shape: MlpShape, case: Dict[str, torch.Tensor], device="cuda"):
+        self.s, self.device = shape, device
+        self.dt = _dt(shape.dtype)
+        self.t = {k: v.to(device) for k, v in case.items()}
+        T, d, f = shape.T, shape.d, shape.f
+        self.out = torch.empty(T, d, dtype=_tdt(shape.dtype), device=device)
+        self.dx = torch.empty_like(self.out)
+        self.saved = _buf(L.lr_dense_saved_bytes(self.dt, T, d, f), device)
+        self.ws_f = _buf(L.lr_dense_fwd_workspace_bytes(self.dt, T, d, f), device)
+        self.ws_b = _buf(L.lr_dense_bwd_workspace_bytes(self.dt, T, d, f), device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.dg = torch.empty(d, **f32)
+        self.grads = {"dW_gate": torch.empty(f, d, **f32), "dW_up": torch.empty(f, d, **f32),
+                      "dW_down": torch.empty(d, f, **f32)}
+
+    def forward(self, x: Optional[torch.Tensor] = None, stream=None):
+        s, t = self.s, self.t
+        x = t["x"] if x is None else x
+        L.lr_dense_fwd(self.dt, s.T, s.d, s.f, s.eps, x, t["g"], t["W_gate"], t["W_up"], t["W_down"], self.out,
+                       self.saved, self.ws_f, stream)
+        return self.out
+
+    def backward(self, dout: Optional[torch.Tensor] = None, x: Optional[torch.Tensor] = None, stream=None):
+        s, t, gr = self.s, self.t, self.grads
+        x = t["x"] if x is None else x
+        dout = t["G"] if dout is None else dout
+        L.lr_dense_bwd(self.dt, s.T, s.d, s.f, s.eps, x, t["g"], t["W_gate"], t["W_up"], t["W_down"], self.saved,
+                       dout, self.dx, self.dg, gr["dW_gate"], gr["dW_up"], gr["dW_down"], self.ws_b, stream)
+        return self.dx
+
+    def step(self, stream=None):
+        self.forward(stream=stream)
+        self.backward(stream=stream)
+
+
 class HostPipeline:
     """fwd + bwd of an MlpBlock over batches that live in (pinned) host memory.
 

@@ -192,6 +192,48 @@ def _check_proj(shape, seed=0, act=0):
     assert not bad, f"{shape}: {errs}"
 
 
+# ------------------------------------------------- dense (full-rank) block
+def check_dense(shape, seed=0):
+    from rank_bottleneck_block_gb300.runner import DenseBlock
+
+    case = I.make_dense_case(shape, seed)
+    blk = DenseBlock(shape, case)
+    blk.forward()
+    blk.backward()
+    _sync_check()
+    ref_out, saved = O.dense_mlp_fwd(case["x"], case["g"], case, shape.eps)
+    gr = O.dense_mlp_bwd(case["g"], case, saved, case["G"])
+    tol = TOL[shape.dtype]
+    errs = {"out": maxrel(blk.out, ref_out), "dx": maxrel(blk.dx, gr["dx"]), "dg": maxrel(blk.dg, gr["dg"])}
+    for k in ("dW_gate", "dW_up", "dW_down"):
+        errs[k] = maxrel(blk.grads[k], gr[k])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"dense {shape}: {errs}"
+    return blk
+
+
+@pytest.mark.parametrize("dims", [(200, 136, 328), (129, 64, 128), (1, 64, 64), (2112, 512, 1376)])
+def test_dense_block_bf16(dims):
+    T, d, f = dims
+    check_dense(I.MlpShape(T=T, d=d, f=f, r=8, dtype="bf16"), seed=41)
+
+
+def test_dense_block_f32():
+    check_dense(I.MlpShape(T=128, d=256, f=688, r=8, dtype="f32"), seed=42)
+
+
+def test_dense_block_deterministic():
+    shape = I.MlpShape(T=700, d=256, f=512, r=8, dtype="bf16")
+    blk = check_dense(shape, seed=43)
+    dx, grads = blk.dx.clone(), {k: v.clone() for k, v in blk.grads.items()}
+    blk.forward()
+    blk.backward()
+    _sync_check()
+    assert torch.equal(dx, blk.dx)
+    for k in grads:
+        assert torch.equal(grads[k], blk.grads[k]), k
+
+
 # ------------------------------------------- sigma = identity (plain W = B A)
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("dims", [(200, 136, 328, 40), (129, 64, 128, 64)])
