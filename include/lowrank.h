@@ -175,6 +175,33 @@ lr_status lr_dense_bwd(lr_dtype dt, int T, int d, int f, float eps, const void* 
                        size_t saved_bytes, const void* dout, void* dx, float* dg, float* dW_gate, float* dW_up,
                        float* dW_down, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------- bottleneck-aware tensor parallelism (BTP)
+ * BTP (technical summary §2.1) keeps activations sharded along d across the
+ * tensor-parallel ranks and runs a normed group of A's row-parallel: each rank
+ * reduces over its own d-shard, and the one collective is an all-reduce at the
+ * bottleneck width r instead of d.  Online-RMSNorm (§2.2) defers the
+ * normalisation and carries the RMS statistics on that same all-reduce.  These
+ * two calls are one rank's compute around that all-reduce (which the caller
+ * runs, e.g. NCCL over `payload`):
+ *
+ * lr_btp_partial: x_shard [T, d_shard], g_shard [d_shard] and the d_shard
+ *   columns of each pairs[i].A ([r, d_shard], row-major; pairs[i].B unused)
+ *   -> payload, fp32, lr_btp_payload_floats(T, r, group) floats:
+ *      acc [T, group*r] = x_shard (A_shard * g_shard)^T   (partial sums), then
+ *      ss  [T]          = sum_j x_shard[t, j]^2           (partial statistics).
+ * lr_btp_finish: the payload summed over all ranks, d = the full width ->
+ *      s = (ss / d + eps)^(-1/2), u = round(s acc), z = sigma(u)  ([T, group*r]
+ *   dtype, s [T] fp32): what lr_proj_fwd's normed group computes unsharded.
+ * ws of lr_btp_partial: lr_btp_workspace_bytes (the folded A shard).
+ */
+size_t lr_btp_payload_floats(int T, int r, int group);
+size_t lr_btp_workspace_bytes(lr_dtype dt, int d_shard, int r, int group);
+lr_status lr_btp_partial(lr_dtype dt, int T, int d_shard, int r, int group, const lr_pair* pairs,
+                         const void* g_shard, const void* x_shard, float* payload, void* ws, size_t ws_bytes,
+                         void* stream);
+lr_status lr_btp_finish(lr_dtype dt, lr_act act, int T, int d, int r, int group, const float* payload, float eps,
+                        void* u, void* z, float* s, void* stream);
+
 /* -------------------------------------------------------------- block stack
  * One training step of `nblocks` residual MLP blocks (as lr_mlp_fwd, sigma = SiLU) and a
  * mean-squared-error loss against `target` [T, d]:

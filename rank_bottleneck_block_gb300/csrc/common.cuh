@@ -37,7 +37,9 @@ enum EpiKind : int {
   EPI_NORM_SWIGLU = 10,     // dense gate/up: a = round(s acc0), b = round(s acc1), h = SiLU(a) b -> (h, a, b)
   EPI_SWIGLU_BWD_NORM = 11, // dense: dh = acc; da, db as SWIGLU_BWD; out0 = s da, out1 = s db;
                             //        rowpart = sum (da a + db b)
-  EPI_COUNT = 12
+  EPI_F32_SS = 12,          // fp32 out0 = acc (no split); the row sums of squares of the A tiles (raw,
+                            //   not 1/rms) -> rowscale_out: the partial of a row-parallel normed GEMM
+  EPI_COUNT = 13
 };
 
 constexpr int kMaxBatch = 4;

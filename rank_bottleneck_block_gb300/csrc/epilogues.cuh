@@ -217,6 +217,18 @@ struct EpiDef<EPI_SWIGLU_BWD_NORM> {  // dh = acc; da, db; out = s da, s db; par
 };
 
 template <>
+struct EpiDef<EPI_F32_SS> {  // fp32 partial sums of a row-parallel GEMM (its row statistics come from the ring)
+  static constexpr int NACC = 1, NAUX = 0, NOUT = 1;
+  static constexpr bool OUT_F32 = true, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn&, const float (&v)[1][W], const float (&)[1][W],
+                                             float (&o)[1][W], float&) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) o[0][j] = v[0][j];
+  }
+};
+
+template <>
 struct EpiDef<EPI_F32> {  // fp32 weight-gradient partial
   static constexpr int NACC = 1, NAUX = 0, NOUT = 1;
   static constexpr bool OUT_F32 = true, NEED_S = false, NEED_RHO = false, ROWPART = false;

@@ -15,5 +15,6 @@ LR_INST(EPI_DX_NORM)
 LR_INST(EPI_F32)
 LR_INST(EPI_NORM_SWIGLU)
 LR_INST(EPI_SWIGLU_BWD_NORM)
+LR_INST(EPI_F32_SS)
 #undef LR_INST
 }  // namespace lr

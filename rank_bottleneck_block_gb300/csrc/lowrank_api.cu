@@ -205,6 +205,7 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
       if (kk && g.nacc == 2) return launch_umma<EPI_NORM_SWIGLU, 256, false, false>(g, st);
       break;
     case EPI_SWIGLU_BWD_NORM: if (km) return umma_bn<EPI_SWIGLU_BWD_NORM, false, true>(g, st); break;
+    case EPI_F32_SS: if (kk && g.ksplit == 1) return umma_bn<EPI_F32_SS, false, false>(g, st); break;
     case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, false, true>(g, st); break;
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
@@ -229,13 +230,15 @@ static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
     case EPI_F32: return launch_simt<EPI_F32>(g, st);
     case EPI_NORM_SWIGLU: return launch_simt<EPI_NORM_SWIGLU>(g, st);
     case EPI_SWIGLU_BWD_NORM: return launch_simt<EPI_SWIGLU_BWD_NORM>(g, st);
+    case EPI_F32_SS: return launch_simt<EPI_F32_SS>(g, st);
     default: return cudaErrorNotSupported;
   }
 }
 
 static const char* epi_name(EpiKind k) {
   static const char* names[] = {"norm_silu", "silu",       "store",  "resid",       "swiglu",        "dsilu",
-                                "dsilu_norm", "swiglu_bwd", "dx_norm", "f32", "norm_swiglu", "swiglu_bwd_norm"};
+                                "dsilu_norm", "swiglu_bwd", "dx_norm", "f32", "norm_swiglu", "swiglu_bwd_norm",
+                                "f32_ss"};
   return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
 }
 
@@ -834,6 +837,58 @@ static lr_status dense_bwd_impl(const Ctx& c, int T, int d, int f, const void* x
   return LR_OK;
 }
 
+// ============================================== BTP row-parallel normed group
+// Bottleneck-aware tensor parallelism (technical summary §2.1) keeps activations sharded
+// along d and makes a normed group of A's row-parallel: each rank computes fp32 partial
+// sums over its d-shard, and the only collective is one all-reduce at the bottleneck
+// width.  Online-RMSNorm (§2.2) puts the statistics on that same all-reduce: the payload
+// is [acc (T x group*r) | ss (T)], the shard's sums of squares of x appended.
+static size_t btp_ws_layout(lr_dtype dt, int d_shard, int r, int group, void* base, void** Af) {
+  Arena ar(base);
+  void* a = ar.take(esize(dt) * group * r * d_shard);
+  if (Af) *Af = a;
+  return ar.size();
+}
+
+static lr_status btp_partial_impl(const Ctx& c, int T, int d_shard, int r, int group, const lr_pair* pairs,
+                                  const void* g, const void* x, float* payload, void* ws) {
+  void* Af = nullptr;
+  btp_ws_layout(c.dt, d_shard, r, group, ws, &Af);
+  StackSrc src = {{nullptr, nullptr, nullptr}};
+  for (int i = 0; i < group; ++i) src.src[i] = pairs[i].A;
+  LR_TRY(fold(c, Af, src, group, r, d_shard, g));
+  const int R = group * r;
+  float* ss = payload + static_cast<size_t>(T) * R;
+  if (c.dt != LR_BF16) {  // fp32 path: the sums of squares from a row pass
+    LaunchScope scope("rowss", c.st, 0, static_cast<double>(c.es) * T * d_shard + 4.0 * T);
+    cudaError_t e = launch_rstd<float>(static_cast<const float*>(x), T, d_shard, 0.f, ss, c.st, true);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "row sums of squares: %s", cudaGetErrorString(e));
+  }
+  GemmCall k = new_call(T, R, d_shard);
+  k.A[0] = {x, d_shard};
+  k.B[0] = {Af, d_shard};
+  k.ep.out0[0] = payload;
+  k.ep.ldo0 = R;
+  k.ep.split_stride = static_cast<long long>(T) * R;
+  k.ep.rowscale_out = c.dt == LR_BF16 ? ss : nullptr;  // tcgen05: the statistics warps write ss
+  k.ep.coef = 1.f;
+  return gemm(c, EPI_F32_SS, k);
+}
+
+static lr_status btp_finish_impl(const Ctx& c, int T, int d, int R, const float* payload, float eps, void* u, void* z,
+                                 float* s) {
+  const float* ss = payload + static_cast<size_t>(T) * R;
+  LaunchScope scope("norm_finish", c.st, 0, 4.0 * T * R + 4.0 * T + 2.0 * c.es * T * R + 4.0 * T);
+  const float coef = 1.f / static_cast<float>(d);
+  cudaError_t e = (c.dt == LR_BF16)
+                      ? launch_norm_finish<bf16>(payload, ss, T, R, coef, eps, c.act, static_cast<bf16*>(u),
+                                                 static_cast<bf16*>(z), s, c.st)
+                      : launch_norm_finish<float>(payload, ss, T, R, coef, eps, c.act, static_cast<float*>(u),
+                                                  static_cast<float*>(z), s, c.st);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "norm finish: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
 // ======================================================= projection group
 struct ProjSaved {
   void *u, *z;
@@ -1415,6 +1470,50 @@ lr_status lr_dense_bwd(lr_dtype dt, int T, int d, int f, float eps, const void* 
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
   return dense_bwd_impl(c, T, d, f, x, g, W_gate, W_up, W_down, saved, dout, dx, dg, dW_gate, dW_up, dW_down, ws);
+}
+
+size_t lr_btp_payload_floats(int T, int r, int group) {
+  if (check_dim(T, "T", false) || check_dim(r, "r", true) || group < 1 || group > kMaxStack) return 0;
+  return static_cast<size_t>(T) * group * r + static_cast<size_t>(T);
+}
+
+size_t lr_btp_workspace_bytes(lr_dtype dt, int d_shard, int r, int group) {
+  if (check_dtype(dt) || check_dim(d_shard, "d_shard", true) || check_dim(r, "r", true) || group < 1 ||
+      group > kMaxStack)
+    return 0;
+  return btp_ws_layout(dt, d_shard, r, group, nullptr, nullptr);
+}
+
+lr_status lr_btp_partial(lr_dtype dt, int T, int d_shard, int r, int group, const lr_pair* pairs, const void* g_shard,
+                         const void* x_shard, float* payload, void* ws, size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_proj_dims(T, d_shard, 8, r, group));
+  if (!pairs) return fail(LR_ERR_NULL, "pairs is NULL");
+  for (int i = 0; i < group; ++i) LR_TRY(check_ptr(pairs[i].A, "pairs[i].A"));
+  LR_TRY(check_ptr(g_shard, "g_shard"));
+  LR_TRY(check_ptr(x_shard, "x_shard"));
+  LR_TRY(check_ptr(payload, "payload"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(ws_bytes, btp_ws_layout(dt, d_shard, r, group, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return btp_partial_impl(c, T, d_shard, r, group, pairs, g_shard, x_shard, payload, ws);
+}
+
+lr_status lr_btp_finish(lr_dtype dt, lr_act act, int T, int d, int r, int group, const float* payload, float eps,
+                        void* u, void* z, float* s, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_dtype(dt));
+  LR_TRY(check_act(act));
+  LR_TRY(check_proj_dims(T, d, 8, r, group));
+  LR_TRY(check_ptr(payload, "payload"));
+  LR_TRY(check_ptr(u, "u"));
+  LR_TRY(check_ptr(z, "z"));
+  LR_TRY(check_ptr(s, "s"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c, act));
+  return btp_finish_impl(c, T, d, group * r, payload, eps, u, z, s);
 }
 
 size_t lr_stack_workspace_bytes(lr_dtype dt, lr_mode mode, int nblocks, int T, int d, int f, int r) {

@@ -36,7 +36,7 @@ cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols
 
 // ------------------------------------------------------------------ rstd
 template <typename ST>
-__global__ void rstd_kernel(const ST* x, int T, int d, float eps, float* s) {
+__global__ void rstd_kernel(const ST* x, int T, int d, float eps, float* s, int raw) {
   pdl_wait();
   pdl_trigger();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -52,14 +52,49 @@ __global__ void rstd_kernel(const ST* x, int T, int d, float eps, float* s) {
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) s[warp] = 1.f / sqrtf(ss / static_cast<float>(d) + eps);
+  if (lane == 0) s[warp] = raw ? ss : 1.f / sqrtf(ss / static_cast<float>(d) + eps);
 }
 
 template <typename ST>
-cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st) {
+cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st, bool raw) {
   if (T == 0) return cudaSuccess;
   const int blocks = (T + 7) / 8;
-  return launch_pdl(rstd_kernel<ST>, dim3(blocks), dim3(256), 0, st, x, T, d, eps, s);
+  return launch_pdl(rstd_kernel<ST>, dim3(blocks), dim3(256), 0, st, x, T, d, eps, s, raw ? 1 : 0);
+}
+
+// ------------------------------------------------------------ norm finish
+template <typename ST>
+__global__ void norm_finish_kernel(const float* acc, const float* ss, int T, int n, float coef, float eps, int act,
+                                   ST* u, ST* z, float* s) {
+  pdl_wait();
+  pdl_trigger();
+  const int groups = n / 8;
+  const long long total = 1LL * T * groups;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
+    const long long t = i / groups;
+    const int c = static_cast<int>(i % groups) * 8;
+    const float st = rsqrtf(ss[t] * coef + eps);
+    if (c == 0) s[t] = st;
+    float v[8], w[8];
+    load8(acc + t * n + c, v);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[q] = Num<ST>::round(st * v[q]);
+      w[q] = act ? v[q] : silu<ST>(v[q]);
+    }
+    store8(u + t * n + c, v);
+    store8(z + t * n + c, w);
+  }
+}
+
+template <typename ST>
+cudaError_t launch_norm_finish(const float* acc, const float* ss, int T, int n, float coef, float eps, int act, ST* u,
+                               ST* z, float* s, cudaStream_t st) {
+  const long long total = 1LL * T * (n / 8);
+  if (total == 0) return cudaSuccess;
+  int blocks = static_cast<int>((total + 255) / 256);
+  if (blocks > 8192) blocks = 8192;
+  return launch_pdl(norm_finish_kernel<ST>, dim3(blocks), dim3(256), 0, st, acc, ss, T, n, coef, eps, act, u, z, s);
 }
 
 // ------------------------------------------------------------------ silu
@@ -266,7 +301,9 @@ cudaError_t launch_wait_selftest(unsigned* err, unsigned long long limit_ns, cud
 // ------------------------------------------------------ instantiations
 #define LR_SMALL_INST(ST)                                                                                          \
   template cudaError_t launch_fold<ST>(ST*, StackSrc, int, int, int, const ST*, cudaStream_t);                   \
-  template cudaError_t launch_rstd<ST>(const ST*, int, int, float, float*, cudaStream_t);                        \
+  template cudaError_t launch_rstd<ST>(const ST*, int, int, float, float*, cudaStream_t, bool);                  \
+  template cudaError_t launch_norm_finish<ST>(const float*, const float*, int, int, float, float, int, ST*, ST*,    \
+                                              float*, cudaStream_t);                                            \
   template cudaError_t launch_silu<ST>(SiluSlab, SiluSlab, int, cudaStream_t);                                  \
   template cudaError_t launch_wgrad_reduce<ST>(const float*, int, long long, int, int, const ST*, WgradDst, int, \
                                                float*, cudaStream_t);                                            \

@@ -25,9 +25,15 @@ struct WgradDst {
 template <typename ST>
 cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols, const ST* g, cudaStream_t st);
 
-// s[t] = (sum_j x[t, j]^2 / d + eps)^(-1/2); one warp per row.
+// s[t] = (sum_j x[t, j]^2 / d + eps)^(-1/2), or with `raw` the sum of squares itself; one warp per row.
 template <typename ST>
-cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st);
+cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st, bool raw = false);
+
+// Finish of a row-parallel normed group from its all-reduced fp32 partials acc [T, n] and row sums of
+// squares ss [T]: s = (ss coef + eps)^(-1/2), u = round(s acc), z = sigma(u) (act 0 SiLU, 1 identity).
+template <typename ST>
+cudaError_t launch_norm_finish(const float* acc, const float* ss, int T, int n, float coef, float eps, int act, ST* u,
+                               ST* z, float* s, cudaStream_t st);
 
 // z[t, j] = SiLU(u[t, j]) for two [T, n] slabs in one launch (u and z with their own leading
 // dimensions; a slab with n = 0 is skipped).

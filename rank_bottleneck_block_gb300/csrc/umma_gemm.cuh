@@ -344,7 +344,7 @@ struct Config {
   static constexpr int WARP_BYTES = NO * OSET + NA * ASET + ABUF;
   static constexpr int EPI_BYTES = kEpiWarps * WARP_BYTES;
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
-  static constexpr bool STATS = (K == EPI_NORM_SILU);
+  static constexpr bool STATS = (K == EPI_NORM_SILU || K == EPI_F32_SS);
   static constexpr int THREADS = kThreads + (STATS ? 128 : 0);
   static constexpr int BAR_BYTES = 1024 + 1024;  // barriers, then s for two tiles of 128 rows
   static constexpr int RING_BUDGET = kMaxSmem - 1024 - EPI_BYTES - BAR_BYTES;
@@ -619,7 +619,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       if (!ok) break;
       const float s_val = rsqrtf(ss * ep.coef + ep.eps);
       const int m = mb * BM + row;
-      if (nb == 0 && m < sh.M && ep.rowscale_out) ep.rowscale_out[m] = s_val;
+      // The 1/rms row scale, or for a row-parallel partial the raw sum of squares of its shard.
+      if (nb == 0 && m < sh.M && ep.rowscale_out) ep.rowscale_out[m] = K == EPI_F32_SS ? ss : s_val;
       const int buf = it & 1;
       const uint32_t tph = static_cast<uint32_t>((it >> 1) & 1);
       if (!mbar_wait(&sempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE)) break;

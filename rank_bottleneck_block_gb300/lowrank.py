@@ -30,7 +30,8 @@ EXPORTED = [
     "lr_check_device_error", "lr_selftest_wait_timeout", "lr_version", "lr_launch_count",
     "lr_profile_start", "lr_profile_stop", "lr_profile_filter", "lr_profile_count", "lr_profile_entry",
     "lr_proj_fwd_noalloc", "lr_dense_saved_bytes", "lr_dense_fwd_workspace_bytes", "lr_dense_bwd_workspace_bytes",
-    "lr_dense_fwd", "lr_dense_bwd",
+    "lr_dense_fwd", "lr_dense_bwd", "lr_btp_payload_floats", "lr_btp_workspace_bytes", "lr_btp_partial",
+    "lr_btp_finish",
 ]
 
 
@@ -71,6 +72,10 @@ _SIGS = {
                                  _P, _SZ, _P]),
     "lr_stack_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "lr_dense_saved_bytes": (_SZ, [_I, _I, _I, _I]),
+    "lr_btp_payload_floats": (_SZ, [_I, _I, _I]),
+    "lr_btp_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "lr_btp_partial": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _P, _P, _P, _SZ, _P]),
+    "lr_btp_finish": (_I, [_I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P]),
     "lr_dense_fwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_dense_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_dense_fwd": (_I, [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P]),
@@ -248,6 +253,24 @@ def lr_dense_bwd(dt, T, d, f, eps, x, g, Wg, Wu, Wd, saved, dout, dx, dg, dWg, d
     _check(lib().lr_dense_bwd(dt, T, d, f, eps, _p(x), _p(g), _p(Wg), _p(Wu), _p(Wd), _p(saved), _nbytes(saved),
                               _p(dout), _p(dx), _p(dg), _p(dWg), _p(dWu), _p(dWd), _p(ws), _nbytes(ws),
                               _stream(stream)))
+
+
+def lr_btp_payload_floats(T, r, group) -> int:
+    return lib().lr_btp_payload_floats(T, r, group)
+
+
+def lr_btp_workspace_bytes(dt, d_shard, r, group) -> int:
+    return lib().lr_btp_workspace_bytes(dt, d_shard, r, group)
+
+
+def lr_btp_partial(dt, T, d_shard, r, pairs: Sequence[lr_pair], g_shard, x_shard, payload, ws, stream=None):
+    group = len(pairs)
+    _check(lib().lr_btp_partial(dt, T, d_shard, r, group, _pairs(pairs), _p(g_shard), _p(x_shard), _p(payload),
+                                _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def lr_btp_finish(dt, act, T, d, r, group, payload, eps, u, z, s, stream=None):
+    _check(lib().lr_btp_finish(dt, act, T, d, r, group, _p(payload), eps, _p(u), _p(z), _p(s), _stream(stream)))
 
 
 def lr_stack_workspace_bytes(dt, mode, nblocks, T, d, f, r) -> int:
