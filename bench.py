@@ -361,6 +361,25 @@ def _time_steps(step, steps, warmup, flush, stream):
     return sum(s.elapsed_time(e) for s, e in evs) / steps
 
 
+def _kernel_table(step, flush, stream, steps: int = 10):
+    """Per-kernel device time from an untimed pass with CUDA events around every launch."""
+    import torch
+
+    from rank_bottleneck_block_gb300 import lowrank as L
+
+    L.lr_profile_filter(None)
+    L.lr_profile_start()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    prof = L.lr_profile_stop()
+    return {k: {"launches": v["launches"], "ms_per_step": round(v["ms"] / steps, 4),
+                **({"tflops": round(v["flops"] / (v["ms"] / 1e3) / 1e12, 1)} if v["flops"] else
+                   {"gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1)})}
+            for k, v in sorted(prof.items(), key=lambda kv: -kv[1]["ms"])}
+
+
 def _proj_flops_bytes(T, d_in, d_out, r, group, norm):
     f = 3.0 * 2.0 * T * r * (d_in + d_out) * group
     params = group * r * (d_in + d_out)
@@ -403,11 +422,13 @@ def run_other(a):
 
         ms = _time_steps(step, a.steps, a.warmup, flush, stream)
         L.lr_check_device_error()
+        kernels = _kernel_table(step, flush, stream)
         f1, b1 = _proj_flops_bytes(16384, 4096, 4096, 1024, 3, True)
         f2, b2 = _proj_flops_bytes(16384, 4096, 4096, 1024, 1, False)
         res = {"workload": "low-rank attention projections fwd+bwd: q/k/v group (3 pairs, r 1024, d 4096, RMSNorm) "
                            "+ o-projection (1 pair, no norm), T 16384", "ms_per_step": round(ms, 4),
-               "tokens_per_s": round(16384 / (ms / 1e3), 1), **_roofline(f1 + f2, b1 + b2, ms, pk)}
+               "tokens_per_s": round(16384 / (ms / 1e3), 1), **_roofline(f1 + f2, b1 + b2, ms, pk),
+               "kernels": kernels}
         print(json.dumps(res), flush=True)
     elif a.workload == "stack":
         shape = I.MLP_BLOCK_BF16
