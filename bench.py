@@ -36,8 +36,8 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * (182.678272e6 + 562.732032e6),
-                          "sources_sha256": "2441a17e0632d0e3b51799380063af9b383a9865bb17d66b11e821eb0191d96b",
+    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * (178.35648e6 + 569.786368e6),
+                          "sources_sha256": "ff184a918a2f1cf4f73e1d070b5e1b4279a9e9dfcc35be6dba76ecf44be6661f",
                           "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
 }
 
