@@ -179,6 +179,23 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 
+// L2 policy that keeps lines in L2 ahead of normal traffic (evict last).
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_store_3d with an L2 cache policy (for data that is read again soon, from L2).
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
 // Explicit 16-byte shared-memory accesses for the staging tiles (their swizzled layout is
 // bank-conflict free only when each thread moves whole 16-byte chunks).
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
@@ -885,8 +902,14 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
             for (int oi = 0; oi < NOUT; ++oi) {
               if (!present[oi]) continue;
-              if constexpr (D::OUT_F32)
-                tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split);
+              if constexpr (D::OUT_F32) {
+                // Split-K partials are summed by the next kernel: keep them in L2 for it.
+                if (sh.ksplit > 1)
+                  tma_store_3d_hint(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split,
+                                    l2_evict_last());
+                else
+                  tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split);
+              }
               else
                 tma_store_2d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0);
             }
