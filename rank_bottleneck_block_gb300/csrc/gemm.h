@@ -29,6 +29,9 @@ struct GemmCall {
   EpiParams ep;
   unsigned* err;  // device error word
   int bn;         // tcgen05 tile width chosen by the planner (128 or 256)
+  // Walk the tiles from the last one: a GEMM that reads a large tensor the previous kernel
+  // wrote in tile order then starts on its most recently written (still L2-resident) part.
+  bool reverse;
 };
 
 // Row-partial chunk width used by the epilogues of each engine.

@@ -545,9 +545,10 @@ static lr_status mlp_fwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
   // B_gate / B_up with the SwiGLU product fused.
   LR_TRY(swiglu_gemm(c, T, f, r, z_gu, gate.B, up.B, h, mode == LR_SAVE_FULL ? S.a : nullptr,
                      mode == LR_SAVE_FULL ? S.b : nullptr));
-  // A_down with SiLU fused.
+  // A_down with SiLU fused (reads h right after the SwiGLU GEMM wrote it: start on the last tiles).
   {
     GemmCall k = new_call(T, r, f);
+    k.reverse = true;
     k.A[0] = {h, f};
     k.B[0] = {down.A, f};
     k.ep.out0[0] = S.u_d;
@@ -583,6 +584,19 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
   StackSrc src = {{gate.A, up.A, nullptr}};
   LR_TRY(fold(c, W.Af, src, 2, r, d, g));
 
+  // du_down = (G B_down) * SiLU'(u_down): needs only dout and the saved u_down, so it runs first
+  // and the SwiGLU backward can follow the re-forward while a, b are still in L2
+  {
+    GemmCall k = new_call(T, r, d);
+    k.b_mn = true;
+    k.A[0] = {G, d};
+    k.B[0] = {down.B, r};
+    k.ep.aux0[0] = S.u_d;
+    k.ep.lda0 = r;
+    k.ep.out0[0] = W.du_d;
+    k.ep.ldo0 = r;
+    LR_TRY(gemm(c, EPI_DSILU, k));
+  }
   void *z_gu, *z_d, *a, *b, *h;
   if (mode == LR_SAVE_CKPT) {
     // Low-rank activation checkpointing (technical summary §2.2): re-forward inside the block
@@ -607,31 +621,10 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     h = S.h;
   }
 
-  // dB_down = G^T z_down
-  {
-    WgradDst dst = {{ddown.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
-    LR_TRY(wgrad(c, d, r, T, {G, d}, {z_d, r}, dst, d, nullptr, nullptr, W.wpart));
-  }
-  // du_down = (G B_down) * SiLU'(u_down)
-  {
-    GemmCall k = new_call(T, r, d);
-    k.b_mn = true;
-    k.A[0] = {G, d};
-    k.B[0] = {down.B, r};
-    k.ep.aux0[0] = S.u_d;
-    k.ep.lda0 = r;
-    k.ep.out0[0] = W.du_d;
-    k.ep.ldo0 = r;
-    LR_TRY(gemm(c, EPI_DSILU, k));
-  }
-  // dA_down = du_down^T h
-  {
-    WgradDst dst = {{ddown.dA, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
-    LR_TRY(wgrad(c, r, f, T, {W.du_d, r}, {h, f}, dst, r, nullptr, nullptr, W.wpart));
-  }
   // dh = du_down A_down; SwiGLU backward fused: da = dh b SiLU'(a), db = dh SiLU(a)
   {
     GemmCall k = new_call(T, f, r);
+    k.reverse = mode == LR_SAVE_CKPT;  // a, b were just written by the re-forward: start on the last tiles
     k.b_mn = true;
     k.A[0] = {W.du_d, r};
     k.B[0] = {down.A, f};
@@ -643,6 +636,16 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.ldo0 = k.ep.ldo1 = f;
     LR_TRY(gemm(c, EPI_SWIGLU_BWD, k));
   }
+  // dB_down = G^T z_down
+  {
+    WgradDst dst = {{ddown.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, d, r, T, {G, d}, {z_d, r}, dst, d, nullptr, nullptr, W.wpart));
+  }
+  // dA_down = du_down^T h
+  {
+    WgradDst dst = {{ddown.dA, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+    LR_TRY(wgrad(c, r, f, T, {W.du_d, r}, {h, f}, dst, r, nullptr, nullptr, W.wpart));
+  }
   // dB_gate = da^T z_gate, dB_up = db^T z_up
   {
     WgradDst dst = {{dgate.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
@@ -653,6 +656,7 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
   // du_{gate,up} = (d{a,b} B) * SiLU'(u), stored pre-scaled by s; rho partials = sum du * u.
   {
     GemmCall k = new_call(T, r, f);
+    k.reverse = true;  // da, db were written tile by tile by the SwiGLU backward (after dB_gate, dB_up)
     k.b_mn = true;
     k.batches = 2;
     k.A[0] = {W.da, f};

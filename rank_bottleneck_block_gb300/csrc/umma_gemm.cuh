@@ -77,6 +77,7 @@ struct Shape {
   int m_tiles, n_tiles;
   int m_pairs;  // pair tiles along M: the CTAs of a cluster take m-tiles 2p and 2p + 1
   int kb_total, kb_per_split;
+  int reverse;  // tiles are taken from the last one (see GemmCall::reverse)
   unsigned* err;
 };
 
@@ -388,6 +389,7 @@ __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank,
                                             int& nb) {
   const int per_batch = sh.m_pairs * sh.n_tiles;
   const int per_split = sh.batches * per_batch;
+  if (sh.reverse) tile = sh.ksplit * per_split - 1 - tile;
   split = tile / per_split;
   int rem = tile - split * per_split;
   batch = rem / per_batch;

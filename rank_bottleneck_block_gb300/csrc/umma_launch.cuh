@@ -91,6 +91,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.kb_per_split = (sh.kb_total + ks - 1) / ks;
   sh.ksplit = (sh.kb_total + sh.kb_per_split - 1) / sh.kb_per_split;  // no empty split
   sh.err = g.err;
+  sh.reverse = g.reverse ? 1 : 0;
 
   const int nsets = NACC > 1 ? NACC : g.batches;
   for (int i = 0; i < nsets; ++i) {
