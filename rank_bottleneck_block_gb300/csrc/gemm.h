@@ -32,6 +32,12 @@ struct GemmCall {
   // Walk the tiles from the last one: a GEMM that reads a large tensor the previous kernel
   // wrote in tile order then starts on its most recently written (still L2-resident) part.
   bool reverse;
+  // Grouped problems (EPI_F32, tcgen05 path, no split): batch b has its own gM[b] x gN[b] output
+  // with leading dimension gldo[b] (elements); all batches share K, the tile width and the operand
+  // layouts, and their tiles are scheduled as one persistent grid.  False: uniform batches of M x N.
+  bool grouped;
+  int gM[kMaxBatch], gN[kMaxBatch];
+  long long gldo[kMaxBatch];
 };
 
 // Row-partial chunk width used by the epilogues of each engine.

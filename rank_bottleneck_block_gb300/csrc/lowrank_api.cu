@@ -259,7 +259,11 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   }
   std::string name = std::string(c.dt == LR_BF16 ? "umma_" : "simt_") + epi_name(k);
   if (g.bn) name += "_bn" + std::to_string(g.bn);
-  const double flops = 2.0 * g.M * g.N * static_cast<double>(g.K) * g.nacc * g.batches;
+  double flops = 2.0 * g.M * g.N * static_cast<double>(g.K) * g.nacc * g.batches;
+  if (g.grouped) {
+    flops = 0.0;
+    for (int b = 0; b < g.batches; ++b) flops += 2.0 * g.gM[b] * g.gN[b] * static_cast<double>(g.K);
+  }
   LaunchScope scope(name, c.st, flops, extra_bytes);
   cudaError_t e = (c.dt == LR_BF16) ? dispatch_bf16(k, g, c.st, c.sms) : dispatch_f32(k, g, c.st);
   if (e != cudaSuccess)
@@ -297,6 +301,7 @@ static int wgrad_split_bound(int K) {
 
 struct WgradPlan {
   int bn, ksplit;
+  double t;  // modelled time (relative units)
 };
 
 static int normalise_split(int K, int ks) {
@@ -305,12 +310,16 @@ static int normalise_split(int K, int ks) {
   return (kb + per - 1) / per;
 }
 
-static WgradPlan wgrad_plan(const Ctx& c, int M, int N, int K, bool needs_pass) {
-  if (c.dt != LR_BF16) return {0, 1};
+// Modelled time of one pair tile of a weight-gradient GEMM over K / ks tokens.
+static double wgrad_tile_time(int bn, int K, int ks) {
   const double per_sm_flops = 2.25e15 / 152.0 * 0.65;  // sustained MMA rate per SM (relative units suffice)
-  const double reduce_bw = 4.0e12;                       // bytes/s of the partial reduction
-  WgradPlan best{256, 1};
-  double best_t = 1e30;
+  return 2.0 * 128 * bn * (static_cast<double>(K) / ks) / per_sm_flops * (bn == 128 ? 1.33 : 1.0);
+}
+
+static WgradPlan wgrad_plan(const Ctx& c, int M, int N, int K, bool needs_pass) {
+  if (c.dt != LR_BF16) return {0, 1, 0.0};
+  const double reduce_bw = 4.0e12;  // bytes/s of the partial reduction
+  WgradPlan best{256, 1, 1e30};
   const long long slots = std::max(1, c.sms / 2);  // SM pairs
   for (int bn : {256, 128}) {
     const long long tiles = 1LL * ((M + 255) / 256) * ((N + bn - 1) / bn);  // pair tiles
@@ -318,13 +327,9 @@ static WgradPlan wgrad_plan(const Ctx& c, int M, int N, int K, bool needs_pass) 
       const int ksn = normalise_split(K, ks);
       if (ksn != ks) continue;
       const long long waves = (tiles * ks + slots - 1) / slots;
-      const double tile_t = 2.0 * 128 * bn * (static_cast<double>(K) / ks) / per_sm_flops * (bn == 128 ? 1.33 : 1.0);
-      double t = waves * tile_t;
+      double t = waves * wgrad_tile_time(bn, K, ks);
       if (ks > 1 || needs_pass) t += (static_cast<double>(ks) + 1.0) * M * N * 4.0 / reduce_bw;
-      if (t < best_t * 0.98) {
-        best_t = t;
-        best = {bn, ks};
-      }
+      if (t < best.t * 0.98) best = {bn, ks, t};
     }
   }
   return best;
@@ -363,6 +368,52 @@ static lr_status wgrad(const Ctx& c, int M, int N, int K, Operand A, Operand B, 
                                                    static_cast<const float*>(colscale), dst, rows_each, dgpart, c.st);
   if (e != cudaSuccess) return fail(LR_ERR_CUDA, "wgrad reduce: %s", cudaGetErrorString(e));
   return LR_OK;
+}
+
+// One plain weight gradient (no column scale, no dg, one destination) of a group sharing K.
+struct WgradJob {
+  int M, N;
+  Operand A, B;
+  float* dst;
+};
+
+// Weight gradients that share K (tokens) and need no pass after the GEMM: one grouped launch whose
+// tiles fill the SM pairs together, without split-K (fp32 results stored directly), when the cost
+// model prefers it to planning each GEMM alone; else each on its own.
+static lr_status wgrad_group(const Ctx& c, int K, int n, const WgradJob* jobs, float* wpart) {
+  bool grouped = c.dt == LR_BF16 && n >= 2 && n <= kMaxBatch;
+  if (grouped) {
+    const long long slots = std::max(1, c.sms / 2);
+    long long tiles = 0;
+    double alone = 0.0;
+    for (int i = 0; i < n; ++i) {
+      tiles += 1LL * ((jobs[i].M + 255) / 256) * ((jobs[i].N + 255) / 256);
+      alone += wgrad_plan(c, jobs[i].M, jobs[i].N, K, false).t;
+    }
+    grouped = ((tiles + slots - 1) / slots) * wgrad_tile_time(256, K, 1) < alone;
+  }
+  if (!grouped) {
+    for (int i = 0; i < n; ++i) {
+      WgradDst dst = {{jobs[i].dst, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+      LR_TRY(wgrad(c, jobs[i].M, jobs[i].N, K, jobs[i].A, jobs[i].B, dst, jobs[i].M, nullptr, nullptr, wpart));
+    }
+    return LR_OK;
+  }
+  GemmCall g = new_call(jobs[0].M, jobs[0].N, K);
+  g.a_mn = g.b_mn = true;
+  g.bn = 256;
+  g.batches = n;
+  g.grouped = true;
+  for (int i = 0; i < n; ++i) {
+    g.A[i] = jobs[i].A;
+    g.B[i] = jobs[i].B;
+    g.gM[i] = jobs[i].M;
+    g.gN[i] = jobs[i].N;
+    g.gldo[i] = jobs[i].N;
+    g.ep.out0[i] = jobs[i].dst;
+  }
+  g.ep.ldo0 = jobs[0].N;
+  return gemm(c, EPI_F32, g);
 }
 
 // ------------------------------------------------------------ small ops
@@ -636,22 +687,14 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.ldo0 = k.ep.ldo1 = f;
     LR_TRY(gemm(c, EPI_SWIGLU_BWD, k));
   }
-  // dB_down = G^T z_down
+  // dB_gate = da^T z_gate, dB_up = db^T z_up, dA_down = du_down^T h, dB_down = G^T z_down: four
+  // weight gradients over the same T tokens, one grouped launch (da, db first: just written)
   {
-    WgradDst dst = {{ddown.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
-    LR_TRY(wgrad(c, d, r, T, {G, d}, {z_d, r}, dst, d, nullptr, nullptr, W.wpart));
-  }
-  // dA_down = du_down^T h
-  {
-    WgradDst dst = {{ddown.dA, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
-    LR_TRY(wgrad(c, r, f, T, {W.du_d, r}, {h, f}, dst, r, nullptr, nullptr, W.wpart));
-  }
-  // dB_gate = da^T z_gate, dB_up = db^T z_up
-  {
-    WgradDst dst = {{dgate.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
-    LR_TRY(wgrad(c, f, r, T, {W.da, f}, {z_gu, 2LL * r}, dst, f, nullptr, nullptr, W.wpart));
-    WgradDst dst2 = {{dup.dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
-    LR_TRY(wgrad(c, f, r, T, {W.db, f}, {off(z_gu, c.es * r), 2LL * r}, dst2, f, nullptr, nullptr, W.wpart));
+    const WgradJob jobs[4] = {{f, r, {W.da, f}, {z_gu, 2LL * r}, static_cast<float*>(dgate.dB)},
+                              {f, r, {W.db, f}, {off(z_gu, c.es * r), 2LL * r}, static_cast<float*>(dup.dB)},
+                              {r, f, {W.du_d, r}, {h, f}, static_cast<float*>(ddown.dA)},
+                              {d, r, {G, d}, {z_d, r}, static_cast<float*>(ddown.dB)}};
+    LR_TRY(wgrad_group(c, T, 4, jobs, W.wpart));
   }
   // du_{gate,up} = (d{a,b} B) * SiLU'(u), stored pre-scaled by s; rho partials = sum du * u.
   {

@@ -78,6 +78,9 @@ struct Shape {
   int m_pairs;  // pair tiles along M: the CTAs of a cluster take m-tiles 2p and 2p + 1
   int kb_total, kb_per_split;
   int reverse;  // tiles are taken from the last one (see GemmCall::reverse)
+  int grouped;  // batches of their own M, N (see GemmCall::grouped); then the next two fields hold
+  int g_n_tiles[kMaxBatch];    // n-tiles of batch b
+  int g_tile0[kMaxBatch + 1];  // first pair tile of batch b (g_tile0[batches] = pair tiles per split)
   unsigned* err;
 };
 
@@ -387,6 +390,20 @@ struct Config {
 // Pair-tile index -> (split, batch, this CTA's m-tile, n-tile); n runs fastest.
 __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
                                             int& nb) {
+  if (sh.grouped) {
+    const int per_split = sh.g_tile0[sh.batches];
+    if (sh.reverse) tile = sh.ksplit * per_split - 1 - tile;
+    split = tile / per_split;
+    int rem = tile - split * per_split;
+    int b = 0;
+    while (b + 1 < sh.batches && rem >= sh.g_tile0[b + 1]) ++b;
+    batch = b;
+    rem -= sh.g_tile0[b];
+    const int mp = rem / sh.g_n_tiles[b];
+    nb = rem - mp * sh.g_n_tiles[b];
+    mb = 2 * mp + rank;
+    return;
+  }
   const int per_batch = sh.m_pairs * sh.n_tiles;
   const int per_split = sh.batches * per_batch;
   if (sh.reverse) tile = sh.ksplit * per_split - 1 - tile;
@@ -467,7 +484,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   const int cid = static_cast<int>(blockIdx.x >> 1);
   const int ncl = static_cast<int>(gridDim.x >> 1);
   constexpr uint16_t kBoth = 0x3;
-  const int total = sh.ksplit * sh.batches * sh.m_pairs * sh.n_tiles;  // pair tiles
+  const int total =  // pair tiles
+      sh.ksplit * (sh.grouped ? sh.g_tile0[sh.batches] : sh.batches * sh.m_pairs * sh.n_tiles);
 
   if (warp == 0) {
     if (lane == 0) {

@@ -92,14 +92,27 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.ksplit = (sh.kb_total + sh.kb_per_split - 1) / sh.kb_per_split;  // no empty split
   sh.err = g.err;
   sh.reverse = g.reverse ? 1 : 0;
+  sh.grouped = 0;
+  if (g.grouped) {  // batches of their own M, N; one split only
+    if (K != EPI_F32 || sh.ksplit != 1 || g.batches < 1 || g.batches > kMaxBatch) return cudaErrorInvalidValue;
+    sh.grouped = 1;
+    sh.g_tile0[0] = 0;
+    for (int b = 0; b < g.batches; ++b) {
+      sh.g_n_tiles[b] = (g.gN[b] + BN - 1) / BN;
+      sh.g_tile0[b + 1] = sh.g_tile0[b] + ((g.gM[b] + 2 * BM - 1) / (2 * BM)) * sh.g_n_tiles[b];
+    }
+  }
+  // Extent of batch (or operand set) b.
+  auto bM = [&](int b) { return g.grouped ? g.gM[b] : g.M; };
+  auto bN = [&](int b) { return g.grouped ? g.gN[b] : g.N; };
 
   const int nsets = NACC > 1 ? NACC : g.batches;
   for (int i = 0; i < nsets; ++i) {
-    const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, g.M, g.K, g.A[i].ld, 64, 64)
-                          : encode_operand(&maps.a[i], g.A[i].ptr, g.K, g.M, g.A[i].ld, 64, BM);
+    const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, bM(i), g.K, g.A[i].ld, 64, 64)
+                          : encode_operand(&maps.a[i], g.A[i].ptr, g.K, bM(i), g.A[i].ld, 64, BM);
     // Each CTA of a pair stages half of the B tile: BN/2 rows (K-major) or 64-column chunks (MN-major).
-    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, g.N, g.K, g.B[i].ld, 64, 64)
-                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, g.N, g.B[i].ld, 64, BN / 2);
+    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, bN(i), g.K, g.B[i].ld, 64, 64)
+                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, bN(i), g.B[i].ld, 64, BN / 2);
     if (!okA || !okB) return cudaErrorInvalidValue;
   }
   const void* const* outs[3] = {g.ep.out0, g.ep.out1, g.ep.out2};
@@ -110,8 +123,10 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
     for (int o = 0; o < D::NOUT; ++o) {
       const void* p = outs[o][b];
       if (!p) continue;
-      const bool ok = D::OUT_F32 ? encode_epi_f32(&maps.out[b][o], p, g.N, g.M, ldo[o], sh.ksplit, g.ep.split_stride)
-                                 : encode_epi_bf16(&maps.out[b][o], p, g.N, g.M, ldo[o]);
+      const long long ld = g.grouped ? g.gldo[b] : ldo[o];
+      const long long stride = g.grouped ? ld * bM(b) : g.ep.split_stride;
+      const bool ok = D::OUT_F32 ? encode_epi_f32(&maps.out[b][o], p, bN(b), bM(b), ld, sh.ksplit, stride)
+                                 : encode_epi_bf16(&maps.out[b][o], p, bN(b), bM(b), ld);
       if (!ok) return cudaErrorInvalidValue;
     }
     for (int a = 0; a < D::NAUX; ++a) {
@@ -121,7 +136,8 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
     }
   }
 
-  const long long total = 1LL * sh.ksplit * sh.batches * sh.m_pairs * sh.n_tiles;  // pair tiles
+  const long long total =  // pair tiles
+      1LL * sh.ksplit * (sh.grouped ? sh.g_tile0[sh.batches] : sh.batches * sh.m_pairs * sh.n_tiles);
   if (total <= 0) return cudaSuccess;
 
   auto kern = gemm_kernel<K, BN, A_MN, B_MN>;
