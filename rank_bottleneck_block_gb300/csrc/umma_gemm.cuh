@@ -78,9 +78,10 @@ struct Shape {
   int m_pairs;  // pair tiles along M: the CTAs of a cluster take m-tiles 2p and 2p + 1
   int kb_total, kb_per_split;
   int reverse;  // tiles are taken from the last one (see GemmCall::reverse)
-  int grouped;  // batches of their own M, N (see GemmCall::grouped); then the next two fields hold
-  int g_n_tiles[kMaxBatch];    // n-tiles of batch b
-  int g_tile0[kMaxBatch + 1];  // first pair tile of batch b (g_tile0[batches] = pair tiles per split)
+  int grouped;  // batches of their own M, N (see GemmCall::grouped); then the next three fields hold
+  int g_n_tiles[kMaxBatch];  // n-tiles of batch b
+  int g_tile0[kMaxBatch];    // first pair tile of batch b
+  int g_tiles;               // pair tiles of all batches
   unsigned* err;
 };
 
@@ -391,16 +392,24 @@ struct Config {
 __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
                                             int& nb) {
   if (sh.grouped) {
-    const int per_split = sh.g_tile0[sh.batches];
+    const int per_split = sh.g_tiles;
     if (sh.reverse) tile = sh.ksplit * per_split - 1 - tile;
     split = tile / per_split;
     int rem = tile - split * per_split;
-    int b = 0;
-    while (b + 1 < sh.batches && rem >= sh.g_tile0[b + 1]) ++b;
+    // The batch whose tile range holds rem (constant indices only: the shape stays in registers).
+    int b = 0, t0 = 0, nt = sh.g_n_tiles[0];
+#pragma unroll
+    for (int i = 1; i < kMaxBatch; ++i) {
+      if (i < sh.batches && rem >= sh.g_tile0[i]) {
+        b = i;
+        t0 = sh.g_tile0[i];
+        nt = sh.g_n_tiles[i];
+      }
+    }
     batch = b;
-    rem -= sh.g_tile0[b];
-    const int mp = rem / sh.g_n_tiles[b];
-    nb = rem - mp * sh.g_n_tiles[b];
+    rem -= t0;
+    const int mp = rem / nt;
+    nb = rem - mp * nt;
     mb = 2 * mp + rank;
     return;
   }
@@ -485,7 +494,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   const int ncl = static_cast<int>(gridDim.x >> 1);
   constexpr uint16_t kBoth = 0x3;
   const int total =  // pair tiles
-      sh.ksplit * (sh.grouped ? sh.g_tile0[sh.batches] : sh.batches * sh.m_pairs * sh.n_tiles);
+      sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * sh.m_pairs * sh.n_tiles);
 
   if (warp == 0) {
     if (lane == 0) {

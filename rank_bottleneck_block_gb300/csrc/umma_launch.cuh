@@ -79,6 +79,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   Maps maps;
   memset(&maps, 0, sizeof(maps));
   Shape sh;
+  memset(&sh, 0, sizeof(sh));
   sh.M = g.M;
   sh.N = g.N;
   sh.K = g.K;
@@ -96,11 +97,13 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   if (g.grouped) {  // batches of their own M, N; one split only
     if (K != EPI_F32 || sh.ksplit != 1 || g.batches < 1 || g.batches > kMaxBatch) return cudaErrorInvalidValue;
     sh.grouped = 1;
-    sh.g_tile0[0] = 0;
-    for (int b = 0; b < g.batches; ++b) {
-      sh.g_n_tiles[b] = (g.gN[b] + BN - 1) / BN;
-      sh.g_tile0[b + 1] = sh.g_tile0[b] + ((g.gM[b] + 2 * BM - 1) / (2 * BM)) * sh.g_n_tiles[b];
+    int t = 0;
+    for (int b = 0; b < kMaxBatch; ++b) {
+      sh.g_n_tiles[b] = b < g.batches ? (g.gN[b] + BN - 1) / BN : 1;
+      sh.g_tile0[b] = t;
+      if (b < g.batches) t += ((g.gM[b] + 2 * BM - 1) / (2 * BM)) * sh.g_n_tiles[b];
     }
+    sh.g_tiles = t;
   }
   // Extent of batch (or operand set) b.
   auto bM = [&](int b) { return g.grouped ? g.gM[b] : g.M; };
@@ -137,7 +140,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   }
 
   const long long total =  // pair tiles
-      1LL * sh.ksplit * (sh.grouped ? sh.g_tile0[sh.batches] : sh.batches * sh.m_pairs * sh.n_tiles);
+      1LL * sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * sh.m_pairs * sh.n_tiles);
   if (total <= 0) return cudaSuccess;
 
   auto kern = gemm_kernel<K, BN, A_MN, B_MN>;
