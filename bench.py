@@ -36,8 +36,8 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * ((45.181696e6 + 133.2096e6) + (69.717248e6 + 499.67872e6)),
-                          "sources_sha256": "4cbd5e9d0aabd1611721813ae59a74ddfd591a5d6688140adb208ea75e5e9d23",
+    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * ((45.186816e6 + 133.404672e6) + (55.457024e6 + 499.862528e6)),
+                          "sources_sha256": "beae1a139ec02e82195cb511ebc74a411654c199a9fb264545145f38a842a84a",
                           "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
 }
 
