@@ -202,6 +202,33 @@ lr_status lr_btp_partial(lr_dtype dt, int T, int d_shard, int r, int group, cons
 lr_status lr_btp_finish(lr_dtype dt, lr_act act, int T, int d, int r, int group, const float* payload, float eps,
                         void* u, void* z, float* s, void* stream);
 
+/* ------------------------------------------------ causal self-attention
+ * The technical summary trains low-rank LLaMA-style transformers: between the q/k/v
+ * projection group and the o-projection sits ordinary causal softmax attention, which
+ * the method leaves unchanged.  Per batch entry and head (b entries of s tokens, H heads
+ * of dh channels):
+ *     S = scale Q K^T (S_ij = -inf for j > i),  P = softmax_j(S),  O = P V,
+ * and the backward of sum(O * dO):
+ *     dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ * q, k, v, o, dout, dq, dk, dv: [b*s, H*dh] bf16, token-major as the projections write
+ * them (head h of token t in columns h*dh .. h*dh + dh - 1 of row t = batch*s + position).
+ * saved: lr_attn_saved_bytes (the row log-sum-exp of S, fp32 [b*H*s]); the backward
+ * recomputes S from q and k.  ws: lr_attn_workspace_bytes (head-major copies of the eight
+ * [b*s, H*dh] tensors, S and dP in fp32, P and dS in bf16, D: 12 b*H*s*s + 16 b*H*s*dh
+ * + 4 b*H*s bytes plus alignment), owned by the caller; the forward uses a part of it.
+ * bf16 only (LR_F32: LR_ERR_UNSUPPORTED).  s a multiple of 256, dh a multiple of 128
+ * (LR_ERR_SHAPE otherwise); pointers 16-byte aligned (LR_ERR_ALIGN).
+ */
+size_t lr_attn_saved_bytes(int b, int s, int H, int dh);
+size_t lr_attn_workspace_bytes(int b, int s, int H, int dh);
+lr_status lr_attn_fwd(lr_dtype dt, int b, int s, int H, int dh, float scale, const void* q, const void* k,
+                      const void* v, void* o, void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                      void* stream);
+lr_status lr_attn_bwd(lr_dtype dt, int b, int s, int H, int dh, float scale, const void* q, const void* k,
+                      const void* v, const void* o, const void* saved, const void* dout, void* dq, void* dk,
+                      void* dv, void* ws, size_t ws_bytes, void* stream);
+
 /* -------------------------------------------------------------- block stack
  * One training step of `nblocks` residual MLP blocks (as lr_mlp_fwd, sigma = SiLU) and a
  * mean-squared-error loss against `target` [T, d]:

@@ -1,0 +1,168 @@
+// Row kernels of causal multi-head attention (see attn_kernels.cuh).
+#include "attn_kernels.cuh"
+
+namespace lr {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// One thread per 8 consecutive channels of one head of one token.
+__global__ void head_permute_kernel(const bf16* src, bf16* dst, int b, int s, int H, int dh, int to_heads) {
+  pdl_wait();
+  pdl_trigger();
+  const int per_tok = H * dh / 8;
+  const long long total = 1LL * b * s * per_tok;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
+    const int t = static_cast<int>(i / per_tok);
+    const int rem = static_cast<int>(i - 1LL * t * per_tok);
+    const int h = rem / (dh / 8);
+    const int c = (rem - h * (dh / 8)) * 8;
+    const int bi = t / s, ti = t - bi * s;
+    const long long tm = 1LL * t * H * dh + 1LL * h * dh + c;
+    const long long hm = (1LL * (bi * H + h) * s + ti) * dh + c;
+    const long long from = to_heads ? tm : hm, to = to_heads ? hm : tm;
+    *reinterpret_cast<uint4*>(dst + to) = *reinterpret_cast<const uint4*>(src + from);
+  }
+}
+
+// Combines two (max, sum) pairs of a streaming log-sum-exp in base 2; an empty pair is (-inf, 0).
+__device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  l = (m == -INFINITY ? 0.f : l * exp2f(m - M)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - M));
+  m = M;
+}
+
+__device__ __forceinline__ void store_bf16x4(bf16* p, float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// One warp per row; lanes take 4 consecutive columns at a time.
+__global__ void attn_softmax_fwd_kernel(const float* S, int R, int s, float scale, bf16* P, float* lse) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const int n = r % s + 1;  // keys visible to this query
+  const float* row = S + 1LL * r * s;
+  const float c = scale * kLog2e;
+  float m = -INFINITY, l = 0.f;
+  for (int j = lane * 4; j < n; j += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(row + j);
+    const float x[4] = {v.x * c, v.y * c, v.z * c, v.w * c};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (j + t < n) lse_merge(m, l, x[t], 1.f);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    lse_merge(m, l, m2, l2);
+  }
+  const float lse2 = m + log2f(l);
+  if (lane == 0) lse[r] = lse2 * kLn2;
+  bf16* prow = P + 1LL * r * s;
+  for (int j = lane * 4; j < s; j += 128) {
+    float p[4] = {0.f, 0.f, 0.f, 0.f};
+    if (j < n) {
+      const float4 v = *reinterpret_cast<const float4*>(row + j);
+      const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (j + t < n) p[t] = exp2f(x[t] * c - lse2);
+    }
+    store_bf16x4(prow + j, p[0], p[1], p[2], p[3]);
+  }
+}
+
+__global__ void attn_rowdot_kernel(const bf16* dO, const bf16* O, int R, int dh, float* D) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  float acc = 0.f;
+  for (int c = lane * 8; c < dh; c += 256) {
+    float a[8], o[8];
+    load8(dO + 1LL * r * dh + c, a);
+    load8(O + 1LL * r * dh + c, o);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc = fmaf(a[t], o[t], acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) D[r] = acc;
+}
+
+__global__ void attn_softmax_bwd_kernel(const float* S, const float* dP, const float* lse, const float* D, int R,
+                                        int s, float scale, bf16* P, bf16* dS) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const int n = r % s + 1;
+  const float c = scale * kLog2e;
+  const float lse2 = lse[r] * kLog2e;
+  const float d = D[r];
+  const long long base = 1LL * r * s;
+  for (int j = lane * 4; j < s; j += 128) {
+    float p[4] = {0.f, 0.f, 0.f, 0.f}, g[4] = {0.f, 0.f, 0.f, 0.f};
+    if (j < n) {
+      const float4 v = *reinterpret_cast<const float4*>(S + base + j);
+      const float4 w = *reinterpret_cast<const float4*>(dP + base + j);
+      const float x[4] = {v.x, v.y, v.z, v.w}, y[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (j + t < n) {
+          p[t] = exp2f(x[t] * c - lse2);
+          g[t] = scale * p[t] * (y[t] - d);
+        }
+      }
+    }
+    store_bf16x4(P + base + j, p[0], p[1], p[2], p[3]);
+    store_bf16x4(dS + base + j, g[0], g[1], g[2], g[3]);
+  }
+}
+
+dim3 warp_rows_grid(int R) { return dim3(static_cast<unsigned>((R + 7) / 8)); }
+
+}  // namespace
+
+cudaError_t launch_head_permute(const bf16* src, bf16* dst, int b, int s, int H, int dh, int to_heads,
+                                cudaStream_t st) {
+  const long long total = 1LL * b * s * H * dh / 8;
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 16384) blocks = 16384;
+  return launch_pdl(head_permute_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, src, dst, b, s, H,
+                    dh, to_heads);
+}
+
+cudaError_t launch_attn_softmax_fwd(const float* S, int R, int s, float scale, bf16* P, float* lse,
+                                    cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  return launch_pdl(attn_softmax_fwd_kernel, warp_rows_grid(R), dim3(256), 0, st, S, R, s, scale, P, lse);
+}
+
+cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int R, int dh, float* D, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  return launch_pdl(attn_rowdot_kernel, warp_rows_grid(R), dim3(256), 0, st, dO, O, R, dh, D);
+}
+
+cudaError_t launch_attn_softmax_bwd(const float* S, const float* dP, const float* lse, const float* D, int R, int s,
+                                    float scale, bf16* P, bf16* dS, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  return launch_pdl(attn_softmax_bwd_kernel, warp_rows_grid(R), dim3(256), 0, st, S, dP, lse, D, R, s, scale, P,
+                    dS);
+}
+
+}  // namespace lr

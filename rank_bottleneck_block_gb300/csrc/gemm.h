@@ -38,6 +38,15 @@ struct GemmCall {
   bool grouped;
   int gM[kMaxBatch], gN[kMaxBatch];
   long long gldo[kMaxBatch];
+  // Row-batched problems (kinds without operand tiles, row statistics or row partials): batch b
+  // of A, B and the output starts rb_a, rb_b, rb_o stored rows after batch b - 1 in one tensor
+  // each (rows_a, rows_b, rows_o stored rows in all), so any number of batches shares one set of
+  // tensor maps.  A stored row is an M index for a K-major A and a K index for an MN-major one
+  // (likewise N or K for B).  Each batch's M, N and K must be whole tiles: M a multiple of 256,
+  // N of the tile width, K of 64.
+  bool rowbatch;
+  int rb_a, rb_b, rb_o;
+  long long rows_a, rows_b, rows_o;
 };
 
 // Row-partial chunk width used by the epilogues of each engine.

@@ -15,6 +15,7 @@
 #include "../../include/lowrank.h"
 #include "common.cuh"
 #include "gemm.h"
+#include "attn_kernels.cuh"
 #include "small_kernels.cuh"
 
 namespace lr {
@@ -196,6 +197,7 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_STORE:
       if (kk) return umma_bn<EPI_STORE, false, false>(g, st);
       if (km) return umma_bn<EPI_STORE, false, true>(g, st);
+      if (mm) return umma_bn<EPI_STORE, true, true>(g, st);
       break;
     case EPI_RESID: if (kk) return umma_bn<EPI_RESID, false, false>(g, st); break;
     case EPI_SWIGLU:
@@ -210,7 +212,10 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
     case EPI_DX_NORM: if (km) return umma_bn<EPI_DX_NORM, false, true>(g, st); break;
-    case EPI_F32: if (mm) return umma_bn<EPI_F32, true, true>(g, st); break;
+    case EPI_F32:
+      if (mm) return umma_bn<EPI_F32, true, true>(g, st);
+      if (kk) return umma_bn<EPI_F32, false, false>(g, st);
+      break;
     default: break;
   }
   return cudaErrorNotSupported;
@@ -1078,6 +1083,112 @@ static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
   return LR_OK;
 }
 
+// ============================================================ causal attention
+// Heads are moved to a head-major layout ([b*H*s, dh]: head (bi, h) owns rows (bi*H + h)*s ..
+// + s - 1), so each GEMM runs once over all b*H heads in row-batched mode (every operand of
+// head n starts n*s stored rows into its tensor).
+struct AttnWs {
+  bf16 *qh, *kh, *vh, *oh, *doh, *dqh, *dkh, *dvh;
+  float *S, *dP, *D;
+  bf16 *P, *dS;
+};
+
+static size_t attn_ws_layout(int b, int s, int H, int dh, void* base, AttnWs* W) {
+  Arena ar(base);
+  AttnWs tmp;
+  if (!W) W = &tmp;
+  const size_t R = static_cast<size_t>(b) * H * s;
+  const size_t E = R * dh * sizeof(bf16);
+  bf16** hm[8] = {&W->qh, &W->kh, &W->vh, &W->oh, &W->doh, &W->dqh, &W->dkh, &W->dvh};
+  for (bf16** p : hm) *p = static_cast<bf16*>(ar.take(E));
+  W->S = static_cast<float*>(ar.take(R * s * sizeof(float)));
+  W->dP = static_cast<float*>(ar.take(R * s * sizeof(float)));
+  W->P = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
+  W->dS = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
+  W->D = static_cast<float*>(ar.take(R * sizeof(float)));
+  return ar.size();
+}
+
+// One GEMM over all heads: batch n = head n; A, B, out start n*s stored rows in.
+static lr_status attn_gemm(const Ctx& c, EpiKind k, int M, int N, int K, int heads, int s, Operand A, bool a_mn,
+                           Operand B, bool b_mn, void* out, long long ldo) {
+  GemmCall g = new_call(M, N, K);
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
+  g.batches = heads;
+  g.rowbatch = true;
+  g.rb_a = g.rb_b = g.rb_o = s;
+  g.rows_a = g.rows_b = g.rows_o = 1LL * heads * s;
+  g.A[0] = A;
+  g.B[0] = B;
+  g.bn = N % 256 == 0 ? 256 : 128;
+  g.ep.out0[0] = out;
+  g.ep.ldo0 = ldo;
+  g.ep.split_stride = ldo * g.rows_o;
+  return gemm(c, k, g);
+}
+
+static lr_status head_permute(const Ctx& c, const void* src, void* dst, int b, int s, int H, int dh, int to_heads) {
+  LaunchScope scope("head_permute", c.st, 0, 4.0 * b * s * H * dh);
+  cudaError_t e = launch_head_permute(static_cast<const bf16*>(src), static_cast<bf16*>(dst), b, s, H, dh, to_heads,
+                                      c.st);
+  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "head permute: %s", cudaGetErrorString(e));
+  return LR_OK;
+}
+
+static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float scale, const void* q, const void* k,
+                               const void* v, void* o, float* lse, void* ws) {
+  AttnWs W;
+  attn_ws_layout(b, s, H, dh, ws, &W);
+  const int heads = b * H, R = heads * s;
+  LR_TRY(head_permute(c, q, W.qh, b, s, H, dh, 1));
+  LR_TRY(head_permute(c, k, W.kh, b, s, H, dh, 1));
+  LR_TRY(head_permute(c, v, W.vh, b, s, H, dh, 1));
+  // S = Q K^T (fp32), both operands K-major (K = dh)
+  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s));
+  {
+    LaunchScope scope("attn_softmax", c.st, 0, 6.0 * R * s);
+    cudaError_t e = launch_attn_softmax_fwd(W.S, R, s, scale, W.P, lse, c.st);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention softmax: %s", cudaGetErrorString(e));
+  }
+  // O = P V: P K-major (K = keys), V read MN-major in its stored [keys, dh] layout
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, false, {W.vh, dh}, true, W.oh, dh));
+  return head_permute(c, W.oh, o, b, s, H, dh, 0);
+}
+
+static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float scale, const void* q, const void* k,
+                               const void* v, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                               void* dv, void* ws) {
+  AttnWs W;
+  attn_ws_layout(b, s, H, dh, ws, &W);
+  const int heads = b * H, R = heads * s;
+  LR_TRY(head_permute(c, q, W.qh, b, s, H, dh, 1));
+  LR_TRY(head_permute(c, k, W.kh, b, s, H, dh, 1));
+  LR_TRY(head_permute(c, v, W.vh, b, s, H, dh, 1));
+  LR_TRY(head_permute(c, o, W.oh, b, s, H, dh, 1));
+  LR_TRY(head_permute(c, dout, W.doh, b, s, H, dh, 1));
+  {
+    LaunchScope scope("attn_rowdot", c.st, 0, 4.0 * R * dh + 4.0 * R);
+    cudaError_t e = launch_attn_rowdot(W.doh, W.oh, R, dh, W.D, c.st);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention row dot: %s", cudaGetErrorString(e));
+  }
+  // S = Q K^T again (only its log-sum-exp was kept), dP = dO V^T
+  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s));
+  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.doh, dh}, false, {W.vh, dh}, false, W.dP, s));
+  {
+    LaunchScope scope("attn_softmax_bwd", c.st, 0, 12.0 * R * s);
+    cudaError_t e = launch_attn_softmax_bwd(W.S, W.dP, lse, W.D, R, s, scale, W.P, W.dS, c.st);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention softmax backward: %s", cudaGetErrorString(e));
+  }
+  // dV = P^T dO (P read MN-major: keys index its columns), dQ = dS K, dK = dS^T Q (dS holds scale)
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, true, {W.doh, dh}, true, W.dvh, dh));
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, false, {W.kh, dh}, true, W.dqh, dh));
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, true, {W.qh, dh}, true, W.dkh, dh));
+  LR_TRY(head_permute(c, W.dqh, dq, b, s, H, dh, 0));
+  LR_TRY(head_permute(c, W.dkh, dk, b, s, H, dh, 0));
+  return head_permute(c, W.dvh, dv, b, s, H, dh, 0);
+}
+
 // ============================================================ block stack
 struct StackWs {
   void* acts;   // x_1 .. x_L, [L][T, d]
@@ -1517,6 +1628,58 @@ lr_status lr_dense_bwd(lr_dtype dt, int T, int d, int f, float eps, const void* 
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
   return dense_bwd_impl(c, T, d, f, x, g, W_gate, W_up, W_down, saved, dout, dx, dg, dW_gate, dW_up, dW_down, ws);
+}
+
+static lr_status check_attn(lr_dtype dt, int b, int s, int H, int dh) {
+  LR_TRY(check_dtype(dt));
+  if (dt != LR_BF16) return fail(LR_ERR_UNSUPPORTED, "attention: bf16 only");
+  if (b < 1 || H < 1 || s < 256 || s % 256 || dh < 128 || dh % 128)
+    return fail(LR_ERR_SHAPE, "attention: b = %d, H = %d >= 1, s = %d a multiple of 256, dh = %d of 128 needed", b,
+                H, s, dh);
+  if (1LL * b * H * s * s > (1LL << 40)) return fail(LR_ERR_SHAPE, "attention: b*H*s*s too large");
+  return LR_OK;
+}
+
+size_t lr_attn_saved_bytes(int b, int s, int H, int dh) {
+  if (check_attn(LR_BF16, b, s, H, dh)) return 0;
+  return static_cast<size_t>(b) * H * s * sizeof(float);
+}
+
+size_t lr_attn_workspace_bytes(int b, int s, int H, int dh) {
+  if (check_attn(LR_BF16, b, s, H, dh)) return 0;
+  return attn_ws_layout(b, s, H, dh, nullptr, nullptr);
+}
+
+lr_status lr_attn_fwd(lr_dtype dt, int b, int s, int H, int dh, float scale, const void* q, const void* k,
+                      const void* v, void* o, void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                      void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_attn(dt, b, s, H, dh));
+  LR_TRY(check_ptr(q, "q"));
+  LR_TRY(check_ptr(k, "k"));
+  LR_TRY(check_ptr(v, "v"));
+  LR_TRY(check_ptr(o, "o"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, lr_attn_saved_bytes(b, s, H, dh), "saved"));
+  LR_TRY(check_size(ws_bytes, attn_ws_layout(b, s, H, dh, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return attn_fwd_impl(c, b, s, H, dh, scale, q, k, v, o, static_cast<float*>(saved), ws);
+}
+
+lr_status lr_attn_bwd(lr_dtype dt, int b, int s, int H, int dh, float scale, const void* q, const void* k,
+                      const void* v, const void* o, const void* saved, const void* dout, void* dq, void* dk,
+                      void* dv, void* ws, size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_attn(dt, b, s, H, dh));
+  const void* ptrs[] = {q, k, v, o, saved, dout, dq, dk, dv, ws};
+  const char* names[] = {"q", "k", "v", "o", "saved", "dout", "dq", "dk", "dv", "ws"};
+  for (int i = 0; i < 10; ++i) LR_TRY(check_ptr(ptrs[i], names[i]));
+  LR_TRY(check_size(ws_bytes, attn_ws_layout(b, s, H, dh, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return attn_bwd_impl(c, b, s, H, dh, scale, q, k, v, o, static_cast<const float*>(saved), dout, dq, dk, dv, ws);
 }
 
 size_t lr_btp_payload_floats(int T, int r, int group) {

@@ -82,6 +82,8 @@ struct Shape {
   int g_n_tiles[kMaxBatch];  // n-tiles of batch b
   int g_tile0[kMaxBatch];    // first pair tile of batch b
   int g_tiles;               // pair tiles of all batches
+  int rowbatch;              // batches offset into one tensor each (see GemmCall::rowbatch), then:
+  int rb_a, rb_b, rb_o;      // stored rows per batch of A, B and the output
   unsigned* err;
 };
 
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     fence_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    const int nsets = NACC > 1 ? NACC : sh.batches;
+    const int nsets = NACC > 1 ? NACC : (sh.rowbatch ? 1 : sh.batches);
     for (int i = 0; i < nsets; ++i) {
       tmap_prefetch(&maps.a[i]);
       tmap_prefetch(&maps.b[i]);
@@ -509,8 +511,10 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         const int kb0 = split * sh.kb_per_split;
         const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
         const int m0 = mb * BM, n0 = nb * BN;
+        const int set0 = sh.rowbatch ? 0 : batch;
+        const int ra = batch * sh.rb_a, rbb = batch * sh.rb_b;  // row-batched offsets (else 0)
         for (int s = 0; s < NACC && ok; ++s) {
-          const int set = NACC > 1 ? s : batch;
+          const int set = NACC > 1 ? s : set0;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_PRODUCER)) {
               ok = false;
@@ -524,17 +528,17 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
             if (A_MN) {
 #pragma unroll
               for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d_pair(a_dst + j * 8192, &maps.a[set], fbar, m0 + 64 * j, kb * BK);
+                tma_load_2d_pair(a_dst + j * 8192, &maps.a[set], fbar, m0 + 64 * j, kb * BK + ra);
             } else {
-              tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK, m0);
+              tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK, m0 + ra);
             }
             const int nb0 = n0 + rank * (BN / 2);  // this CTA's half of the B tile
             if (B_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 128; ++j)
-                tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j, kb * BK);
+                tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j, kb * BK + rbb);
             } else {
-              tma_load_2d_pair(b_dst, &maps.b[set], fbar, kb * BK, nb0);
+              tma_load_2d_pair(b_dst, &maps.b[set], fbar, kb * BK, nb0 + rbb);
             }
             ++issued;
             if (++st == STAGES) {
@@ -746,7 +750,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       const int sbuf = it & 1;  // statistics double buffer (independent of TMEM)
       const uint32_t sph = static_cast<uint32_t>((it >> 1) & 1);
       const int m = mb * BM + row;
-      const int r0 = mb * BM + q * ER;  // first row of this warp's boxes
+      const int ob = sh.rowbatch ? 0 : batch;                 // output maps and pointers of this batch
+      const int r0 = mb * BM + q * ER + batch * sh.rb_o;  // first stored row of this warp's boxes
       RowIn ri;
       if constexpr (C::STATS) {
         ri.k = 0.f;
@@ -760,10 +765,10 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       }
       bool present[NOUT];
 #pragma unroll
-      for (int o = 0; o < NOUT; ++o) present[o] = epi_out_ptr(ep, o, batch) != nullptr;
+      for (int o = 0; o < NOUT; ++o) present[o] = epi_out_ptr(ep, o, ob) != nullptr;
       bool aux_present[NAUX > 0 ? NAUX : 1];
 #pragma unroll
-      for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, batch) != nullptr;
+      for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, ob) != nullptr;
 
       if constexpr (C::SPLIT) {
         // Phase 1: round(a) of this warp's chunks into its a tiles in shared memory (exact:
@@ -796,7 +801,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           if (leader) {
 #pragma unroll
             for (int ci = 0; ci < NC; ++ci)
-              tma_store_2d(&maps.out[batch][1], abuf + ci * C::OUT_BUF, nb * BN + (g + 2 * ci) * CW, r0);
+              tma_store_2d(&maps.out[ob][1], abuf + ci * C::OUT_BUF, nb * BN + (g + 2 * ci) * CW, r0);
             bulk_commit();
           }
         }
@@ -853,8 +858,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (leader) {
-            if (present[0]) tma_store_2d(&maps.out[batch][0], ostage(b), nb * BN + c * CW, r0);
-            if (present[2]) tma_store_2d(&maps.out[batch][2], ostage(b) + C::OUT_BUF, nb * BN + c * CW, r0);
+            if (present[0]) tma_store_2d(&maps.out[ob][0], ostage(b), nb * BN + c * CW, r0);
+            if (present[2]) tma_store_2d(&maps.out[ob][2], ostage(b) + C::OUT_BUF, nb * BN + c * CW, r0);
             bulk_commit();
           }
           ++qi;
@@ -934,13 +939,13 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               if constexpr (D::OUT_F32) {
                 // Split-K partials are summed by the next kernel: keep them in L2 for it.
                 if (sh.ksplit > 1)
-                  tma_store_3d_hint(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split,
+                  tma_store_3d_hint(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split,
                                     l2_evict_last());
                 else
-                  tma_store_3d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split);
+                  tma_store_3d(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split);
               }
               else
-                tma_store_2d(&maps.out[batch][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0);
+                tma_store_2d(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0);
             }
             bulk_commit();
           }

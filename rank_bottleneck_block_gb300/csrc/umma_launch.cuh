@@ -93,6 +93,16 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.ksplit = (sh.kb_total + sh.kb_per_split - 1) / sh.kb_per_split;  // no empty split
   sh.err = g.err;
   sh.reverse = g.reverse ? 1 : 0;
+  if (!g.rowbatch && !g.grouped && NACC == 1 && (g.batches < 1 || g.batches > kMaxBatch)) return cudaErrorInvalidValue;
+  if (g.rowbatch) {  // one tensor per operand, batches offset by rows
+    if (D::NAUX > 0 || C::STATS || C::SPLIT || D::ROWPART || NACC > 1 || g.grouped || sh.ksplit != 1 ||
+        g.M % (2 * BM) || g.N % BN || g.K % BK || g.rb_a < 0 || g.rb_b < 0 || g.rb_o < 0)
+      return cudaErrorInvalidValue;
+    sh.rowbatch = 1;
+    sh.rb_a = g.rb_a;
+    sh.rb_b = g.rb_b;
+    sh.rb_o = g.rb_o;
+  }
   sh.grouped = 0;
   if (g.grouped) {  // batches of their own M, N; one split only
     if (K != EPI_F32 || sh.ksplit != 1 || g.batches < 1 || g.batches > kMaxBatch) return cudaErrorInvalidValue;
@@ -108,28 +118,33 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   // Extent of batch (or operand set) b.
   auto bM = [&](int b) { return g.grouped ? g.gM[b] : g.M; };
   auto bN = [&](int b) { return g.grouped ? g.gN[b] : g.N; };
+  // Stored rows of operand A / B / the output (all batches' rows when row-batched).
+  auto rowsA = [&](int b) -> long long { return g.rowbatch ? g.rows_a : (A_MN ? g.K : bM(b)); };
+  auto rowsB = [&](int b) -> long long { return g.rowbatch ? g.rows_b : (B_MN ? g.K : bN(b)); };
 
-  const int nsets = NACC > 1 ? NACC : g.batches;
+  const int nsets = NACC > 1 ? NACC : (g.rowbatch ? 1 : g.batches);
   for (int i = 0; i < nsets; ++i) {
-    const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, bM(i), g.K, g.A[i].ld, 64, 64)
-                          : encode_operand(&maps.a[i], g.A[i].ptr, g.K, bM(i), g.A[i].ld, 64, BM);
+    const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, bM(i), rowsA(i), g.A[i].ld, 64, 64)
+                          : encode_operand(&maps.a[i], g.A[i].ptr, g.K, rowsA(i), g.A[i].ld, 64, BM);
     // Each CTA of a pair stages half of the B tile: BN/2 rows (K-major) or 64-column chunks (MN-major).
-    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, bN(i), g.K, g.B[i].ld, 64, 64)
-                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, bN(i), g.B[i].ld, 64, BN / 2);
+    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, bN(i), rowsB(i), g.B[i].ld, 64, 64)
+                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, rowsB(i), g.B[i].ld, 64, BN / 2);
     if (!okA || !okB) return cudaErrorInvalidValue;
   }
   const void* const* outs[3] = {g.ep.out0, g.ep.out1, g.ep.out2};
   const long long ldo[3] = {g.ep.ldo0, g.ep.ldo1, g.ep.ldo2};
   const void* const* auxs[2] = {g.ep.aux0, g.ep.aux1};
   const long long lda[2] = {g.ep.lda0, g.ep.lda1};
-  for (int b = 0; b < sh.batches; ++b) {
+  const int nmaps = g.rowbatch ? 1 : sh.batches;
+  for (int b = 0; b < nmaps; ++b) {
     for (int o = 0; o < D::NOUT; ++o) {
       const void* p = outs[o][b];
       if (!p) continue;
       const long long ld = g.grouped ? g.gldo[b] : ldo[o];
-      const long long stride = g.grouped ? ld * bM(b) : g.ep.split_stride;
-      const bool ok = D::OUT_F32 ? encode_epi_f32(&maps.out[b][o], p, bN(b), bM(b), ld, sh.ksplit, stride)
-                                 : encode_epi_bf16(&maps.out[b][o], p, bN(b), bM(b), ld);
+      const long long orows = g.rowbatch ? g.rows_o : bM(b);
+      const long long stride = g.grouped ? ld * bM(b) : (g.rowbatch ? ld * orows : g.ep.split_stride);
+      const bool ok = D::OUT_F32 ? encode_epi_f32(&maps.out[b][o], p, bN(b), orows, ld, sh.ksplit, stride)
+                                 : encode_epi_bf16(&maps.out[b][o], p, bN(b), orows, ld);
       if (!ok) return cudaErrorInvalidValue;
     }
     for (int a = 0; a < D::NAUX; ++a) {

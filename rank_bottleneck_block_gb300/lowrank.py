@@ -31,7 +31,7 @@ EXPORTED = [
     "lr_profile_start", "lr_profile_stop", "lr_profile_filter", "lr_profile_count", "lr_profile_entry",
     "lr_proj_fwd_noalloc", "lr_dense_saved_bytes", "lr_dense_fwd_workspace_bytes", "lr_dense_bwd_workspace_bytes",
     "lr_dense_fwd", "lr_dense_bwd", "lr_btp_payload_floats", "lr_btp_workspace_bytes", "lr_btp_partial",
-    "lr_btp_finish",
+    "lr_btp_finish", "lr_attn_saved_bytes", "lr_attn_workspace_bytes", "lr_attn_fwd", "lr_attn_bwd",
 ]
 
 
@@ -76,6 +76,10 @@ _SIGS = {
     "lr_btp_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_btp_partial": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _P, _P, _P, _SZ, _P]),
     "lr_btp_finish": (_I, [_I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P]),
+    "lr_attn_saved_bytes": (_SZ, [_I, _I, _I, _I]),
+    "lr_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "lr_attn_fwd": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P]),
+    "lr_attn_bwd": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "lr_dense_fwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_dense_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_dense_fwd": (_I, [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P]),
@@ -253,6 +257,24 @@ def lr_dense_bwd(dt, T, d, f, eps, x, g, Wg, Wu, Wd, saved, dout, dx, dg, dWg, d
     _check(lib().lr_dense_bwd(dt, T, d, f, eps, _p(x), _p(g), _p(Wg), _p(Wu), _p(Wd), _p(saved), _nbytes(saved),
                               _p(dout), _p(dx), _p(dg), _p(dWg), _p(dWu), _p(dWd), _p(ws), _nbytes(ws),
                               _stream(stream)))
+
+
+def lr_attn_saved_bytes(b, s, H, dh) -> int:
+    return lib().lr_attn_saved_bytes(b, s, H, dh)
+
+
+def lr_attn_workspace_bytes(b, s, H, dh) -> int:
+    return lib().lr_attn_workspace_bytes(b, s, H, dh)
+
+
+def lr_attn_fwd(dt, b, s, H, dh, scale, q, k, v, o, saved, ws, stream=None):
+    _check(lib().lr_attn_fwd(dt, b, s, H, dh, scale, _p(q), _p(k), _p(v), _p(o), _p(saved), _nbytes(saved), _p(ws),
+                             _nbytes(ws), _stream(stream)))
+
+
+def lr_attn_bwd(dt, b, s, H, dh, scale, q, k, v, o, saved, dout, dq, dk, dv, ws, stream=None):
+    _check(lib().lr_attn_bwd(dt, b, s, H, dh, scale, _p(q), _p(k), _p(v), _p(o), _p(saved), _p(dout), _p(dq),
+                             _p(dk), _p(dv), _p(ws), _nbytes(ws), _stream(stream)))
 
 
 def lr_btp_payload_floats(T, r, group) -> int:

@@ -280,3 +280,35 @@ class GraphStep:
 
     def __call__(self) -> None:
         self.graph.replay()
+
+
+class Attention:
+    """Causal multi-head self-attention between the projection groups, resident on the device.
+
+    q, k, v [b*s, H*dh] bf16 (token-major, as the projections write them); forward() writes o
+    and keeps the row log-sum-exp; backward() takes dout and writes dq, dk, dv.
+    """
+
+    def __init__(self, b: int, s: int, H: int, dh: int, q, k, v, device="cuda", scale: Optional[float] = None):
+        self.b, self.s, self.H, self.dh = b, s, H, dh
+        self.scale = float(scale if scale is not None else dh ** -0.5)
+        self.q, self.k, self.v = (t.to(device=device, dtype=torch.bfloat16).contiguous() for t in (q, k, v))
+        self.o = torch.empty_like(self.q)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.dout = torch.empty_like(self.q)
+        self.saved = _buf(L.lr_attn_saved_bytes(b, s, H, dh), device)
+        self.ws = _buf(L.lr_attn_workspace_bytes(b, s, H, dh), device)
+
+    def forward(self, stream=None):
+        L.lr_attn_fwd(L.LR_BF16, self.b, self.s, self.H, self.dh, self.scale, self.q, self.k, self.v, self.o,
+                      self.saved, self.ws, stream)
+
+    def backward(self, dout: Optional[torch.Tensor] = None, stream=None):
+        if dout is not None:
+            self.dout.copy_(dout)
+        L.lr_attn_bwd(L.LR_BF16, self.b, self.s, self.H, self.dh, self.scale, self.q, self.k, self.v, self.o,
+                      self.saved, self.dout, self.dq, self.dk, self.dv, self.ws, stream)
+
+    def step(self, stream=None):
+        self.forward(stream)
+        self.backward(None, stream)

@@ -94,3 +94,15 @@ def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(lowrank, "_lib", None)
     with pytest.raises(RuntimeError):
         lowrank.lib()
+
+
+def test_attention_shape_rules(L):
+    assert L.lr_attn_saved_bytes(2, 256, 3, 128) == 2 * 3 * 256 * 4
+    assert L.lr_attn_workspace_bytes(2, 256, 3, 128) > 12 * 2 * 3 * 256 * 256
+    assert L.lr_attn_saved_bytes(1, 200, 1, 128) == 0  # s not a multiple of 256
+    assert L.lr_attn_workspace_bytes(1, 256, 1, 64) == 0  # dh not a multiple of 128
+    lib = L.lib()
+    null = None
+    assert lib.lr_attn_fwd(L.LR_F32, 1, 256, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 8
+    assert lib.lr_attn_fwd(L.LR_BF16, 1, 100, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 2
+    assert lib.lr_attn_fwd(L.LR_BF16, 1, 256, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 1
