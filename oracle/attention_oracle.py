@@ -21,10 +21,18 @@ Tensors are token-major as the projections produce them: q, k, v, o are [b*s, H*
 head h of token t in columns h*dh .. h*dh + dh - 1 of row t.  float64 throughout; matrix
 products use numpy's ``@`` (a library primitive).
 
-Pins (tests/test_oracle.py): a brute-force triple loop on tiny sizes, central finite
-differences of every gradient, causality (later keys and values do not change earlier
-outputs), the first token's output equals its own value, and q = 0 gives the running mean
-of the values.  No function here is parity unpinned.
+The full low-rank transformer block composes this attention with the projection groups and
+the MLP block of ``lowrank_oracle`` (pre-norm residual form, as in LLaMA):
+
+    [q; k; v] = LR_{q,k,v}(RMSNorm_a(x)),  y = LR_o(attention(q, k, v)),  x1 = x + y,
+    out = x1 + LR_down(SiLU(LR_gate(n1)) * LR_up(n1)),  n1 = RMSNorm_m(x1),
+
+and its backward chains the pieces' backward functions, the residual adding its gradient.
+
+Pins (tests/test_attention_oracle.py): a brute-force triple loop on tiny sizes, central finite
+differences of every gradient (of the attention and of the whole block), causality (later keys
+and values do not change earlier outputs), the first token's output equals its own value, and
+q = 0 gives the running mean of the values.  No function here is parity unpinned.
 """
 from __future__ import annotations
 
@@ -34,7 +42,7 @@ import numpy as np
 
 F64 = np.float64
 
-__all__ = ["heads", "unheads", "attention_fwd", "attention_bwd"]
+__all__ = ["heads", "unheads", "attention_fwd", "attention_bwd", "block_fwd", "block_bwd"]
 
 
 def heads(x: np.ndarray, b: int, s: int, H: int, dh: int) -> np.ndarray:
@@ -81,3 +89,43 @@ def attention_bwd(q, k, v, o, saved: Dict, do, b: int, s: int, H: int, dh: int, 
     dQ = scale * (dS @ K)
     dK = scale * (dS.transpose(0, 1, 3, 2) @ Q)
     return {"dq": unheads(dQ), "dk": unheads(dK), "dv": unheads(dV)}
+
+
+# ---------------------------------------------------------------------------
+# The full low-rank transformer block.
+# ---------------------------------------------------------------------------
+def block_fwd(x, W: Dict, b: int, s: int, H: int, dh: int, scale: float, eps: float = 1e-6):
+    """W: g_attn, A_q/B_q, A_k/B_k, A_v/B_v, A_o/B_o, g_mlp and the MLP's A_*/B_* (gate, up,
+    down).  Returns (out, saved)."""
+    from . import lowrank_oracle as O
+
+    x = O.to64(x)
+    qkv, s_qkv = O.proj_group_fwd(x, W["g_attn"], [W["A_q"], W["A_k"], W["A_v"]],
+                                  [W["B_q"], W["B_k"], W["B_v"]], eps)
+    o, s_att = attention_fwd(qkv[0], qkv[1], qkv[2], b, s, H, dh, scale)
+    (y,), s_o = O.proj_group_fwd(o, None, [W["A_o"]], [W["B_o"]], eps)
+    x1 = x + y
+    mlp = {k: W[k] for k in ("A_gate", "B_gate", "A_up", "B_up", "A_down", "B_down")}
+    out, s_mlp = O.mlp_block_fwd(x1, W["g_mlp"], mlp, eps, O.FULL)
+    return out, dict(qkv=qkv, s_qkv=s_qkv, o=o, s_att=s_att, s_o=s_o, mlp=mlp, s_mlp=s_mlp)
+
+
+def block_bwd(W: Dict, saved: Dict, G, b: int, s: int, H: int, dh: int, scale: float, eps: float = 1e-6):
+    """Gradients of sum(out * G): dx, dg_attn, dg_mlp, and dA_*/dB_* for q, k, v, o, gate,
+    up, down."""
+    from . import lowrank_oracle as O
+
+    gm = O.mlp_block_bwd(W["g_mlp"], saved["mlp"], saved["s_mlp"], O.to64(G), eps)
+    dx1 = gm["dx"]  # includes the residual path of the MLP block
+    go = O.proj_group_bwd(None, [W["A_o"]], [W["B_o"]], saved["s_o"], [dx1])
+    q, k, v = saved["qkv"]
+    ga = attention_bwd(q, k, v, saved["o"], saved["s_att"], go["dx"], b, s, H, dh, scale)
+    gq = O.proj_group_bwd(W["g_attn"], [W["A_q"], W["A_k"], W["A_v"]], [W["B_q"], W["B_k"], W["B_v"]],
+                          saved["s_qkv"], [ga["dq"], ga["dk"], ga["dv"]])
+    out = {"dx": dx1 + gq["dx"], "dg_attn": gq["dg"], "dg_mlp": gm["dg"]}
+    for i, n in enumerate("qkv"):
+        out[f"dA_{n}"], out[f"dB_{n}"] = gq["dA"][i], gq["dB"][i]
+    out["dA_o"], out["dB_o"] = go["dA"][0], go["dB"][0]
+    for n in ("gate", "up", "down"):
+        out[f"dA_{n}"], out[f"dB_{n}"] = gm[f"dA_{n}"], gm[f"dB_{n}"]
+    return out

@@ -97,3 +97,51 @@ def test_gradients_match_finite_differences():
                 args_m[idx][i, j] -= h
                 num[i, j] = (loss(*args_p) - loss(*args_m)) / (2 * h)
         np.testing.assert_allclose(gr[name], num, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def _tiny_block(seed=9, b=1, s=3, H=2, dh=2, f=6, r=2):
+    R = np.random.default_rng(seed)
+    d = H * dh
+    W = {"g_attn": 1 + 0.1 * R.standard_normal(d), "g_mlp": 1 + 0.1 * R.standard_normal(d)}
+    for n in "qkvo":
+        W[f"A_{n}"] = R.standard_normal((r, d)) / np.sqrt(d)
+        W[f"B_{n}"] = R.standard_normal((d, r)) / np.sqrt(r)
+    for n, (din, dout) in (("gate", (d, f)), ("up", (d, f)), ("down", (f, d))):
+        W[f"A_{n}"] = R.standard_normal((r, din)) / np.sqrt(din)
+        W[f"B_{n}"] = R.standard_normal((dout, r)) / np.sqrt(r)
+    x = R.standard_normal((b * s, d))
+    G = R.standard_normal((b * s, d))
+    return W, x, G, (b, s, H, dh)
+
+
+def test_block_gradients_match_finite_differences():
+    """The whole transformer block (q/k/v group, attention, o-projection and its residual,
+    MLP block): every gradient against central differences of sum(out * G)."""
+    W, x, G, shp = _tiny_block()
+    scale = 0.7
+    out, saved = A.block_fwd(x, W, *shp, scale)
+    gr = A.block_bwd(W, saved, G, *shp, scale)
+
+    def loss(xx, WW):
+        return float(np.sum(A.block_fwd(xx, WW, *shp, scale)[0] * G))
+
+    h = 1e-6
+
+    def fd(get, shape):
+        num = np.zeros(shape)
+        for idx in np.ndindex(*shape):
+            xp, Wp = x.copy(), {k: v.copy() for k, v in W.items()}
+            xm, Wm = x.copy(), {k: v.copy() for k, v in W.items()}
+            get(xp, Wp)[idx] += h
+            get(xm, Wm)[idx] -= h
+            num[idx] = (loss(xp, Wp) - loss(xm, Wm)) / (2 * h)
+        return num
+
+    np.testing.assert_allclose(gr["dx"], fd(lambda xx, WW: xx, x.shape), rtol=1e-6, atol=1e-8)
+    for key, g in (("g_attn", "dg_attn"), ("g_mlp", "dg_mlp")):
+        np.testing.assert_allclose(gr[g], fd(lambda xx, WW, key=key: WW[key], W[key].shape), rtol=1e-6, atol=1e-8)
+    for n in ("q", "k", "v", "o", "gate", "down"):
+        for m in ("A", "B"):
+            key = f"{m}_{n}"
+            np.testing.assert_allclose(gr[f"d{key}"], fd(lambda xx, WW, key=key: WW[key], W[key].shape),
+                                       rtol=1e-6, atol=1e-8, err_msg=key)
