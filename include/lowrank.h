@@ -229,6 +229,42 @@ lr_status lr_attn_bwd(lr_dtype dt, int b, int s, int H, int dh, float scale, con
                       const void* v, const void* o, const void* saved, const void* dout, void* dq, void* dk,
                       void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------- low-rank transformer block
+ * One pre-norm LLaMA-style block whose linear maps are all low-rank pairs (d = H*dh,
+ * T = b*s tokens, attention rank ra, MLP rank rm, MLP width f):
+ *     [q; k; v] = LR_{q,k,v}(RMSNorm(x; g_attn))       (one normed group, as lr_proj_fwd)
+ *     o = causal attention(q, k, v), scale 1/sqrt(dh)  (as lr_attn_fwd)
+ *     x1 = x + LR_o(o)                                 (LR = B SiLU(A .), no norm)
+ *     out = MLP block(x1; g_mlp, gate, up, down)       (as lr_mlp_fwd, LR_SAVE_CKPT)
+ * lr_block_bwd returns dx and every gradient (fp32; the gains' dg_attn, dg_mlp [d]).
+ * x, out, dout, dx: [T, d] bf16; all pairs' shapes follow lr_pair (q, k, v, o: A [ra, d],
+ * B [d, ra]; gate, up: A [rm, d], B [f, rm]; down: A [rm, f], B [d, rm]).  saved keeps the
+ * pieces' saved sets plus q, k, v, o and x1 ([T, d] each); ws is shared by the pieces.
+ * bf16 only; the shape rules of lr_attn_fwd and lr_mlp_fwd apply.
+ */
+typedef struct {
+  const void* g_attn;
+  lr_pair q, k, v, o;
+  const void* g_mlp;
+  lr_pair gate, up, down;
+} lr_block_weights;
+
+typedef struct {
+  float* dg_attn;
+  lr_pair_grad q, k, v, o;
+  float* dg_mlp;
+  lr_pair_grad gate, up, down;
+} lr_block_grads;
+
+size_t lr_block_saved_bytes(int b, int s, int H, int dh, int f, int ra, int rm);
+size_t lr_block_workspace_bytes(int b, int s, int H, int dh, int f, int ra, int rm);
+lr_status lr_block_fwd(lr_dtype dt, int b, int s, int H, int dh, int f, int ra, int rm, float eps, const void* x,
+                       const lr_block_weights* w, void* out, void* saved, size_t saved_bytes, void* ws,
+                       size_t ws_bytes, void* stream);
+lr_status lr_block_bwd(lr_dtype dt, int b, int s, int H, int dh, int f, int ra, int rm, float eps, const void* x,
+                       const lr_block_weights* w, const void* saved, size_t saved_bytes, const void* dout, void* dx,
+                       const lr_block_grads* g, void* ws, size_t ws_bytes, void* stream);
+
 /* -------------------------------------------------------------- block stack
  * One training step of `nblocks` residual MLP blocks (as lr_mlp_fwd, sigma = SiLU) and a
  * mean-squared-error loss against `target` [T, d]:

@@ -981,8 +981,10 @@ static size_t proj_ws_layout(lr_dtype dt, bool bwd, int T, int d_in, int d_out, 
   return ar.size();
 }
 
+// resid (group 1, d_out == d_in, or null): outs[0] = resid + LR(x), the residual fused into the B GEMM.
 static lr_status proj_fwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
-                               const void* g, float eps, const void* x, void* const* outs, void* saved, void* ws) {
+                               const void* g, float eps, const void* x, void* const* outs, void* saved, void* ws,
+                               const void* resid = nullptr) {
   const int norm = g != nullptr;
   ProjSaved S;
   ProjWs W;
@@ -1015,14 +1017,20 @@ static lr_status proj_fwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
       k.ep.out0[i] = outs[i];
     }
     k.ep.ldo0 = d_out;
-    LR_TRY(gemm(c, EPI_STORE, k));
+    if (resid) {
+      k.ep.aux0[0] = resid;
+      k.ep.lda0 = d_out;
+    }
+    LR_TRY(gemm(c, resid ? EPI_RESID : EPI_STORE, k));
   }
   return LR_OK;
 }
 
+// dres (normed groups, or null): the gradient reaching x through a residual, added into dx by the
+// dx GEMM's epilogue.
 static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, int group, const lr_pair* pairs,
                                const void* g, const void* x, const void* saved, const void* const* douts, void* dx,
-                               float* dg, const lr_pair_grad* grads, void* ws) {
+                               float* dg, const lr_pair_grad* grads, void* ws, const void* dres = nullptr) {
   const int norm = g != nullptr;
   ProjSaved S;
   ProjWs W;
@@ -1071,6 +1079,8 @@ static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
     k.ep.out0[0] = dx;
     k.ep.ldo0 = d_in;
     if (norm) {
+      k.ep.aux0[0] = dres;
+      k.ep.lda0 = d_in;
       k.ep.aux1[0] = x;
       k.ep.lda1 = d_in;
       k.ep.rowscale = S.s;
@@ -1187,6 +1197,94 @@ static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   LR_TRY(head_permute(c, W.dqh, dq, b, s, H, dh, 0));
   LR_TRY(head_permute(c, W.dkh, dk, b, s, H, dh, 0));
   return head_permute(c, W.dvh, dv, b, s, H, dh, 0);
+}
+
+// ============================================================ transformer block
+// Pre-norm low-rank transformer block: [q; k; v] = normed group (gain g_attn), causal attention,
+// x1 = x + LR_o(o) (residual fused into the o-projection's B GEMM), out = MLP block(x1) in
+// checkpoint mode.  bf16.  The saved set keeps q, k, v, o and x1 besides the pieces' own sets.
+struct BlockSaved {
+  void *qkv, *q, *k, *v, *o, *oproj, *x1, *mlp;
+  float* lse;
+};
+
+static size_t block_saved_layout(int b, int s, int H, int dh, int f, int ra, int rm, void* base, BlockSaved* S) {
+  Arena ar(base);
+  BlockSaved tmp;
+  if (!S) S = &tmp;
+  const int T = b * s, d = H * dh;
+  const size_t act = sizeof(bf16) * static_cast<size_t>(T) * d;
+  S->qkv = ar.take(proj_saved_layout(LR_BF16, T, ra, 3, 1, nullptr, nullptr));
+  S->q = ar.take(act);
+  S->k = ar.take(act);
+  S->v = ar.take(act);
+  S->o = ar.take(act);
+  S->lse = static_cast<float*>(ar.take(sizeof(float) * static_cast<size_t>(b) * H * s));
+  S->oproj = ar.take(proj_saved_layout(LR_BF16, T, ra, 1, 0, nullptr, nullptr));
+  S->x1 = ar.take(act);
+  S->mlp = ar.take(mlp_saved_layout(LR_BF16, LR_SAVE_CKPT, T, d, f, rm, nullptr, nullptr));
+  return ar.size();
+}
+
+struct BlockWs {
+  void* sub;  // the workspace of whichever piece runs
+  void *dx1, *dO, *dq, *dk, *dv;
+};
+
+static size_t block_ws_layout(int b, int s, int H, int dh, int f, int ra, int rm, void* base, BlockWs* W) {
+  Arena ar(base);
+  BlockWs tmp;
+  if (!W) W = &tmp;
+  const int T = b * s, d = H * dh;
+  const size_t act = sizeof(bf16) * static_cast<size_t>(T) * d;
+  const size_t sub = std::max({proj_ws_layout(LR_BF16, true, T, d, d, ra, 3, 1, nullptr, nullptr),
+                               proj_ws_layout(LR_BF16, true, T, d, d, ra, 1, 0, nullptr, nullptr),
+                               attn_ws_layout(b, s, H, dh, nullptr, nullptr),
+                               mlp_fwd_ws_layout(LR_BF16, LR_SAVE_CKPT, T, d, f, rm, nullptr, nullptr),
+                               mlp_bwd_ws_layout(LR_BF16, LR_SAVE_CKPT, T, d, f, rm, nullptr, nullptr)});
+  W->sub = ar.take(sub);
+  void** bufs[5] = {&W->dx1, &W->dO, &W->dq, &W->dk, &W->dv};
+  for (void** p : bufs) *p = ar.take(act);
+  return ar.size();
+}
+
+static lr_status block_fwd_impl(const Ctx& c, int b, int s, int H, int dh, int f, int ra, int rm, float eps,
+                                const void* x, const lr_block_weights& w, void* out, void* saved, void* ws) {
+  BlockSaved S;
+  BlockWs W;
+  block_saved_layout(b, s, H, dh, f, ra, rm, saved, &S);
+  block_ws_layout(b, s, H, dh, f, ra, rm, ws, &W);
+  const int T = b * s, d = H * dh;
+  const lr_pair qkv[3] = {w.q, w.k, w.v};
+  void* const outs[3] = {S.q, S.k, S.v};
+  LR_TRY(proj_fwd_impl(c, T, d, d, ra, 3, qkv, w.g_attn, eps, x, outs, S.qkv, W.sub));
+  LR_TRY(attn_fwd_impl(c, b, s, H, dh, 1.f / sqrtf(static_cast<float>(dh)), S.q, S.k, S.v, S.o, S.lse, W.sub));
+  void* const x1[1] = {S.x1};
+  LR_TRY(proj_fwd_impl(c, T, d, d, ra, 1, &w.o, nullptr, eps, S.o, x1, S.oproj, W.sub, x));
+  return mlp_fwd_impl(c, LR_SAVE_CKPT, T, d, f, rm, eps, S.x1, w.g_mlp, w.gate, w.up, w.down, out, S.mlp, W.sub);
+}
+
+static lr_status block_bwd_impl(const Ctx& c, int b, int s, int H, int dh, int f, int ra, int rm, float eps,
+                                const void* x, const lr_block_weights& w, const void* saved, const void* dout,
+                                void* dx, const lr_block_grads& gr, void* ws) {
+  BlockSaved S;
+  BlockWs W;
+  block_saved_layout(b, s, H, dh, f, ra, rm, const_cast<void*>(saved), &S);
+  block_ws_layout(b, s, H, dh, f, ra, rm, ws, &W);
+  const int T = b * s, d = H * dh;
+  // MLP block: dx1 already holds the gradient its residual passes through
+  LR_TRY(mlp_bwd_impl(c, LR_SAVE_CKPT, T, d, f, rm, eps, S.x1, w.g_mlp, w.gate, w.up, w.down, S.mlp, dout, W.dx1,
+                      gr.dg_mlp, gr.gate, gr.up, gr.down, W.sub));
+  // o-projection: its output's gradient is dx1; its dx is dL/do
+  const void* const d1[1] = {W.dx1};
+  LR_TRY(proj_bwd_impl(c, T, d, d, ra, 1, &w.o, nullptr, S.o, S.oproj, d1, W.dO, nullptr, &gr.o, W.sub));
+  LR_TRY(attn_bwd_impl(c, b, s, H, dh, 1.f / sqrtf(static_cast<float>(dh)), S.q, S.k, S.v, S.o, S.lse, W.dO, W.dq,
+                       W.dk, W.dv, W.sub));
+  // q/k/v group, with the residual's gradient dx1 added into dx
+  const lr_pair qkv[3] = {w.q, w.k, w.v};
+  const void* const dqkv[3] = {W.dq, W.dk, W.dv};
+  const lr_pair_grad gq[3] = {gr.q, gr.k, gr.v};
+  return proj_bwd_impl(c, T, d, d, ra, 3, qkv, w.g_attn, x, S.qkv, dqkv, dx, gr.dg_attn, gq, W.sub, W.dx1);
 }
 
 // ============================================================ block stack
@@ -1680,6 +1778,69 @@ lr_status lr_attn_bwd(lr_dtype dt, int b, int s, int H, int dh, float scale, con
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
   return attn_bwd_impl(c, b, s, H, dh, scale, q, k, v, o, static_cast<const float*>(saved), dout, dq, dk, dv, ws);
+}
+
+static lr_status check_block(lr_dtype dt, int b, int s, int H, int dh, int f, int ra, int rm) {
+  LR_TRY(check_attn(dt, b, s, H, dh));
+  LR_TRY(check_mlp_dims(b * s, H * dh, f, rm));
+  return check_mlp_dims(b * s, H * dh, H * dh, ra);
+}
+
+size_t lr_block_saved_bytes(int b, int s, int H, int dh, int f, int ra, int rm) {
+  if (check_block(LR_BF16, b, s, H, dh, f, ra, rm)) return 0;
+  return block_saved_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr);
+}
+
+size_t lr_block_workspace_bytes(int b, int s, int H, int dh, int f, int ra, int rm) {
+  if (check_block(LR_BF16, b, s, H, dh, f, ra, rm)) return 0;
+  return block_ws_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr);
+}
+
+static lr_status check_block_weights(const lr_block_weights* w) {
+  LR_TRY(check_ptr(w, "w"));
+  const void* ptrs[] = {w->g_attn, w->q.A, w->q.B, w->k.A, w->k.B, w->v.A, w->v.B, w->o.A, w->o.B,
+                        w->g_mlp, w->gate.A, w->gate.B, w->up.A, w->up.B, w->down.A, w->down.B};
+  for (const void* p : ptrs) LR_TRY(check_ptr(p, "block weight"));
+  return LR_OK;
+}
+
+lr_status lr_block_fwd(lr_dtype dt, int b, int s, int H, int dh, int f, int ra, int rm, float eps, const void* x,
+                       const lr_block_weights* w, void* out, void* saved, size_t saved_bytes, void* ws,
+                       size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_block(dt, b, s, H, dh, f, ra, rm));
+  LR_TRY(check_block_weights(w));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(out, "out"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, block_saved_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, block_ws_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return block_fwd_impl(c, b, s, H, dh, f, ra, rm, eps, x, *w, out, saved, ws);
+}
+
+lr_status lr_block_bwd(lr_dtype dt, int b, int s, int H, int dh, int f, int ra, int rm, float eps, const void* x,
+                       const lr_block_weights* w, const void* saved, size_t saved_bytes, const void* dout, void* dx,
+                       const lr_block_grads* g, void* ws, size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  LR_TRY(check_block(dt, b, s, H, dh, f, ra, rm));
+  LR_TRY(check_block_weights(w));
+  LR_TRY(check_ptr(g, "g"));
+  const void* gp[] = {g->dg_attn, g->q.dA, g->q.dB, g->k.dA, g->k.dB, g->v.dA, g->v.dB, g->o.dA, g->o.dB,
+                      g->dg_mlp, g->gate.dA, g->gate.dB, g->up.dA, g->up.dB, g->down.dA, g->down.dB};
+  for (const void* p : gp) LR_TRY(check_ptr(p, "block gradient"));
+  LR_TRY(check_ptr(x, "x"));
+  LR_TRY(check_ptr(saved, "saved"));
+  LR_TRY(check_ptr(dout, "dout"));
+  LR_TRY(check_ptr(dx, "dx"));
+  LR_TRY(check_ptr(ws, "ws"));
+  LR_TRY(check_size(saved_bytes, block_saved_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr), "saved"));
+  LR_TRY(check_size(ws_bytes, block_ws_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr), "ws"));
+  Ctx c;
+  LR_TRY(make_ctx(dt, stream, &c));
+  return block_bwd_impl(c, b, s, H, dh, f, ra, rm, eps, x, *w, saved, dout, dx, *g, ws);
 }
 
 size_t lr_btp_payload_floats(int T, int r, int group) {

@@ -124,6 +124,52 @@ def make_mlp_case(shape: MlpShape, seed: int = 0, with_grad: bool = True, device
     return c
 
 
+@dataclasses.dataclass(frozen=True)
+class BlockShape:
+    """One low-rank transformer block: b sequences of s tokens, H heads of dh (d = H*dh),
+    attention rank ra, MLP width f and rank rm; bf16."""
+    b: int
+    s: int
+    H: int
+    dh: int
+    f: int
+    ra: int
+    rm: int
+    eps: float = 1e-6
+
+    @property
+    def T(self) -> int:
+        return self.b * self.s
+
+    @property
+    def d(self) -> int:
+        return self.H * self.dh
+
+
+# LLaMA-7B-class widths (d 4096, f 11008) on 8 x 2048 tokens, ranks d/4.
+BLOCK_7B = BlockShape(b=8, s=2048, H=32, dh=128, f=11008, ra=1024, rm=1024)
+
+
+def make_block_case(shape: BlockShape, seed: int = 0, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """Host tensors for one transformer block (bf16): x, g_attn, A/B of q, k, v, o, g_mlp,
+    A/B of gate, up, down, and the upstream grad G."""
+    dt = torch.bfloat16
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    d = shape.d
+    c: Dict[str, torch.Tensor] = {}
+    c["x"] = _normal(gen, (shape.T, d), 1.0).to(dt)
+    c["g_attn"] = _normal(gen, (d,), 0.1, mean=1.0).to(dt)
+    for n in "qkvo":
+        c[f"A_{n}"], c[f"B_{n}"] = _pair(gen, shape.ra, d, d, dt)
+    c["g_mlp"] = _normal(gen, (d,), 0.1, mean=1.0).to(dt)
+    c["A_gate"], c["B_gate"] = _pair(gen, shape.rm, d, shape.f, dt)
+    c["A_up"], c["B_up"] = _pair(gen, shape.rm, d, shape.f, dt)
+    c["A_down"], c["B_down"] = _pair(gen, shape.rm, shape.f, d, dt)
+    c["G"] = _normal(gen, (shape.T, d), 1.0).to(dt)
+    return c
+
+
 def make_dense_case(shape: MlpShape, seed: int = 0, with_grad: bool = True, device: str = "cpu") -> Dict[str, torch.Tensor]:
     """Host tensors for the dense (full-rank) MLP block of the same d, f: x, g, W_gate, W_up [f, d],
     W_down [d, f] (N(0, 1/fan_in)) and upstream grad G.  shape.r is not used."""

@@ -32,6 +32,7 @@ EXPORTED = [
     "lr_proj_fwd_noalloc", "lr_dense_saved_bytes", "lr_dense_fwd_workspace_bytes", "lr_dense_bwd_workspace_bytes",
     "lr_dense_fwd", "lr_dense_bwd", "lr_btp_payload_floats", "lr_btp_workspace_bytes", "lr_btp_partial",
     "lr_btp_finish", "lr_attn_saved_bytes", "lr_attn_workspace_bytes", "lr_attn_fwd", "lr_attn_bwd",
+    "lr_block_saved_bytes", "lr_block_workspace_bytes", "lr_block_fwd", "lr_block_bwd",
 ]
 
 
@@ -47,6 +48,17 @@ class lr_pair(ctypes.Structure):
 
 class lr_pair_grad(ctypes.Structure):
     _fields_ = [("dA", ctypes.c_void_p), ("dB", ctypes.c_void_p)]
+
+
+class lr_block_weights(ctypes.Structure):
+    _fields_ = [("g_attn", ctypes.c_void_p), ("q", lr_pair), ("k", lr_pair), ("v", lr_pair), ("o", lr_pair),
+                ("g_mlp", ctypes.c_void_p), ("gate", lr_pair), ("up", lr_pair), ("down", lr_pair)]
+
+
+class lr_block_grads(ctypes.Structure):
+    _fields_ = [("dg_attn", ctypes.c_void_p), ("q", lr_pair_grad), ("k", lr_pair_grad), ("v", lr_pair_grad),
+                ("o", lr_pair_grad), ("dg_mlp", ctypes.c_void_p), ("gate", lr_pair_grad), ("up", lr_pair_grad),
+                ("down", lr_pair_grad)]
 
 
 _lib = None
@@ -76,6 +88,12 @@ _SIGS = {
     "lr_btp_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_btp_partial": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(lr_pair), _P, _P, _P, _P, _SZ, _P]),
     "lr_btp_finish": (_I, [_I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P]),
+    "lr_block_saved_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "lr_block_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "lr_block_fwd": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _F, _P, ctypes.POINTER(lr_block_weights), _P, _P, _SZ, _P,
+                          _SZ, _P]),
+    "lr_block_bwd": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _F, _P, ctypes.POINTER(lr_block_weights), _P, _SZ, _P, _P,
+                          ctypes.POINTER(lr_block_grads), _P, _SZ, _P]),
     "lr_attn_saved_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "lr_attn_fwd": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _SZ, _P, _SZ, _P]),
@@ -275,6 +293,25 @@ def lr_attn_fwd(dt, b, s, H, dh, scale, q, k, v, o, saved, ws, stream=None):
 def lr_attn_bwd(dt, b, s, H, dh, scale, q, k, v, o, saved, dout, dq, dk, dv, ws, stream=None):
     _check(lib().lr_attn_bwd(dt, b, s, H, dh, scale, _p(q), _p(k), _p(v), _p(o), _p(saved), _p(dout), _p(dq),
                              _p(dk), _p(dv), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def lr_block_saved_bytes(b, s, H, dh, f, ra, rm) -> int:
+    return lib().lr_block_saved_bytes(b, s, H, dh, f, ra, rm)
+
+
+def lr_block_workspace_bytes(b, s, H, dh, f, ra, rm) -> int:
+    return lib().lr_block_workspace_bytes(b, s, H, dh, f, ra, rm)
+
+
+def lr_block_fwd(dt, b, s, H, dh, f, ra, rm, eps, x, w: lr_block_weights, out, saved, ws, stream=None):
+    _check(lib().lr_block_fwd(dt, b, s, H, dh, f, ra, rm, eps, _p(x), ctypes.byref(w), _p(out), _p(saved),
+                              _nbytes(saved), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def lr_block_bwd(dt, b, s, H, dh, f, ra, rm, eps, x, w: lr_block_weights, saved, dout, dx, g: lr_block_grads, ws,
+                 stream=None):
+    _check(lib().lr_block_bwd(dt, b, s, H, dh, f, ra, rm, eps, _p(x), ctypes.byref(w), _p(saved), _nbytes(saved),
+                              _p(dout), _p(dx), ctypes.byref(g), _p(ws), _nbytes(ws), _stream(stream)))
 
 
 def lr_btp_payload_floats(T, r, group) -> int:

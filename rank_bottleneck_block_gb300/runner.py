@@ -312,3 +312,43 @@ class Attention:
     def step(self, stream=None):
         self.forward(stream)
         self.backward(None, stream)
+
+
+class TransformerBlock:
+    """One low-rank transformer block (q/k/v group, causal attention, o-projection with its
+    residual, MLP block in checkpoint mode) resident on the device, bf16."""
+
+    def __init__(self, shape, case: Dict[str, torch.Tensor], device="cuda"):
+        self.sh = shape
+        self.t = {k: v.to(device).contiguous() for k, v in case.items()}
+        t = self.t
+        self.w = L.lr_block_weights(
+            L._p(t["g_attn"]), *(L.pair(t[f"A_{n}"], t[f"B_{n}"]) for n in "qkvo"), L._p(t["g_mlp"]),
+            *(L.pair(t[f"A_{n}"], t[f"B_{n}"]) for n in ("gate", "up", "down")))
+        self.grads = {}
+        for n in ("q", "k", "v", "o", "gate", "up", "down"):
+            self.grads[f"dA_{n}"] = torch.empty(t[f"A_{n}"].shape, dtype=torch.float32, device=device)
+            self.grads[f"dB_{n}"] = torch.empty(t[f"B_{n}"].shape, dtype=torch.float32, device=device)
+        self.dg_attn = torch.empty(shape.d, dtype=torch.float32, device=device)
+        self.dg_mlp = torch.empty(shape.d, dtype=torch.float32, device=device)
+        gr = self.grads
+        self.g = L.lr_block_grads(
+            L._p(self.dg_attn), *(L.pair_grad(gr[f"dA_{n}"], gr[f"dB_{n}"]) for n in "qkvo"), L._p(self.dg_mlp),
+            *(L.pair_grad(gr[f"dA_{n}"], gr[f"dB_{n}"]) for n in ("gate", "up", "down")))
+        dims = (shape.b, shape.s, shape.H, shape.dh, shape.f, shape.ra, shape.rm)
+        self.dims = dims
+        self.out = torch.empty_like(t["x"])
+        self.dx = torch.empty_like(t["x"])
+        self.saved = _buf(L.lr_block_saved_bytes(*dims), device)
+        self.ws = _buf(L.lr_block_workspace_bytes(*dims), device)
+
+    def forward(self, stream=None):
+        L.lr_block_fwd(L.LR_BF16, *self.dims, self.sh.eps, self.t["x"], self.w, self.out, self.saved, self.ws, stream)
+
+    def backward(self, stream=None):
+        L.lr_block_bwd(L.LR_BF16, *self.dims, self.sh.eps, self.t["x"], self.w, self.saved, self.t["G"], self.dx,
+                       self.g, self.ws, stream)
+
+    def step(self, stream=None):
+        self.forward(stream)
+        self.backward(stream)

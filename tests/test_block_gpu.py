@@ -1,0 +1,90 @@
+"""Parity of the low-rank transformer block (through the C ABI) with the fp64 oracle.
+
+The block chains the q/k/v group, causal attention, the o-projection with its residual and
+the MLP block; the oracle chains its own pieces (pinned on their own and, composed, by finite
+differences).  Metric: per-tensor max-relative error, bound 2e-2 (bf16 storage).  At full
+width the oracle runs on whole sequences: each sequence's outputs and input gradient depend
+only on that sequence.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention_oracle as A
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from rank_bottleneck_block_gb300 import build
+
+    build.build()
+    from rank_bottleneck_block_gb300 import lowrank as L
+
+    L.lib()
+    yield
+
+
+def _maxrel(gpu, ref):
+    g = gpu.float().cpu().double().numpy()
+    assert np.all(np.isfinite(g))
+    return float(np.max(np.abs(g - ref)) / np.max(np.abs(ref)))
+
+
+def _run(shape, seed):
+    from rank_bottleneck_block_gb300 import inputs as I
+    from rank_bottleneck_block_gb300 import lowrank as L
+    from rank_bottleneck_block_gb300.runner import TransformerBlock
+
+    case = I.make_block_case(shape, seed)
+    blk = TransformerBlock(shape, case)
+    blk.forward()
+    blk.backward()
+    torch.cuda.synchronize()
+    L.lr_check_device_error()
+    return case, blk
+
+
+def _oracle(case, shape, rows=None):
+    W = {k: v.double().numpy() for k, v in case.items() if k not in ("x", "G")}
+    x, G = case["x"].double().numpy(), case["G"].double().numpy()
+    b = shape.b
+    if rows is not None:
+        x, G, b = x[rows], G[rows], 1
+    scale = shape.dh ** -0.5
+    out, saved = A.block_fwd(x, W, b, shape.s, shape.H, shape.dh, scale, shape.eps)
+    return out, A.block_bwd(W, saved, G, b, shape.s, shape.H, shape.dh, scale, shape.eps)
+
+
+@pytest.mark.parametrize("dims", [(2, 256, 2, 128, 344, 32, 48), (1, 512, 3, 128, 264, 24, 40)])
+def test_block_matches_oracle(dims):
+    from rank_bottleneck_block_gb300 import inputs as I
+
+    shape = I.BlockShape(*dims)
+    case, blk = _run(shape, seed=sum(dims))
+    out, gr = _oracle(case, shape)
+    errs = {"out": _maxrel(blk.out, out), "dx": _maxrel(blk.dx, gr["dx"]),
+            "dg_attn": _maxrel(blk.dg_attn, gr["dg_attn"]), "dg_mlp": _maxrel(blk.dg_mlp, gr["dg_mlp"])}
+    for n in ("q", "k", "v", "o", "gate", "up", "down"):
+        for m in ("A", "B"):
+            errs[f"d{m}_{n}"] = _maxrel(blk.grads[f"d{m}_{n}"], gr[f"d{m}_{n}"])
+    bad = {k: v for k, v in errs.items() if not v <= TOL}
+    assert not bad, errs
+
+
+@pytest.mark.slow
+def test_block_full_width_sampled_sequences():
+    """d 4096 (32 heads of 128), f 11008, ranks 1024, 8 sequences of 2048 tokens: out and dx of
+    the first and the last sequence against the oracle run on that sequence alone."""
+    from rank_bottleneck_block_gb300 import inputs as I
+
+    shape = I.BLOCK_7B
+    case, blk = _run(shape, seed=0)
+    for bi in (0, shape.b - 1):
+        rows = slice(bi * shape.s, (bi + 1) * shape.s)
+        out, gr = _oracle(case, shape, rows)
+        errs = {"out": _maxrel(blk.out[rows], out), "dx": _maxrel(blk.dx[rows], gr["dx"])}
+        assert all(e <= TOL for e in errs.values()), (bi, errs)
