@@ -398,7 +398,7 @@ def _roofline(flops, nbytes, ms, pk):
 
 
 def run_other(a):
-    """Non-default workloads (one JSON line each): attn_proj, stack, sweep, dense."""
+    """Non-default workloads (one JSON line each): attn_proj, stack, sweep, dense, block."""
     import torch
 
     from rank_bottleneck_block_gb300 import build as B
@@ -406,7 +406,8 @@ def run_other(a):
     B.build()
     from rank_bottleneck_block_gb300 import inputs as I
     from rank_bottleneck_block_gb300 import lowrank as L
-    from rank_bottleneck_block_gb300.runner import BlockStack, DenseBlock, GraphStep, MlpBlock, ProjGroup
+    from rank_bottleneck_block_gb300.runner import (BlockStack, DenseBlock, GraphStep, MlpBlock, ProjGroup,
+                                                     TransformerBlock)
 
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
@@ -475,6 +476,33 @@ def run_other(a):
                         "params": 3 * d * f, **_roofline(fl_dn, nb_dn, ms_dn, pk)}
         res["lowrank_speedup"] = round(ms_dn / ms_lr, 3)
         print(json.dumps(res), flush=True)
+    elif a.workload == "block":
+        # The full low-rank transformer block at LLaMA-7B widths: q/k/v group, causal attention,
+        # o-projection with residual, checkpointed MLP block; fwd+bwd.
+        shape = I.BLOCK_7B
+        T, d, f, ra, rm = shape.T, shape.d, shape.f, shape.ra, shape.rm
+        blk = TransformerBlock(shape, I.make_block_case(shape, seed=0, device="cuda"), device=dev)
+        ms = _time_steps(blk.step, a.steps, a.warmup, flush, stream)
+        L.lr_check_device_error()
+        kernels = _kernel_table(blk.step, flush, stream)
+
+        def pair(din, dout, r):  # one pair's forward FLOPs
+            return 2.0 * T * r * (din + dout)
+
+        proj = 4 * pair(d, d, ra)  # q, k, v, o
+        mlp = 2 * pair(d, f, rm) + pair(f, d, rm)
+        causal = 2.0 * shape.b * shape.H * shape.s * shape.s * shape.dh  # QK^T and PV over the causal half
+        flops = 3 * (proj + mlp) + 2.0 * 2 * T * rm * f + causal * (1 + 2.5)  # bwd 2x; MLP re-forward
+        params = 4 * 2 * d * ra + 2 * (d + f) * rm + (f + d) * rm
+        nbytes = 4.0 * T * d * 2 + params * (2 + 4) + 2.0 * T * (3 * ra + 3 * rm + 8 * d) * 2
+        res = {"workload": f"low-rank transformer block fwd+bwd (q/k/v group, causal attention, o-projection + "
+                           f"residual, checkpointed SwiGLU MLP), b={shape.b} s={shape.s} H={shape.H} dh={shape.dh} "
+                           f"d={d} f={f} ranks {ra}/{rm}, bf16",
+               "ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "params": params,
+               "flops_note": "algorithmic: attention counted over the causal half (its kernels compute the "
+                             "full s x s products and discard the masked half)",
+               **_roofline(flops, nbytes, ms, pk), "kernels": kernels}
+        print(json.dumps(res), flush=True)
     elif a.workload == "sweep":
         rows = []
         for shp in I.sweep_shapes():
@@ -536,7 +564,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["mlp_block", "attn_proj", "stack", "sweep", "dense"], default="mlp_block",
+    ap.add_argument("--workload", choices=["mlp_block", "attn_proj", "stack", "sweep", "dense", "block"],
+                    default="mlp_block",
                     help="mlp_block is the benchmark line; the others print their own measurement lines")
     a = ap.parse_args(argv)
     if a.warmup < 3:
