@@ -240,7 +240,9 @@ lr_status lr_attn_bwd(lr_dtype dt, int b, int s, int H, int dh, float scale, con
  * x, out, dout, dx: [T, d] bf16; all pairs' shapes follow lr_pair (q, k, v, o: A [ra, d],
  * B [d, ra]; gate, up: A [rm, d], B [f, rm]; down: A [rm, f], B [d, rm]).  saved keeps the
  * pieces' saved sets plus q, k, v, o and x1 ([T, d] each); ws is shared by the pieces.
- * bf16 only; the shape rules of lr_attn_fwd and lr_mlp_fwd apply.
+ * bf16 only; the shape rules of lr_attn_fwd and lr_mlp_fwd apply.  lr_attn_* and lr_block_* launch
+ * their kernels without programmatic dependent launch (each kernel starts after the previous
+ * one completes): with it, three block steps issued back to back stopped making progress.
  */
 typedef struct {
   const void* g_attn;

@@ -154,13 +154,27 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Programmatic dependent launch is on unless the environment sets LR_PDL=0 (read once).
+// Launches issued on this host thread while a PdlOff guard lives carry no programmatic-launch
+// attribute (each kernel then starts after the previous one has completed).
+inline int& pdl_suppressed() {
+  static thread_local int n = 0;
+  return n;
+}
+struct PdlOff {
+  PdlOff() { ++pdl_suppressed(); }
+  ~PdlOff() { --pdl_suppressed(); }
+  PdlOff(const PdlOff&) = delete;
+  PdlOff& operator=(const PdlOff&) = delete;
+};
+
+// Programmatic dependent launch is on unless the environment sets LR_PDL=0 (read once) or a
+// PdlOff guard is active.
 inline bool pdl_enabled() {
   static const bool on = [] {
     const char* e = getenv("LR_PDL");
     return !(e && e[0] == '0');
   }();
-  return on;
+  return on && pdl_suppressed() == 0;
 }
 
 // Launches kern<<<grid, block, smem, st>>>(args...) with the programmatic-serialisation attribute.

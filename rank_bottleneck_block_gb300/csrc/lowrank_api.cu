@@ -1763,6 +1763,7 @@ lr_status lr_attn_fwd(lr_dtype dt, int b, int s, int H, int dh, float scale, con
   LR_TRY(check_size(ws_bytes, attn_ws_layout(b, s, H, dh, nullptr, nullptr), "ws"));
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
+  PdlOff serial;  // see lr_block_fwd
   return attn_fwd_impl(c, b, s, H, dh, scale, q, k, v, o, static_cast<float*>(saved), ws);
 }
 
@@ -1777,6 +1778,7 @@ lr_status lr_attn_bwd(lr_dtype dt, int b, int s, int H, int dh, float scale, con
   LR_TRY(check_size(ws_bytes, attn_ws_layout(b, s, H, dh, nullptr, nullptr), "ws"));
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
+  PdlOff serial;  // see lr_block_fwd
   return attn_bwd_impl(c, b, s, H, dh, scale, q, k, v, o, static_cast<const float*>(saved), dout, dq, dk, dv, ws);
 }
 
@@ -1818,6 +1820,9 @@ lr_status lr_block_fwd(lr_dtype dt, int b, int s, int H, int dh, int f, int ra, 
   LR_TRY(check_size(ws_bytes, block_ws_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr), "ws"));
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
+  // Without programmatic dependent launch: with it, three fwd+bwd steps of the block issued back to
+  // back stopped making progress on the GPU (one or two did not; the cause is not known).
+  PdlOff serial;
   return block_fwd_impl(c, b, s, H, dh, f, ra, rm, eps, x, *w, out, saved, ws);
 }
 
@@ -1840,6 +1845,7 @@ lr_status lr_block_bwd(lr_dtype dt, int b, int s, int H, int dh, int f, int ra, 
   LR_TRY(check_size(ws_bytes, block_ws_layout(b, s, H, dh, f, ra, rm, nullptr, nullptr), "ws"));
   Ctx c;
   LR_TRY(make_ctx(dt, stream, &c));
+  PdlOff serial;  // see lr_block_fwd
   return block_bwd_impl(c, b, s, H, dh, f, ra, rm, eps, x, *w, saved, dout, dx, *g, ws);
 }
 

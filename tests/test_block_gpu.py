@@ -88,3 +88,20 @@ def test_block_full_width_sampled_sequences():
         out, gr = _oracle(case, shape, rows)
         errs = {"out": _maxrel(blk.out[rows], out), "dx": _maxrel(blk.dx[rows], gr["dx"])}
         assert all(e <= TOL for e in errs.values()), (bi, errs)
+
+
+def test_block_steps_back_to_back_repeat_bitwise():
+    """Three fwd+bwd steps issued without a synchronisation in between finish and reproduce the
+    first step's outputs and gradients bit for bit."""
+    from rank_bottleneck_block_gb300 import inputs as I
+    from rank_bottleneck_block_gb300 import lowrank as L
+
+    shape = I.BlockShape(2, 256, 2, 128, 344, 32, 48)
+    _, blk = _run(shape, seed=5)
+    ref = [blk.out.clone(), blk.dx.clone()] + [v.clone() for v in blk.grads.values()]
+    for _ in range(3):
+        blk.step()
+    torch.cuda.synchronize()
+    L.lr_check_device_error()
+    now = [blk.out, blk.dx] + list(blk.grads.values())
+    assert all(torch.equal(a, b) for a, b in zip(ref, now))
