@@ -36,8 +36,8 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * ((45.186816e6 + 133.404672e6) + (55.457024e6 + 499.862528e6)),
-                          "sources_sha256": "beae1a139ec02e82195cb511ebc74a411654c199a9fb264545145f38a842a84a",
+    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * ((45.187072e6 + 132.815872e6) + (68.370432e6 + 499.517696e6)),
+                          "sources_sha256": "0396ba8456ff9ea4d467866be4d1e0d92c49e3fc79ac4364b4a05b3f64ed853b",
                           "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
 }
 
