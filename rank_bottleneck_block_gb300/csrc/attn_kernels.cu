@@ -6,6 +6,9 @@ namespace lr {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+// Rows of the pair tiles of the attention GEMMs: P and dS are written up to the end of the row's
+// tile of keys (the GEMMs that read them stop their K range there or start it at the tile).
+constexpr int kTileRows = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // One thread per 8 consecutive channels of one head of one token.
@@ -70,7 +73,8 @@ __global__ void attn_softmax_fwd_kernel(const float* S, int R, int s, float scal
   const float lse2 = m + log2f(l);
   if (lane == 0) lse[r] = lse2 * kLn2;
   bf16* prow = P + 1LL * r * s;
-  for (int j = lane * 4; j < s; j += 128) {
+  const int wend = min(s, ((n - 1) / kTileRows + 1) * kTileRows);  // zeros past n up to the tile end
+  for (int j = lane * 4; j < wend; j += 128) {
     float p[4] = {0.f, 0.f, 0.f, 0.f};
     if (j < n) {
       const float4 v = *reinterpret_cast<const float4*>(row + j);
@@ -114,7 +118,8 @@ __global__ void attn_softmax_bwd_kernel(const float* S, const float* dP, const f
   const float lse2 = lse[r] * kLog2e;
   const float d = D[r];
   const long long base = 1LL * r * s;
-  for (int j = lane * 4; j < s; j += 128) {
+  const int wend = min(s, ((n - 1) / kTileRows + 1) * kTileRows);
+  for (int j = lane * 4; j < wend; j += 128) {
     float p[4] = {0.f, 0.f, 0.f, 0.f}, g[4] = {0.f, 0.f, 0.f, 0.f};
     if (j < n) {
       const float4 v = *reinterpret_cast<const float4*>(S + base + j);

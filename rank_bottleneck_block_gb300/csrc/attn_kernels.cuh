@@ -17,15 +17,17 @@ namespace lr {
 cudaError_t launch_head_permute(const bf16* src, bf16* dst, int b, int s, int H, int dh, int to_heads,
                                 cudaStream_t st);
 
-// Row r of S [R, s] fp32 (R = heads * s; query i = r mod s) -> P [R, s] bf16 with
-// P_rj = exp(scale S_rj - lse_r) for j <= i and 0 for j > i, and lse_r = log sum_{j<=i} exp(scale S_rj).
+// Row r of S [R, s] fp32 (R = heads * s; query i = r mod s; only j <= i is read) -> P [R, s] bf16
+// with P_rj = exp(scale S_rj - lse_r) for j <= i and 0 for i < j < the end of i's 256-row tile
+// (columns past it are not written), and lse_r = log sum_{j<=i} exp(scale S_rj).
 cudaError_t launch_attn_softmax_fwd(const float* S, int R, int s, float scale, bf16* P, float* lse,
                                     cudaStream_t st);
 
 // D_r = sum_c dO[r, c] O[r, c] over the dh columns of head-major rows.
 cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int R, int dh, float* D, cudaStream_t st);
 
-// P_rj as in the forward (from S and lse) and dS_rj = scale P_rj (dP_rj - D_r), both bf16.
+// P_rj as in the forward (from S and lse) and dS_rj = scale P_rj (dP_rj - D_r), both bf16, written
+// over the same columns as the forward writes P.
 cudaError_t launch_attn_softmax_bwd(const float* S, const float* dP, const float* lse, const float* D, int R, int s,
                                     float scale, bf16* P, bf16* dS, cudaStream_t st);
 

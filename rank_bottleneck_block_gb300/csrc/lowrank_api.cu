@@ -1121,8 +1121,9 @@ static size_t attn_ws_layout(int b, int s, int H, int dh, void* base, AttnWs* W)
 
 // One GEMM over all heads: batch n = head n; A, B, out start n*s stored rows in.
 static lr_status attn_gemm(const Ctx& c, EpiKind k, int M, int N, int K, int heads, int s, Operand A, bool a_mn,
-                           Operand B, bool b_mn, void* out, long long ldo) {
+                           Operand B, bool b_mn, void* out, long long ldo, int causal) {
   GemmCall g = new_call(M, N, K);
+  g.causal = causal;
   g.a_mn = a_mn;
   g.b_mn = b_mn;
   g.batches = heads;
@@ -1155,14 +1156,14 @@ static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   LR_TRY(head_permute(c, k, W.kh, b, s, H, dh, 1));
   LR_TRY(head_permute(c, v, W.vh, b, s, H, dh, 1));
   // S = Q K^T (fp32), both operands K-major (K = dh)
-  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s));
+  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s, 1));
   {
     LaunchScope scope("attn_softmax", c.st, 0, 6.0 * R * s);
     cudaError_t e = launch_attn_softmax_fwd(W.S, R, s, scale, W.P, lse, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention softmax: %s", cudaGetErrorString(e));
   }
   // O = P V: P K-major (K = keys), V read MN-major in its stored [keys, dh] layout
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, false, {W.vh, dh}, true, W.oh, dh));
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, false, {W.vh, dh}, true, W.oh, dh, 2));
   return head_permute(c, W.oh, o, b, s, H, dh, 0);
 }
 
@@ -1183,17 +1184,17 @@ static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention row dot: %s", cudaGetErrorString(e));
   }
   // S = Q K^T again (only its log-sum-exp was kept), dP = dO V^T
-  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s));
-  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.doh, dh}, false, {W.vh, dh}, false, W.dP, s));
+  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s, 1));
+  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.doh, dh}, false, {W.vh, dh}, false, W.dP, s, 1));
   {
     LaunchScope scope("attn_softmax_bwd", c.st, 0, 12.0 * R * s);
     cudaError_t e = launch_attn_softmax_bwd(W.S, W.dP, lse, W.D, R, s, scale, W.P, W.dS, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention softmax backward: %s", cudaGetErrorString(e));
   }
   // dV = P^T dO (P read MN-major: keys index its columns), dQ = dS K, dK = dS^T Q (dS holds scale)
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, true, {W.doh, dh}, true, W.dvh, dh));
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, false, {W.kh, dh}, true, W.dqh, dh));
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, true, {W.qh, dh}, true, W.dkh, dh));
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, true, {W.doh, dh}, true, W.dvh, dh, 3));
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, false, {W.kh, dh}, true, W.dqh, dh, 2));
+  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, true, {W.qh, dh}, true, W.dkh, dh, 3));
   LR_TRY(head_permute(c, W.dqh, dq, b, s, H, dh, 0));
   LR_TRY(head_permute(c, W.dkh, dk, b, s, H, dh, 0));
   return head_permute(c, W.dvh, dv, b, s, H, dh, 0);

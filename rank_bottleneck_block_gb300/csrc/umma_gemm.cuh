@@ -84,6 +84,7 @@ struct Shape {
   int g_tiles;               // pair tiles of all batches
   int rowbatch;              // batches offset into one tensor each (see GemmCall::rowbatch), then:
   int rb_a, rb_b, rb_o;      // stored rows per batch of A, B and the output
+  int causal;                // causal use of a row-batched problem (see GemmCall::causal), else 0
   unsigned* err;
 };
 
@@ -391,6 +392,16 @@ struct Config {
 };
 
 // Pair-tile index -> (split, batch, this CTA's m-tile, n-tile); n runs fastest.
+// K blocks of the tile in CTA row block mb (split range, narrowed by a causal mask: mode 2 drops keys
+// past the pair tile's last query, mode 3 queries before its first key).
+__device__ __forceinline__ void k_range(const Shape& sh, int split, int mb, int& kb0, int& kb1) {
+  kb0 = split * sh.kb_per_split;
+  kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
+  const int row0 = (mb >> 1) * 2 * BM;  // first row of the pair tile
+  if (sh.causal == 2) kb1 = min(kb1, (row0 + 2 * BM) / BK);
+  if (sh.causal == 3) kb0 = max(kb0, row0 / BK);
+}
+
 __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
                                             int& nb) {
   if (sh.grouped) {
@@ -508,8 +519,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       for (int tile = cid; tile < total && ok; tile += ncl) {
         int split, batch, mb, nb;
         decode_tile(sh, tile, rank, split, batch, mb, nb);
-        const int kb0 = split * sh.kb_per_split;
-        const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
+        int kb0, kb1;
+        k_range(sh, split, mb, kb0, kb1);
         const int m0 = mb * BM, n0 = nb * BN;
         const int set0 = sh.rowbatch ? 0 : batch;
         const int ra = batch * sh.rb_a, rbb = batch * sh.rb_b;  // row-batched offsets (else 0)
@@ -574,8 +585,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
         int split, batch, mb, nb;
         decode_tile(sh, tile, rank, split, batch, mb, nb);
-        const int kb0 = split * sh.kb_per_split;
-        const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
+        int kb0, kb1;
+        k_range(sh, split, mb, kb0, kb1);
         const int buf = C::NBUF == 2 ? (it & 1) : 0;
         const uint32_t tph = static_cast<uint32_t>(C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1));
         if (!C::SPLIT) {
@@ -641,8 +652,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
       decode_tile(sh, tile, rank, split, batch, mb, nb);
-      const int kb0 = split * sh.kb_per_split;
-      const int kb1 = min(sh.kb_total, kb0 + sh.kb_per_split);
+      int kb0, kb1;
+      k_range(sh, split, mb, kb0, kb1);
       float ss = 0.f;
       for (int kb = kb0; kb < kb1; ++kb) {
         // The MMAs have read the stage of both CTAs (so it has landed); it is refilled only
@@ -752,6 +763,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       const int m = mb * BM + row;
       const int ob = sh.rowbatch ? 0 : batch;                 // output maps and pointers of this batch
       const int r0 = mb * BM + q * ER + batch * sh.rb_o;  // first stored row of this warp's boxes
+      // Causal mode 1: a tile wholly above the diagonal (every column past every row) is not stored.
+      const bool no_store = sh.causal == 1 && nb * BN >= (mb >> 1) * 2 * BM + 2 * BM;
       RowIn ri;
       if constexpr (C::STATS) {
         ri.k = 0.f;
@@ -869,8 +882,10 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         ok = mbar_wait(&tfull[buf], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         tc_fence_after();
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::ACC_COLS;
+        // A tile that is not stored (causal mode 1: wholly above the diagonal) skips the chunk work;
+        // such launches have no operand tiles, so only this warp's output-set rotation shifts.
 #pragma unroll 1
-        for (int c = g; c < NCH; c += 2, ++qi) {
+        for (int c = no_store ? NCH : g; c < NCH; c += 2, ++qi) {
           const int b = qi % NO;  // output set
           const int ba = NA > 0 ? qi % NA : 0;  // operand set
           if constexpr (NAUX > 0) {
@@ -932,7 +947,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           }
           fence_async_smem();
           __syncwarp();
-          if (leader) {
+          if (leader && !no_store) {
 #pragma unroll
             for (int oi = 0; oi < NOUT; ++oi) {
               if (!present[oi]) continue;

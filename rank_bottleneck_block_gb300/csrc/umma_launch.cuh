@@ -102,7 +102,9 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
     sh.rb_a = g.rb_a;
     sh.rb_b = g.rb_b;
     sh.rb_o = g.rb_o;
+    sh.causal = g.causal;
   }
+  if (g.causal && (!g.rowbatch || g.causal > 3 || g.M % (2 * BM))) return cudaErrorInvalidValue;
   sh.grouped = 0;
   if (g.grouped) {  // batches of their own M, N; one split only
     if (K != EPI_F32 || sh.ksplit != 1 || g.batches < 1 || g.batches > kMaxBatch) return cudaErrorInvalidValue;
