@@ -106,3 +106,17 @@ def test_attention_shape_rules(L):
     assert lib.lr_attn_fwd(L.LR_F32, 1, 256, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 8
     assert lib.lr_attn_fwd(L.LR_BF16, 1, 100, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 2
     assert lib.lr_attn_fwd(L.LR_BF16, 1, 256, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 1
+
+
+def test_block_shape_rules(L):
+    dims = (1, 256, 2, 128, 344, 32, 48)
+    assert L.lr_block_saved_bytes(*dims) > 4 * 256 * 256 * 2  # q, k, v, o at least
+    assert L.lr_block_workspace_bytes(*dims) >= L.lr_attn_workspace_bytes(1, 256, 2, 128)
+    assert L.lr_block_saved_bytes(1, 200, 2, 128, 344, 32, 48) == 0  # s not a multiple of 256
+    assert L.lr_block_saved_bytes(1, 256, 2, 128, 343, 32, 48) == 0  # f not a multiple of 8
+    lib = L.lib()
+    w, g = L.lr_block_weights(), L.lr_block_grads()
+    assert lib.lr_block_fwd(L.LR_F32, *dims, 1e-6, None, ctypes.byref(w), None, None, 0, None, 0, None) == 8
+    assert lib.lr_block_fwd(L.LR_BF16, *dims, 1e-6, None, ctypes.byref(w), None, None, 0, None, 0, None) == 1
+    assert lib.lr_block_bwd(L.LR_BF16, *dims, 1e-6, None, ctypes.byref(w), None, 0, None, None, ctypes.byref(g),
+                            None, 0, None) == 1
