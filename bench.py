@@ -500,7 +500,7 @@ def run_other(a):
                            f"d={d} f={f} ranks {ra}/{rm}, bf16",
                "ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "params": params,
                "flops_note": "algorithmic: attention counted over the causal half (its kernels compute the "
-                             "full s x s products and discard the masked half)",
+                             "256 x 256 tiles on or below the diagonal; the per-kernel figures count those)",
                **_roofline(flops, nbytes, ms, pk), "kernels": kernels}
         print(json.dumps(res), flush=True)
     elif a.workload == "sweep":

@@ -106,38 +106,6 @@ __global__ void attn_rowdot_kernel(const bf16* dO, const bf16* O, int R, int dh,
   if (lane == 0) D[r] = acc;
 }
 
-__global__ void attn_softmax_bwd_kernel(const float* S, const float* dP, const float* lse, const float* D, int R,
-                                        int s, float scale, bf16* P, bf16* dS) {
-  pdl_wait();
-  pdl_trigger();
-  const int r = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= R) return;
-  const int n = r % s + 1;
-  const float c = scale * kLog2e;
-  const float lse2 = lse[r] * kLog2e;
-  const float d = D[r];
-  const long long base = 1LL * r * s;
-  const int wend = min(s, ((n - 1) / kTileRows + 1) * kTileRows);
-  for (int j = lane * 4; j < wend; j += 128) {
-    float p[4] = {0.f, 0.f, 0.f, 0.f}, g[4] = {0.f, 0.f, 0.f, 0.f};
-    if (j < n) {
-      const float4 v = *reinterpret_cast<const float4*>(S + base + j);
-      const float4 w = *reinterpret_cast<const float4*>(dP + base + j);
-      const float x[4] = {v.x, v.y, v.z, v.w}, y[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (j + t < n) {
-          p[t] = exp2f(x[t] * c - lse2);
-          g[t] = scale * p[t] * (y[t] - d);
-        }
-      }
-    }
-    store_bf16x4(P + base + j, p[0], p[1], p[2], p[3]);
-    store_bf16x4(dS + base + j, g[0], g[1], g[2], g[3]);
-  }
-}
-
 dim3 warp_rows_grid(int R) { return dim3(static_cast<unsigned>((R + 7) / 8)); }
 
 }  // namespace
@@ -161,13 +129,6 @@ cudaError_t launch_attn_softmax_fwd(const float* S, int R, int s, float scale, b
 cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int R, int dh, float* D, cudaStream_t st) {
   if (R == 0) return cudaSuccess;
   return launch_pdl(attn_rowdot_kernel, warp_rows_grid(R), dim3(256), 0, st, dO, O, R, dh, D);
-}
-
-cudaError_t launch_attn_softmax_bwd(const float* S, const float* dP, const float* lse, const float* D, int R, int s,
-                                    float scale, bf16* P, bf16* dS, cudaStream_t st) {
-  if (R == 0) return cudaSuccess;
-  return launch_pdl(attn_softmax_bwd_kernel, warp_rows_grid(R), dim3(256), 0, st, S, dP, lse, D, R, s, scale, P,
-                    dS);
 }
 
 }  // namespace lr

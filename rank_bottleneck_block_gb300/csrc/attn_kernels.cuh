@@ -1,9 +1,10 @@
 // Row kernels of causal multi-head attention between the low-rank projections (bf16
-// storage, fp32 arithmetic).  The two GEMMs of each pass run on the tcgen05 engine in
-// row-batched mode over head-major tensors; these kernels move heads between the
-// token-major layout the projections use ([b*s, H*dh], head h of token t in columns
-// h*dh .. h*dh + dh - 1) and the head-major one ([b*H*s, dh], head (bi, h) in rows
-// (bi*H + h)*s .. + s - 1), and do the softmax parts.
+// storage, fp32 arithmetic).  The GEMMs run on the tcgen05 engine in row-batched mode over
+// head-major tensors (the backward's P and dS come out of one dual-accumulator GEMM's
+// epilogue); these kernels move heads between the token-major layout the projections use
+// ([b*s, H*dh], head h of token t in columns h*dh .. h*dh + dh - 1) and the head-major one
+// ([b*H*s, dh], head (bi, h) in rows (bi*H + h)*s .. + s - 1), and do the forward softmax
+// and the backward's row dot D = rowsum(dO * O).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -25,10 +26,5 @@ cudaError_t launch_attn_softmax_fwd(const float* S, int R, int s, float scale, b
 
 // D_r = sum_c dO[r, c] O[r, c] over the dh columns of head-major rows.
 cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int R, int dh, float* D, cudaStream_t st);
-
-// P_rj as in the forward (from S and lse) and dS_rj = scale P_rj (dP_rj - D_r), both bf16, written
-// over the same columns as the forward writes P.
-cudaError_t launch_attn_softmax_bwd(const float* S, const float* dP, const float* lse, const float* D, int R, int s,
-                                    float scale, bf16* P, bf16* dS, cudaStream_t st);
 
 }  // namespace lr

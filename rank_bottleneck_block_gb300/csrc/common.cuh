@@ -39,7 +39,10 @@ enum EpiKind : int {
                             //        rowpart = sum (da a + db b)
   EPI_F32_SS = 12,          // fp32 out0 = acc (no split); the row sums of squares of the A tiles (raw,
                             //   not 1/rms) -> rowscale_out: the partial of a row-parallel normed GEMM
-  EPI_COUNT = 13
+  EPI_ATTN_BWD = 13,        // causal attention backward scores, row-batched over heads: acc0 = Q K^T,
+                            //   acc1 = dO V^T; out0 = P = exp(coef acc0 - lse) (0 past the diagonal),
+                            //   out1 = dS = coef P (acc1 - D); lse = rowscale, D = rowpart_in (global rows)
+  EPI_COUNT = 14
 };
 
 constexpr int kMaxBatch = 4;

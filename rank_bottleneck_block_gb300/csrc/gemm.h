@@ -48,8 +48,8 @@ struct GemmCall {
   int rb_a, rb_b, rb_o;
   long long rows_a, rows_b, rows_o;
   // Causal masking of a row-batched attention GEMM over s positions (rows and columns or K index
-  // positions, whole pair tiles of 256): 1 = rows are queries and columns keys, tiles wholly above
-  // the diagonal are not stored; 2 = rows are queries and K keys, K stops after the tile's last row;
+  // positions, whole pair tiles of 256): 1 = rows are queries and columns keys (M = N), only the
+  // tiles on or below the diagonal are scheduled; 2 = rows are queries and K keys, K stops after the tile's last row;
   // 3 = rows are keys and K queries, K starts at the tile's first row.  0: none.
   int causal;
 };

@@ -1,6 +1,6 @@
-// tcgen05 GEMM instantiations used by causal attention on row-batched heads: S = Q K^T and
-// dP = dO V^T with fp32 output (both operands K-major), dK = dS^T Q and dV = P^T dO (both
-// operands MN-major).
+// tcgen05 GEMM instantiations used by causal attention on row-batched heads: S = Q K^T with fp32
+// output (both operands K-major), O = P V, dK = dS^T Q and dV = P^T dO (MN-major operands), and
+// the backward's dual-accumulator scores kernel (S = Q K^T and dP = dO V^T of one tile, out P and dS).
 #include "umma_launch.cuh"
 
 namespace lr {
@@ -10,5 +10,6 @@ LR_INST(EPI_F32, 128, false, false)
 LR_INST(EPI_F32, 256, false, false)
 LR_INST(EPI_STORE, 128, true, true)
 LR_INST(EPI_STORE, 256, true, true)
+LR_INST(EPI_ATTN_BWD, 256, false, false)
 #undef LR_INST
 }  // namespace lr

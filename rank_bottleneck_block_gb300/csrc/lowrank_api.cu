@@ -212,6 +212,9 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
     case EPI_DX_NORM: if (km) return umma_bn<EPI_DX_NORM, false, true>(g, st); break;
+    case EPI_ATTN_BWD:
+      if (kk && g.nacc == 2 && g.rowbatch) return launch_umma<EPI_ATTN_BWD, 256, false, false>(g, st);
+      break;
     case EPI_F32:
       if (mm) return umma_bn<EPI_F32, true, true>(g, st);
       if (kk) return umma_bn<EPI_F32, false, false>(g, st);
@@ -243,7 +246,7 @@ static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
 static const char* epi_name(EpiKind k) {
   static const char* names[] = {"norm_silu", "silu",       "store",  "resid",       "swiglu",        "dsilu",
                                 "dsilu_norm", "swiglu_bwd", "dx_norm", "f32", "norm_swiglu", "swiglu_bwd_norm",
-                                "f32_ss"};
+                                "f32_ss", "attn_bwd"};
   return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
 }
 
@@ -257,7 +260,7 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   g.ep.act = c.act;
   if (c.dt == LR_BF16) {
     if (k == EPI_SWIGLU) g.bn = kSwigluBn;
-    else if (k == EPI_NORM_SWIGLU) g.bn = 256;  // the split-phase dual-accumulator kernel
+    else if (k == EPI_NORM_SWIGLU || k == EPI_ATTN_BWD) g.bn = 256;  // split-phase dual-accumulator kernels
     else if (g.bn != 128 && g.bn != 256) g.bn = pick_bn(g, c.sms);
   } else {
     g.bn = 0;
@@ -265,6 +268,10 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   std::string name = std::string(c.dt == LR_BF16 ? "umma_" : "simt_") + epi_name(k);
   if (g.bn) name += "_bn" + std::to_string(g.bn);
   double flops = 2.0 * g.M * g.N * static_cast<double>(g.K) * g.nacc * g.batches;
+  if (g.causal) {  // every causal mode computes the pair tiles (or K ranges) on or below the diagonal
+    const double mp = g.M / 256.0;
+    flops *= (mp + 1.0) / (2.0 * mp);
+  }
   if (g.grouped) {
     flops = 0.0;
     for (int b = 0; b < g.batches; ++b) flops += 2.0 * g.gM[b] * g.gN[b] * static_cast<double>(g.K);
@@ -1099,8 +1106,8 @@ static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
 // head n starts n*s stored rows into its tensor).
 struct AttnWs {
   bf16 *qh, *kh, *vh, *oh, *doh, *dqh, *dkh, *dvh;
-  float *S, *dP, *D;
-  bf16 *P, *dS;
+  float *S, *D;
+  bf16 *P, *dS;  // dS takes the first half of S's bytes (S is the forward's, dS the backward's)
 };
 
 static size_t attn_ws_layout(int b, int s, int H, int dh, void* base, AttnWs* W) {
@@ -1112,9 +1119,8 @@ static size_t attn_ws_layout(int b, int s, int H, int dh, void* base, AttnWs* W)
   bf16** hm[8] = {&W->qh, &W->kh, &W->vh, &W->oh, &W->doh, &W->dqh, &W->dkh, &W->dvh};
   for (bf16** p : hm) *p = static_cast<bf16*>(ar.take(E));
   W->S = static_cast<float*>(ar.take(R * s * sizeof(float)));
-  W->dP = static_cast<float*>(ar.take(R * s * sizeof(float)));
   W->P = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
-  W->dS = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
+  W->dS = reinterpret_cast<bf16*>(W->S);
   W->D = static_cast<float*>(ar.take(R * sizeof(float)));
   return ar.size();
 }
@@ -1183,13 +1189,29 @@ static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
     cudaError_t e = launch_attn_rowdot(W.doh, W.oh, R, dh, W.D, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention row dot: %s", cudaGetErrorString(e));
   }
-  // S = Q K^T again (only its log-sum-exp was kept), dP = dO V^T
-  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s, 1));
-  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.doh, dh}, false, {W.vh, dh}, false, W.dP, s, 1));
   {
-    LaunchScope scope("attn_softmax_bwd", c.st, 0, 12.0 * R * s);
-    cudaError_t e = launch_attn_softmax_bwd(W.S, W.dP, lse, W.D, R, s, scale, W.P, W.dS, c.st);
-    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention softmax backward: %s", cudaGetErrorString(e));
+    // One dual-accumulator launch per tile of every head: S = Q K^T again (only its log-sum-exp
+    // was kept) and dP = dO V^T, turned in the epilogue into P = exp(scale S - lse) and
+    // dS = scale P (dP - D), stored bf16 up to the end of each row's 256-key tile.
+    GemmCall g = new_call(s, s, dh);
+    g.causal = 1;
+    g.nacc = 2;
+    g.batches = heads;
+    g.rowbatch = true;
+    g.rb_a = g.rb_b = g.rb_o = s;
+    g.rows_a = g.rows_b = g.rows_o = 1LL * R;
+    g.A[0] = {W.qh, dh};
+    g.B[0] = {W.kh, dh};
+    g.A[1] = {W.doh, dh};
+    g.B[1] = {W.vh, dh};
+    g.ep.out0[0] = W.P;
+    g.ep.out1[0] = W.dS;
+    g.ep.ldo0 = g.ep.ldo1 = s;
+    g.ep.rowscale = lse;
+    g.ep.rowpart_in = W.D;
+    g.ep.rowpart_in_chunks = 1;
+    g.ep.coef = scale;
+    LR_TRY(gemm(c, EPI_ATTN_BWD, g, 8.0 * R));
   }
   // dV = P^T dO (P read MN-major: keys index its columns), dQ = dS K, dK = dS^T Q (dS holds scale)
   LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, true, {W.doh, dh}, true, W.dvh, dh, 3));

@@ -357,7 +357,7 @@ struct Config {
   // are released separately.  Phase 1 stages round(a) in shared memory (exact: a is stored
   // rounded) and frees a's columns for the next tile while b still accumulates; phase 2 moves
   // round(b) into registers, frees b's columns, then computes h.
-  static constexpr bool SPLIT = (K == EPI_SWIGLU || K == EPI_NORM_SWIGLU) && NBUF == 1;
+  static constexpr bool SPLIT = (K == EPI_SWIGLU || K == EPI_NORM_SWIGLU || K == EPI_ATTN_BWD) && NBUF == 1;
   // Staging per epilogue warp: NO output sets of NOUT tiles (ping-pong when stores would
   // otherwise stall the next chunk), NA operand sets of NAUX tiles (loads NA chunks ahead),
   // and for the split SwiGLU the round(a) tiles of the warp's chunks.
@@ -402,7 +402,14 @@ __device__ __forceinline__ void k_range(const Shape& sh, int split, int mb, int&
   if (sh.causal == 3) kb0 = max(kb0, row0 / BK);
 }
 
-__device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
+// Pair tiles of one batch.  Causal mode 1 (M = N) schedules only the tiles on or below the
+// diagonal: pair p (rows 256 p .. 256 p + 255) takes its first (p + 1) u key tiles, u = 256 / BN.
+__host__ __device__ inline int batch_tiles(const Shape& sh) {
+  if (sh.causal == 1) return sh.n_tiles / sh.m_pairs * (sh.m_pairs * (sh.m_pairs + 1) / 2);
+  return sh.m_pairs * sh.n_tiles;
+}
+
+__host__ __device__ inline void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
                                             int& nb) {
   if (sh.grouped) {
     const int per_split = sh.g_tiles;
@@ -426,13 +433,23 @@ __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank,
     mb = 2 * mp + rank;
     return;
   }
-  const int per_batch = sh.m_pairs * sh.n_tiles;
+  const int per_batch = batch_tiles(sh);
   const int per_split = sh.batches * per_batch;
   if (sh.reverse) tile = sh.ksplit * per_split - 1 - tile;
   split = tile / per_split;
   int rem = tile - split * per_split;
   batch = rem / per_batch;
   rem -= batch * per_batch;
+  if (sh.causal == 1) {
+    const int u = sh.n_tiles / sh.m_pairs;  // key tiles per pair of query tiles
+    const int q = rem / u;                  // pair p holds q in [p (p + 1) / 2, (p + 1) (p + 2) / 2)
+    int p = static_cast<int>((sqrtf(8.f * q + 1.f) - 1.f) * 0.5f);
+    while ((p + 1) * (p + 2) / 2 <= q) ++p;
+    while (p > 0 && p * (p + 1) / 2 > q) --p;
+    nb = rem - u * (p * (p + 1) / 2);
+    mb = 2 * p + rank;
+    return;
+  }
   const int mp = rem / sh.n_tiles;
   nb = rem - mp * sh.n_tiles;
   mb = 2 * mp + rank;
@@ -507,7 +524,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   const int ncl = static_cast<int>(gridDim.x >> 1);
   constexpr uint16_t kBoth = 0x3;
   const int total =  // pair tiles
-      sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * sh.m_pairs * sh.n_tiles);
+      sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * batch_tiles(sh));
 
   if (warp == 0) {
     if (lane == 0) {
@@ -763,7 +780,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       const int m = mb * BM + row;
       const int ob = sh.rowbatch ? 0 : batch;                 // output maps and pointers of this batch
       const int r0 = mb * BM + q * ER + batch * sh.rb_o;  // first stored row of this warp's boxes
-      // Causal mode 1: a tile wholly above the diagonal (every column past every row) is not stored.
+      // Causal mode 1: a tile wholly above the diagonal (every column past every row) is not stored
+      // (the schedule holds none; the test guards the stores all the same).
       const bool no_store = sh.causal == 1 && nb * BN >= (mb >> 1) * 2 * BM + 2 * BM;
       RowIn ri;
       if constexpr (C::STATS) {
@@ -783,7 +801,88 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
       for (int a = 0; a < NAUX; ++a) aux_present[a] = epi_aux_ptr(ep, a, ob) != nullptr;
 
-      if constexpr (C::SPLIT) {
+      if constexpr (K == EPI_ATTN_BWD) {
+        // Causal attention backward scores.  Phase 1: P = exp(scale S - lse) from accumulator 0
+        // (0 where the key is past the query) into the warp's shared-memory tiles and out to P;
+        // S's columns are released.  Phase 2: dS = scale P (dP - D) from accumulator 1 (fp32) and
+        // those tiles, out to dS; then dP's columns are released.  Tiles wholly above the diagonal
+        // only pass their accumulators back.
+        constexpr int NC = NCH / 2;
+        constexpr float kLog2e = 1.4426950408889634f;
+        uint8_t* abuf = wstage + NO * C::OSET + NA * C::ASET;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const int grow = m + batch * sh.rb_o;  // the row of lse and D (all heads' rows in one vector)
+        const bool row_in = m < sh.M;
+        const float lse2 = row_in ? ep.rowscale[grow] * kLog2e : 0.f;
+        const float dval = row_in ? ep.rowpart_in[grow] : 0.f;
+        const float c2 = ep.coef * kLog2e;
+        ok = mbar_wait(&tfull[0], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        tc_fence_after();
+        if (!no_store) {
+          if (leader) bulk_wait_read_all();  // the previous tile's P stores have read abuf
+          __syncwarp();
+#pragma unroll
+          for (int ci = 0; ci < NC; ++ci) {
+            const int c = g + 2 * ci;
+            float v[CW];
+            tmem_ld32(t_row + c * CW, v);
+            tmem_ld_wait();
+            const int n0 = nb * BN + c * CW;
+#pragma unroll
+            for (int j = 0; j < CW; ++j) v[j] = (n0 + j <= m && row_in) ? exp2f(v[j] * c2 - lse2) : 0.f;
+            const uint32_t base = smem_addr(abuf + ci * C::OUT_BUF);
+#pragma unroll
+            for (int j = 0; j < CW / 8; ++j) sts_bf16x8(base + stage_off<64>(lane, j), &v[8 * j]);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (leader && present[0]) {
+#pragma unroll
+            for (int ci = 0; ci < NC; ++ci)
+              tma_store_2d(&maps.out[ob][0], abuf + ci * C::OUT_BUF, nb * BN + (g + 2 * ci) * CW, r0);
+            bulk_commit();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[0]), 0));
+        ok = mbar_wait(&tfull[1], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        tc_fence_after();
+        if (!no_store) {
+#pragma unroll 1
+          for (int ci = 0; ci < NC; ++ci) {
+            const int c = g + 2 * ci;
+            const int b = qi % NO;
+            wait_set_free();
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            float v[CW];
+            tmem_ld32(t_row + BN + c * CW, v);
+            tmem_ld_wait();
+            const uint32_t abase = smem_addr(abuf + ci * C::OUT_BUF);
+            const uint32_t dbase = smem_addr(ostage(b));
+#pragma unroll
+            for (int j = 0; j < CW / 8; ++j) {
+              float p[8], d8[8];
+              lds_bf16x8(abase + stage_off<64>(lane, j), p);
+#pragma unroll
+              for (int t = 0; t < 8; ++t) d8[t] = ep.coef * p[t] * (v[8 * j + t] - dval);
+              sts_bf16x8(dbase + stage_off<64>(lane, j), d8);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (leader) {
+              if (present[1]) tma_store_2d(&maps.out[ob][1], ostage(b), nb * BN + c * CW, r0);
+              bulk_commit();
+            }
+            ++qi;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[1]), 0));
+        if (!ok) break;
+      } else if constexpr (C::SPLIT) {
         // Phase 1: round(a) of this warp's chunks into its a tiles in shared memory (exact:
         // a is stored rounded), optionally TMA-stored from there; then a's TMEM columns are
         // released, so the next tile's a accumulation overlaps the rest of this epilogue.

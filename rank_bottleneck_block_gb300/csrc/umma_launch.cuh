@@ -83,7 +83,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.M = g.M;
   sh.N = g.N;
   sh.K = g.K;
-  sh.batches = NACC > 1 ? 1 : g.batches;
+  sh.batches = NACC > 1 && !g.rowbatch ? 1 : g.batches;
   sh.m_tiles = (g.M + BM - 1) / BM;
   sh.n_tiles = (g.N + BN - 1) / BN;
   sh.m_pairs = (sh.m_tiles + 1) / 2;
@@ -95,7 +95,8 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.reverse = g.reverse ? 1 : 0;
   if (!g.rowbatch && !g.grouped && NACC == 1 && (g.batches < 1 || g.batches > kMaxBatch)) return cudaErrorInvalidValue;
   if (g.rowbatch) {  // one tensor per operand, batches offset by rows
-    if (D::NAUX > 0 || C::STATS || C::SPLIT || D::ROWPART || NACC > 1 || g.grouped || sh.ksplit != 1 ||
+    if (D::NAUX > 0 || C::STATS || ((C::SPLIT || NACC > 1) && K != EPI_ATTN_BWD) || D::ROWPART || g.grouped ||
+        sh.ksplit != 1 ||
         g.M % (2 * BM) || g.N % BN || g.K % BK || g.rb_a < 0 || g.rb_b < 0 || g.rb_o < 0)
       return cudaErrorInvalidValue;
     sh.rowbatch = 1;
@@ -104,7 +105,8 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
     sh.rb_o = g.rb_o;
     sh.causal = g.causal;
   }
-  if (g.causal && (!g.rowbatch || g.causal > 3 || g.M % (2 * BM))) return cudaErrorInvalidValue;
+  if (g.causal && (!g.rowbatch || g.causal > 3 || g.M % (2 * BM) || (g.causal == 1 && g.N != g.M)))
+    return cudaErrorInvalidValue;
   sh.grouped = 0;
   if (g.grouped) {  // batches of their own M, N; one split only
     if (K != EPI_F32 || sh.ksplit != 1 || g.batches < 1 || g.batches > kMaxBatch) return cudaErrorInvalidValue;
@@ -157,7 +159,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   }
 
   const long long total =  // pair tiles
-      1LL * sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * sh.m_pairs * sh.n_tiles);
+      1LL * sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * batch_tiles(sh));
   if (total <= 0) return cudaSuccess;
 
   auto kern = gemm_kernel<K, BN, A_MN, B_MN>;

@@ -98,7 +98,7 @@ def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
 
 def test_attention_shape_rules(L):
     assert L.lr_attn_saved_bytes(2, 256, 3, 128) == 2 * 3 * 256 * 4
-    assert L.lr_attn_workspace_bytes(2, 256, 3, 128) > 12 * 2 * 3 * 256 * 256
+    assert L.lr_attn_workspace_bytes(2, 256, 3, 128) > 6 * 2 * 3 * 256 * 256  # fp32 S and bf16 P
     assert L.lr_attn_saved_bytes(1, 200, 1, 128) == 0  # s not a multiple of 256
     assert L.lr_attn_workspace_bytes(1, 256, 1, 64) == 0  # dh not a multiple of 128
     lib = L.lib()
