@@ -11,25 +11,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileRows = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// One thread per 8 consecutive channels of one head of one token.
-__global__ void head_permute_kernel(const bf16* src, bf16* dst, int b, int s, int H, int dh, int to_heads) {
-  pdl_wait();
-  pdl_trigger();
-  const int per_tok = H * dh / 8;
-  const long long total = 1LL * b * s * per_tok;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += 256LL * gridDim.x) {
-    const int t = static_cast<int>(i / per_tok);
-    const int rem = static_cast<int>(i - 1LL * t * per_tok);
-    const int h = rem / (dh / 8);
-    const int c = (rem - h * (dh / 8)) * 8;
-    const int bi = t / s, ti = t - bi * s;
-    const long long tm = 1LL * t * H * dh + 1LL * h * dh + c;
-    const long long hm = (1LL * (bi * H + h) * s + ti) * dh + c;
-    const long long from = to_heads ? tm : hm, to = to_heads ? hm : tm;
-    *reinterpret_cast<uint4*>(dst + to) = *reinterpret_cast<const uint4*>(src + from);
-  }
-}
-
 // Combines two (max, sum) pairs of a streaming log-sum-exp in base 2; an empty pair is (-inf, 0).
 __device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2) {
   const float M = fmaxf(m, m2);
@@ -87,17 +68,21 @@ __global__ void attn_softmax_fwd_kernel(const float* S, int R, int s, float scal
   }
 }
 
-__global__ void attn_rowdot_kernel(const bf16* dO, const bf16* O, int R, int dh, float* D) {
+__global__ void attn_rowdot_kernel(const bf16* dO, const bf16* O, int b, int s, int H, int dh, float* D) {
   pdl_wait();
   pdl_trigger();
+  const int R = b * H * s;
   const int r = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= R) return;
+  const int n = r / s, i = r - n * s;  // head n = bi*H + h, query i
+  const int bi = n / H, h = n - bi * H;
+  const long long base = (1LL * bi * s + i) * H * dh + 1LL * h * dh;
   float acc = 0.f;
   for (int c = lane * 8; c < dh; c += 256) {
     float a[8], o[8];
-    load8(dO + 1LL * r * dh + c, a);
-    load8(O + 1LL * r * dh + c, o);
+    load8(dO + base + c, a);
+    load8(O + base + c, o);
 #pragma unroll
     for (int t = 0; t < 8; ++t) acc = fmaf(a[t], o[t], acc);
   }
@@ -110,25 +95,17 @@ dim3 warp_rows_grid(int R) { return dim3(static_cast<unsigned>((R + 7) / 8)); }
 
 }  // namespace
 
-cudaError_t launch_head_permute(const bf16* src, bf16* dst, int b, int s, int H, int dh, int to_heads,
-                                cudaStream_t st) {
-  const long long total = 1LL * b * s * H * dh / 8;
-  if (total == 0) return cudaSuccess;
-  long long blocks = (total + 255) / 256;
-  if (blocks > 16384) blocks = 16384;
-  return launch_pdl(head_permute_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, src, dst, b, s, H,
-                    dh, to_heads);
-}
-
 cudaError_t launch_attn_softmax_fwd(const float* S, int R, int s, float scale, bf16* P, float* lse,
                                     cudaStream_t st) {
   if (R == 0) return cudaSuccess;
   return launch_pdl(attn_softmax_fwd_kernel, warp_rows_grid(R), dim3(256), 0, st, S, R, s, scale, P, lse);
 }
 
-cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int R, int dh, float* D, cudaStream_t st) {
+cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int b, int s, int H, int dh, float* D,
+                               cudaStream_t st) {
+  const int R = b * H * s;
   if (R == 0) return cudaSuccess;
-  return launch_pdl(attn_rowdot_kernel, warp_rows_grid(R), dim3(256), 0, st, dO, O, R, dh, D);
+  return launch_pdl(attn_rowdot_kernel, warp_rows_grid(R), dim3(256), 0, st, dO, O, b, s, H, dh, D);
 }
 
 }  // namespace lr

@@ -38,15 +38,18 @@ struct GemmCall {
   bool grouped;
   int gM[kMaxBatch], gN[kMaxBatch];
   long long gldo[kMaxBatch];
-  // Row-batched problems (kinds without operand tiles, row statistics or row partials): batch b
-  // of A, B and the output starts rb_a, rb_b, rb_o stored rows after batch b - 1 in one tensor
-  // each (rows_a, rows_b, rows_o stored rows in all), so any number of batches shares one set of
-  // tensor maps.  A stored row is an M index for a K-major A and a K index for an MN-major one
-  // (likewise N or K for B).  Each batch's M, N and K must be whole tiles: M a multiple of 256,
-  // N of the tile width, K of 64.
+  // Row-batched problems (kinds without operand tiles, row statistics or row partials): every
+  // batch reads and writes one tensor per operand at an offset, so any number of batches shares
+  // one set of tensor maps.  Batch b = hi bh + lo (bh >= 1) of operand X starts hi rb_X + lo rl_X
+  // stored rows and lo cb_X stored columns in (rows_X stored rows in all; cols_X stored columns,
+  // or 0 for the batch's own extent).  A stored row is an M index for a K-major A and a K index
+  // for an MN-major one (likewise N or K for B), a stored column the other index.  Each batch's
+  // M, N and K must be whole tiles: M a multiple of 256, N of the tile width, K of 64; column
+  // offsets multiples of 8.
   bool rowbatch;
-  int rb_a, rb_b, rb_o;
-  long long rows_a, rows_b, rows_o;
+  int bh;
+  int rb_a, rb_b, rb_o, rl_a, rl_b, rl_o, cb_a, cb_b, cb_o;
+  long long rows_a, rows_b, rows_o, cols_a, cols_b, cols_o;
   // Causal masking of a row-batched attention GEMM over s positions (rows and columns or K index
   // positions, whole pair tiles of 256): 1 = rows are queries and columns keys (M = N), only the
   // tiles on or below the diagonal are scheduled; 2 = rows are queries and K keys, K stops after the tile's last row;

@@ -1101,23 +1101,22 @@ static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
 }
 
 // ============================================================ causal attention
-// Heads are moved to a head-major layout ([b*H*s, dh]: head (bi, h) owns rows (bi*H + h)*s ..
-// + s - 1), so each GEMM runs once over all b*H heads in row-batched mode (every operand of
-// head n starts n*s stored rows into its tensor).
+// Each GEMM runs once over all b*H heads in row-batched mode; head n = bi*H + h is batch n.
+// q, k, v, o and their gradients stay token-major ([b*s, H*dh]: head (bi, h) is rows bi*s ..
+// bi*s + s - 1, columns h*dh .. h*dh + dh - 1), read and written in place through per-head row
+// and column offsets.  The s x s score tensors (S, P, dS) are head-major ([b*H*s, s]: head n is
+// rows n*s .. n*s + s - 1), as are lse and D.
 struct AttnWs {
-  bf16 *qh, *kh, *vh, *oh, *doh, *dqh, *dkh, *dvh;
   float *S, *D;
   bf16 *P, *dS;  // dS takes the first half of S's bytes (S is the forward's, dS the backward's)
 };
 
 static size_t attn_ws_layout(int b, int s, int H, int dh, void* base, AttnWs* W) {
+  (void)dh;
   Arena ar(base);
   AttnWs tmp;
   if (!W) W = &tmp;
   const size_t R = static_cast<size_t>(b) * H * s;
-  const size_t E = R * dh * sizeof(bf16);
-  bf16** hm[8] = {&W->qh, &W->kh, &W->vh, &W->oh, &W->doh, &W->dqh, &W->dkh, &W->dvh};
-  for (bf16** p : hm) *p = static_cast<bf16*>(ar.take(E));
   W->S = static_cast<float*>(ar.take(R * s * sizeof(float)));
   W->P = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
   W->dS = reinterpret_cast<bf16*>(W->S);
@@ -1125,52 +1124,63 @@ static size_t attn_ws_layout(int b, int s, int H, int dh, void* base, AttnWs* W)
   return ar.size();
 }
 
-// One GEMM over all heads: batch n = head n; A, B, out start n*s stored rows in.
-static lr_status attn_gemm(const Ctx& c, EpiKind k, int M, int N, int K, int heads, int s, Operand A, bool a_mn,
-                           Operand B, bool b_mn, void* out, long long ldo, int causal) {
+struct AttnDims {
+  int b, s, H, dh;
+};
+
+// Places operand X of head n = bi*H + h: token-major (rows bi*s, columns h*dh of a [b*s, H*dh]
+// tensor) or head-major (rows n*s of a [b*H*s, *] tensor).
+static void attn_place(const AttnDims& a, bool tok, int& rb, int& rl, int& cb, long long& rows, long long& cols) {
+  if (tok) {
+    rb = a.s, rl = 0, cb = a.dh, rows = 1LL * a.b * a.s, cols = 1LL * a.H * a.dh;
+  } else {
+    rb = a.H * a.s, rl = a.s, cb = 0, rows = 1LL * a.b * a.H * a.s, cols = 0;
+  }
+}
+
+// One GEMM over all heads.  tok_*: whether A, B, the output are token-major (else head-major).
+static GemmCall attn_call(const AttnDims& a, int M, int N, int K, bool a_tok, bool b_tok, bool o_tok, int causal) {
   GemmCall g = new_call(M, N, K);
   g.causal = causal;
+  g.batches = a.b * a.H;
+  g.rowbatch = true;
+  g.bh = a.H;
+  attn_place(a, a_tok, g.rb_a, g.rl_a, g.cb_a, g.rows_a, g.cols_a);
+  attn_place(a, b_tok, g.rb_b, g.rl_b, g.cb_b, g.rows_b, g.cols_b);
+  attn_place(a, o_tok, g.rb_o, g.rl_o, g.cb_o, g.rows_o, g.cols_o);
+  g.bn = N % 256 == 0 ? 256 : 128;
+  return g;
+}
+
+static lr_status attn_gemm(const Ctx& c, EpiKind k, const AttnDims& a, int M, int N, int K, Operand A, bool a_mn,
+                           bool a_tok, Operand B, bool b_mn, bool b_tok, void* out, long long ldo, bool o_tok,
+                           int causal) {
+  GemmCall g = attn_call(a, M, N, K, a_tok, b_tok, o_tok, causal);
   g.a_mn = a_mn;
   g.b_mn = b_mn;
-  g.batches = heads;
-  g.rowbatch = true;
-  g.rb_a = g.rb_b = g.rb_o = s;
-  g.rows_a = g.rows_b = g.rows_o = 1LL * heads * s;
   g.A[0] = A;
   g.B[0] = B;
-  g.bn = N % 256 == 0 ? 256 : 128;
   g.ep.out0[0] = out;
   g.ep.ldo0 = ldo;
   g.ep.split_stride = ldo * g.rows_o;
   return gemm(c, k, g);
 }
 
-static lr_status head_permute(const Ctx& c, const void* src, void* dst, int b, int s, int H, int dh, int to_heads) {
-  LaunchScope scope("head_permute", c.st, 0, 4.0 * b * s * H * dh);
-  cudaError_t e = launch_head_permute(static_cast<const bf16*>(src), static_cast<bf16*>(dst), b, s, H, dh, to_heads,
-                                      c.st);
-  if (e != cudaSuccess) return fail(LR_ERR_CUDA, "head permute: %s", cudaGetErrorString(e));
-  return LR_OK;
-}
-
 static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float scale, const void* q, const void* k,
                                const void* v, void* o, float* lse, void* ws) {
   AttnWs W;
   attn_ws_layout(b, s, H, dh, ws, &W);
-  const int heads = b * H, R = heads * s;
-  LR_TRY(head_permute(c, q, W.qh, b, s, H, dh, 1));
-  LR_TRY(head_permute(c, k, W.kh, b, s, H, dh, 1));
-  LR_TRY(head_permute(c, v, W.vh, b, s, H, dh, 1));
-  // S = Q K^T (fp32), both operands K-major (K = dh)
-  LR_TRY(attn_gemm(c, EPI_F32, s, s, dh, heads, s, {W.qh, dh}, false, {W.kh, dh}, false, W.S, s, 1));
+  const AttnDims a{b, s, H, dh};
+  const int R = b * H * s, d = H * dh;
+  // S = Q K^T (fp32, head-major), both operands K-major (K = dh) in their token-major rows
+  LR_TRY(attn_gemm(c, EPI_F32, a, s, s, dh, {q, d}, false, true, {k, d}, false, true, W.S, s, false, 1));
   {
     LaunchScope scope("attn_softmax", c.st, 0, 6.0 * R * s);
     cudaError_t e = launch_attn_softmax_fwd(W.S, R, s, scale, W.P, lse, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention softmax: %s", cudaGetErrorString(e));
   }
-  // O = P V: P K-major (K = keys), V read MN-major in its stored [keys, dh] layout
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, false, {W.vh, dh}, true, W.oh, dh, 2));
-  return head_permute(c, W.oh, o, b, s, H, dh, 0);
+  // O = P V: P K-major (K = keys), V read MN-major in its stored [keys, dh] columns; O token-major
+  return attn_gemm(c, EPI_STORE, a, s, dh, s, {W.P, s}, false, false, {v, d}, true, true, o, d, true, 2);
 }
 
 static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float scale, const void* q, const void* k,
@@ -1178,32 +1188,24 @@ static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
                                void* dv, void* ws) {
   AttnWs W;
   attn_ws_layout(b, s, H, dh, ws, &W);
-  const int heads = b * H, R = heads * s;
-  LR_TRY(head_permute(c, q, W.qh, b, s, H, dh, 1));
-  LR_TRY(head_permute(c, k, W.kh, b, s, H, dh, 1));
-  LR_TRY(head_permute(c, v, W.vh, b, s, H, dh, 1));
-  LR_TRY(head_permute(c, o, W.oh, b, s, H, dh, 1));
-  LR_TRY(head_permute(c, dout, W.doh, b, s, H, dh, 1));
+  const AttnDims a{b, s, H, dh};
+  const int R = b * H * s, d = H * dh;
   {
     LaunchScope scope("attn_rowdot", c.st, 0, 4.0 * R * dh + 4.0 * R);
-    cudaError_t e = launch_attn_rowdot(W.doh, W.oh, R, dh, W.D, c.st);
+    cudaError_t e = launch_attn_rowdot(static_cast<const bf16*>(dout), static_cast<const bf16*>(o), b, s, H, dh,
+                                       W.D, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention row dot: %s", cudaGetErrorString(e));
   }
   {
     // One dual-accumulator launch per tile of every head: S = Q K^T again (only its log-sum-exp
     // was kept) and dP = dO V^T, turned in the epilogue into P = exp(scale S - lse) and
-    // dS = scale P (dP - D), stored bf16 up to the end of each row's 256-key tile.
-    GemmCall g = new_call(s, s, dh);
-    g.causal = 1;
+    // dS = scale P (dP - D), stored bf16 (head-major) up to the end of each row's 256-key tile.
+    GemmCall g = attn_call(a, s, s, dh, true, true, false, 1);
     g.nacc = 2;
-    g.batches = heads;
-    g.rowbatch = true;
-    g.rb_a = g.rb_b = g.rb_o = s;
-    g.rows_a = g.rows_b = g.rows_o = 1LL * R;
-    g.A[0] = {W.qh, dh};
-    g.B[0] = {W.kh, dh};
-    g.A[1] = {W.doh, dh};
-    g.B[1] = {W.vh, dh};
+    g.A[0] = {q, d};
+    g.B[0] = {k, d};
+    g.A[1] = {dout, d};
+    g.B[1] = {v, d};
     g.ep.out0[0] = W.P;
     g.ep.out1[0] = W.dS;
     g.ep.ldo0 = g.ep.ldo1 = s;
@@ -1213,13 +1215,11 @@ static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
     g.ep.coef = scale;
     LR_TRY(gemm(c, EPI_ATTN_BWD, g, 8.0 * R));
   }
-  // dV = P^T dO (P read MN-major: keys index its columns), dQ = dS K, dK = dS^T Q (dS holds scale)
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.P, s}, true, {W.doh, dh}, true, W.dvh, dh, 3));
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, false, {W.kh, dh}, true, W.dqh, dh, 2));
-  LR_TRY(attn_gemm(c, EPI_STORE, s, dh, s, heads, s, {W.dS, s}, true, {W.qh, dh}, true, W.dkh, dh, 3));
-  LR_TRY(head_permute(c, W.dqh, dq, b, s, H, dh, 0));
-  LR_TRY(head_permute(c, W.dkh, dk, b, s, H, dh, 0));
-  return head_permute(c, W.dvh, dv, b, s, H, dh, 0);
+  // dV = P^T dO (P read MN-major: keys index its columns), dQ = dS K, dK = dS^T Q (dS holds scale);
+  // the gradients land token-major in place
+  LR_TRY(attn_gemm(c, EPI_STORE, a, s, dh, s, {W.P, s}, true, false, {dout, d}, true, true, dv, d, true, 3));
+  LR_TRY(attn_gemm(c, EPI_STORE, a, s, dh, s, {W.dS, s}, false, false, {k, d}, true, true, dq, d, true, 2));
+  return attn_gemm(c, EPI_STORE, a, s, dh, s, {W.dS, s}, true, false, {q, d}, true, true, dk, d, true, 3);
 }
 
 // ============================================================ transformer block

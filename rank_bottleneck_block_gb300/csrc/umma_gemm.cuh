@@ -82,8 +82,11 @@ struct Shape {
   int g_n_tiles[kMaxBatch];  // n-tiles of batch b
   int g_tile0[kMaxBatch];    // first pair tile of batch b
   int g_tiles;               // pair tiles of all batches
-  int rowbatch;              // batches offset into one tensor each (see GemmCall::rowbatch), then:
-  int rb_a, rb_b, rb_o;      // stored rows per batch of A, B and the output
+  int rowbatch;              // batches offset into one tensor each (see GemmCall::rowbatch), then
+  int bh;                    // batch = hi bh + lo, and A, B, the output start at rows hi rb + lo rl,
+  int rb_a, rb_b, rb_o;      //   columns lo cb of their tensors
+  int rl_a, rl_b, rl_o;
+  int cb_a, cb_b, cb_o;
   int causal;                // causal use of a row-batched problem (see GemmCall::causal), else 0
   unsigned* err;
 };
@@ -402,6 +405,17 @@ __device__ __forceinline__ void k_range(const Shape& sh, int split, int mb, int&
   if (sh.causal == 3) kb0 = max(kb0, row0 / BK);
 }
 
+// Where batch `batch` of a row-batched problem starts in each tensor (all 0 otherwise).
+struct BatchOff {
+  int ra, ca, rb, cb, ro, co;  // stored row and column of A, B and the output
+};
+__device__ __forceinline__ BatchOff batch_off(const Shape& sh, int batch) {
+  if (!sh.rowbatch) return BatchOff{0, 0, 0, 0, 0, 0};
+  const int hi = batch / sh.bh, lo = batch - hi * sh.bh;
+  return BatchOff{hi * sh.rb_a + lo * sh.rl_a, lo * sh.cb_a, hi * sh.rb_b + lo * sh.rl_b,
+                  lo * sh.cb_b, hi * sh.rb_o + lo * sh.rl_o, lo * sh.cb_o};
+}
+
 // Pair tiles of one batch.  Causal mode 1 (M = N) schedules only the tiles on or below the
 // diagonal: pair p (rows 256 p .. 256 p + 255) takes its first (p + 1) u key tiles, u = 256 / BN.
 __host__ __device__ inline int batch_tiles(const Shape& sh) {
@@ -540,7 +554,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         k_range(sh, split, mb, kb0, kb1);
         const int m0 = mb * BM, n0 = nb * BN;
         const int set0 = sh.rowbatch ? 0 : batch;
-        const int ra = batch * sh.rb_a, rbb = batch * sh.rb_b;  // row-batched offsets (else 0)
+        const BatchOff bo = batch_off(sh, batch);
         for (int s = 0; s < NACC && ok; ++s) {
           const int set = NACC > 1 ? s : set0;
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -556,17 +570,17 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
             if (A_MN) {
 #pragma unroll
               for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d_pair(a_dst + j * 8192, &maps.a[set], fbar, m0 + 64 * j, kb * BK + ra);
+                tma_load_2d_pair(a_dst + j * 8192, &maps.a[set], fbar, m0 + 64 * j + bo.ca, kb * BK + bo.ra);
             } else {
-              tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK, m0 + ra);
+              tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK + bo.ca, m0 + bo.ra);
             }
             const int nb0 = n0 + rank * (BN / 2);  // this CTA's half of the B tile
             if (B_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 128; ++j)
-                tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j, kb * BK + rbb);
+                tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j + bo.cb, kb * BK + bo.rb);
             } else {
-              tma_load_2d_pair(b_dst, &maps.b[set], fbar, kb * BK, nb0 + rbb);
+              tma_load_2d_pair(b_dst, &maps.b[set], fbar, kb * BK + bo.cb, nb0 + bo.rb);
             }
             ++issued;
             if (++st == STAGES) {
@@ -779,7 +793,9 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       const uint32_t sph = static_cast<uint32_t>((it >> 1) & 1);
       const int m = mb * BM + row;
       const int ob = sh.rowbatch ? 0 : batch;                 // output maps and pointers of this batch
-      const int r0 = mb * BM + q * ER + batch * sh.rb_o;  // first stored row of this warp's boxes
+      const BatchOff bo = batch_off(sh, batch);
+      const int r0 = mb * BM + q * ER + bo.ro;  // first stored row of this warp's boxes
+      const int x0 = nb * BN + bo.co;           // first stored column of the tile
       // Causal mode 1: a tile wholly above the diagonal (every column past every row) is not stored
       // (the schedule holds none; the test guards the stores all the same).
       const bool no_store = sh.causal == 1 && nb * BN >= (mb >> 1) * 2 * BM + 2 * BM;
@@ -811,7 +827,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         constexpr float kLog2e = 1.4426950408889634f;
         uint8_t* abuf = wstage + NO * C::OSET + NA * C::ASET;
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const int grow = m + batch * sh.rb_o;  // the row of lse and D (all heads' rows in one vector)
+        const int grow = m + bo.ro;  // lse and D are indexed like the output's rows
         const bool row_in = m < sh.M;
         const float lse2 = row_in ? ep.rowscale[grow] * kLog2e : 0.f;
         const float dval = row_in ? ep.rowpart_in[grow] : 0.f;
@@ -839,7 +855,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           if (leader && present[0]) {
 #pragma unroll
             for (int ci = 0; ci < NC; ++ci)
-              tma_store_2d(&maps.out[ob][0], abuf + ci * C::OUT_BUF, nb * BN + (g + 2 * ci) * CW, r0);
+              tma_store_2d(&maps.out[ob][0], abuf + ci * C::OUT_BUF, x0 + (g + 2 * ci) * CW, r0);
             bulk_commit();
           }
         }
@@ -872,7 +888,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
             fence_async_smem();
             __syncwarp();
             if (leader) {
-              if (present[1]) tma_store_2d(&maps.out[ob][1], ostage(b), nb * BN + c * CW, r0);
+              if (present[1]) tma_store_2d(&maps.out[ob][1], ostage(b), x0 + c * CW, r0);
               bulk_commit();
             }
             ++qi;
@@ -913,7 +929,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           if (leader) {
 #pragma unroll
             for (int ci = 0; ci < NC; ++ci)
-              tma_store_2d(&maps.out[ob][1], abuf + ci * C::OUT_BUF, nb * BN + (g + 2 * ci) * CW, r0);
+              tma_store_2d(&maps.out[ob][1], abuf + ci * C::OUT_BUF, x0 + (g + 2 * ci) * CW, r0);
             bulk_commit();
           }
         }
@@ -970,8 +986,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (leader) {
-            if (present[0]) tma_store_2d(&maps.out[ob][0], ostage(b), nb * BN + c * CW, r0);
-            if (present[2]) tma_store_2d(&maps.out[ob][2], ostage(b) + C::OUT_BUF, nb * BN + c * CW, r0);
+            if (present[0]) tma_store_2d(&maps.out[ob][0], ostage(b), x0 + c * CW, r0);
+            if (present[2]) tma_store_2d(&maps.out[ob][2], ostage(b) + C::OUT_BUF, x0 + c * CW, r0);
             bulk_commit();
           }
           ++qi;
@@ -1053,13 +1069,13 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               if constexpr (D::OUT_F32) {
                 // Split-K partials are summed by the next kernel: keep them in L2 for it.
                 if (sh.ksplit > 1)
-                  tma_store_3d_hint(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split,
+                  tma_store_3d_hint(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, x0 + c * CW, r0, split,
                                     l2_evict_last());
                 else
-                  tma_store_3d(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0, split);
+                  tma_store_3d(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, x0 + c * CW, r0, split);
               }
               else
-                tma_store_2d(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, nb * BN + c * CW, r0);
+                tma_store_2d(&maps.out[ob][oi], ostage(b) + oi * C::OUT_BUF, x0 + c * CW, r0);
             }
             bulk_commit();
           }

@@ -96,13 +96,22 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   if (!g.rowbatch && !g.grouped && NACC == 1 && (g.batches < 1 || g.batches > kMaxBatch)) return cudaErrorInvalidValue;
   if (g.rowbatch) {  // one tensor per operand, batches offset by rows
     if (D::NAUX > 0 || C::STATS || ((C::SPLIT || NACC > 1) && K != EPI_ATTN_BWD) || D::ROWPART || g.grouped ||
-        sh.ksplit != 1 ||
-        g.M % (2 * BM) || g.N % BN || g.K % BK || g.rb_a < 0 || g.rb_b < 0 || g.rb_o < 0)
+        sh.ksplit != 1 || g.M % (2 * BM) || g.N % BN || g.K % BK || g.bh < 0 ||
+        g.rb_a < 0 || g.rb_b < 0 || g.rb_o < 0 || g.rl_a < 0 || g.rl_b < 0 || g.rl_o < 0 ||
+        g.cb_a < 0 || g.cb_b < 0 || g.cb_o < 0 || g.cb_a % 8 || g.cb_b % 8 || g.cb_o % 8 ||
+        g.cols_a < 0 || g.cols_b < 0 || g.cols_o < 0)
       return cudaErrorInvalidValue;
     sh.rowbatch = 1;
+    sh.bh = g.bh > 0 ? g.bh : 1;
     sh.rb_a = g.rb_a;
     sh.rb_b = g.rb_b;
     sh.rb_o = g.rb_o;
+    sh.rl_a = g.rl_a;
+    sh.rl_b = g.rl_b;
+    sh.rl_o = g.rl_o;
+    sh.cb_a = g.cb_a;
+    sh.cb_b = g.cb_b;
+    sh.cb_o = g.cb_o;
     sh.causal = g.causal;
   }
   if (g.causal && (!g.rowbatch || g.causal > 3 || g.M % (2 * BM) || (g.causal == 1 && g.N != g.M)))
@@ -125,14 +134,17 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   // Stored rows of operand A / B / the output (all batches' rows when row-batched).
   auto rowsA = [&](int b) -> long long { return g.rowbatch ? g.rows_a : (A_MN ? g.K : bM(b)); };
   auto rowsB = [&](int b) -> long long { return g.rowbatch ? g.rows_b : (B_MN ? g.K : bN(b)); };
+  // Stored columns (the inner extent): all batches' columns when row-batched with column offsets.
+  auto colsA = [&](int b) -> long long { return g.rowbatch && g.cols_a ? g.cols_a : (A_MN ? bM(b) : g.K); };
+  auto colsB = [&](int b) -> long long { return g.rowbatch && g.cols_b ? g.cols_b : (B_MN ? bN(b) : g.K); };
 
   const int nsets = NACC > 1 ? NACC : (g.rowbatch ? 1 : g.batches);
   for (int i = 0; i < nsets; ++i) {
-    const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, bM(i), rowsA(i), g.A[i].ld, 64, 64)
-                          : encode_operand(&maps.a[i], g.A[i].ptr, g.K, rowsA(i), g.A[i].ld, 64, BM);
+    const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, colsA(i), rowsA(i), g.A[i].ld, 64, 64)
+                          : encode_operand(&maps.a[i], g.A[i].ptr, colsA(i), rowsA(i), g.A[i].ld, 64, BM);
     // Each CTA of a pair stages half of the B tile: BN/2 rows (K-major) or 64-column chunks (MN-major).
-    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, bN(i), rowsB(i), g.B[i].ld, 64, 64)
-                          : encode_operand(&maps.b[i], g.B[i].ptr, g.K, rowsB(i), g.B[i].ld, 64, BN / 2);
+    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, colsB(i), rowsB(i), g.B[i].ld, 64, 64)
+                          : encode_operand(&maps.b[i], g.B[i].ptr, colsB(i), rowsB(i), g.B[i].ld, 64, BN / 2);
     if (!okA || !okB) return cudaErrorInvalidValue;
   }
   const void* const* outs[3] = {g.ep.out0, g.ep.out1, g.ep.out2};
@@ -146,9 +158,10 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
       if (!p) continue;
       const long long ld = g.grouped ? g.gldo[b] : ldo[o];
       const long long orows = g.rowbatch ? g.rows_o : bM(b);
+      const long long ocols = g.rowbatch && g.cols_o ? g.cols_o : bN(b);
       const long long stride = g.grouped ? ld * bM(b) : (g.rowbatch ? ld * orows : g.ep.split_stride);
-      const bool ok = D::OUT_F32 ? encode_epi_f32(&maps.out[b][o], p, bN(b), orows, ld, sh.ksplit, stride)
-                                 : encode_epi_bf16(&maps.out[b][o], p, bN(b), orows, ld);
+      const bool ok = D::OUT_F32 ? encode_epi_f32(&maps.out[b][o], p, ocols, orows, ld, sh.ksplit, stride)
+                                 : encode_epi_bf16(&maps.out[b][o], p, ocols, orows, ld);
       if (!ok) return cudaErrorInvalidValue;
     }
     for (int a = 0; a < D::NAUX; ++a) {
