@@ -27,7 +27,8 @@ __device__ __forceinline__ void store_bf16x4(bf16* p, float a, float b, float c,
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// One warp per row; lanes take 4 consecutive columns at a time.
+// Rows of any length: one warp per row; lanes take 4 consecutive columns at a time, a streaming
+// log-sum-exp first, then P from a second read of the row.
 __global__ void attn_softmax_fwd_kernel(const float* S, int R, int s, float scale, bf16* P, float* lse) {
   pdl_wait();
   pdl_trigger();
@@ -68,6 +69,58 @@ __global__ void attn_softmax_fwd_kernel(const float* S, int R, int s, float scal
   }
 }
 
+// Rows of up to kRegKeys keys: each lane keeps its columns of S in registers, so S is read once
+// and every element takes one exp2: P = 2^(c S - m) / l with m the row maximum of c S and l the
+// row sum of 2^(c S - m).
+constexpr int kRegVec = 16;              // float4 per lane
+constexpr int kRegKeys = kRegVec * 128;  // 2048
+__global__ void __launch_bounds__(128, 4) attn_softmax_fwd_reg_kernel(const float* S, int R, int s, float scale, bf16* P, float* lse) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const int n = r % s + 1;
+  const float* row = S + 1LL * r * s;
+  const float c = scale * kLog2e;
+  float x[kRegVec][4];  // c S, -inf past the diagonal (so 2^(x - m) is 0 there)
+#pragma unroll
+  for (int k = 0; k < kRegVec; ++k) {
+    const int j = (k * 32 + lane) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < n) v = *reinterpret_cast<const float4*>(row + j);
+    x[k][0] = j < n ? v.x * c : -INFINITY;
+    x[k][1] = j + 1 < n ? v.y * c : -INFINITY;
+    x[k][2] = j + 2 < n ? v.z * c : -INFINITY;
+    x[k][3] = j + 3 < n ? v.w * c : -INFINITY;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kRegVec; ++k) m = fmaxf(fmaxf(m, fmaxf(x[k][0], x[k][1])), fmaxf(x[k][2], x[k][3]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float l = 0.f;
+#pragma unroll
+  for (int k = 0; k < kRegVec; ++k) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      x[k][t] = exp2f(x[k][t] - m);
+      l += x[k][t];
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  if (lane == 0) lse[r] = (m + log2f(l)) * kLn2;
+  const float inv = 1.f / l;
+  bf16* prow = P + 1LL * r * s;
+  const int wend = min(s, ((n - 1) / kTileRows + 1) * kTileRows);  // zeros past n up to the tile end
+#pragma unroll
+  for (int k = 0; k < kRegVec; ++k) {
+    const int j = (k * 32 + lane) * 4;
+    if (j < wend) store_bf16x4(prow + j, x[k][0] * inv, x[k][1] * inv, x[k][2] * inv, x[k][3] * inv);
+  }
+}
+
 __global__ void attn_rowdot_kernel(const bf16* dO, const bf16* O, int b, int s, int H, int dh, float* D) {
   pdl_wait();
   pdl_trigger();
@@ -98,6 +151,9 @@ dim3 warp_rows_grid(int R) { return dim3(static_cast<unsigned>((R + 7) / 8)); }
 cudaError_t launch_attn_softmax_fwd(const float* S, int R, int s, float scale, bf16* P, float* lse,
                                     cudaStream_t st) {
   if (R == 0) return cudaSuccess;
+  if (s <= kRegKeys)
+    return launch_pdl(attn_softmax_fwd_reg_kernel, dim3(static_cast<unsigned>((R + 3) / 4)), dim3(128), 0, st, S, R,
+                      s, scale, P, lse);
   return launch_pdl(attn_softmax_fwd_kernel, warp_rows_grid(R), dim3(256), 0, st, S, R, s, scale, P, lse);
 }
 

@@ -1175,7 +1175,9 @@ static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   // S = Q K^T (fp32, head-major), both operands K-major (K = dh) in their token-major rows
   LR_TRY(attn_gemm(c, EPI_F32, a, s, s, dh, {q, d}, false, true, {k, d}, false, true, W.S, s, false, 1));
   {
-    LaunchScope scope("attn_softmax", c.st, 0, 6.0 * R * s);
+    double row_bytes = 0.0;  // S read up to the diagonal, P written up to the end of the key tile
+    for (int i = 0; i < s; ++i) row_bytes += 4.0 * (i + 1) + 2.0 * std::min(s, (i / 256 + 1) * 256);
+    LaunchScope scope("attn_softmax", c.st, 0, row_bytes * b * H);
     cudaError_t e = launch_attn_softmax_fwd(W.S, R, s, scale, W.P, lse, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention softmax: %s", cudaGetErrorString(e));
   }
@@ -1757,7 +1759,8 @@ static lr_status check_attn(lr_dtype dt, int b, int s, int H, int dh) {
   if (b < 1 || H < 1 || s < 256 || s % 256 || dh < 128 || dh % 128)
     return fail(LR_ERR_SHAPE, "attention: b = %d, H = %d >= 1, s = %d a multiple of 256, dh = %d of 128 needed", b,
                 H, s, dh);
-  if (1LL * b * H * s * s > (1LL << 40)) return fail(LR_ERR_SHAPE, "attention: b*H*s*s too large");
+  if (1LL * b * H * s * s > (1LL << 40) || 1LL * b * H * s > (1LL << 30))
+    return fail(LR_ERR_SHAPE, "attention: b*H*s*s or b*H*s too large");
   return LR_OK;
 }
 
