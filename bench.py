@@ -398,7 +398,7 @@ def _roofline(flops, nbytes, ms, pk):
 
 
 def run_other(a):
-    """Non-default workloads (one JSON line each): attn_proj, stack, sweep, dense, block."""
+    """Non-default workloads (one JSON line each): attn_proj, stack, sweep, dense, block, attention."""
     import torch
 
     from rank_bottleneck_block_gb300 import build as B
@@ -406,8 +406,8 @@ def run_other(a):
     B.build()
     from rank_bottleneck_block_gb300 import inputs as I
     from rank_bottleneck_block_gb300 import lowrank as L
-    from rank_bottleneck_block_gb300.runner import (BlockStack, DenseBlock, GraphStep, MlpBlock, ProjGroup,
-                                                     TransformerBlock)
+    from rank_bottleneck_block_gb300.runner import (Attention, BlockStack, DenseBlock, GraphStep, MlpBlock,
+                                                     ProjGroup, TransformerBlock)
 
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
@@ -503,6 +503,26 @@ def run_other(a):
                              "256 x 256 tiles on or below the diagonal; the per-kernel figures count those)",
                **_roofline(flops, nbytes, ms, pk), "kernels": kernels}
         print(json.dumps(res), flush=True)
+    elif a.workload == "attention":
+        # Causal multi-head attention alone at LLaMA-7B widths (32 heads of 128, 2048 tokens per
+        # sequence), fwd+bwd; --attn-batch sequences.
+        b, s, H, dh = a.attn_batch, 2048, 32, 128
+        g = torch.Generator().manual_seed(0)
+        q, k, v, dout = (torch.randn(b * s, H * dh, generator=g).to(torch.bfloat16) for _ in range(4))
+        at = Attention(b, s, H, dh, q, k, v, device=dev)
+        at.dout.copy_(dout.to(dev))
+        ms = _time_steps(at.step, a.steps, a.warmup, flush, stream)
+        L.lr_check_device_error()
+        kernels = _kernel_table(at.step, flush, stream)
+        half = 1.0 * b * H * s * s * dh  # one causal GEMM: 2 (s^2 / 2) dh per head
+        flops = 7 * half  # fwd Q K^T, P V; bwd Q K^T, dO V^T, P^T dO, dS K, dS^T Q
+        elems = 1.0 * b * H * s * (s + 256) / 2  # stored score elements (up to each row's key-tile end)
+        nbytes = 22.0 * elems + 4.0 * b * s * H * dh * 2 * 3  # scores: S 4+4, P 2+2+2+2, dS 2+2+2; q,k,v,o,grads
+        res = {"workload": f"causal attention fwd+bwd, b={b} s={s} H={H} dh={dh}, bf16 (scores materialised in HBM)",
+               "ms_per_step": round(ms, 4), "tokens_per_s": round(b * s / (ms / 1e3), 1),
+               "flops_note": "algorithmic: the causal half of the seven s x s x dh products",
+               **_roofline(flops, nbytes, ms, pk), "kernels": kernels}
+        print(json.dumps(res), flush=True)
     elif a.workload == "sweep":
         rows = []
         for shp in I.sweep_shapes():
@@ -564,7 +584,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["mlp_block", "attn_proj", "stack", "sweep", "dense", "block"],
+    ap.add_argument("--attn-batch", type=int, default=8, help="sequences of the attention workload")
+    ap.add_argument("--workload", choices=["mlp_block", "attn_proj", "stack", "sweep", "dense", "block", "attention"],
                     default="mlp_block",
                     help="mlp_block is the benchmark line; the others print their own measurement lines")
     a = ap.parse_args(argv)
