@@ -61,7 +61,8 @@ struct GemmCall {
 constexpr int kChunkUmma = 32;  // the tcgen05 epilogue chunk (umma::CW)
 constexpr int kChunkSimt = 8;
 
-template <EpiKind K, int BN, bool A_MN, bool B_MN>
+// RB: the kernel built for row-batched calls (g.rowbatch must equal it).
+template <EpiKind K, int BN, bool A_MN, bool B_MN, bool RB = false>
 cudaError_t launch_umma(const GemmCall& g, cudaStream_t st);
 
 template <EpiKind K>

@@ -182,14 +182,32 @@ static int pick_bn(const GemmCall& g, int sms) {
   return c128 < c256 ? 128 : 256;
 }
 
-template <EpiKind K, bool A_MN, bool B_MN>
+template <EpiKind K, bool A_MN, bool B_MN, bool RB = false>
 static cudaError_t umma_bn(const GemmCall& g, cudaStream_t st) {
-  if (g.bn == 128) return launch_umma<K, 128, A_MN, B_MN>(g, st);
-  return launch_umma<K, 256, A_MN, B_MN>(g, st);
+  if (g.bn == 128) return launch_umma<K, 128, A_MN, B_MN, RB>(g, st);
+  return launch_umma<K, 256, A_MN, B_MN, RB>(g, st);
+}
+
+// Row-batched calls (the attention GEMMs over all heads) run the kernels built for them.
+static cudaError_t dispatch_rowbatch(EpiKind k, GemmCall& g, cudaStream_t st) {
+  const bool kk = !g.a_mn && !g.b_mn, km = !g.a_mn && g.b_mn, mm = g.a_mn && g.b_mn;
+  switch (k) {
+    case EPI_F32: if (kk) return umma_bn<EPI_F32, false, false, true>(g, st); break;
+    case EPI_STORE:
+      if (km) return umma_bn<EPI_STORE, false, true, true>(g, st);
+      if (mm) return umma_bn<EPI_STORE, true, true, true>(g, st);
+      break;
+    case EPI_ATTN_BWD:
+      if (kk && g.nacc == 2) return launch_umma<EPI_ATTN_BWD, 256, false, false, true>(g, st);
+      break;
+    default: break;
+  }
+  return cudaErrorNotSupported;
 }
 
 static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sms) {
   (void)sms;
+  if (g.rowbatch) return dispatch_rowbatch(k, g, st);
   const bool kk = !g.a_mn && !g.b_mn, km = !g.a_mn && g.b_mn, mm = g.a_mn && g.b_mn;
   switch (k) {
     case EPI_NORM_SILU: if (kk) return umma_bn<EPI_NORM_SILU, false, false>(g, st); break;
@@ -197,7 +215,6 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_STORE:
       if (kk) return umma_bn<EPI_STORE, false, false>(g, st);
       if (km) return umma_bn<EPI_STORE, false, true>(g, st);
-      if (mm) return umma_bn<EPI_STORE, true, true>(g, st);
       break;
     case EPI_RESID: if (kk) return umma_bn<EPI_RESID, false, false>(g, st); break;
     case EPI_SWIGLU:
@@ -212,12 +229,8 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
     case EPI_DX_NORM: if (km) return umma_bn<EPI_DX_NORM, false, true>(g, st); break;
-    case EPI_ATTN_BWD:
-      if (kk && g.nacc == 2 && g.rowbatch) return launch_umma<EPI_ATTN_BWD, 256, false, false>(g, st);
-      break;
     case EPI_F32:
       if (mm) return umma_bn<EPI_F32, true, true>(g, st);
-      if (kk) return umma_bn<EPI_F32, false, false>(g, st);
       break;
     default: break;
   }

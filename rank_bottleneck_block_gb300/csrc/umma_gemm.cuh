@@ -405,12 +405,15 @@ __device__ __forceinline__ void k_range(const Shape& sh, int split, int mb, int&
   if (sh.causal == 3) kb0 = max(kb0, row0 / BK);
 }
 
-// Where batch `batch` of a row-batched problem starts in each tensor (all 0 otherwise).
+// Where batch `batch` of a row-batched problem starts in each tensor (all 0 otherwise).  RB: the
+// kernel is built for row-batched problems (the per-batch offsets and the causal tile schedule
+// exist only there, so the other kernels carry none of that code).
 struct BatchOff {
   int ra, ca, rb, cb, ro, co;  // stored row and column of A, B and the output
 };
+template <bool RB>
 __device__ __forceinline__ BatchOff batch_off(const Shape& sh, int batch) {
-  if (!sh.rowbatch) return BatchOff{0, 0, 0, 0, 0, 0};
+  if (!RB || !sh.rowbatch) return BatchOff{0, 0, 0, 0, 0, 0};
   const int hi = batch / sh.bh, lo = batch - hi * sh.bh;
   return BatchOff{hi * sh.rb_a + lo * sh.rl_a, lo * sh.cb_a, hi * sh.rb_b + lo * sh.rl_b,
                   lo * sh.cb_b, hi * sh.rb_o + lo * sh.rl_o, lo * sh.cb_o};
@@ -418,12 +421,14 @@ __device__ __forceinline__ BatchOff batch_off(const Shape& sh, int batch) {
 
 // Pair tiles of one batch.  Causal mode 1 (M = N) schedules only the tiles on or below the
 // diagonal: pair p (rows 256 p .. 256 p + 255) takes its first (p + 1) u key tiles, u = 256 / BN.
-__host__ __device__ inline int batch_tiles(const Shape& sh) {
-  if (sh.causal == 1) return sh.n_tiles / sh.m_pairs * (sh.m_pairs * (sh.m_pairs + 1) / 2);
+template <bool RB>
+__host__ __device__ __forceinline__ int batch_tiles(const Shape& sh) {
+  if (RB && sh.causal == 1) return sh.n_tiles / sh.m_pairs * (sh.m_pairs * (sh.m_pairs + 1) / 2);
   return sh.m_pairs * sh.n_tiles;
 }
 
-__host__ __device__ inline void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
+template <bool RB>
+__host__ __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, int rank, int& split, int& batch, int& mb,
                                             int& nb) {
   if (sh.grouped) {
     const int per_split = sh.g_tiles;
@@ -447,14 +452,14 @@ __host__ __device__ inline void decode_tile(const Shape& sh, int tile, int rank,
     mb = 2 * mp + rank;
     return;
   }
-  const int per_batch = batch_tiles(sh);
+  const int per_batch = batch_tiles<RB>(sh);
   const int per_split = sh.batches * per_batch;
   if (sh.reverse) tile = sh.ksplit * per_split - 1 - tile;
   split = tile / per_split;
   int rem = tile - split * per_split;
   batch = rem / per_batch;
   rem -= batch * per_batch;
-  if (sh.causal == 1) {
+  if (RB && sh.causal == 1) {
     const int u = sh.n_tiles / sh.m_pairs;  // key tiles per pair of query tiles
     const int q = rem / u;                  // pair p holds q in [p (p + 1) / 2, (p + 1) (p + 2) / 2)
     int p = static_cast<int>((sqrtf(8.f * q + 1.f) - 1.f) * 0.5f);
@@ -469,7 +474,7 @@ __host__ __device__ inline void decode_tile(const Shape& sh, int tile, int rank,
   mb = 2 * mp + rank;
 }
 
-template <EpiKind K, int BN, bool A_MN, bool B_MN>
+template <EpiKind K, int BN, bool A_MN, bool B_MN, bool RB>
 __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     gemm_kernel(const __grid_constant__ Maps maps, const Shape sh, const EpiParams ep) {
   using C = Config<K, BN>;
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   const int ncl = static_cast<int>(gridDim.x >> 1);
   constexpr uint16_t kBoth = 0x3;
   const int total =  // pair tiles
-      sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * batch_tiles(sh));
+      sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * batch_tiles<RB>(sh));
 
   if (warp == 0) {
     if (lane == 0) {
@@ -549,12 +554,12 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       bool ok = true;
       for (int tile = cid; tile < total && ok; tile += ncl) {
         int split, batch, mb, nb;
-        decode_tile(sh, tile, rank, split, batch, mb, nb);
+        decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
         int kb0, kb1;
         k_range(sh, split, mb, kb0, kb1);
         const int m0 = mb * BM, n0 = nb * BN;
         const int set0 = sh.rowbatch ? 0 : batch;
-        const BatchOff bo = batch_off(sh, batch);
+        const BatchOff bo = batch_off<RB>(sh, batch);
         for (int s = 0; s < NACC && ok; ++s) {
           const int set = NACC > 1 ? s : set0;
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -615,7 +620,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       bool ok = true;
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
         int split, batch, mb, nb;
-        decode_tile(sh, tile, rank, split, batch, mb, nb);
+        decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
         int kb0, kb1;
         k_range(sh, split, mb, kb0, kb1);
         const int buf = C::NBUF == 2 ? (it & 1) : 0;
@@ -682,7 +687,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     bool ok = true;
     for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
-      decode_tile(sh, tile, rank, split, batch, mb, nb);
+      decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
       int kb0, kb1;
       k_range(sh, split, mb, kb0, kb1);
       float ss = 0.f;
@@ -751,7 +756,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     };
     auto issue_aux = [&](int t, int c, int b) {
       int split, batch, mb, nb;
-      decode_tile(sh, t, rank, split, batch, mb, nb);
+      decode_tile<RB>(sh, t, rank, split, batch, mb, nb);
       uint32_t bytes = 0;
 #pragma unroll
       for (int a = 0; a < NAUX; ++a)
@@ -786,14 +791,14 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     int qi = 0;  // index of the warp's current chunk in its sequence
     for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
-      decode_tile(sh, tile, rank, split, batch, mb, nb);
+      decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
       const int buf = C::NBUF == 2 ? (it & 1) : 0;
       const uint32_t tph = static_cast<uint32_t>(C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1));
       const int sbuf = it & 1;  // statistics double buffer (independent of TMEM)
       const uint32_t sph = static_cast<uint32_t>((it >> 1) & 1);
       const int m = mb * BM + row;
       const int ob = sh.rowbatch ? 0 : batch;                 // output maps and pointers of this batch
-      const BatchOff bo = batch_off(sh, batch);
+      const BatchOff bo = batch_off<RB>(sh, batch);
       const int r0 = mb * BM + q * ER + bo.ro;  // first stored row of this warp's boxes
       const int x0 = nb * BN + bo.co;           // first stored column of the tile
       // Causal mode 1: a tile wholly above the diagonal (every column past every row) is not stored

@@ -70,7 +70,7 @@ inline bool encode_epi_f32(CUtensorMap* m, const void* ptr, long long N, long lo
 
 }  // namespace umma
 
-template <EpiKind K, int BN, bool A_MN, bool B_MN>
+template <EpiKind K, int BN, bool A_MN, bool B_MN, bool RB>
 cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   using namespace umma;
   using C = Config<K, BN>;
@@ -93,6 +93,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   sh.ksplit = (sh.kb_total + sh.kb_per_split - 1) / sh.kb_per_split;  // no empty split
   sh.err = g.err;
   sh.reverse = g.reverse ? 1 : 0;
+  if (g.rowbatch != RB) return cudaErrorInvalidValue;
   if (!g.rowbatch && !g.grouped && NACC == 1 && (g.batches < 1 || g.batches > kMaxBatch)) return cudaErrorInvalidValue;
   if (g.rowbatch) {  // one tensor per operand, batches offset by rows
     if (D::NAUX > 0 || C::STATS || ((C::SPLIT || NACC > 1) && K != EPI_ATTN_BWD) || D::ROWPART || g.grouped ||
@@ -172,10 +173,10 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   }
 
   const long long total =  // pair tiles
-      1LL * sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * batch_tiles(sh));
+      1LL * sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * batch_tiles<RB>(sh));
   if (total <= 0) return cudaSuccess;
 
-  auto kern = gemm_kernel<K, BN, A_MN, B_MN>;
+  auto kern = gemm_kernel<K, BN, A_MN, B_MN, RB>;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[2];
