@@ -36,8 +36,8 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * ((45.188608e6 + 133.24928e6) + (71.276544e6 + 499.664128e6)),
-                          "sources_sha256": "9559d1a3eb17984d1e920e3ba043ae3e38e990f3324b4122055b2eb76db5904d",
+    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * ((45.190144e6 + 133.039104e6) + (67.503872e6 + 499.80032e6)),
+                          "sources_sha256": "2327805bc78d7178ddd44eb78cfd658bf493f240c50c65edb4608b871bdf19ed",
                           "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
 }
 

@@ -214,11 +214,12 @@ lr_status lr_btp_finish(lr_dtype dt, lr_act act, int T, int d, int r, int group,
  * q, k, v, o, dout, dq, dk, dv: [b*s, H*dh] bf16, token-major as the projections write
  * them (head h of token t in columns h*dh .. h*dh + dh - 1 of row t = batch*s + position).
  * saved: lr_attn_saved_bytes (the row log-sum-exp of S, fp32 [b*H*s]); the backward
- * recomputes S from q and k.  ws: lr_attn_workspace_bytes (head-major copies of the eight
- * [b*s, H*dh] tensors, S and dP in fp32, P and dS in bf16, D: 12 b*H*s*s + 16 b*H*s*dh
- * + 4 b*H*s bytes plus alignment), owned by the caller; the forward uses a part of it.
- * bf16 only (LR_F32: LR_ERR_UNSUPPORTED).  s a multiple of 256, dh a multiple of 128
- * (LR_ERR_SHAPE otherwise); pointers 16-byte aligned (LR_ERR_ALIGN).
+ * recomputes S from q and k.  ws: lr_attn_workspace_bytes (the head-major scores
+ * [b*H*s, s]: S in fp32, whose first half holds dS in bf16 during the backward, P in bf16;
+ * D in fp32 [b*H*s]: 6 b*H*s*s + 4 b*H*s bytes plus alignment), owned by the caller.  The
+ * kernels read q, k, v, o, dout and write o, dq, dk, dv in place.  bf16 only (LR_F32:
+ * LR_ERR_UNSUPPORTED).  s a multiple of 256, dh a multiple of 128, b*H*s at most 2^30 and
+ * b*H*s*s at most 2^40 (LR_ERR_SHAPE otherwise); pointers 16-byte aligned (LR_ERR_ALIGN).
  */
 size_t lr_attn_saved_bytes(int b, int s, int H, int dh);
 size_t lr_attn_workspace_bytes(int b, int s, int H, int dh);
