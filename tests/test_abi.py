@@ -101,6 +101,9 @@ def test_attention_shape_rules(L):
     assert L.lr_attn_workspace_bytes(2, 256, 3, 128) > 6 * 2 * 3 * 256 * 256  # fp32 S and bf16 P
     assert L.lr_attn_saved_bytes(1, 200, 1, 128) == 0  # s not a multiple of 256
     assert L.lr_attn_workspace_bytes(1, 256, 1, 64) == 0  # dh not a multiple of 128
+    assert L.lr_attn_saved_bytes(1 << 15, 256, 1 << 8, 128) == 0  # b*H*s = 2^31 score rows
+    assert L.lr_attn_saved_bytes(1 << 14, 256, 1 << 8, 128) > 0  # 2^30: the largest allowed
+    assert L.lr_attn_saved_bytes(1, 1 << 16, 1 << 9, 128) == 0  # b*H*s*s = 2^41
     lib = L.lib()
     null = None
     assert lib.lr_attn_fwd(L.LR_F32, 1, 256, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 8
