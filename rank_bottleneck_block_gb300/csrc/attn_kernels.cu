@@ -121,27 +121,32 @@ __global__ void __launch_bounds__(128, 4) attn_softmax_fwd_reg_kernel(const floa
   }
 }
 
+// G lanes per row (32 when dh is a multiple of 256, else 16: dh is a multiple of 128), 32 / G rows
+// per warp; each lane takes 8 consecutive channels at a time.
+template <int G>
 __global__ void attn_rowdot_kernel(const bf16* dO, const bf16* O, int b, int s, int H, int dh, float* D) {
   pdl_wait();
   pdl_trigger();
   const int R = b * H * s;
-  const int r = static_cast<int>((blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= R) return;
+  const long long gt = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const int r = static_cast<int>(gt / G);
+  const int sub = threadIdx.x & (G - 1);
+  if (r >= R) return;  // whole lane groups leave together (R rows of G lanes each)
   const int n = r / s, i = r - n * s;  // head n = bi*H + h, query i
   const int bi = n / H, h = n - bi * H;
   const long long base = (1LL * bi * s + i) * H * dh + 1LL * h * dh;
   float acc = 0.f;
-  for (int c = lane * 8; c < dh; c += 256) {
+  for (int c = sub * 8; c < dh; c += G * 8) {
     float a[8], o[8];
     load8(dO + base + c, a);
     load8(O + base + c, o);
 #pragma unroll
     for (int t = 0; t < 8; ++t) acc = fmaf(a[t], o[t], acc);
   }
+  const unsigned mask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (threadIdx.x & 31 & ~(G - 1)));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) D[r] = acc;
+  for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
+  if (sub == 0) D[r] = acc;
 }
 
 dim3 warp_rows_grid(int R) { return dim3(static_cast<unsigned>((R + 7) / 8)); }
@@ -161,7 +166,11 @@ cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int b, int s, int 
                                cudaStream_t st) {
   const int R = b * H * s;
   if (R == 0) return cudaSuccess;
-  return launch_pdl(attn_rowdot_kernel, warp_rows_grid(R), dim3(256), 0, st, dO, O, b, s, H, dh, D);
+  if (dh % 256 == 0)  // a warp per row
+    return launch_pdl(attn_rowdot_kernel<32>, warp_rows_grid(R), dim3(256), 0, st, dO, O, b, s, H, dh, D);
+  // dh = 128 (mod 256): a half warp per row, 16 rows per block of 256 threads
+  return launch_pdl(attn_rowdot_kernel<16>, dim3(static_cast<unsigned>((R + 15) / 16)), dim3(256), 0, st, dO, O, b,
+                    s, H, dh, D);
 }
 
 }  // namespace lr
