@@ -1772,6 +1772,10 @@ static lr_status check_attn(lr_dtype dt, int b, int s, int H, int dh) {
   if (b < 1 || H < 1 || s < 256 || s % 256 || dh < 128 || dh % 128)
     return fail(LR_ERR_SHAPE, "attention: b = %d, H = %d >= 1, s = %d a multiple of 256, dh = %d of 128 needed", b,
                 H, s, dh);
+  // Tokens b*s and channels H*dh are formed in int by the callers of this check: bound them first.
+  if (1LL * b * s > (1 << 24) || 1LL * H * dh > (1 << 24))
+    return fail(LR_ERR_SHAPE, "attention: b*s = %lld tokens and H*dh = %lld channels must not exceed 16777216",
+                1LL * b * s, 1LL * H * dh);
   if (1LL * b * H * s * s > (1LL << 40) || 1LL * b * H * s > (1LL << 30))
     return fail(LR_ERR_SHAPE, "attention: b*H*s*s or b*H*s too large");
   return LR_OK;

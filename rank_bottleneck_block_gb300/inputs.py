@@ -37,6 +37,9 @@ __all__ = [
     "ATTN_PROJ_BF16",
     "STACK_BF16",
     "sweep_shapes",
+    "EXTREMES",
+    "make_extreme_mlp_case",
+    "make_extreme_proj_case",
 ]
 
 
@@ -234,3 +237,60 @@ def sample_rows(T: int, n: int, seed: int = 1) -> torch.Tensor:
     idx = torch.randperm(T, generator=gen)[: n - 2]
     idx = torch.cat([idx, torch.tensor([0, T - 1])]).unique()
     return idx.sort().values
+
+
+# Inputs at the edges of the arithmetic (same draws as the plain cases, then reshaped):
+#   "saturated": the A factors that read the input (gate and up of a block, every A of a group)
+#                scaled by 30 and their B factors by 1/30, so their pre-activations u reach
+#                |u| ~ 30-130 in both signs (SiLU and SiLU' saturated, e^-u past the fp32 range)
+#                while what follows the pair keeps its usual scale.  The scaled pairs are those
+#                whose u is computed from the stored input itself: a pre-activation of large
+#                scale computed from rounded intermediates carries an absolute error of that
+#                scale times the storage precision, which SiLU' (slope 1/2 at 0) turns into
+#                relative errors of several percent near u = 0 for any bf16-storing path;
+#   "zero_rows": rows 0 and the last of x set to 0 (1/rms = eps^-1/2 = 1000 on a zero row) and row 5
+#                scaled by 1e-3 (mean square ~ eps: the eps term decides 1/rms);
+#   "big_rows":  rows 1 and 6 of x scaled by 1e3 (sums of squares ~1e9 next to rows of ~1).
+EXTREMES = ("saturated", "zero_rows", "big_rows")
+_SAT_SCALE = 30.0
+_BIG = 1e3
+
+
+def _reshape_x(x: torch.Tensor, kind: str) -> torch.Tensor:
+    x = x.clone()
+    T = x.shape[0]
+    if kind == "zero_rows":
+        tiny = min(5, T - 1)
+        x[tiny] = (x[tiny].float() * 1e-3).to(x.dtype)
+        x[[0, T - 1]] = 0
+    elif kind == "big_rows":
+        rows = sorted({min(1, T - 1), min(6, T - 1)})
+        x[rows] = (x[rows].float() * _BIG).to(x.dtype)
+    return x
+
+
+def make_extreme_mlp_case(shape: MlpShape, kind: str, seed: int = 0) -> Dict[str, torch.Tensor]:
+    """make_mlp_case(shape, seed) reshaped to one of EXTREMES (host tensors, rounded to the dtype)."""
+    if kind not in EXTREMES:
+        raise ValueError(kind)
+    c = make_mlp_case(shape, seed)
+    if kind == "saturated":
+        for k in ("gate", "up"):
+            c["A_" + k] = (c["A_" + k].float() * _SAT_SCALE).to(c["A_" + k].dtype)
+            c["B_" + k] = (c["B_" + k].float() / _SAT_SCALE).to(c["B_" + k].dtype)
+    else:
+        c["x"] = _reshape_x(c["x"], kind)
+    return c
+
+
+def make_extreme_proj_case(shape: ProjShape, kind: str, seed: int = 0) -> Dict[str, object]:
+    """make_proj_case(shape, seed) reshaped to one of EXTREMES."""
+    if kind not in EXTREMES:
+        raise ValueError(kind)
+    c = make_proj_case(shape, seed)
+    if kind == "saturated":
+        c["A"] = [(A.float() * _SAT_SCALE).to(A.dtype) for A in c["A"]]
+        c["B"] = [(B.float() / _SAT_SCALE).to(B.dtype) for B in c["B"]]
+    else:
+        c["x"] = _reshape_x(c["x"], kind)
+    return c

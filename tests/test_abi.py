@@ -104,6 +104,12 @@ def test_attention_shape_rules(L):
     assert L.lr_attn_saved_bytes(1 << 15, 256, 1 << 8, 128) == 0  # b*H*s = 2^31 score rows
     assert L.lr_attn_saved_bytes(1 << 14, 256, 1 << 8, 128) > 0  # 2^30: the largest allowed
     assert L.lr_attn_saved_bytes(1, 1 << 16, 1 << 9, 128) == 0  # b*H*s*s = 2^41
+    # tokens b*s and channels H*dh bounded before anything forms them in int
+    assert L.lr_attn_saved_bytes(1 << 16, 512, 1, 128) == 0  # b*s = 2^25 tokens
+    assert L.lr_attn_saved_bytes(1 << 15, 512, 1, 128) > 0  # 2^24: the largest allowed
+    assert L.lr_attn_workspace_bytes(1, 256, 1 << 20, 4096) == 0  # H*dh = 2^32 would wrap an int
+    assert L.lr_attn_saved_bytes(1, 256, 1 << 17, 128) > 0  # H*dh = 2^24: the largest allowed
+    assert L.lr_attn_saved_bytes(1, 256, (1 << 17) + 1, 128) == 0  # one head more
     lib = L.lib()
     null = None
     assert lib.lr_attn_fwd(L.LR_F32, 1, 256, 1, 128, 1.0, null, null, null, null, null, 0, null, 0, null) == 8
@@ -117,6 +123,8 @@ def test_block_shape_rules(L):
     assert L.lr_block_workspace_bytes(*dims) >= L.lr_attn_workspace_bytes(1, 256, 2, 128)
     assert L.lr_block_saved_bytes(1, 200, 2, 128, 344, 32, 48) == 0  # s not a multiple of 256
     assert L.lr_block_saved_bytes(1, 256, 2, 128, 343, 32, 48) == 0  # f not a multiple of 8
+    assert L.lr_block_saved_bytes(1 << 16, 512, 1, 128, 344, 32, 48) == 0  # b*s = 2^25 tokens
+    assert L.lr_block_workspace_bytes(1, 256, 1 << 20, 4096, 344, 32, 48) == 0  # H*dh = 2^32
     lib = L.lib()
     w, g = L.lr_block_weights(), L.lr_block_grads()
     assert lib.lr_block_fwd(L.LR_F32, *dims, 1e-6, None, ctypes.byref(w), None, None, 0, None, 0, None) == 8

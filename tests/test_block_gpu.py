@@ -2,19 +2,18 @@
 
 The block chains the q/k/v group, causal attention, the o-projection with its residual and
 the MLP block; the oracle chains its own pieces (pinned on their own and, composed, by finite
-differences).  Metric: per-tensor max-relative error, bound 2e-2 (bf16 storage).  At full
+differences).  Figures (oracle.compare): per-tensor max-relative error, the same per row and
+per column, and the element-wise error above the bf16 floor, each bound 2e-2 (bf16 storage).  At full
 width the oracle runs on whole sequences: each sequence's outputs and input gradient depend
 only on that sequence.
 """
-import numpy as np
 import pytest
 import torch
 
 import oracle.attention_oracle as A
+import oracle.compare as C
 
 pytestmark = pytest.mark.gpu
-
-TOL = 2e-2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,12 +25,6 @@ def _lib():
 
     L.lib()
     yield
-
-
-def _maxrel(gpu, ref):
-    g = gpu.float().cpu().double().numpy()
-    assert np.all(np.isfinite(g))
-    return float(np.max(np.abs(g - ref)) / np.max(np.abs(ref)))
 
 
 def _run(shape, seed):
@@ -66,13 +59,12 @@ def test_block_matches_oracle(dims):
     shape = I.BlockShape(*dims)
     case, blk = _run(shape, seed=sum(dims))
     out, gr = _oracle(case, shape)
-    errs = {"out": _maxrel(blk.out, out), "dx": _maxrel(blk.dx, gr["dx"]),
-            "dg_attn": _maxrel(blk.dg_attn, gr["dg_attn"]), "dg_mlp": _maxrel(blk.dg_mlp, gr["dg_mlp"])}
+    errs = {"out": C.metrics(blk.out, out), "dx": C.metrics(blk.dx, gr["dx"]),
+            "dg_attn": C.metrics(blk.dg_attn, gr["dg_attn"]), "dg_mlp": C.metrics(blk.dg_mlp, gr["dg_mlp"])}
     for n in ("q", "k", "v", "o", "gate", "up", "down"):
         for m in ("A", "B"):
-            errs[f"d{m}_{n}"] = _maxrel(blk.grads[f"d{m}_{n}"], gr[f"d{m}_{n}"])
-    bad = {k: v for k, v in errs.items() if not v <= TOL}
-    assert not bad, errs
+            errs[f"d{m}_{n}"] = C.weight(blk.grads[f"d{m}_{n}"], gr[f"d{m}_{n}"])
+    C.assert_close(errs, "bf16", f"block {dims}")
 
 
 @pytest.mark.slow
@@ -86,8 +78,8 @@ def test_block_full_width_sampled_sequences():
     for bi in (0, shape.b - 1):
         rows = slice(bi * shape.s, (bi + 1) * shape.s)
         out, gr = _oracle(case, shape, rows)
-        errs = {"out": _maxrel(blk.out[rows], out), "dx": _maxrel(blk.dx[rows], gr["dx"])}
-        assert all(e <= TOL for e in errs.values()), (bi, errs)
+        errs = {"out": C.metrics(blk.out[rows], out), "dx": C.metrics(blk.dx[rows], gr["dx"])}
+        C.assert_close(errs, "bf16", f"sequence {bi}")
 
 
 def test_block_steps_back_to_back_repeat_bitwise():

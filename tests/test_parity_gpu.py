@@ -1,14 +1,18 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
-Metric: per tensor, max_i |gpu_i - ref_i| / max_i |ref_i| (max-relative error),
-bound 2e-2 for bf16 storage and 1e-5 for fp32.  Inputs are the seeded host
-arrays of rank_bottleneck_block_gb300.inputs; the oracle reads them widened to
-fp64, the GPU reads them as stored.
+Figures per tensor (oracle.compare): the max-relative error
+max_i |gpu_i - ref_i| / max_i |ref_i|, the same error per row and per column
+against that row's (column's) own largest value, and the element-wise error
+against max(|ref_i|, floor * max |ref|); each bound by 2e-2 for bf16 storage and
+1e-5 for fp32.  Inputs are the seeded host arrays of
+rank_bottleneck_block_gb300.inputs; the oracle reads them widened to fp64, the
+GPU reads them as stored.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle.compare as C
 import oracle.lowrank_oracle as O
 from rank_bottleneck_block_gb300 import inputs as I
 
@@ -28,12 +32,9 @@ def _lib():
     yield
 
 
-def maxrel(gpu, ref):
-    g = gpu.detach().float().cpu().double().numpy() if hasattr(gpu, "detach") else np.asarray(gpu)
-    ref = np.asarray(ref)
-    assert g.shape == ref.shape, (g.shape, ref.shape)
-    assert np.all(np.isfinite(g))
-    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-300))
+def close(gpu, ref, dtype, what=""):
+    """Every figure of oracle.compare within the dtype's tolerance."""
+    C.assert_close({what or "tensor": C.metrics(gpu, ref, dtype)}, dtype, what)
 
 
 def _sync_check():
@@ -46,10 +47,10 @@ def _sync_check():
 ACT_NAMES = {0: "silu", 1: "identity"}
 
 
-def run_mlp(shape, mode, seed=0, act=0):
+def run_mlp(shape, mode, seed=0, act=0, case=None):
     from rank_bottleneck_block_gb300.runner import MlpBlock
 
-    case = I.make_mlp_case(shape, seed)
+    case = I.make_mlp_case(shape, seed) if case is None else case
     blk = MlpBlock(shape, case, mode, act=act)
     blk.forward()
     blk.backward()
@@ -57,17 +58,18 @@ def run_mlp(shape, mode, seed=0, act=0):
     return case, blk
 
 
-def check_mlp(shape, mode, seed=0, act=0):
-    case, blk = run_mlp(shape, mode, seed, act)
+def check_mlp(shape, mode, seed=0, act=0, case=None):
+    case, blk = run_mlp(shape, mode, seed, act, case)
     ref_out, saved = O.mlp_block_fwd(case["x"], case["g"], case, shape.eps, O.FULL, act=ACT_NAMES[act])
     gr = O.mlp_block_bwd(case["g"], case, saved, case["G"], shape.eps, act=ACT_NAMES[act])
-    tol = TOL[shape.dtype]
-    errs = {"out": maxrel(blk.out, ref_out), "dx": maxrel(blk.dx, gr["dx"]), "dg": maxrel(blk.dg, gr["dg"])}
+    dt = shape.dtype
+    dgs = C.dg_scale([gr["dA_gate"], gr["dA_up"]], [case["A_gate"], case["A_up"]], case["g"])
+    errs = {"out": C.metrics(blk.out, ref_out, dt), "dx": C.metrics(blk.dx, gr["dx"], dt),
+            "dg": C.metrics(blk.dg, gr["dg"], dt, scale=dgs)}
     for k in ("gate", "up", "down"):
-        errs[f"dA_{k}"] = maxrel(blk.grads[f"dA_{k}"], gr[f"dA_{k}"])
-        errs[f"dB_{k}"] = maxrel(blk.grads[f"dB_{k}"], gr[f"dB_{k}"])
-    bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, f"{shape} mode={mode} act={act}: {errs}"
+        errs[f"dA_{k}"] = C.weight(blk.grads[f"dA_{k}"], gr[f"dA_{k}"], dt, shape.T)
+        errs[f"dB_{k}"] = C.weight(blk.grads[f"dB_{k}"], gr[f"dB_{k}"], dt, shape.T)
+    C.assert_close(errs, dt, f"{shape} mode={mode} act={act}")
     return errs, blk
 
 
@@ -211,26 +213,67 @@ def test_proj_group(norm, group, dtype):
     _check_proj(shape, seed=group)
 
 
-def _check_proj(shape, seed=0, act=0):
+def _check_proj(shape, seed=0, act=0, case=None):
     from rank_bottleneck_block_gb300.runner import ProjGroup
 
-    case = I.make_proj_case(shape, seed)
+    case = I.make_proj_case(shape, seed) if case is None else case
     pg = ProjGroup(shape, case, act=act)
     pg.forward()
     pg.backward()
     _sync_check()
     outs, saved = O.proj_group_fwd(case["x"], case["g"], case["A"], case["B"], shape.eps, act=ACT_NAMES[act])
     gr = O.proj_group_bwd(case["g"], case["A"], case["B"], saved, case["G"], act=ACT_NAMES[act])
-    tol = TOL[shape.dtype]
-    errs = {"dx": maxrel(pg.dx, gr["dx"])}
+    dt = shape.dtype
+    errs = {"dx": C.metrics(pg.dx, gr["dx"], dt)}
     if shape.norm:
-        errs["dg"] = maxrel(pg.dg, gr["dg"])
+        errs["dg"] = C.metrics(pg.dg, gr["dg"], dt, scale=C.dg_scale(gr["dA"], case["A"], case["g"]))
     for i in range(shape.group):
-        errs[f"out{i}"] = maxrel(pg.outs[i], outs[i])
-        errs[f"dA{i}"] = maxrel(pg.dA[i], gr["dA"][i])
-        errs[f"dB{i}"] = maxrel(pg.dB[i], gr["dB"][i])
-    bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, f"{shape}: {errs}"
+        errs[f"out{i}"] = C.metrics(pg.outs[i], outs[i], dt)
+        errs[f"dA{i}"] = C.weight(pg.dA[i], gr["dA"][i], dt, shape.T)
+        errs[f"dB{i}"] = C.weight(pg.dB[i], gr["dB"][i], dt, shape.T)
+    C.assert_close(errs, dt, str(shape))
+
+
+# ------------------------------------------------- inputs at the edges of the arithmetic
+# Pre-activations of |u| ~ 30-130 in both signs (SiLU saturated, e^-u beyond the fp32 range), zero
+# rows and an eps-dominated row of x (1/rms = 1000 and ~700), and rows of magnitude 1e3 next to rows
+# of magnitude 1: the online-RMSNorm statistics, the fused SiLU / SwiGLU epilogues and their
+# derivatives against the oracle where a clamp, an overflow or a sum of squares would show.
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("kind", I.EXTREMES)
+def test_mlp_extreme_inputs(kind, dtype, mode):
+    shape = I.MlpShape(T=200, d=136, f=328, r=40, dtype=dtype)
+    check_mlp(shape, mode, case=I.make_extreme_mlp_case(shape, kind, seed=9))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("kind", I.EXTREMES)
+def test_mlp_extreme_inputs_many_tiles(kind, mode):
+    """The same edges with several tiles in every GEMM dimension and split-K weight gradients."""
+    shape = I.MlpShape(T=2112, d=512, f=1376, r=128, dtype="bf16")
+    check_mlp(shape, mode, case=I.make_extreme_mlp_case(shape, kind, seed=10))
+
+
+# Rows of magnitude 1e3 are an edge of the RMSNorm statistics; a group without the norm would feed
+# them unnormalised into its pair, whose pre-activations then have a scale of 1e3 and an absolute
+# rounding error to match (the case the saturated inputs avoid), so that combination is not a case.
+@pytest.mark.parametrize("norm,kind", [(True, k) for k in I.EXTREMES] + [(False, "saturated"), (False, "zero_rows")])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_proj_group_extreme_inputs(kind, dtype, norm):
+    shape = I.ProjShape(T=260, d_in=200, d_out=136, r=48, group=3, norm=norm, dtype=dtype)
+    _check_proj(shape, case=I.make_extreme_proj_case(shape, kind, seed=12))
+
+
+def test_mlp_extreme_checkpoint_bitwise_equals_full():
+    """Checkpointed and full modes agree bit for bit with saturated pre-activations too."""
+    shape = I.MlpShape(T=520, d=256, f=688, r=64, dtype="bf16")
+    case = I.make_extreme_mlp_case(shape, "saturated", seed=13)
+    _, full = run_mlp(shape, 0, case=case)
+    _, ck = run_mlp(shape, 1, case=case)
+    assert torch.equal(full.out, ck.out) and torch.equal(full.dx, ck.dx) and torch.equal(full.dg, ck.dg)
+    for k in full.grads:
+        assert torch.equal(full.grads[k], ck.grads[k]), k
 
 
 # ------------------------------------------------- dense (full-rank) block
@@ -244,12 +287,12 @@ def check_dense(shape, seed=0):
     _sync_check()
     ref_out, saved = O.dense_mlp_fwd(case["x"], case["g"], case, shape.eps)
     gr = O.dense_mlp_bwd(case["g"], case, saved, case["G"])
-    tol = TOL[shape.dtype]
-    errs = {"out": maxrel(blk.out, ref_out), "dx": maxrel(blk.dx, gr["dx"]), "dg": maxrel(blk.dg, gr["dg"])}
+    dt = shape.dtype
+    errs = {"out": C.metrics(blk.out, ref_out, dt), "dx": C.metrics(blk.dx, gr["dx"], dt),
+            "dg": C.metrics(blk.dg, gr["dg"], dt)}
     for k in ("dW_gate", "dW_up", "dW_down"):
-        errs[k] = maxrel(blk.grads[k], gr[k])
-    bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, f"dense {shape}: {errs}"
+        errs[k] = C.weight(blk.grads[k], gr[k], dt, shape.T)
+    C.assert_close(errs, dt, f"dense {shape}")
     return blk
 
 
@@ -349,12 +392,15 @@ def test_stack_small(mode, dtype):
     loss, grads, dx = O.stack_step(case["x"], case["target"], case["blocks"], shape.eps, O.FULL)
     tol = TOL[dtype]
     assert abs(st.loss.item() - loss) / abs(loss) <= tol
-    assert maxrel(st.dx, dx) <= tol
+    errs = {"dx": C.metrics(st.dx, dx, dtype)}
     for l in range(3):
-        assert maxrel(st.dgs[l], grads[l]["dg"]) <= tol
+        b = case["blocks"][l]
+        dgs = C.dg_scale([grads[l]["dA_gate"], grads[l]["dA_up"]], [b["A_gate"], b["A_up"]], b["g"])
+        errs[f"dg{l}"] = C.metrics(st.dgs[l], grads[l]["dg"], dtype, scale=dgs)
         for k in ("gate", "up", "down"):
-            assert maxrel(st.grads[l][f"dA_{k}"], grads[l][f"dA_{k}"]) <= tol, (l, k)
-            assert maxrel(st.grads[l][f"dB_{k}"], grads[l][f"dB_{k}"]) <= tol, (l, k)
+            errs[f"dA_{k}{l}"] = C.weight(st.grads[l][f"dA_{k}"], grads[l][f"dA_{k}"], dtype)
+            errs[f"dB_{k}{l}"] = C.weight(st.grads[l][f"dB_{k}"], grads[l][f"dB_{k}"], dtype)
+    C.assert_close(errs, dtype, f"stack {shape} mode={mode}")
 
 
 def test_stack_checkpoint_bitwise():
@@ -389,7 +435,7 @@ def test_stack_full_size_sampled_rows():
     _sync_check()
     rows = I.sample_rows(shape.T, 24).numpy()
     ref = _oracle_stack_rows(case, rows, shape.T, shape.eps)
-    assert maxrel(st.dx[torch.from_numpy(rows).cuda()], ref) <= TOL["bf16"]
+    close(st.dx[torch.from_numpy(rows).cuda()], ref, "bf16", "stack dx (sampled rows)")
     assert np.isfinite(st.loss.item())
     full = L.lr_stack_workspace_bytes(L.LR_BF16, 0, 24, shape.T, shape.d, shape.f, shape.r)
     ckpt = L.lr_stack_workspace_bytes(L.LR_BF16, 1, 24, shape.T, shape.d, shape.f, shape.r)
