@@ -42,7 +42,10 @@ enum EpiKind : int {
   EPI_ATTN_BWD = 13,        // causal attention backward scores, row-batched over heads: acc0 = Q K^T,
                             //   acc1 = dO V^T; out0 = P = exp(coef acc0 - lse) (0 past the diagonal),
                             //   out1 = dS = coef P (acc1 - D); lse = rowscale, D = rowpart_in (global rows)
-  EPI_COUNT = 14
+  EPI_SWIGLU_REBWD = 14,    // checkpointed re-forward and SwiGLU backward of one tile: three accumulators
+                            //   a = round(acc0), b = round(acc1), dh = acc2; h = SiLU(a) b -> out0,
+                            //   da = dh b SiLU'(a) -> out1, db = dh SiLU(a) -> out2
+  EPI_COUNT = 15
 };
 
 constexpr int kMaxBatch = 4;

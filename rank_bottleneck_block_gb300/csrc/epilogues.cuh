@@ -235,6 +235,12 @@ struct EpiDef<EPI_ATTN_BWD> {  // P and dS of causal attention (the math lives i
 };
 
 template <>
+struct EpiDef<EPI_SWIGLU_REBWD> {  // h, da, db of a tile from a, b, dh (the math lives in the split-phase epilogue)
+  static constexpr int NACC = 3, NAUX = 0, NOUT = 3;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+};
+
+template <>
 struct EpiDef<EPI_F32> {  // fp32 weight-gradient partial
   static constexpr int NACC = 1, NAUX = 0, NOUT = 1;
   static constexpr bool OUT_F32 = true, NEED_S = false, NEED_RHO = false, ROWPART = false;

@@ -20,5 +20,7 @@ LR_INST(EPI_STORE, 128, false, true)
 LR_INST(EPI_STORE, 256, false, true)
 LR_INST(EPI_F32, 128, true, true)
 LR_INST(EPI_F32, 256, true, true)
+// the checkpointed re-forward fused with the SwiGLU backward (three K-major accumulators)
+LR_INST(EPI_SWIGLU_REBWD, 256, false, false)
 #undef LR_INST
 }  // namespace lr

@@ -228,6 +228,9 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, false, true>(g, st); break;
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
+    case EPI_SWIGLU_REBWD:
+      if (kk && g.nacc == 3) return launch_umma<EPI_SWIGLU_REBWD, 256, false, false>(g, st);
+      break;
     case EPI_DX_NORM: if (km) return umma_bn<EPI_DX_NORM, false, true>(g, st); break;
     case EPI_F32:
       if (mm) return umma_bn<EPI_F32, true, true>(g, st);
@@ -259,7 +262,7 @@ static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
 static const char* epi_name(EpiKind k) {
   static const char* names[] = {"norm_silu", "silu",       "store",  "resid",       "swiglu",        "dsilu",
                                 "dsilu_norm", "swiglu_bwd", "dx_norm", "f32", "norm_swiglu", "swiglu_bwd_norm",
-                                "f32_ss", "attn_bwd"};
+                                "f32_ss", "attn_bwd", "swiglu_rebwd"};
   return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
 }
 
@@ -274,6 +277,7 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   if (c.dt == LR_BF16) {
     if (k == EPI_SWIGLU) g.bn = kSwigluBn;
     else if (k == EPI_NORM_SWIGLU || k == EPI_ATTN_BWD) g.bn = 256;  // split-phase dual-accumulator kernels
+    else if (k == EPI_SWIGLU_REBWD) g.bn = 256;  // three accumulators take two TMEM regions in turn
     else if (g.bn != 128 && g.bn != 256) g.bn = pick_bn(g, c.sms);
   } else {
     g.bn = 0;
@@ -540,7 +544,8 @@ static size_t mlp_fwd_ws_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, 
 }
 
 struct MlpBwdWs {
-  void *Af, *z_gu, *z_d, *a, *b, *h;  // z/a/b/h: LR_SAVE_CKPT recompute only
+  void *Af, *z_gu, *z_d, *a, *b, *h;  // z/a/b/h: LR_SAVE_CKPT recompute only (a, b: fp32 engine)
+  void* AdT;                          // A_down^T [f, r]: LR_SAVE_CKPT on the tcgen05 engine
   void *du_d, *da, *db, *du_s;
   float *rowpart, *wpart, *dgpart;
 };
@@ -555,8 +560,12 @@ static size_t mlp_bwd_ws_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, 
   if (mode == LR_SAVE_CKPT) {
     W->z_gu = ar.take(es * T * 2 * r);
     W->z_d = ar.take(es * T * r);
-    W->a = ar.take(es * T * f);
-    W->b = ar.take(es * T * f);
+    if (dt == LR_BF16) {  // a and b live only in TMEM (the fused re-forward + SwiGLU backward)
+      W->AdT = ar.take(es * f * r);
+    } else {
+      W->a = ar.take(es * T * f);
+      W->b = ar.take(es * T * f);
+    }
     W->h = ar.take(es * T * f);
   }
   W->du_d = ar.take(es * T * r);
@@ -688,7 +697,32 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     } else {
       LR_TRY(silu_slabs(c, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, r}, T));
     }
-    LR_TRY(swiglu_gemm(c, T, f, r, z_gu, gate.B, up.B, h, a, b));
+    if (c.dt == LR_BF16) {
+      // One launch recomputes a = z_g B_gate^T and b = z_u B_up^T and computes dh = du_down A_down
+      // for each tile in three TMEM accumulators; its epilogue writes h (for dA_down) and the
+      // SwiGLU backward's da, db.  a and b never reach memory.  A_down is read K-major from a
+      // transposed copy, as are the other two B operands.
+      {
+        LaunchScope scope("transpose", c.st, 0, 2.0 * c.es * r * f);
+        cudaError_t e = launch_transpose(static_cast<const bf16*>(down.A), r, f, static_cast<bf16*>(W.AdT), c.st);
+        if (e != cudaSuccess) return fail(LR_ERR_CUDA, "transpose: %s", cudaGetErrorString(e));
+      }
+      GemmCall k = new_call(T, f, r);
+      k.nacc = 3;
+      k.A[0] = {z_gu, 2LL * r};
+      k.A[1] = {off(z_gu, c.es * r), 2LL * r};
+      k.A[2] = {W.du_d, r};
+      k.B[0] = {gate.B, r};
+      k.B[1] = {up.B, r};
+      k.B[2] = {W.AdT, r};
+      k.ep.out0[0] = h;
+      k.ep.out1[0] = W.da;
+      k.ep.out2[0] = W.db;
+      k.ep.ldo0 = k.ep.ldo1 = k.ep.ldo2 = f;
+      LR_TRY(gemm(c, EPI_SWIGLU_REBWD, k));
+    } else {
+      LR_TRY(swiglu_gemm(c, T, f, r, z_gu, gate.B, up.B, h, a, b));
+    }
   } else {
     z_gu = S.z_gu;
     z_d = S.z_d;
@@ -698,7 +732,7 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
   }
 
   // dh = du_down A_down; SwiGLU backward fused: da = dh b SiLU'(a), db = dh SiLU(a)
-  {
+  if (!(mode == LR_SAVE_CKPT && c.dt == LR_BF16)) {
     GemmCall k = new_call(T, f, r);
     k.reverse = mode == LR_SAVE_CKPT;  // a, b were just written by the re-forward: start on the last tiles
     k.b_mn = true;

@@ -53,6 +53,7 @@ constexpr int BK = 64;  // one 128-byte swizzle atom of bf16 along K
 constexpr int CW = 32;  // epilogue chunk width (columns)
 constexpr int ER = 32;  // rows of an epilogue staging tile: one warp's TMEM lane quarter
 constexpr int kMaxAuxSets = 4;  // operand-tile staging sets per epilogue warp, at most
+constexpr int kMaxAcc = 4;      // TMEM full / empty barrier pairs (a buffer each, or an accumulator each)
 
 // Operand-tile sets per epilogue warp: how many chunks ahead the operand loads run.  The
 // residual GEMM (K = r, one [T, d] operand streamed from HBM) gains from four; for the others
@@ -353,14 +354,20 @@ struct Config {
   static constexpr int OUT_ROW = CW * (D::OUT_F32 ? 4 : 2);
   static constexpr int OUT_BUF = ER * OUT_ROW;  // one warp's rows of a chunk
   static constexpr int AUX_BUF = ER * CW * 2;
-  static constexpr uint32_t ACC_COLS = NACC * BN;
+  // The three-accumulator re-forward + SwiGLU backward (a, b, dh of 256 columns each) keeps two
+  // TMEM regions of BN columns that its accumulators take in turn: in tile i, a and dh use region
+  // i mod 2 (dh once phase 1 has moved a out) and b the other one.
+  static constexpr bool TRIPLE = K == EPI_SWIGLU_REBWD;
+  static constexpr uint32_t ACC_COLS = TRIPLE ? 2 * BN : NACC * BN;
   // Two accumulator buffers when they fit in the 512 TMEM columns, else one.
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
   // SwiGLU with 256-wide accumulators (a and b fill TMEM): the two accumulators complete and
   // are released separately.  Phase 1 stages round(a) in shared memory (exact: a is stored
   // rounded) and frees a's columns for the next tile while b still accumulates; phase 2 moves
   // round(b) into registers, frees b's columns, then computes h.
-  static constexpr bool SPLIT = (K == EPI_SWIGLU || K == EPI_NORM_SWIGLU || K == EPI_ATTN_BWD) && NBUF == 1;
+  static constexpr bool SPLIT =
+      (K == EPI_SWIGLU || K == EPI_NORM_SWIGLU || K == EPI_ATTN_BWD || K == EPI_SWIGLU_REBWD) && NBUF == 1;
+  static_assert(!TRIPLE || BN == 256, "the three-accumulator kernel uses two regions of 256 columns");
   // Staging per epilogue warp: NO output sets of NOUT tiles (ping-pong when stores would
   // otherwise stall the next chunk), NA operand sets of NAUX tiles (loads NA chunks ahead),
   // and for the split SwiGLU the round(a) tiles of the warp's chunks.
@@ -390,7 +397,9 @@ struct Config {
   static_assert(OSET % 1024 == 0 || (OSET % 512 == 0 && !D::OUT_F32), "staging tiles keep swizzle alignment");
   static_assert(ASET % 512 == 0 && ABUF % 512 == 0, "staging tiles keep swizzle alignment");
   static_assert(NA <= kMaxAuxSets, "operand-tile barriers per warp");
-  static_assert(3 * 8 + 2 + 2 + 1 + kMaxAuxSets * kEpiWarps + 2 + 2 <= 127, "barriers, TMEM slot and flag fit");
+  static_assert(NACC <= kMaxAcc, "accumulator barriers");
+  static_assert(3 * 8 + kMaxAcc + kMaxAcc + 1 + kMaxAuxSets * kEpiWarps + 2 + 2 <= 127,
+                "barriers, TMEM slot and flag fit");
   static_assert(SMEM_BYTES <= kMaxSmem, "shared memory budget");
 };
 
@@ -492,8 +501,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* consumed = empty + STAGES;  // MMA done with a stage (statistics warps may read it)
   uint64_t* tfull = consumed + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + kMaxAcc;
+  uint64_t* drain = tempty + kMaxAcc;
   uint64_t* aux_full = drain + 1;                       // per epilogue warp and operand set
   uint64_t* sfull = aux_full + kMaxAuxSets * kEpiWarps;  // stats -> epilogue, per TMEM buffer
   uint64_t* sempty = sfull + 2;     // epilogue -> stats, per TMEM buffer
@@ -510,9 +519,11 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       mbar_init(&empty[i], C::STATS ? 4 : 1);  // MMA commit, or the statistics warps after it
       mbar_init(&consumed[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 2 * kEpiWarps);  // leader: one arrive per epilogue warp of both CTAs
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 4);
       mbar_init(&sempty[i], kEpiWarps);
     }
@@ -618,6 +629,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
+      uint32_t ruse[2] = {0u, 0u};  // TRIPLE: accumulations started in each TMEM region
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
         int split, batch, mb, nb;
         decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
@@ -633,14 +645,17 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           tc_fence_after();
         }
         for (int s = 0; s < NACC && ok; ++s) {
-          if (C::SPLIT) {  // accumulator s has its own full / empty barrier pair
-            if (!mbar_wait(&tempty[s], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+          // Split-phase kernels: accumulator s lives in region reg (its own full / empty pair).
+          const int reg = C::TRIPLE ? (s == 1 ? 1 - (it & 1) : (it & 1)) : s;
+          if (C::SPLIT) {
+            const uint32_t uph = C::TRIPLE ? (ruse[reg] & 1u) : tph;
+            if (!mbar_wait(&tempty[reg], uph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
             tc_fence_after();
           }
-          const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS + s * BN;
+          const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS + reg * BN;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
               ok = false;
@@ -664,7 +679,10 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               ph ^= 1u;
             }
           }
-          if (C::SPLIT && ok) umma_commit(&tfull[s], kBoth);
+          if (C::SPLIT && ok) {
+            umma_commit(&tfull[reg], kBoth);
+            if (C::TRIPLE) ++ruse[reg];
+          }
         }
         if (!C::SPLIT && ok) umma_commit(&tfull[buf], kBoth);
       }
@@ -789,6 +807,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     bool ok = true;
     int it = 0;
     int qi = 0;  // index of the warp's current chunk in its sequence
+    uint32_t euse[2] = {0u, 0u};  // TRIPLE: accumulations consumed from each TMEM region
     for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
       int split, batch, mb, nb;
       decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
@@ -902,6 +921,106 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[1]), 0));
+        if (!ok) break;
+      } else if constexpr (C::TRIPLE) {
+        // Checkpointed re-forward and SwiGLU backward of one tile.  The accumulators are a (z_g
+        // B_gate^T), b (z_u B_up^T) and dh (du_down A_down), in that MMA order; a and dh take region
+        // it mod 2 of TMEM, b the other.  Phase 1 stages round(a) in shared memory and releases its
+        // region (dh accumulates there next); phase 2 packs round(b) into registers and releases
+        // its region (the next tile's a); phase 3 reads dh chunk by chunk, releasing the region
+        // after the last load, and forms h = SiLU(a) b, da = dh b SiLU'(a), db = dh SiLU(a) (the
+        // expressions of the forward SwiGLU and of the separate SwiGLU backward: both paths give
+        // the same bits).  h is written over the chunk's a tile and stored from there; da, db go
+        // through the two output sets.
+        constexpr int NC = NCH / 2;
+        uint8_t* abuf = wstage + NO * C::OSET + NA * C::ASET;
+        const int r0g = it & 1, r1g = 1 - r0g;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        ok = mbar_wait(&tfull[r0g], euse[r0g] & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        ++euse[r0g];
+        tc_fence_after();
+        if (leader) bulk_wait_read_all();  // the previous tile's h stores have read the a tiles
+        __syncwarp();
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+          float v[CW];
+          tmem_ld32(t_row + r0g * BN + (g + 2 * ci) * CW, v);
+          tmem_ld_wait();
+          const uint32_t base = smem_addr(abuf + ci * C::OUT_BUF);
+#pragma unroll
+          for (int j = 0; j < CW / 8; ++j) sts_bf16x8(base + stage_off<64>(lane, j), &v[8 * j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[r0g]), 0));
+        uint32_t bpk[NC][CW / 2];
+        ok = mbar_wait(&tfull[r1g], euse[r1g] & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        ++euse[r1g];
+        tc_fence_after();
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+          float v[CW];
+          tmem_ld32(t_row + r1g * BN + (g + 2 * ci) * CW, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CW / 2; ++j) bpk[ci][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[r1g]), 0));
+        ok = mbar_wait(&tfull[r0g], euse[r0g] & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
+        ++euse[r0g];
+        tc_fence_after();
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+          const int c = g + 2 * ci;
+          wait_set_free();
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const int b = qi % NO;
+          const uint32_t abase = smem_addr(abuf + ci * C::OUT_BUF);
+          const uint32_t dbase = smem_addr(ostage(b));
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {  // 16 columns of dh at a time (register pressure)
+            float dh[CW / 2];
+            tmem_ld16(t_row + r0g * BN + c * CW + hh * (CW / 2), dh);
+            tmem_ld_wait();
+            if (ci == NC - 1 && hh == 1) {  // every dh column of this warp is in registers: region free
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[r0g]), 0));
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = 2 * hh + jj;
+              float av[8], hv[8], dav[8], dbv[8];
+              lds_bf16x8(abase + stage_off<64>(lane, j), av);
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                float b0, b1;
+                unpack_bf16x2(bpk[ci][4 * j + t / 2], b0, b1);
+                const float bv = (t & 1) ? b1 : b0;
+                const float a = av[t], d = dh[8 * jj + t];
+                const float l = Num<bf16>::logistic(a);
+                hv[t] = silu<bf16>(a) * bv;
+                dav[t] = d * bv * (l * (1.f + a * (1.f - l)));
+                dbv[t] = d * (a * l);
+              }
+              sts_bf16x8(abase + stage_off<64>(lane, j), hv);  // over this lane's own a values
+              sts_bf16x8(dbase + stage_off<64>(lane, j), dav);
+              sts_bf16x8(dbase + C::OUT_BUF + stage_off<64>(lane, j), dbv);
+            }
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (leader) {
+            if (present[0]) tma_store_2d(&maps.out[ob][0], abuf + ci * C::OUT_BUF, x0 + c * CW, r0);
+            if (present[1]) tma_store_2d(&maps.out[ob][1], ostage(b), x0 + c * CW, r0);
+            if (present[2]) tma_store_2d(&maps.out[ob][2], ostage(b) + C::OUT_BUF, x0 + c * CW, r0);
+            bulk_commit();
+          }
+          ++qi;
+        }
         if (!ok) break;
       } else if constexpr (C::SPLIT) {
         // Phase 1: round(a) of this warp's chunks into its a tiles in shared memory (exact:
