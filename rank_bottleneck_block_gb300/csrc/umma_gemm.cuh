@@ -27,7 +27,11 @@
 // Warp roles (320 threads per CTA, one CTA per SM, persistent over pair tiles):
 //   warp 0     TMA producer of the CTA's half of the operand ring (one lane)
 //   warp 1     TMEM allocator; in the leader CTA also the MMA issuer (one lane)
-//   warps 2-9  epilogue of the CTA's 128 rows
+//   warps 2-3  idle (they complete the first warpgroup, whose registers go to the epilogue)
+//   warps 4-11 epilogue of the CTA's 128 rows (two warpgroups)
+// setmaxnreg moves registers from the first warpgroup to the epilogue warpgroups.  The kernels
+// that compute online-RMSNorm statistics keep the compact layout without the split: warps 2-9
+// epilogue, warps 10-13 statistics.
 // Two TMEM accumulator buffers let the epilogue of tile i overlap the
 // mainloop of tile i+1.  NACC > 1 gives each tile several accumulators fed by
 // consecutive K segments with their own operand maps (the SwiGLU dual GEMM).
@@ -61,7 +65,14 @@ constexpr int kMaxAcc = 4;      // TMEM full / empty barrier pairs (a buffer eac
 // three sets and two stages, and the dz_down GEMM with three sets, were slower).
 __host__ __device__ constexpr int aux_sets(EpiKind k) { return k == EPI_RESID ? 4 : 2; }
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Register split between the warpgroups (setmaxnreg) of the kernels without statistics warps
+// (12 warps): warps 0-3 (producer, MMA issuer / TMEM allocator, two idle warps) keep kRegCtl
+// registers per thread, the two epilogue warpgroups take kRegEpi.  The launch gives each thread
+// 168 registers (three warps per SM sub-partition); one warp of every warpgroup lives on each
+// sub-partition, so the split must satisfy kRegCtl + 2 kRegEpi <= 3 x 168.
+constexpr int kRegCtl = 80;
+constexpr int kRegEpi = 208;
+static_assert(kRegCtl + 2 * kRegEpi <= 3 * 168, "register split of the 12-warp kernels");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxSmem = 227 * 1024;
 
@@ -380,7 +391,10 @@ struct Config {
   static constexpr int EPI_BYTES = kEpiWarps * WARP_BYTES;
   // Online RMSNorm: four extra warps accumulate the row sums of squares of the x tiles in the ring.
   static constexpr bool STATS = (K == EPI_NORM_SILU || K == EPI_F32_SS);
-  static constexpr int THREADS = kThreads + (STATS ? 128 : 0);
+  // First epilogue warp: 4 with the register split (warpgroup-aligned epilogue), 2 without.
+  static constexpr bool REGSPLIT = !STATS;
+  static constexpr int EPI0 = REGSPLIT ? 4 : 2;
+  static constexpr int THREADS = 32 * (EPI0 + kEpiWarps) + (STATS ? 128 : 0);
   static constexpr int BAR_BYTES = 1024 + 1024;  // barriers, then s for two tiles of 128 rows
   static constexpr int RING_BUDGET = kMaxSmem - 1024 - EPI_BYTES - BAR_BYTES;
   static constexpr int STAGES = RING_BUDGET / STAGE_BYTES > 8 ? 8 : RING_BUDGET / STAGE_BYTES;
@@ -556,149 +570,154 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   const int total =  // pair tiles
       sh.ksplit * (sh.grouped ? sh.g_tiles : sh.batches * batch_tiles<RB>(sh));
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer
-      int st = 0;
-      uint32_t ph = 0;
-      long long issued = 0;
-      bool ok = true;
-      for (int tile = cid; tile < total && ok; tile += ncl) {
-        int split, batch, mb, nb;
-        decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
-        int kb0, kb1;
-        k_range(sh, split, mb, kb0, kb1);
-        const int m0 = mb * BM, n0 = nb * BN;
-        const int set0 = sh.rowbatch ? 0 : batch;
-        const BatchOff bo = batch_off<RB>(sh, batch);
-        for (int s = 0; s < NACC && ok; ++s) {
-          const int set = NACC > 1 ? s : set0;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_PRODUCER)) {
-              ok = false;
-              break;
+  // Each warpgroup's branch starts with its share of the register split (setmaxnreg; the launcher
+  // checks that the split fits the launch's registers before launching).
+  if (warp < C::EPI0) {
+    if constexpr (C::REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCtl));
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int st = 0;
+        uint32_t ph = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int tile = cid; tile < total && ok; tile += ncl) {
+          int split, batch, mb, nb;
+          decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
+          int kb0, kb1;
+          k_range(sh, split, mb, kb0, kb1);
+          const int m0 = mb * BM, n0 = nb * BN;
+          const int set0 = sh.rowbatch ? 0 : batch;
+          const BatchOff bo = batch_off<RB>(sh, batch);
+          for (int s = 0; s < NACC && ok; ++s) {
+            const int set = NACC > 1 ? s : set0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+              if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_PRODUCER)) {
+                ok = false;
+                break;
+              }
+              // The leader's full barrier counts the bytes of both CTAs' halves of the stage.
+              if (rank == 0) mbar_expect_tx(&full[st], 2 * C::STAGE_BYTES);
+              const uint32_t fbar = mapa(smem_addr(&full[st]), 0);
+              uint8_t* a_dst = sA + st * C::A_BYTES;
+              uint8_t* b_dst = sB + st * C::B_BYTES;
+              if (A_MN) {
+  #pragma unroll
+                for (int j = 0; j < BM / 64; ++j)
+                  tma_load_2d_pair(a_dst + j * 8192, &maps.a[set], fbar, m0 + 64 * j + bo.ca, kb * BK + bo.ra);
+              } else {
+                tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK + bo.ca, m0 + bo.ra);
+              }
+              const int nb0 = n0 + rank * (BN / 2);  // this CTA's half of the B tile
+              if (B_MN) {
+  #pragma unroll
+                for (int j = 0; j < BN / 128; ++j)
+                  tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j + bo.cb, kb * BK + bo.rb);
+              } else {
+                tma_load_2d_pair(b_dst, &maps.b[set], fbar, kb * BK + bo.cb, nb0 + bo.rb);
+              }
+              ++issued;
+              if (++st == STAGES) {
+                st = 0;
+                ph ^= 1u;
+              }
             }
-            // The leader's full barrier counts the bytes of both CTAs' halves of the stage.
-            if (rank == 0) mbar_expect_tx(&full[st], 2 * C::STAGE_BYTES);
-            const uint32_t fbar = mapa(smem_addr(&full[st]), 0);
-            uint8_t* a_dst = sA + st * C::A_BYTES;
-            uint8_t* b_dst = sB + st * C::B_BYTES;
-            if (A_MN) {
-#pragma unroll
-              for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d_pair(a_dst + j * 8192, &maps.a[set], fbar, m0 + 64 * j + bo.ca, kb * BK + bo.ra);
-            } else {
-              tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK + bo.ca, m0 + bo.ra);
-            }
-            const int nb0 = n0 + rank * (BN / 2);  // this CTA's half of the B tile
-            if (B_MN) {
-#pragma unroll
-              for (int j = 0; j < BN / 128; ++j)
-                tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j + bo.cb, kb * BK + bo.rb);
-            } else {
-              tma_load_2d_pair(b_dst, &maps.b[set], fbar, kb * BK + bo.cb, nb0 + bo.rb);
-            }
-            ++issued;
-            if (++st == STAGES) {
-              st = 0;
-              ph ^= 1u;
+          }
+        }
+        pdl_trigger();  // every load of this CTA is issued: the next kernel may be scheduled
+        if (!ok && rank == 0) {
+          // Wait (bounded) for the pair's copies still in flight before the CTAs may exit.
+          const long long n_back = issued < STAGES ? issued : STAGES;
+          for (long long i = 1; i <= n_back; ++i) {
+            const long long n = issued - i;
+            const int s = static_cast<int>(n % STAGES);
+            const uint32_t p = static_cast<uint32_t>((n / STAGES) & 1);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_test(&full[s], p) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
           }
         }
       }
-      pdl_trigger();  // every load of this CTA is issued: the next kernel may be scheduled
-      if (!ok && rank == 0) {
-        // Wait (bounded) for the pair's copies still in flight before the CTAs may exit.
-        const long long n_back = issued < STAGES ? issued : STAGES;
-        for (long long i = 1; i <= n_back; ++i) {
-          const long long n = issued - i;
-          const int s = static_cast<int>(n % STAGES);
-          const uint32_t p = static_cast<uint32_t>((n / STAGES) & 1);
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_test(&full[s], p) && global_timer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ------------------------------------------------ MMA issuer (leader CTA)
-      const uint32_t a_base = smem_addr(sA);
-      const uint32_t b_base = smem_addr(sB);
-      int st = 0;
-      uint32_t ph = 0;
-      int it = 0;
-      bool ok = true;
-      uint32_t ruse[2] = {0u, 0u};  // TRIPLE: accumulations started in each TMEM region
-      for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
-        int split, batch, mb, nb;
-        decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
-        int kb0, kb1;
-        k_range(sh, split, mb, kb0, kb1);
-        const int buf = C::NBUF == 2 ? (it & 1) : 0;
-        const uint32_t tph = static_cast<uint32_t>(C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1));
-        if (!C::SPLIT) {
-          if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        for (int s = 0; s < NACC && ok; ++s) {
-          // Split-phase kernels: accumulator s lives in region reg (its own full / empty pair).
-          const int reg = C::TRIPLE ? (s == 1 ? 1 - (it & 1) : (it & 1)) : s;
-          if (C::SPLIT) {
-            const uint32_t uph = C::TRIPLE ? (ruse[reg] & 1u) : tph;
-            if (!mbar_wait(&tempty[reg], uph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+    } else if (warp == 1) {
+      if (lane == 0 && rank == 0) {
+        // ------------------------------------------------ MMA issuer (leader CTA)
+        const uint32_t a_base = smem_addr(sA);
+        const uint32_t b_base = smem_addr(sB);
+        int st = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        uint32_t ruse[2] = {0u, 0u};  // TRIPLE: accumulations started in each TMEM region
+        for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
+          int split, batch, mb, nb;
+          decode_tile<RB>(sh, tile, rank, split, batch, mb, nb);
+          int kb0, kb1;
+          k_range(sh, split, mb, kb0, kb1);
+          const int buf = C::NBUF == 2 ? (it & 1) : 0;
+          const uint32_t tph = static_cast<uint32_t>(C::NBUF == 2 ? ((it >> 1) & 1) : (it & 1));
+          if (!C::SPLIT) {
+            if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
             tc_fence_after();
           }
-          const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS + reg * BN;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&full[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
-              ok = false;
-              break;
+          for (int s = 0; s < NACC && ok; ++s) {
+            // Split-phase kernels: accumulator s lives in region reg (its own full / empty pair).
+            const int reg = C::TRIPLE ? (s == 1 ? 1 - (it & 1) : (it & 1)) : s;
+            if (C::SPLIT) {
+              const uint32_t uph = C::TRIPLE ? (ruse[reg] & 1u) : tph;
+              if (!mbar_wait(&tempty[reg], uph ^ 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
             }
-            tc_fence_after();
-            const uint32_t a_st = a_base + st * C::A_BYTES;
-            const uint32_t b_st = b_base + st * C::B_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              // K-major: the 16-wide K slice sits 32 bytes further along each swizzled 128-byte row.
-              // MN-major: it is 16 rows (2 atoms of 8 rows x 128 bytes) further on.
-              const uint64_t ad = A_MN ? sdesc(a_st + kk * 2048, 8192, 1024) : sdesc(a_st + kk * 32, 16, 1024);
-              const uint64_t bd = B_MN ? sdesc(b_st + kk * 2048, 8192, 1024) : sdesc(b_st + kk * 32, 16, 1024);
-              umma_f16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            const uint32_t d_tmem = tmem_base + buf * C::ACC_COLS + reg * BN;
+            for (int kb = kb0; kb < kb1; ++kb) {
+              if (!mbar_wait(&full[st], ph, abort_flag, sh.err, DEV_ERR_TIMEOUT_MMA)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_st = a_base + st * C::A_BYTES;
+              const uint32_t b_st = b_base + st * C::B_BYTES;
+  #pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                // K-major: the 16-wide K slice sits 32 bytes further along each swizzled 128-byte row.
+                // MN-major: it is 16 rows (2 atoms of 8 rows x 128 bytes) further on.
+                const uint64_t ad = A_MN ? sdesc(a_st + kk * 2048, 8192, 1024) : sdesc(a_st + kk * 32, 16, 1024);
+                const uint64_t bd = B_MN ? sdesc(b_st + kk * 2048, 8192, 1024) : sdesc(b_st + kk * 32, 16, 1024);
+                umma_f16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+              }
+              // Both CTAs' halves of the stage are free once these MMAs complete.
+              umma_commit(C::STATS ? &consumed[st] : &empty[st], kBoth);
+              if (++st == STAGES) {
+                st = 0;
+                ph ^= 1u;
+              }
             }
-            // Both CTAs' halves of the stage are free once these MMAs complete.
-            umma_commit(C::STATS ? &consumed[st] : &empty[st], kBoth);
-            if (++st == STAGES) {
-              st = 0;
-              ph ^= 1u;
+            if (C::SPLIT && ok) {
+              umma_commit(&tfull[reg], kBoth);
+              if (C::TRIPLE) ++ruse[reg];
             }
           }
-          if (C::SPLIT && ok) {
-            umma_commit(&tfull[reg], kBoth);
-            if (C::TRIPLE) ++ruse[reg];
-          }
+          if (!C::SPLIT && ok) umma_commit(&tfull[buf], kBoth);
         }
-        if (!C::SPLIT && ok) umma_commit(&tfull[buf], kBoth);
+        // Drain: all MMAs issued by this thread have completed once this barrier flips.
+        umma_commit(drain, 0x1);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test(drain, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+        }
       }
-      // Drain: all MMAs issued by this thread have completed once this barrier flips.
-      umma_commit(drain, 0x1);
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_test(drain, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
-      }
-    }
-  } else if (C::STATS && warp >= 2 + kEpiWarps) {
+    }  // with the register split, warps 2 and 3 are idle
+  } else if (C::STATS && warp >= C::EPI0 + kEpiWarps) {
     // ------------------------------------------------ online-RMSNorm statistics warps
     // Row r of the x tile is 128 bytes per stage with its 16-byte chunks permuted by the
     // swizzle; a sum of squares over the whole row does not depend on that order, and
     // reading logical chunk j at physical position j ^ (r & 7) keeps the 8-thread phases
     // of each 16-byte shared load on distinct banks.
-    const int row = (warp - 2 - kEpiWarps) * 32 + lane;
+    const int row = (warp - C::EPI0 - kEpiWarps) * 32 + lane;
     int st = 0;
     uint32_t ph = 0;
     int it = 0;
@@ -744,6 +763,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
       if (lane == 0) mbar_arrive(&sfull[buf]);
     }
   } else {
+    if constexpr (C::REGSPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegEpi));
     // ------------------------------------------------ epilogue warps
     // Each epilogue warp is an independent unit: warp (g, q) owns TMEM lane quarter q (rows
     // 32 q .. 32 q + 31 of the CTA's tile) and the chunks c = g, g+2, ... of each tile.  Its
@@ -752,9 +772,9 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
     constexpr int NAUX = D::NAUX, NOUT = D::NOUT;
     constexpr int NCH = BN / CW;
     constexpr int NO = C::NO, NA = C::NA;
-    const int ew = warp - 2;
+    const int ew = warp - C::EPI0;
     const int g = ew >> 2;   // chunk parity
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;  // TMEM lane quarter this warp may access (warp id mod 4)
     const int row = q * 32 + lane;
     const bool leader = lane == 0;
     uint8_t* wstage = sE + ew * C::WARP_BYTES;  // NO output sets | NA operand sets | round(a) tiles

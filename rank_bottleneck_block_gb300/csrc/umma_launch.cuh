@@ -201,6 +201,13 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   if (!(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // The kernel's setmaxnreg split must fit the registers it is launched with (a split above
+    // them would leave the epilogue warps waiting for registers forever): checked once here.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (C::REGSPLIT && 1LL * fa.numRegs * C::THREADS < 128LL * kRegCtl + 256LL * kRegEpi)
+      return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(2, 1, 1);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
