@@ -45,7 +45,8 @@ enum EpiKind : int {
   EPI_SWIGLU_REBWD = 14,    // checkpointed re-forward and SwiGLU backward of one tile: three accumulators
                             //   a = round(acc0), b = round(acc1), dh = acc2; h = SiLU(a) b -> out0,
                             //   da = dh b SiLU'(a) -> out1, db = dh SiLU(a) -> out2
-  EPI_COUNT = 15
+  EPI_SWIGLU_H = 15,        // EPI_SWIGLU storing h only (the forward of the checkpointed block)
+  EPI_COUNT = 16
 };
 
 constexpr int kMaxBatch = 4;

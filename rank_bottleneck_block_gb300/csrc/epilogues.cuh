@@ -118,6 +118,11 @@ struct EpiDef<EPI_SWIGLU> {  // a = round(acc0), b = round(acc1), h = SiLU(a) b 
 };
 
 template <>
+struct EpiDef<EPI_SWIGLU_H> : EpiDef<EPI_SWIGLU> {  // h = SiLU(round(acc0)) round(acc1) only
+  static constexpr int NOUT = 1;
+};
+
+template <>
 struct EpiDef<EPI_DSILU> {  // du = acc sigma'(u)  (aux0 = u)
   static constexpr int NACC = 1, NAUX = 1, NOUT = 1;
   static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;

@@ -15,6 +15,7 @@ LR_INST(EPI_RESID, 256, false, false)
 LR_INST(EPI_SWIGLU, 128, false, false)
 LR_INST(EPI_SWIGLU, 256, false, false)
 LR_INST(EPI_NORM_SWIGLU, 256, false, false)
+LR_INST(EPI_SWIGLU_H, 256, false, false)
 LR_INST(EPI_F32_SS, 128, false, false)
 LR_INST(EPI_F32_SS, 256, false, false)
 #undef LR_INST

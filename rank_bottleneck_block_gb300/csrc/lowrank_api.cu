@@ -220,6 +220,9 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_SWIGLU:
       if (kk && g.nacc == 2) return umma_bn<EPI_SWIGLU, false, false>(g, st);
       break;
+    case EPI_SWIGLU_H:
+      if (kk && g.nacc == 2) return launch_umma<EPI_SWIGLU_H, 256, false, false>(g, st);
+      break;
     case EPI_NORM_SWIGLU:
       if (kk && g.nacc == 2) return launch_umma<EPI_NORM_SWIGLU, 256, false, false>(g, st);
       break;
@@ -262,7 +265,7 @@ static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
 static const char* epi_name(EpiKind k) {
   static const char* names[] = {"norm_silu", "silu",       "store",  "resid",       "swiglu",        "dsilu",
                                 "dsilu_norm", "swiglu_bwd", "dx_norm", "f32", "norm_swiglu", "swiglu_bwd_norm",
-                                "f32_ss", "attn_bwd", "swiglu_rebwd"};
+                                "f32_ss", "attn_bwd", "swiglu_rebwd", "swiglu"};
   return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
 }
 
@@ -275,7 +278,7 @@ static lr_status gemm(const Ctx& c, EpiKind k, GemmCall& g, double extra_bytes =
   g.ep.N = g.N;
   g.ep.act = c.act;
   if (c.dt == LR_BF16) {
-    if (k == EPI_SWIGLU) g.bn = kSwigluBn;
+    if (k == EPI_SWIGLU || k == EPI_SWIGLU_H) g.bn = kSwigluBn;
     else if (k == EPI_NORM_SWIGLU || k == EPI_ATTN_BWD) g.bn = 256;  // split-phase dual-accumulator kernels
     else if (k == EPI_SWIGLU_REBWD) g.bn = 256;  // three accumulators take two TMEM regions in turn
     else if (g.bn != 128 && g.bn != 256) g.bn = pick_bn(g, c.sms);
@@ -583,6 +586,8 @@ static size_t mlp_bwd_ws_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, 
 // The SwiGLU dual GEMM: a = z_g B_gate^T, b = z_u B_up^T, h = SiLU(a) * b.
 static lr_status swiglu_gemm(const Ctx& c, int T, int f, int r, const void* z_gu, const void* Bg, const void* Bu,
                              void* h, void* a, void* b) {
+  // h alone (the checkpointed forward) runs the kernel built for one output: one more operand stage.
+  const EpiKind kind = (a || b || c.dt != LR_BF16) ? EPI_SWIGLU : EPI_SWIGLU_H;
   GemmCall g = new_call(T, f, r);
   g.nacc = 2;
   g.A[0] = {z_gu, 2LL * r};
@@ -593,7 +598,7 @@ static lr_status swiglu_gemm(const Ctx& c, int T, int f, int r, const void* z_gu
   g.ep.out1[0] = a;
   g.ep.out2[0] = b;
   g.ep.ldo0 = g.ep.ldo1 = g.ep.ldo2 = f;
-  return gemm(c, EPI_SWIGLU, g);
+  return gemm(c, kind, g);
 }
 
 static lr_status mlp_fwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, int r, float eps, const void* x,

@@ -376,16 +376,20 @@ struct Config {
   // are released separately.  Phase 1 stages round(a) in shared memory (exact: a is stored
   // rounded) and frees a's columns for the next tile while b still accumulates; phase 2 moves
   // round(b) into registers, frees b's columns, then computes h.
-  static constexpr bool SPLIT =
-      (K == EPI_SWIGLU || K == EPI_NORM_SWIGLU || K == EPI_ATTN_BWD || K == EPI_SWIGLU_REBWD) && NBUF == 1;
+  static constexpr bool SPLIT = (K == EPI_SWIGLU || K == EPI_SWIGLU_H || K == EPI_NORM_SWIGLU || K == EPI_ATTN_BWD ||
+                                 K == EPI_SWIGLU_REBWD) && NBUF == 1;
   static_assert(!TRIPLE || BN == 256, "the three-accumulator kernel uses two regions of 256 columns");
   // Staging per epilogue warp: NO output sets of NOUT tiles (ping-pong when stores would
   // otherwise stall the next chunk), NA operand sets of NAUX tiles (loads NA chunks ahead),
   // and for the split SwiGLU the round(a) tiles of the warp's chunks.
-  static constexpr int OSET = (SPLIT ? 2 : D::NOUT) * OUT_BUF;
+  // Split-phase kinds stage h and b (a is staged in the round(a) tiles); the h-only SwiGLU stages h.
+  static constexpr int OSET = (SPLIT ? (K == EPI_SWIGLU_H ? 1 : 2) : D::NOUT) * OUT_BUF;
   static constexpr int ASET = D::NAUX * AUX_BUF;
   static constexpr int ABUF = SPLIT ? (BN / CW / 2) * OUT_BUF : 0;
-  static constexpr int NO = (D::NAUX > 0 || SPLIT) ? 2 : 1;
+  // The three-accumulator kernel uses one set of da, db tiles: its shared memory goes to a fourth
+  // operand stage, which is worth more (the MMA waits less for operands) than overlapping a chunk's
+  // staging with the previous chunk's stores.
+  static constexpr int NO = TRIPLE ? 1 : (D::NAUX > 0 || SPLIT) ? 2 : 1;
   static constexpr int NA = D::NAUX > 0 ? aux_sets(K) : 0;
   static constexpr int WARP_BYTES = NO * OSET + NA * ASET + ABUF;
   static constexpr int EPI_BYTES = kEpiWarps * WARP_BYTES;
@@ -1051,7 +1055,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         ok = mbar_wait(&tfull[0], tph, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         tc_fence_after();
-        if (present[1] && leader) bulk_wait_read_all();  // the previous tile's a stores have read abuf
+        constexpr bool OUT_AB = D::NOUT == 3;  // a and b are outputs of the kind (when present)
+        if (OUT_AB && present[OUT_AB ? 1 : 0] && leader) bulk_wait_read_all();  // the previous a stores have read abuf
         __syncwarp();
 #pragma unroll
         for (int ci = 0; ci < NC; ++ci) {
@@ -1067,13 +1072,13 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < CW / 8; ++j) sts_bf16x8(base + stage_off<64>(lane, j), &v[8 * j]);
         }
-        if (present[1]) {
+        if (OUT_AB && present[OUT_AB ? 1 : 0]) {
           fence_async_smem();
           __syncwarp();
           if (leader) {
 #pragma unroll
             for (int ci = 0; ci < NC; ++ci)
-              tma_store_2d(&maps.out[ob][1], abuf + ci * C::OUT_BUF, x0 + (g + 2 * ci) * CW, r0);
+              tma_store_2d(&maps.out[ob][OUT_AB ? 1 : 0], abuf + ci * C::OUT_BUF, x0 + (g + 2 * ci) * CW, r0);
             bulk_commit();
           }
         }
@@ -1123,7 +1128,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
               hv[2 * t + 1] = silu<bf16>(av[2 * t + 1]) * b1;
             }
             sts_bf16x8(hbase + stage_off<64>(lane, j), hv);
-            if (present[2])
+            if (OUT_AB && present[OUT_AB ? 2 : 0])
               sts128(bbase + stage_off<64>(lane, j), bpk[ci][4 * j], bpk[ci][4 * j + 1], bpk[ci][4 * j + 2],
                      bpk[ci][4 * j + 3]);
           }
@@ -1131,7 +1136,8 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
           __syncwarp();
           if (leader) {
             if (present[0]) tma_store_2d(&maps.out[ob][0], ostage(b), x0 + c * CW, r0);
-            if (present[2]) tma_store_2d(&maps.out[ob][2], ostage(b) + C::OUT_BUF, x0 + c * CW, r0);
+            if (OUT_AB && present[OUT_AB ? 2 : 0])
+              tma_store_2d(&maps.out[ob][OUT_AB ? 2 : 0], ostage(b) + C::OUT_BUF, x0 + c * CW, r0);
             bulk_commit();
           }
           ++qi;
