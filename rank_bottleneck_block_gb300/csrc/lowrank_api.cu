@@ -548,7 +548,6 @@ static size_t mlp_fwd_ws_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, 
 
 struct MlpBwdWs {
   void *Af, *z_gu, *z_d, *a, *b, *h;  // z/a/b/h: LR_SAVE_CKPT recompute only (a, b: fp32 engine)
-  void* AdT;                          // A_down^T [f, r]: LR_SAVE_CKPT on the tcgen05 engine
   void *du_d, *da, *db, *du_s;
   float *rowpart, *wpart, *dgpart;
 };
@@ -563,9 +562,7 @@ static size_t mlp_bwd_ws_layout(lr_dtype dt, lr_mode mode, int T, int d, int f, 
   if (mode == LR_SAVE_CKPT) {
     W->z_gu = ar.take(es * T * 2 * r);
     W->z_d = ar.take(es * T * r);
-    if (dt == LR_BF16) {  // a and b live only in TMEM (the fused re-forward + SwiGLU backward)
-      W->AdT = ar.take(es * f * r);
-    } else {
+    if (dt != LR_BF16) {  // bf16: a and b live only in TMEM (the fused re-forward + SwiGLU backward)
       W->a = ar.take(es * T * f);
       W->b = ar.take(es * T * f);
     }
@@ -705,13 +702,8 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     if (c.dt == LR_BF16) {
       // One launch recomputes a = z_g B_gate^T and b = z_u B_up^T and computes dh = du_down A_down
       // for each tile in three TMEM accumulators; its epilogue writes h (for dA_down) and the
-      // SwiGLU backward's da, db.  a and b never reach memory.  A_down is read K-major from a
-      // transposed copy, as are the other two B operands.
-      {
-        LaunchScope scope("transpose", c.st, 0, 2.0 * c.es * r * f);
-        cudaError_t e = launch_transpose(static_cast<const bf16*>(down.A), r, f, static_cast<bf16*>(W.AdT), c.st);
-        if (e != cudaSuccess) return fail(LR_ERR_CUDA, "transpose: %s", cudaGetErrorString(e));
-      }
+      // SwiGLU backward's da, db.  a and b never reach memory.  A_down [r, f] is read in its stored
+      // orientation (MN-major), B_gate and B_up K-major.
       GemmCall k = new_call(T, f, r);
       k.nacc = 3;
       k.A[0] = {z_gu, 2LL * r};
@@ -719,7 +711,7 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
       k.A[2] = {W.du_d, r};
       k.B[0] = {gate.B, r};
       k.B[1] = {up.B, r};
-      k.B[2] = {W.AdT, r};
+      k.B[2] = {down.A, f};
       k.ep.out0[0] = h;
       k.ep.out1[0] = W.da;
       k.ep.out2[0] = W.db;

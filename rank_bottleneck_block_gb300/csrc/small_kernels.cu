@@ -34,33 +34,6 @@ cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols
   return launch_pdl(fold_kernel<ST>, dim3(blocks), dim3(256), 0, st, out, src, rows_each, rows, cols, g);
 }
 
-// ------------------------------------------------------------- transpose
-// 32 x 32 tiles through shared memory (one padding column: no bank conflicts on the column reads);
-// blocks of 32 x 8 threads, each thread moves four elements in and four out.
-__global__ void transpose_kernel(const bf16* src, int rows, int cols, bf16* dst) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ bf16 tile[32][33];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-#pragma unroll
-  for (int k = 0; k < 32; k += 8) {
-    const int r = r0 + threadIdx.y + k, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) tile[threadIdx.y + k][threadIdx.x] = src[static_cast<long long>(r) * cols + c];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 32; k += 8) {
-    const int c = c0 + threadIdx.y + k, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) dst[static_cast<long long>(c) * rows + r] = tile[threadIdx.x][threadIdx.y + k];
-  }
-}
-
-cudaError_t launch_transpose(const bf16* src, int rows, int cols, bf16* dst, cudaStream_t st) {
-  if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((cols + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
-  return launch_pdl(transpose_kernel, grid, dim3(32, 8), 0, st, src, rows, cols, dst);
-}
-
 // ------------------------------------------------------------------ rstd
 template <typename ST>
 __global__ void rstd_kernel(const ST* x, int T, int d, float eps, float* s, int raw) {

@@ -25,9 +25,6 @@ struct WgradDst {
 template <typename ST>
 cudaError_t launch_fold(ST* out, StackSrc src, int nsrc, int rows_each, int cols, const ST* g, cudaStream_t st);
 
-// dst[j, i] = src[i, j] for a row-major [rows, cols] bf16 matrix (dst is [cols, rows], row-major).
-cudaError_t launch_transpose(const bf16* src, int rows, int cols, bf16* dst, cudaStream_t st);
-
 // s[t] = (sum_j x[t, j]^2 / d + eps)^(-1/2), or with `raw` the sum of squares itself; one warp per row.
 template <typename ST>
 cudaError_t launch_rstd(const ST* x, int T, int d, float eps, float* s, cudaStream_t st, bool raw = false);

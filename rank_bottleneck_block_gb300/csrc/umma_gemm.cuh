@@ -379,6 +379,9 @@ struct Config {
   static constexpr bool SPLIT = (K == EPI_SWIGLU || K == EPI_SWIGLU_H || K == EPI_NORM_SWIGLU || K == EPI_ATTN_BWD ||
                                  K == EPI_SWIGLU_REBWD) && NBUF == 1;
   static_assert(!TRIPLE || BN == 256, "the three-accumulator kernel uses two regions of 256 columns");
+  // Operand sets whose B is read MN-major whatever the kernel's B_MN: the three-accumulator kernel's
+  // dh = du_down A_down reads A_down [r, f] in its stored orientation (sets 0, 1 are K-major).
+  static constexpr unsigned B_MN_SETS = TRIPLE ? 4u : 0u;
   // Staging per epilogue warp: NO output sets of NOUT tiles (ping-pong when stores would
   // otherwise stall the next chunk), NA operand sets of NAUX tiles (loads NA chunks ahead),
   // and for the split SwiGLU the round(a) tiles of the warp's chunks.
@@ -509,6 +512,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
   constexpr int NACC = D::NACC;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t IDESC = idesc_bf16<BN, A_MN, B_MN>();
+  constexpr uint32_t IDESC_BMN = idesc_bf16<BN, A_MN, true>();  // sets in C::B_MN_SETS
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -613,7 +617,7 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
                 tma_load_2d_pair(a_dst, &maps.a[set], fbar, kb * BK + bo.ca, m0 + bo.ra);
               }
               const int nb0 = n0 + rank * (BN / 2);  // this CTA's half of the B tile
-              if (B_MN) {
+              if (B_MN || ((C::B_MN_SETS >> set) & 1u)) {
   #pragma unroll
                 for (int j = 0; j < BN / 128; ++j)
                   tma_load_2d_pair(b_dst + j * 8192, &maps.b[set], fbar, nb0 + 64 * j + bo.cb, kb * BK + bo.rb);
@@ -691,8 +695,9 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
                 // K-major: the 16-wide K slice sits 32 bytes further along each swizzled 128-byte row.
                 // MN-major: it is 16 rows (2 atoms of 8 rows x 128 bytes) further on.
                 const uint64_t ad = A_MN ? sdesc(a_st + kk * 2048, 8192, 1024) : sdesc(a_st + kk * 32, 16, 1024);
-                const uint64_t bd = B_MN ? sdesc(b_st + kk * 2048, 8192, 1024) : sdesc(b_st + kk * 32, 16, 1024);
-                umma_f16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                const bool bmn = B_MN || ((C::B_MN_SETS >> s) & 1u);
+                const uint64_t bd = bmn ? sdesc(b_st + kk * 2048, 8192, 1024) : sdesc(b_st + kk * 32, 16, 1024);
+                umma_f16(d_tmem, ad, bd, bmn ? IDESC_BMN : IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
               }
               // Both CTAs' halves of the stage are free once these MMAs complete.
               umma_commit(C::STATS ? &consumed[st] : &empty[st], kBoth);

@@ -134,17 +134,19 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   auto bN = [&](int b) { return g.grouped ? g.gN[b] : g.N; };
   // Stored rows of operand A / B / the output (all batches' rows when row-batched).
   auto rowsA = [&](int b) -> long long { return g.rowbatch ? g.rows_a : (A_MN ? g.K : bM(b)); };
-  auto rowsB = [&](int b) -> long long { return g.rowbatch ? g.rows_b : (B_MN ? g.K : bN(b)); };
+  // B of operand set b MN-major: the kernel's B_MN, or a set the kind reads MN-major
+  auto bmn = [&](int b) { return B_MN || ((C::B_MN_SETS >> b) & 1u); };
+  auto rowsB = [&](int b) -> long long { return g.rowbatch ? g.rows_b : (bmn(b) ? g.K : bN(b)); };
   // Stored columns (the inner extent): all batches' columns when row-batched with column offsets.
   auto colsA = [&](int b) -> long long { return g.rowbatch && g.cols_a ? g.cols_a : (A_MN ? bM(b) : g.K); };
-  auto colsB = [&](int b) -> long long { return g.rowbatch && g.cols_b ? g.cols_b : (B_MN ? bN(b) : g.K); };
+  auto colsB = [&](int b) -> long long { return g.rowbatch && g.cols_b ? g.cols_b : (bmn(b) ? bN(b) : g.K); };
 
   const int nsets = NACC > 1 ? NACC : (g.rowbatch ? 1 : g.batches);
   for (int i = 0; i < nsets; ++i) {
     const bool okA = A_MN ? encode_operand(&maps.a[i], g.A[i].ptr, colsA(i), rowsA(i), g.A[i].ld, 64, 64)
                           : encode_operand(&maps.a[i], g.A[i].ptr, colsA(i), rowsA(i), g.A[i].ld, 64, BM);
     // Each CTA of a pair stages half of the B tile: BN/2 rows (K-major) or 64-column chunks (MN-major).
-    const bool okB = B_MN ? encode_operand(&maps.b[i], g.B[i].ptr, colsB(i), rowsB(i), g.B[i].ld, 64, 64)
+    const bool okB = bmn(i) ? encode_operand(&maps.b[i], g.B[i].ptr, colsB(i), rowsB(i), g.B[i].ld, 64, 64)
                           : encode_operand(&maps.b[i], g.B[i].ptr, colsB(i), rowsB(i), g.B[i].ld, 64, BN / 2);
     if (!okA || !okB) return cudaErrorInvalidValue;
   }
