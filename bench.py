@@ -41,17 +41,19 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_bn256": {"bytes_per_launch": 0.5 * ((45.190144e6 + 133.039104e6) + (67.503872e6 + 499.80032e6)),
-                          "sources_sha256": "2327805bc78d7178ddd44eb78cfd658bf493f240c50c65edb4608b871bdf19ed",
-                          "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
+    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 96.8e6 + 501.1e6,
+                                "sources_sha256": "a39158b9fa907833510e3bcbb8e142bba5df6c50a1e413d1bbf5a6387dbb287e",
+                                "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
 }
 
 
 # Algorithmic bytes per launch of a dominant kernel: the operands it must read and the outputs the
 # method defines, without the [T, f] intermediates (h, a, b) this design materialises (a fully fused
-# implementation need not store them).  SwiGLU dual GEMM: z_g, z_u [T, r] and B_gate, B_up [f, r].
+# implementation need not store them).
 ALG_BYTES = {
     "umma_swiglu_bn256": lambda s: 2.0 * (2 * s.T * s.r + 2 * s.f * s.r),
+    # three-accumulator re-forward + SwiGLU backward: z_g, z_u, du_down [T, r]; B_gate, B_up, A_down
+    "umma_swiglu_rebwd_bn256": lambda s: 2.0 * (3 * s.T * s.r + 3 * s.f * s.r),
 }
 
 
