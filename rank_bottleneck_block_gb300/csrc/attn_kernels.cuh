@@ -23,4 +23,11 @@ cudaError_t launch_attn_softmax_fwd(const float* S, int R, int s, float scale, b
 cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int b, int s, int H, int dh, float* D,
                                cudaStream_t st);
 
+// Causal attention forward without materialised scores (tcgen05; the head width it is built for):
+// o [b*s, H*dh] token-major and lse [b*H*s] head-major (natural log), from token-major q, k, v.  s a
+// multiple of 128; every wait bounded (a timeout sets a bit of *err).
+bool attn_flash_fwd_supported(int dh);
+cudaError_t launch_attn_flash_fwd(const bf16* q, const bf16* k, const bf16* v, bf16* o, int b, int s, int H, int dh,
+                                  float scale, float* lse, unsigned* err, cudaStream_t st);
+
 }  // namespace lr

@@ -1216,6 +1216,17 @@ static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   attn_ws_layout(b, s, H, dh, ws, &W);
   const AttnDims a{b, s, H, dh};
   const int R = b * H * s, d = H * dh;
+  if (attn_flash_fwd_supported(dh)) {
+    // One launch per (head, 128 queries): S and O in TMEM, the softmax in the epilogue warps; no scores
+    // in memory.  Algorithmic FLOPs: Q K^T and P V over the causal half.
+    const double causal = 2.0 * 2.0 * b * H * static_cast<double>(s) * s * dh * 0.5;
+    LaunchScope scope("attn_flash_fwd", c.st, causal, 8.0 * b * s * d + 4.0 * R);
+    cudaError_t e = launch_attn_flash_fwd(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                          static_cast<const bf16*>(v), static_cast<bf16*>(o), b, s, H, dh, scale,
+                                          lse, c.err, c.st);
+    if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention forward: %s", cudaGetErrorString(e));
+    return LR_OK;
+  }
   // S = Q K^T (fp32, head-major), both operands K-major (K = dh) in their token-major rows
   LR_TRY(attn_gemm(c, EPI_F32, a, s, s, dh, {q, d}, false, true, {k, d}, false, true, W.S, s, false, 1));
   {
