@@ -15,8 +15,9 @@ tokens of all ranks over the slowest rank's time.  Besides the headline (the
 single block above), the line carries records of the metric's other workloads
 at full size, timed after the headline on the same GPU: ``attn_proj`` (q/k/v
 group + o-projection, d 4096, r 1024), ``stack24`` (24 blocks + MSE, with and
-without checkpointing, peak device memory of each) and ``sweep`` (144 shapes);
-``--no-extras`` leaves them out.
+without checkpointing, peak device memory of each), ``sweep`` (144 shapes), and the
+widening workloads ``block`` (the low-rank transformer block at LLaMA-7B widths) and
+``attention`` (its causal attention alone); ``--no-extras`` leaves them out.
 """
 from __future__ import annotations
 
@@ -371,6 +372,8 @@ def run_ours(a, ws, rank, local):
         res["attn_proj"] = measure_attn_proj(pk, flush, stream, a.extra_steps, 3)
         res["stack24"] = measure_stack(pk, flush, stream, a.extra_steps, 3, dev)
         res["sweep"] = measure_sweep(pk, flush, stream, a.sweep_steps, 3)
+        res["block"] = measure_block(pk, flush, stream, a.extra_steps, 3, dev)
+        res["attention"] = measure_attention(pk, flush, stream, a.extra_steps, 3, dev)
         L.lr_check_device_error()
     if ws == 1 and not a.no_cpu_baseline:
         tps, reps, el = oracle_tokens_per_s(shape, a.cpu_rows, a.cpu_seconds, a.mode)
@@ -543,6 +546,71 @@ def measure_sweep(pk, flush, stream, steps, warmup, emit=None, eager=False):
             "per_shape_fields": ["d", "r", "T", "group", "ms", "frac_nominal"]}
 
 
+def measure_block(pk, flush, stream, steps, warmup, dev, with_kernels=False):
+    """The full low-rank transformer block at LLaMA-7B widths: q/k/v group, causal attention,
+    o-projection with residual, checkpointed MLP block; fwd+bwd."""
+    from rank_bottleneck_block_gb300 import inputs as I
+    from rank_bottleneck_block_gb300 import lowrank as L
+    from rank_bottleneck_block_gb300.runner import TransformerBlock
+
+    shape = I.BLOCK_7B
+    T, d, f, ra, rm = shape.T, shape.d, shape.f, shape.ra, shape.rm
+    blk = TransformerBlock(shape, I.make_block_case(shape, seed=0, device="cuda"), device=dev)
+    ms = _time_steps(blk.step, steps, warmup, flush, stream)
+    L.lr_check_device_error()
+
+    def pair(din, dout, r):  # one pair's forward FLOPs
+        return 2.0 * T * r * (din + dout)
+
+    proj = 4 * pair(d, d, ra)  # q, k, v, o
+    mlp = 2 * pair(d, f, rm) + pair(f, d, rm)
+    causal = 2.0 * shape.b * shape.H * shape.s * shape.s * shape.dh  # QK^T and PV over the causal half
+    flops = 3 * (proj + mlp) + 2.0 * 2 * T * rm * f + causal * (1 + 2.5)  # bwd 2x; MLP re-forward
+    params = 4 * 2 * d * ra + 2 * (d + f) * rm + (f + d) * rm
+    nbytes = 4.0 * T * d * 2 + params * (2 + 4) + 2.0 * T * (3 * ra + 3 * rm + 8 * d) * 2
+    res = {"workload": f"low-rank transformer block fwd+bwd (q/k/v group, causal attention, o-projection + "
+                       f"residual, checkpointed SwiGLU MLP), b={shape.b} s={shape.s} H={shape.H} dh={shape.dh} "
+                       f"d={d} f={f} ranks {ra}/{rm}, bf16", "steps": steps,
+           "ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "params": params,
+           "flops_note": "algorithmic: attention counted over the causal half",
+           **_roofline(flops, nbytes, ms, pk)}
+    if with_kernels:
+        res["kernels"] = _kernel_table(blk.step, flush, stream)
+    del blk
+    return res
+
+
+def measure_attention(pk, flush, stream, steps, warmup, dev, b=8, with_kernels=False):
+    """Causal multi-head attention alone at LLaMA-7B widths (32 heads of 128, 2048 tokens per sequence),
+    fwd+bwd over b sequences."""
+    import torch
+
+    from rank_bottleneck_block_gb300 import lowrank as L
+    from rank_bottleneck_block_gb300.runner import Attention
+
+    s, H, dh = 2048, 32, 128
+    g = torch.Generator().manual_seed(0)
+    q, k, v, dout = (torch.randn(b * s, H * dh, generator=g).to(torch.bfloat16) for _ in range(4))
+    at = Attention(b, s, H, dh, q, k, v, device=dev)
+    at.dout.copy_(dout.to(dev))
+    ms = _time_steps(at.step, steps, warmup, flush, stream)
+    L.lr_check_device_error()
+    half = 1.0 * b * H * s * s * dh  # one causal product: 2 (s^2 / 2) dh per head
+    flops = 7 * half  # fwd Q K^T, P V; bwd Q K^T, dO V^T, P^T dO, dS K, dS^T Q
+    # compulsory bytes: q, k, v read and o written (forward); q, k, v, o, dO read and dq, dk, dv written
+    # (backward); the row log-sum-exp (the scores themselves are intermediates)
+    nbytes = 12.0 * b * s * H * dh * 2 + 2 * 4.0 * b * H * s
+    res = {"workload": f"causal attention fwd+bwd, b={b} s={s} H={H} dh={dh}, bf16 (forward without stored scores, "
+                       f"backward with its P and dS in HBM)", "steps": steps,
+           "ms_per_step": round(ms, 4), "tokens_per_s": round(b * s / (ms / 1e3), 1),
+           "flops_note": "algorithmic: the causal half of the seven s x s x dh products",
+           **_roofline(flops, nbytes, ms, pk)}
+    if with_kernels:
+        res["kernels"] = _kernel_table(at.step, flush, stream)
+    del at
+    return res
+
+
 def run_other(a):
     """Non-default workloads (one JSON line each): attn_proj, stack, sweep, dense, block, attention."""
     import torch
@@ -552,8 +620,7 @@ def run_other(a):
     B.build()
     from rank_bottleneck_block_gb300 import inputs as I
     from rank_bottleneck_block_gb300 import lowrank as L
-    from rank_bottleneck_block_gb300.runner import (Attention, BlockStack, DenseBlock, GraphStep, MlpBlock,
-                                                     ProjGroup, TransformerBlock)
+    from rank_bottleneck_block_gb300.runner import DenseBlock, MlpBlock
 
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
@@ -586,52 +653,10 @@ def run_other(a):
         res["lowrank_speedup"] = round(ms_dn / ms_lr, 3)
         print(json.dumps(res), flush=True)
     elif a.workload == "block":
-        # The full low-rank transformer block at LLaMA-7B widths: q/k/v group, causal attention,
-        # o-projection with residual, checkpointed MLP block; fwd+bwd.
-        shape = I.BLOCK_7B
-        T, d, f, ra, rm = shape.T, shape.d, shape.f, shape.ra, shape.rm
-        blk = TransformerBlock(shape, I.make_block_case(shape, seed=0, device="cuda"), device=dev)
-        ms = _time_steps(blk.step, a.steps, a.warmup, flush, stream)
-        L.lr_check_device_error()
-        kernels = _kernel_table(blk.step, flush, stream)
-
-        def pair(din, dout, r):  # one pair's forward FLOPs
-            return 2.0 * T * r * (din + dout)
-
-        proj = 4 * pair(d, d, ra)  # q, k, v, o
-        mlp = 2 * pair(d, f, rm) + pair(f, d, rm)
-        causal = 2.0 * shape.b * shape.H * shape.s * shape.s * shape.dh  # QK^T and PV over the causal half
-        flops = 3 * (proj + mlp) + 2.0 * 2 * T * rm * f + causal * (1 + 2.5)  # bwd 2x; MLP re-forward
-        params = 4 * 2 * d * ra + 2 * (d + f) * rm + (f + d) * rm
-        nbytes = 4.0 * T * d * 2 + params * (2 + 4) + 2.0 * T * (3 * ra + 3 * rm + 8 * d) * 2
-        res = {"workload": f"low-rank transformer block fwd+bwd (q/k/v group, causal attention, o-projection + "
-                           f"residual, checkpointed SwiGLU MLP), b={shape.b} s={shape.s} H={shape.H} dh={shape.dh} "
-                           f"d={d} f={f} ranks {ra}/{rm}, bf16",
-               "ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "params": params,
-               "flops_note": "algorithmic: attention counted over the causal half (its kernels compute the "
-                             "256 x 256 tiles on or below the diagonal; the per-kernel figures count those)",
-               **_roofline(flops, nbytes, ms, pk), "kernels": kernels}
-        print(json.dumps(res), flush=True)
+        print(json.dumps(measure_block(pk, flush, stream, a.steps, a.warmup, dev, with_kernels=True)), flush=True)
     elif a.workload == "attention":
-        # Causal multi-head attention alone at LLaMA-7B widths (32 heads of 128, 2048 tokens per
-        # sequence), fwd+bwd; --attn-batch sequences.
-        b, s, H, dh = a.attn_batch, 2048, 32, 128
-        g = torch.Generator().manual_seed(0)
-        q, k, v, dout = (torch.randn(b * s, H * dh, generator=g).to(torch.bfloat16) for _ in range(4))
-        at = Attention(b, s, H, dh, q, k, v, device=dev)
-        at.dout.copy_(dout.to(dev))
-        ms = _time_steps(at.step, a.steps, a.warmup, flush, stream)
-        L.lr_check_device_error()
-        kernels = _kernel_table(at.step, flush, stream)
-        half = 1.0 * b * H * s * s * dh  # one causal GEMM: 2 (s^2 / 2) dh per head
-        flops = 7 * half  # fwd Q K^T, P V; bwd Q K^T, dO V^T, P^T dO, dS K, dS^T Q
-        elems = 1.0 * b * H * s * (s + 256) / 2  # stored score elements (up to each row's key-tile end)
-        nbytes = 22.0 * elems + 4.0 * b * s * H * dh * 2 * 3  # scores: S 4+4, P 2+2+2+2, dS 2+2+2; q,k,v,o,grads
-        res = {"workload": f"causal attention fwd+bwd, b={b} s={s} H={H} dh={dh}, bf16 (scores materialised in HBM)",
-               "ms_per_step": round(ms, 4), "tokens_per_s": round(b * s / (ms / 1e3), 1),
-               "flops_note": "algorithmic: the causal half of the seven s x s x dh products",
-               **_roofline(flops, nbytes, ms, pk), "kernels": kernels}
-        print(json.dumps(res), flush=True)
+        print(json.dumps(measure_attention(pk, flush, stream, a.steps, a.warmup, dev, a.attn_batch,
+                                           with_kernels=True)), flush=True)
     elif a.workload == "sweep":
         res = measure_sweep(pk, flush, stream, a.steps, a.warmup,
                             emit=lambda row: print(json.dumps(row), flush=True), eager=True)
