@@ -216,7 +216,8 @@ lr_status lr_btp_finish(lr_dtype dt, lr_act act, int T, int d, int r, int group,
  * saved: lr_attn_saved_bytes (the row log-sum-exp of S, fp32 [b*H*s]); the backward
  * recomputes S from q and k.  ws: lr_attn_workspace_bytes (the head-major scores
  * [b*H*s, s]: S in fp32, whose first half holds dS in bf16 during the backward, P in bf16;
- * D in fp32 [b*H*s]: 6 b*H*s*s + 4 b*H*s bytes plus alignment), owned by the caller.  The
+ * D in fp32 [b*H*s]: 6 b*H*s*s + 4 b*H*s bytes plus alignment; the forward uses one word of
+ * it, the counter of its work items), owned by the caller.  The
  * kernels read q, k, v, o, dout and write o, dq, dk, dv in place.  bf16 only (LR_F32:
  * LR_ERR_UNSUPPORTED).  s a multiple of 256, dh a multiple of 128, b*H*s at most 2^30 and
  * b*H*s*s at most 2^40 (LR_ERR_SHAPE otherwise); pointers 16-byte aligned (LR_ERR_ALIGN).

@@ -1,11 +1,14 @@
 // Causal attention forward without materialised scores (tcgen05, dh = 128).
 //
-// One CTA takes 128 queries of one head (query block i) and walks the key blocks 0 .. i of 128 keys:
+// A persistent grid (one CTA per SM) takes work items of 128 queries of one head (query block i) from a
+// global counter, in groups of heads whose K and V fit in L2 and heaviest first inside a group; for
+// each item the CTA walks the key blocks 0 .. i of 128 keys:
 //
 //   S_j = Q K_j^T                      MMA, fp32 in TMEM (two buffers: S_{j+1} overlaps the softmax of j)
-//   P_j = 2^(c S_j - m)                the softmax warps, one thread per query row (a TMEM lane), c = scale
-//                                      log2(e); m is the row's running maximum of c S, raised lazily
-//   O  += P_j V_j                      MMA, A = P_j (bf16, shared memory), fp32 accumulator in TMEM
+//   P_j = 2^(c S_j - m)                the softmax warps, c = scale log2(e); m is the row's running
+//                                      maximum of c S, raised lazily; P_j (bf16) is written back into
+//                                      the columns of S_j's TMEM buffer
+//   O  += P_j V_j                      MMA with A = P_j read from TMEM, fp32 accumulator in TMEM
 //
 // with the running row sum l = sum 2^(c S - m).  m is raised only when a block's maximum exceeds it by
 // more than 8 (powers of two): P then stays below 2^8 and O, l keep their scale until a real change, at
@@ -13,12 +16,16 @@
 // issued.  Every formula is exact for any m; only overflow limits the laziness.  At the end O / l goes to
 // the token-major output and lse = ln 2 (m + log2 l) to the head-major row log-sum-exp the backward reads.
 //
-// Warps: 0 TMA producer (Q once, then K_j and V_j into a two-stage ring), 1 TMEM allocator and MMA
-// issuer (one lane), 2-3 idle, 4-7 softmax / output (warp w reads TMEM lanes 32 (w mod 4) ..).  Shared
-// memory: Q, K[2], V[2], P[2], each 128 x 128 bf16 (32 KB) in the 128-byte-swizzled UMMA layouts: Q, K, P
-// K-major in two 64-column halves, V MN-major in two 64-key halves of two 64-column chunks.  TMEM: S[2]
-// at columns 0 and 128, O at 256.  Every mbarrier wait is bounded (error word, abort flag; each role
-// then drains what it issued and TMEM is freed).
+// Warps: 0 item scheduler and TMA producer of Q (per item) and K_j (two-stage ring), 1 TMEM allocator and
+// MMA issuer (one lane), 2 TMA producer of V_j (its own two-stage ring: K_{j+2} loads once S_j is done,
+// V_{j+2} once P_j V_j is), 3 idle, 4-11 softmax and output in two warpgroups: warp w reads TMEM lanes 32 (w mod 4)
+// .. (its 32 query rows); warpgroup 0 takes keys 0-63 of each block and output columns 0-63, warpgroup 1
+// keys 64-127 and columns 64-127.  The two halves of a row agree on m through shared memory once per
+// block (a named barrier of the eight warps, which also orders every read of S before any write of P
+// over it).  Shared memory: Q, K[2], V[2] and the staged output O, each 128 x 128
+// bf16 in the 128-byte-swizzled UMMA layouts (K-major Q, K in two 64-column halves; V MN-major in two
+// 64-key halves of two 64-column chunks).  TMEM: S/P[2] at columns 0 and 128, O at 256.  Every mbarrier
+// wait is bounded (error word, abort flag; each role drains what it issued and TMEM is freed).
 #include <cuda.h>
 
 #include "attn_kernels.cuh"
@@ -50,9 +57,9 @@ constexpr int kRows = 128;     // queries per CTA = keys per block = MMA M = N
 constexpr int kDh = 128;       // head width this kernel is built for
 constexpr int kTile = kRows * kDh * 2;  // 32 KB: one 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;        // 64 columns (one 128-byte swizzle atom wide)
-constexpr int kThreads = 256;
-constexpr int kSoftmax0 = 4;   // first softmax warp
-constexpr int kSmem = 1024 + 7 * kTile + 256;
+constexpr int kThreads = 384;
+constexpr int kSoftmax0 = 4;   // first softmax warp (two warpgroups)
+constexpr int kSmem = 1024 + 6 * kTile + 2048 + 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.f;   // raise the running maximum only past this margin (log2 domain)
@@ -109,52 +116,108 @@ __device__ __forceinline__ uint32_t kmaj_off(int r, int c) {
   return (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-// Named barrier of the four softmax warps.
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of the eight softmax warps.
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// The same barrier, returning the AND of `ok` over the eight warps: every softmax thread takes the
+// same branch after it, so an error stops all of them at the same barrier.
+__device__ __forceinline__ bool softmax_sync_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, 256, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(ok ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// O += P V with A = P read from TMEM (bf16 pairs packed in 32-bit columns, K-major by construction).
+__device__ __forceinline__ void mma1_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers (each thread its lane's 32 values).
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// Work item t (in fetch order) -> query block qb and head n.  Items come in groups of `group` heads
+// (whose K and V stay in L2 while the group is worked on); inside a group the heaviest query blocks
+// (the most key blocks) come first, so the last items fetched are light ones.
+__device__ __forceinline__ void item_of(int t, int nheads, int nqb, int group, int& qb, int& n) {
+  const int per_group = group * nqb;
+  const int gi = t / per_group, r = t - gi * per_group;
+  const int gh = min(group, nheads - gi * group);
+  qb = nqb - 1 - r / gh;
+  n = gi * group + (r - (r / gh) * gh);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_flash_fwd_kernel(const __grid_constant__ Maps maps, int nheads, int H, int s, float scale, float* lse,
-                          unsigned* err) {
+    attn_flash_fwd_kernel(const __grid_constant__ Maps maps, int nheads, int H, int s, int group, float scale,
+                          float* lse, unsigned* sched, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + kTile;      // [2]
   uint8_t* sV = sK + 2 * kTile;  // [2]
-  uint8_t* sP = sV + 2 * kTile;  // [2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kTile);
+  uint8_t* sO = sV + 2 * kTile;  // the item's output, staged for the TMA store
+  float* xch = reinterpret_cast<float*>(sO + kTile);  // [2 parities][2 halves][128 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xch + 2 * 2 * kRows);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_empty = bars + 7;   // [2]
-  uint64_t* p_full = bars + 9;    // [2]
-  uint64_t* p_empty = bars + 11;  // [2]
-  uint64_t* o_done = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* q_free = bars + 1;      // the item's last S MMA has read the Q tile
+  uint64_t* k_full = bars + 2;      // [2]
+  uint64_t* k_empty = bars + 4;     // [2] the S MMA has read K
+  uint64_t* v_full = bars + 6;      // [2]
+  uint64_t* v_empty = bars + 8;     // [2] the P V MMA has read V
+  uint64_t* s_full = bars + 10;     // [2]
+  uint64_t* p_full = bars + 12;     // [2]
+  uint64_t* o_done = bars + 14;     // one completion per P V
+  uint64_t* o_last = bars + 15;     // one completion per item: its last P V
+  uint64_t* o_free = bars + 16;     // the softmax warps have read the item's O
+  uint64_t* drain = bars + 17;
+  uint64_t* item_full = bars + 18;  // [2] the item ring
+  uint64_t* item_empty = bars + 20; // [2]
+  int* sitem = reinterpret_cast<int*>(bars + 22);  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sitem + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Heaviest query blocks first (block i has i + 1 key blocks).
   const int nqb = s / kRows;
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x) / nheads;
-  const int n = static_cast<int>(blockIdx.x) % nheads;
-  const int bi = n / H, h = n - bi * H;
-  const int nkb = qb + 1;
-  const int row0 = bi * s + qb * kRows;  // first token of the query block
-  const int col0 = h * kDh;              // first column of the head
+  const int items = nheads * nqb;
+  constexpr int kItemReaders = 1 + 1 + 8;  // V producer, MMA issuer, softmax warps
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
-      mbar_init(&p_full[i], 4);
-      mbar_init(&p_empty[i], 1);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], kItemReaders);
     }
     mbar_init(o_done, 1);
+    mbar_init(o_last, 1);
+    mbar_init(o_free, 8);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -171,43 +234,114 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
 
+  // The k-th item of this CTA (the first negative one ends the walk), read from the ring; false when the
+  // wait gave up.
+  auto next_item = [&](int k, int& t) -> bool {
+    const int slot = k & 1;
+    if (!mbar_wait(&item_full[slot], static_cast<uint32_t>((k >> 1) & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA))
+      return false;
+    t = *reinterpret_cast<volatile int*>(&sitem[slot]);
+    return true;
+  };
+
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
+      // ------------------------------------------------ scheduler and Q / K producer
       bool ok = true;
-      int issued = 0;
-      mbar_expect_tx(q_full, kTile);
-      tma_load_2d(sQ, &maps.q, q_full, col0, row0);
-      tma_load_2d(sQ + kHalf, &maps.q, q_full, col0 + 64, row0);
-      for (int j = 0; j < nkb && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-        if (!mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_PRODUCER)) {
+      int it = 0, q_issued = 0;
+      long long g = 0;  // key blocks issued over all items
+      for (;; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&item_empty[slot], static_cast<uint32_t>((it >> 1) & 1) ^ 1u, abort_flag, err,
+                       DEV_ERR_TIMEOUT_PRODUCER)) {
           ok = false;
           break;
         }
-        mbar_expect_tx(&kv_full[st], 2 * kTile);
-        const int key0 = bi * s + j * kRows;
-        uint8_t* k_dst = sK + st * kTile;
-        uint8_t* v_dst = sV + st * kTile;
-        tma_load_2d(k_dst, &maps.k, &kv_full[st], col0, key0);
-        tma_load_2d(k_dst + kHalf, &maps.k, &kv_full[st], col0 + 64, key0);
-        // V as the MN-major B operand: per 64-key half, two 64-column chunks of 64 keys x 128 bytes
-        for (int kh = 0; kh < 2; ++kh)
-          for (int ch = 0; ch < 2; ++ch)
-            tma_load_2d(v_dst + kh * kHalf + ch * (kHalf / 2), &maps.v, &kv_full[st], col0 + 64 * ch, key0 + 64 * kh);
-        ++issued;
+        const unsigned tk = atomicAdd(sched, 1u);
+        const int t = tk < static_cast<unsigned>(items) ? static_cast<int>(tk) : -1;
+        sitem[slot] = t;
+        mbar_arrive(&item_full[slot]);  // release: the item id is visible to the readers
+        if (t < 0) break;
+        int qb, n;
+        item_of(t, nheads, nqb, group, qb, n);
+        const int bi = n / H, h = n - bi * H;
+        const int col0 = h * kDh;
+        // Q of this item once the previous item's last S MMA has read the previous Q.
+        if (!mbar_wait(q_free, static_cast<uint32_t>(it & 1) ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_PRODUCER)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(q_full, kTile);
+        tma_load_2d(sQ, &maps.q, q_full, col0, bi * s + qb * kRows);
+        tma_load_2d(sQ + kHalf, &maps.q, q_full, col0 + 64, bi * s + qb * kRows);
+        ++q_issued;
+        for (int j = 0; j <= qb && ok; ++j, ++g) {
+          const int st = static_cast<int>(g & 1);
+          const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
+          if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&k_full[st], kTile);
+          const int key0 = bi * s + j * kRows;
+          tma_load_2d(sK + st * kTile, &maps.k, &k_full[st], col0, key0);
+          tma_load_2d(sK + st * kTile + kHalf, &maps.k, &k_full[st], col0 + 64, key0);
+        }
+        if (!ok) break;
       }
-      // Wait (bounded) for every copy still in flight before the CTA may exit.
-      if (!ok) {
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
+      if (!ok) {  // wait (bounded) for the copies still in flight before the CTA may exit
+        for (long long k = (g > 2 ? g - 2 : 0); k < g; ++k) {
           const uint64_t t0 = global_timer_ns();
-          while (!mbar_test(&kv_full[j & 1], static_cast<uint32_t>((j >> 1) & 1)) &&
+          while (!mbar_test(&k_full[k & 1], static_cast<uint32_t>((k >> 1) & 1)) &&
                  global_timer_ns() - t0 < umma::kWaitLimitNs) {
           }
         }
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_test(q_full, 0) && global_timer_ns() - t0 < umma::kWaitLimitNs) {
+        while (q_issued > 0 && !mbar_test(q_full, static_cast<uint32_t>((q_issued - 1) & 1)) &&
+               global_timer_ns() - t0 < umma::kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ------------------------------------------------ V producer
+      bool ok = true;
+      long long g = 0;
+      for (int it = 0;; ++it) {
+        int t;
+        if (!next_item(it, t)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive(&item_empty[it & 1]);
+        if (t < 0) break;
+        int qb, n;
+        item_of(t, nheads, nqb, group, qb, n);
+        const int bi = n / H, h = n - bi * H;
+        for (int j = 0; j <= qb && ok; ++j, ++g) {
+          const int st = static_cast<int>(g & 1);
+          const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
+          if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&v_full[st], kTile);
+          const int key0 = bi * s + j * kRows;
+          uint8_t* v_dst = sV + st * kTile;
+          // V as the MN-major B operand: per 64-key half, two 64-column chunks of 64 keys x 128 bytes
+          for (int kh = 0; kh < 2; ++kh)
+            for (int ch = 0; ch < 2; ++ch)
+              tma_load_2d(v_dst + kh * kHalf + ch * (kHalf / 2), &maps.v, &v_full[st], h * kDh + 64 * ch,
+                          key0 + 64 * kh);
+        }
+        if (!ok) break;
+      }
+      if (!ok) {
+        for (long long k = (g > 2 ? g - 2 : 0); k < g; ++k) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_test(&v_full[k & 1], static_cast<uint32_t>((k >> 1) & 1)) &&
+                 global_timer_ns() - t0 < umma::kWaitLimitNs) {
+          }
         }
       }
     }
@@ -215,47 +349,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       constexpr uint32_t kIdS = idesc_m128<false>();  // S = Q K^T: both K-major
-      constexpr uint32_t kIdO = idesc_m128<true>();   // O += P V: P K-major, V MN-major
-      const uint32_t q_base = smem_addr(sQ), k_base = smem_addr(sK), v_base = smem_addr(sV), p_base = smem_addr(sP);
-      bool ok = mbar_wait(q_full, 0, abort_flag, err, DEV_ERR_TIMEOUT_MMA);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1, sb = j & 1;
-        const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-        if (!mbar_wait(&s_empty[sb], ph ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) return false;
-        if (!mbar_wait(&kv_full[st], ph, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) return false;
+      constexpr uint32_t kIdO = idesc_m128<true>();   // O += P V: P from TMEM, V MN-major
+      const uint32_t q_base = smem_addr(sQ), k_base = smem_addr(sK), v_base = smem_addr(sV);
+      bool ok = true;
+      long long g = 0;  // key blocks over all items
+      auto issue_s = [&](long long gg, bool last) -> bool {
+        const int st = static_cast<int>(gg & 1);
+        const uint32_t ph = static_cast<uint32_t>((gg >> 1) & 1);
+        if (!mbar_wait(&k_full[st], ph, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) return false;
         tc_fence_after();
         const uint32_t kt = k_base + st * kTile;
+        // buffer st last held P_{gg-2}, whose P V was issued before this (the MMAs of a thread run in order)
 #pragma unroll
         for (int kk = 0; kk < kDh / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          mma1(tmem + sb * kRows, sdesc(q_base + off, 16, 1024), sdesc(kt + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          mma1(tmem + st * kRows, sdesc(q_base + off, 16, 1024), sdesc(kt + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
         }
-        commit1(&s_full[sb]);
+        commit1(&s_full[st]);
+        commit1(&k_empty[st]);
+        if (last) commit1(q_free);  // Q may be replaced once this S is complete
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < nkb && ok; ++j) {
-        if (j + 1 < nkb && !issue_s(j + 1)) {
+      for (int it = 0; ok; ++it) {
+        int t;
+        if (!next_item(it, t)) {
           ok = false;
           break;
         }
-        const int st = j & 1, pb = j & 1;
-        const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-        if (!mbar_wait(&p_full[pb], ph, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
+        mbar_arrive(&item_empty[it & 1]);
+        if (t < 0) break;
+        int qb, n;
+        item_of(t, nheads, nqb, group, qb, n);
+        if (!mbar_wait(q_full, static_cast<uint32_t>(it & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA) ||
+            !issue_s(g, qb == 0)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t pt = p_base + pb * kTile, vt = v_base + st * kTile;
+        for (int j = 0; j <= qb && ok; ++j, ++g) {
+          if (j + 1 <= qb && !issue_s(g + 1, j + 1 == qb)) {
+            ok = false;
+            break;
+          }
+          const int st = static_cast<int>(g & 1);
+          const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
+          if (!mbar_wait(&p_full[st], ph, abort_flag, err, DEV_ERR_TIMEOUT_MMA) ||
+              !mbar_wait(&v_full[st], ph, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          // The item's first P V overwrites O: the previous item's O must have been read.
+          if (j == 0 && !mbar_wait(o_free, static_cast<uint32_t>(it & 1) ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vt = v_base + st * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk) {  // K = the block's 128 keys
-          const uint64_t ad = sdesc(pt + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc(vt + (kk >> 2) * kHalf + (kk & 3) * 2048, kHalf / 2, 1024);
-          mma1(tmem + 2 * kRows, ad, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kRows / 16; ++kk) {  // K = the block's 128 keys: 8 packed columns each
+            const uint64_t bd = sdesc(vt + (kk >> 2) * kHalf + (kk & 3) * 2048, kHalf / 2, 1024);
+            mma1_ta(tmem + 2 * kRows, tmem + st * kRows + kk * 8, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          commit1(o_done);
+          if (j == qb) commit1(o_last);
+          commit1(&v_empty[st]);
         }
-        commit1(o_done);
-        commit1(&p_empty[pb]);
-        commit1(&kv_empty[st]);
       }
       // Drain: every MMA issued by this thread has completed once this barrier flips.
       commit1(drain);
@@ -264,111 +421,139 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= kSoftmax0) {
-    // ------------------------------------------------ softmax and output (one thread per query row)
+    // ------------------------------------------------ softmax and output
+    // Errors: `fail` is this warp's view (a wait of its own gave up); `ok` changes only at a
+    // softmax_sync_and, so it is the same in all eight warps and every branch on it that skips a named
+    // barrier is taken by all of them.  A warp that failed skips its TMEM accesses and carries on to the
+    // next such barrier (the abort flag makes every later wait return at once).
     const int q = warp & 3;
-    const int row = q * 32 + lane;  // query row within the block (TMEM lane)
+    const int half = (warp - kSoftmax0) >> 2;  // keys / output columns 64 half .. 64 half + 63
+    const int row = q * 32 + lane;             // query row within the block (TMEM lane)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const bool storer = threadIdx.x == kSoftmax0 * 32;
     const float c = scale * kLog2e;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkb && ok; ++j) {
-      const int sb = j & 1;
-      const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-      ok = mbar_wait(&s_full[sb], ph, abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      float x[kRows];
-#pragma unroll
-      for (int cc = 0; cc < kRows / 32; ++cc) tmem_ld32(t_lane + sb * kRows + cc * 32, &x[cc * 32]);
-      tmem_ld_wait();
-      tc_fence_before();
+    bool ok = true, fail = false;
+    long long g = 0;
+    for (int it = 0;; ++it) {
+      int t = -1;
+      bool okw = next_item(it, t);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[sb]);  // S buffer free for S_{j+2}
-      const bool diag = j == qb;
-      float bm = -INFINITY;
+      if (lane == 0) mbar_arrive(&item_empty[it & 1]);
+      ok = softmax_sync_and(okw && !fail);
+      if (!ok || t < 0) break;  // uniform: every warp read the same item
+      int qb, n;
+      item_of(t, nheads, nqb, group, qb, n);
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j <= qb; ++j, ++g) {
+        const int st = static_cast<int>(g & 1);
+        const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
+        okw = mbar_wait(&s_full[st], ph, abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE);
+        okw = __all_sync(0xffffffffu, okw && !fail);
+        float x[64];
+        if (okw) {
+          tc_fence_after();
+          tmem_ld32(t_lane + st * kRows + 64 * half, x);
+          tmem_ld32(t_lane + st * kRows + 64 * half + 32, x + 32);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-      for (int kk = 0; kk < kRows; ++kk) {
-        x[kk] = (diag && kk > row) ? -INFINITY : x[kk] * c;
-        bm = fmaxf(bm, x[kk]);
-      }
-      // Lazy maximum: raise m (and rescale O, l) only when the block's maximum passes it by kLazy.
-      const bool raise = m == -INFINITY ? true : bm > m + kLazy;
-      const float m_new = raise ? fmaxf(m, bm) : m;
-      const float alpha = (raise && m != -INFINITY) ? exp2f(m - m_new) : 1.f;
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O holds the blocks before j: wait for P_{j-1} V_{j-1}, then scale this row of O.
-        const uint32_t op = static_cast<uint32_t>((j - 1) & 1);
-        ok = mbar_wait(o_done, op, abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
-        ok = __all_sync(0xffffffffu, ok);
+          for (int kk = 0; kk < 64; ++kk) x[kk] = 0.f;
+        }
+        const bool diag = j == qb;
+        float bm = -INFINITY;
+#pragma unroll
+        for (int kk = 0; kk < 64; ++kk) {
+          x[kk] = (diag && 64 * half + kk > row) ? -INFINITY : x[kk] * c;
+          bm = fmaxf(bm, x[kk]);
+        }
+        // Both halves of the row agree on the block maximum (this barrier also orders every read of
+        // S_j before any write of P_j over its columns).
+        float* xb = xch + (g & 1) * (2 * kRows);
+        xb[half * kRows + row] = bm;
+        tc_fence_before();
+        ok = softmax_sync_and(okw);
         if (!ok) break;
         tc_fence_after();
+        bm = fmaxf(bm, xb[(1 - half) * kRows + row]);
+        // Lazy maximum: raise m (and rescale O, l) only when the block's maximum passes it by kLazy.
+        const bool raise = m == -INFINITY ? true : bm > m + kLazy;
+        const float m_new = raise ? fmaxf(m, bm) : m;
+        const float alpha = (raise && m != -INFINITY) ? exp2f(m - m_new) : 1.f;
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds the blocks before j: wait for P_{j-1} V_{j-1}, then scale this row's half of O.  (S_j
+          // complete implies P_{j-2} V_{j-2} complete, so o_done is at most one phase behind here.)
+          okw = mbar_wait(o_done, static_cast<uint32_t>((g - 1) & 1), abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE);
+          fail = !__all_sync(0xffffffffu, okw);
+          if (!fail) {
+            tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < kDh / 32; ++cc) {
-          float o[32];
-          tmem_ld32(t_lane + 2 * kRows + cc * 32, o);
-          tmem_ld_wait();
+            for (int cc = 0; cc < 2; ++cc) {
+              float o[32];
+              const uint32_t oa = t_lane + 2 * kRows + 64 * half + 32 * cc;
+              tmem_ld32(oa, o);
+              tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] *= alpha;
-          tmem_st32(t_lane + 2 * kRows + cc * 32, o);
+              for (int u = 0; u < 32; ++u) o[u] *= alpha;
+              tmem_st32(oa, o);
+            }
+          }
         }
+        l *= alpha;
+        m = m_new;
+        // P (bf16 pairs) over the first 64 columns of S's buffer: this half's 64 keys in 32 columns.
+        uint32_t pk[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const float p0 = exp2f(x[2 * u] - m), p1 = exp2f(x[2 * u + 1] - m);
+          l += p0 + p1;
+          pk[u] = pack_bf16x2(p0, p1);
+        }
+        if (!fail) tmem_st32u(t_lane + st * kRows + 32 * half, pk);
         tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[st]);
       }
-      l *= alpha;
-      m = m_new;
-      // P into buffer j mod 2 once P_{j-2} V_{j-2} has read it.
-      const int pb = j & 1;
-      ok = mbar_wait(&p_empty[pb], ph ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
-      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;  // uniform: taken after a softmax_sync_and
+      // O = O / l after the item's last P V (l summed over both halves of the row), staged in sO once
+      // the previous item's store has read it, then stored.
+      okw = mbar_wait(o_last, static_cast<uint32_t>(it & 1), abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE);
+      okw = __all_sync(0xffffffffu, okw && !fail);
+      if (storer) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      float* xb = xch + (g & 1) * (2 * kRows);
+      xb[half * kRows + row] = l;
+      ok = softmax_sync_and(okw);
       if (!ok) break;
-      const uint32_t pt = smem_addr(sP + pb * kTile);
-#pragma unroll
-      for (int cc = 0; cc < kRows / 8; ++cc) {
-        float p[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          p[t] = exp2f(x[8 * cc + t] - m);
-          l += p[t];
-        }
-        sts128(pt + kmaj_off(row, cc), pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-               pack_bf16x2(p[6], p[7]));
-      }
-      fence_async_smem();  // the generic-proxy writes of P become visible to the MMA (async proxy)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[pb]);
-    }
-    if (ok) {
-      // O = O / l after the last P V; stage it in the Q tile (every S MMA has completed) and store.
-      ok = mbar_wait(o_done, static_cast<uint32_t>((nkb - 1) & 1), abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    softmax_sync();  // every softmax warp has decided (each either staged or not)
-    if (ok) {
+      const float lt = l + xb[(1 - half) * kRows + row];
       tc_fence_after();
-      const float inv = 1.f / l;
-      const uint32_t ob = smem_addr(sQ);
+      const float inv = 1.f / lt;
+      const uint32_t ob = smem_addr(sO);
 #pragma unroll
-      for (int cc = 0; cc < kDh / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         float o[32];
-        tmem_ld32(t_lane + 2 * kRows + cc * 32, o);
+        tmem_ld32(t_lane + 2 * kRows + 64 * half + 32 * cc, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-          sts128(ob + kmaj_off(row, cc * 4 + g), pack_bf16x2(o[8 * g] * inv, o[8 * g + 1] * inv),
-                 pack_bf16x2(o[8 * g + 2] * inv, o[8 * g + 3] * inv), pack_bf16x2(o[8 * g + 4] * inv, o[8 * g + 5] * inv),
-                 pack_bf16x2(o[8 * g + 6] * inv, o[8 * g + 7] * inv));
+        for (int gq = 0; gq < 4; ++gq)
+          sts128(ob + kmaj_off(row, 8 * half + 4 * cc + gq), pack_bf16x2(o[8 * gq] * inv, o[8 * gq + 1] * inv),
+                 pack_bf16x2(o[8 * gq + 2] * inv, o[8 * gq + 3] * inv),
+                 pack_bf16x2(o[8 * gq + 4] * inv, o[8 * gq + 5] * inv),
+                 pack_bf16x2(o[8 * gq + 6] * inv, o[8 * gq + 7] * inv));
       }
-      lse[static_cast<long long>(n) * s + qb * kRows + row] = (m + log2f(l)) * kLn2;
+      if (half == 0) lse[static_cast<long long>(n) * s + qb * kRows + row] = (m + log2f(lt)) * kLn2;
       fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);  // this warp has read its part of O
+      softmax_sync();                        // staging complete; every partner has read l
+      if (storer) {
+        const int bi = n / H, h = n - bi * H;
+        tma_store_2d(&maps.o, sO, h * kDh, bi * s + qb * kRows);
+        tma_store_2d(&maps.o, sO + kHalf, h * kDh + 64, bi * s + qb * kRows);
+        bulk_commit();
+      }
     }
-    softmax_sync();
-    if (ok && threadIdx.x == kSoftmax0 * 32) {
-      tma_store_2d(&maps.o, sQ, col0, row0);
-      tma_store_2d(&maps.o, sQ + kHalf, col0 + 64, row0);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    if (storer) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -384,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool attn_flash_fwd_supported(int dh) { return dh == flash::kDh; }
 
 cudaError_t launch_attn_flash_fwd(const bf16* q, const bf16* k, const bf16* v, bf16* o, int b, int s, int H, int dh,
-                                  float scale, float* lse, unsigned* err, cudaStream_t st) {
+                                  float scale, float* lse, unsigned* sched, unsigned* err, cudaStream_t st) {
   using namespace flash;
   if (dh != kDh || s % kRows) return cudaErrorInvalidValue;
   Maps maps;
@@ -404,10 +589,17 @@ cudaError_t launch_attn_flash_fwd(const bf16* q, const bf16* k, const bf16* v, b
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
-  const long long blocks = 1LL * b * H * (s / kRows);
-  if (blocks == 0) return cudaSuccess;
-  return launch_pdl(attn_flash_fwd_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), kSmem, st, maps,
-                    b * H, H, s, scale, lse, err);
+  const long long items = 1LL * b * H * (s / kRows);
+  if (items == 0) return cudaSuccess;
+  if (items > (1LL << 30)) return cudaErrorInvalidValue;
+  // Heads per group: their K and V (s keys x dh x 2 tensors x 2 bytes each) about 32 MiB, well inside L2.
+  const long long per_head = 4LL * s * dh;
+  const int group = static_cast<int>(std::max<long long>(1, std::min<long long>(1LL * b * H, (32LL << 20) / per_head)));
+  cudaError_t e = cudaMemsetAsync(sched, 0, sizeof(unsigned), st);  // the item counter of this launch
+  if (e != cudaSuccess) return e;
+  const long long grid = std::min<long long>(items, device_sm_count());  // persistent: one CTA per SM
+  return launch_pdl(attn_flash_fwd_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmem, st, maps,
+                    b * H, H, s, group, scale, lse, sched, err);
 }
 
 }  // namespace lr

@@ -25,9 +25,10 @@ cudaError_t launch_attn_rowdot(const bf16* dO, const bf16* O, int b, int s, int 
 
 // Causal attention forward without materialised scores (tcgen05; the head width it is built for):
 // o [b*s, H*dh] token-major and lse [b*H*s] head-major (natural log), from token-major q, k, v.  s a
-// multiple of 128; every wait bounded (a timeout sets a bit of *err).
+// multiple of 128; every wait bounded (a timeout sets a bit of *err).  sched: one device word, the
+// launch's work-item counter (cleared on `st` before the launch; no other use may overlap the launch).
 bool attn_flash_fwd_supported(int dh);
 cudaError_t launch_attn_flash_fwd(const bf16* q, const bf16* k, const bf16* v, bf16* o, int b, int s, int H, int dh,
-                                  float scale, float* lse, unsigned* err, cudaStream_t st);
+                                  float scale, float* lse, unsigned* sched, unsigned* err, cudaStream_t st);
 
 }  // namespace lr

@@ -1217,13 +1217,14 @@ static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   const AttnDims a{b, s, H, dh};
   const int R = b * H * s, d = H * dh;
   if (attn_flash_fwd_supported(dh)) {
-    // One launch per (head, 128 queries): S and O in TMEM, the softmax in the epilogue warps; no scores
-    // in memory.  Algorithmic FLOPs: Q K^T and P V over the causal half.
+    // One persistent launch over the (head, 128 queries) items: S and O in TMEM, the softmax in the
+    // epilogue warps; no scores in memory (the workspace's first word counts the items taken).
+    // Algorithmic FLOPs: Q K^T and P V over the causal half.
     const double causal = 2.0 * 2.0 * b * H * static_cast<double>(s) * s * dh * 0.5;
     LaunchScope scope("attn_flash_fwd", c.st, causal, 8.0 * b * s * d + 4.0 * R);
     cudaError_t e = launch_attn_flash_fwd(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
                                           static_cast<const bf16*>(v), static_cast<bf16*>(o), b, s, H, dh, scale,
-                                          lse, c.err, c.st);
+                                          lse, reinterpret_cast<unsigned*>(W.D), c.err, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention forward: %s", cudaGetErrorString(e));
     return LR_OK;
   }
