@@ -601,7 +601,7 @@ def measure_attention(pk, flush, stream, steps, warmup, dev, b=8, with_kernels=F
     # (backward); the row log-sum-exp (the scores themselves are intermediates)
     nbytes = 12.0 * b * s * H * dh * 2 + 2 * 4.0 * b * H * s
     res = {"workload": f"causal attention fwd+bwd, b={b} s={s} H={H} dh={dh}, bf16 (forward without stored scores, "
-                       f"backward with its P and dS in HBM)", "steps": steps,
+                       f"backward with only dS^T in HBM, for the dQ GEMM)", "steps": steps,
            "ms_per_step": round(ms, 4), "tokens_per_s": round(b * s / (ms / 1e3), 1),
            "flops_note": "algorithmic: the causal half of the seven s x s x dh products",
            **_roofline(flops, nbytes, ms, pk)}

@@ -26,147 +26,18 @@
 // bf16 in the 128-byte-swizzled UMMA layouts (K-major Q, K in two 64-column halves; V MN-major in two
 // 64-key halves of two 64-column chunks).  TMEM: S/P[2] at columns 0 and 128, O at 256.  Every mbarrier
 // wait is bounded (error word, abort flag; each role drains what it issued and TMEM is freed).
-#include <cuda.h>
-
+#include "attn_flash.cuh"
 #include "attn_kernels.cuh"
-#include "umma_launch.cuh"
 
 namespace lr {
 namespace flash {
 
-using umma::bulk_commit;
-using umma::bulk_wait_all;
-using umma::fence_async_smem;
-using umma::mbar_arrive;
-using umma::mbar_expect_tx;
-using umma::mbar_init;
-using umma::mbar_test;
-using umma::mbar_wait;
-using umma::pack_bf16x2;
-using umma::sdesc;
-using umma::smem_addr;
-using umma::sts128;
-using umma::tc_fence_after;
-using umma::tc_fence_before;
-using umma::tma_load_2d;
-using umma::tma_store_2d;
-using umma::tmem_ld32;
-using umma::tmem_ld_wait;
-
-constexpr int kRows = 128;     // queries per CTA = keys per block = MMA M = N
-constexpr int kDh = 128;       // head width this kernel is built for
-constexpr int kTile = kRows * kDh * 2;  // 32 KB: one 128 x 128 bf16 tile
-constexpr int kHalf = kTile / 2;        // 64 columns (one 128-byte swizzle atom wide)
-constexpr int kThreads = 384;
-constexpr int kSoftmax0 = 4;   // first softmax warp (two warpgroups)
 constexpr int kSmem = 1024 + 6 * kTile + 2048 + 256;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.f;   // raise the running maximum only past this margin (log2 domain)
 
 struct Maps {
   CUtensorMap q, k, v, o;  // q, k, o: boxes of 64 columns x 128 rows; v: 64 x 64
 };
-
-// Instruction descriptor of kind::f16, fp32 accumulator, bf16 operands, M = 128, N = 128.
-template <bool B_MN>
-__host__ __device__ constexpr uint32_t idesc_m128() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((B_MN ? 1u : 0u) << 16) | (static_cast<uint32_t>(kRows >> 3) << 17) |
-         (static_cast<uint32_t>(kRows >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma1(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void commit1(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Byte offset of 16-byte chunk c (8 consecutive columns) of row r in a K-major 128 x 128 tile stored as
-// two 64-column halves with the 128-byte swizzle (the TMA box layout and the UMMA descriptor layout).
-__device__ __forceinline__ uint32_t kmaj_off(int r, int c) {
-  return (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
-
-// Named barrier of the eight softmax warps.
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// The same barrier, returning the AND of `ok` over the eight warps: every softmax thread takes the
-// same branch after it, so an error stops all of them at the same barrier.
-__device__ __forceinline__ bool softmax_sync_and(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, 1, 256, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(ok ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
-
-// O += P V with A = P read from TMEM (bf16 pairs packed in 32-bit columns, K-major by construction).
-__device__ __forceinline__ void mma1_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// 32 lanes x 32 consecutive 32-bit columns from registers (each thread its lane's 32 values).
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// Work item t (in fetch order) -> query block qb and head n.  Items come in groups of `group` heads
-// (whose K and V stay in L2 while the group is worked on); inside a group the heaviest query blocks
-// (the most key blocks) come first, so the last items fetched are light ones.
-__device__ __forceinline__ void item_of(int t, int nheads, int nqb, int group, int& qb, int& n) {
-  const int per_group = group * nqb;
-  const int gi = t / per_group, r = t - gi * per_group;
-  const int gh = min(group, nheads - gi * group);
-  qb = nqb - 1 - r / gh;
-  n = gi * group + (r - (r / gh) * gh);
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_flash_fwd_kernel(const __grid_constant__ Maps maps, int nheads, int H, int s, int group, float scale,
@@ -264,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         int qb, n;
         item_of(t, nheads, nqb, group, qb, n);
+        qb = nqb - 1 - qb;  // rank 0: the last query block (the most key blocks)
         const int bi = n / H, h = n - bi * H;
         const int col0 = h * kDh;
         // Q of this item once the previous item's last S MMA has read the previous Q.
@@ -317,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         int qb, n;
         item_of(t, nheads, nqb, group, qb, n);
+        qb = nqb - 1 - qb;  // rank 0: the last query block (the most key blocks)
         const int bi = n / H, h = n - bi * H;
         for (int j = 0; j <= qb && ok; ++j, ++g) {
           const int st = static_cast<int>(g & 1);
@@ -380,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         int qb, n;
         item_of(t, nheads, nqb, group, qb, n);
+        qb = nqb - 1 - qb;  // rank 0: the last query block (the most key blocks)
         if (!mbar_wait(q_full, static_cast<uint32_t>(it & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA) ||
             !issue_s(g, qb == 0)) {
           ok = false;
@@ -443,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok || t < 0) break;  // uniform: every warp read the same item
       int qb, n;
       item_of(t, nheads, nqb, group, qb, n);
+      qb = nqb - 1 - qb;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j <= qb; ++j, ++g) {
         const int st = static_cast<int>(g & 1);
@@ -459,13 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 64; ++kk) x[kk] = 0.f;
         }
-        const bool diag = j == qb;
-        float bm = -INFINITY;
+        if (j == qb) {  // the diagonal block: keys after the row's query are masked
 #pragma unroll
-        for (int kk = 0; kk < 64; ++kk) {
-          x[kk] = (diag && 64 * half + kk > row) ? -INFINITY : x[kk] * c;
-          bm = fmaxf(bm, x[kk]);
+          for (int kk = 0; kk < 64; ++kk)
+            if (64 * half + kk > row) x[kk] = -INFINITY;
         }
+        // Block maximum of c S (c > 0, so the maximum of S scaled), in eight independent chains.
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = x[u];
+#pragma unroll
+        for (int kk = 8; kk < 64; ++kk) mx[kk & 7] = fmaxf(mx[kk & 7], x[kk]);
+        float bm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        bm *= c;
         // Both halves of the row agree on the block maximum (this barrier also orders every read of
         // S_j before any write of P_j over its columns).
         float* xb = xch + (g & 1) * (2 * kRows);
@@ -500,14 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l *= alpha;
         m = m_new;
-        // P (bf16 pairs) over the first 64 columns of S's buffer: this half's 64 keys in 32 columns.
+        // P = 2^(c S - m) (bf16 pairs) over the first 64 columns of S's buffer: this half's 64 keys in
+        // 32 columns; the row sum in four independent chains.
         uint32_t pk[32];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const float nm = -m;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-          const float p0 = exp2f(x[2 * u] - m), p1 = exp2f(x[2 * u + 1] - m);
-          l += p0 + p1;
+          const float p0 = ex2_ftz(fmaf(x[2 * u], c, nm)), p1 = ex2_ftz(fmaf(x[2 * u + 1], c, nm));
+          ls[u & 3] += p0 + p1;
           pk[u] = pack_bf16x2(p0, p1);
         }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         if (!fail) tmem_st32u(t_lane + st * kRows + 32 * half, pk);
         tmem_st_wait();
         tc_fence_before();
@@ -592,9 +477,7 @@ cudaError_t launch_attn_flash_fwd(const bf16* q, const bf16* k, const bf16* v, b
   const long long items = 1LL * b * H * (s / kRows);
   if (items == 0) return cudaSuccess;
   if (items > (1LL << 30)) return cudaErrorInvalidValue;
-  // Heads per group: their K and V (s keys x dh x 2 tensors x 2 bytes each) about 32 MiB, well inside L2.
-  const long long per_head = 4LL * s * dh;
-  const int group = static_cast<int>(std::max<long long>(1, std::min<long long>(1LL * b * H, (32LL << 20) / per_head)));
+  const int group = heads_per_group(1LL * b * H, 4LL * s * dh);  // K and V of a head: s x dh x 2 x 2 bytes
   cudaError_t e = cudaMemsetAsync(sched, 0, sizeof(unsigned), st);  // the item counter of this launch
   if (e != cudaSuccess) return e;
   const long long grid = std::min<long long>(items, device_sm_count());  // persistent: one CTA per SM

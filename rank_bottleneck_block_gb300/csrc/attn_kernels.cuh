@@ -31,4 +31,13 @@ bool attn_flash_fwd_supported(int dh);
 cudaError_t launch_attn_flash_fwd(const bf16* q, const bf16* k, const bf16* v, bf16* o, int b, int s, int H, int dh,
                                   float scale, float* lse, unsigned* sched, unsigned* err, cudaStream_t st);
 
+// Causal attention backward without materialised P (tcgen05; the head width it is built for): dk, dv
+// [b*s, H*dh] token-major and dst = scale dS^T, head-major [b*H*s keys, s queries] bf16 (the blocks on
+// and below the diagonal, plus key block j against query block j - 1 for odd j, zero), from token-major
+// q, k, v, dout, the forward's lse and D_q = sum_c dO_qc O_qc (both head-major [b*H*s]).  s a multiple of
+// 128; sched as for the forward.
+cudaError_t launch_attn_flash_bwd(const bf16* q, const bf16* k, const bf16* v, const bf16* dout, const float* lse,
+                                  const float* D, bf16* dst, bf16* dk, bf16* dv, int b, int s, int H, int dh,
+                                  float scale, unsigned* sched, unsigned* err, cudaStream_t st);
+
 }  // namespace lr

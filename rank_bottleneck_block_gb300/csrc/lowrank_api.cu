@@ -1218,13 +1218,13 @@ static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   const int R = b * H * s, d = H * dh;
   if (attn_flash_fwd_supported(dh)) {
     // One persistent launch over the (head, 128 queries) items: S and O in TMEM, the softmax in the
-    // epilogue warps; no scores in memory (the workspace's first word counts the items taken).
+    // epilogue warps; no scores in memory (the first word of S's workspace counts the items taken).
     // Algorithmic FLOPs: Q K^T and P V over the causal half.
     const double causal = 2.0 * 2.0 * b * H * static_cast<double>(s) * s * dh * 0.5;
     LaunchScope scope("attn_flash_fwd", c.st, causal, 8.0 * b * s * d + 4.0 * R);
     cudaError_t e = launch_attn_flash_fwd(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
                                           static_cast<const bf16*>(v), static_cast<bf16*>(o), b, s, H, dh, scale,
-                                          lse, reinterpret_cast<unsigned*>(W.D), c.err, c.st);
+                                          lse, reinterpret_cast<unsigned*>(W.S), c.err, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention forward: %s", cudaGetErrorString(e));
     return LR_OK;
   }
@@ -1253,6 +1253,23 @@ static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
     cudaError_t e = launch_attn_rowdot(static_cast<const bf16*>(dout), static_cast<const bf16*>(o), b, s, H, dh,
                                        W.D, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention row dot: %s", cudaGetErrorString(e));
+  }
+  if (attn_flash_fwd_supported(dh)) {
+    // dK and dV in one persistent launch over (head, 128 keys) items (S^T, dP^T, dV, dK in TMEM; P^T and
+    // dS^T as the TMEM A operands of dV and dK), which also stores scale dS^T (bf16, head-major, in P's
+    // workspace); then dQ = dS K as one GEMM that reads it MN-major.  Algorithmic FLOPs: four products
+    // over the causal half; bytes: q, k, v, dO read, dk, dv and the causal half of dS^T written.
+    bf16* dst = W.P;
+    {
+      const double causal4 = 4.0 * 2.0 * b * H * static_cast<double>(s) * s * dh * 0.5;
+      LaunchScope scope("attn_flash_bwd", c.st, causal4, 12.0 * b * s * d + 1.0 * R * s + 8.0 * R);
+      cudaError_t e = launch_attn_flash_bwd(
+          static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
+          static_cast<const bf16*>(dout), lse, W.D, dst, static_cast<bf16*>(dk), static_cast<bf16*>(dv), b, s, H, dh,
+          scale, reinterpret_cast<unsigned*>(W.S), c.err, c.st);
+      if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention backward: %s", cudaGetErrorString(e));
+    }
+    return attn_gemm(c, EPI_STORE, a, s, dh, s, {dst, s}, true, false, {k, d}, true, true, dq, d, true, 2);
   }
   {
     // One dual-accumulator launch per tile of every head: S = Q K^T again (only its log-sum-exp
