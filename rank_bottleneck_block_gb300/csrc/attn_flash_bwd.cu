@@ -3,26 +3,28 @@
 //
 // A work item is a block of 128 keys j of one head (taken from a global counter, in groups of heads whose
 // Q and dO fit in L2, the blocks with the most queries first).  The CTA keeps K_j and V_j in shared memory
-// and walks the query steps i = 64-query blocks from the diagonal on, with the keys on the MMA rows:
+// and walks the query blocks i = j, j+1, ... of 128 queries, with the keys on the MMA rows:
 //
-//   S^T  = K_j Q_i^T, dP^T = V_j dO_i^T        MMA, fp32 in TMEM (two buffers: step i+1 overlaps the
-//                                              element-wise work of step i)
+//   S^T  = K_j Q_i^T, dP^T = V_j dO_i^T        MMA (N = 128), fp32 in TMEM
 //   P^T  = 2^(c S^T - lse log2 e)              element-wise warps, c = scale log2 e (lse: the forward's
 //   dS^T = scale P^T (dP^T - D)                 row log-sum-exp; D_q = sum dO_q O_q); causal mask on the
-//                                              diagonal; both written back to TMEM as bf16 over the
+//                                              diagonal block; both written back to TMEM as bf16 over the
 //                                              columns they were computed from, dS^T also to memory
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i         MMA with A from TMEM, fp32 accumulators in TMEM
 //
-// and at the end of the item dV_j and dK_j go to the token-major outputs.  The stored dS^T is head-major
-// [b*H*s keys, s queries]; entries above the diagonal are not written except for key block j against
-// query block j - 1 when j is odd, which are zeroed: the dQ GEMM's causal K range of a 256-query tile ends
-// at its last query, so it reads that block.
+// TMEM holds S^T, dP^T, dV and dK (128 columns each), so S^T and dP^T have one buffer.  The element-wise
+// warps work on the block's queries in two halves of 64, and the dV and dK MMAs of the first half run
+// while they compute the second.  At the end of the item dV_j and dK_j go to the token-major outputs.
+// The stored dS^T is head-major [b*H*s keys, s queries]; entries above the diagonal are not written
+// except for key block j against query block j - 1 when j is odd, which are zeroed: the dQ GEMM's causal
+// K range of a 256-query tile ends at its last query, so it reads that block.
 //
-// Warps: 0 item scheduler and TMA producer (K_j, V_j per item; Q_i, dO_i, lse_i, D_i per step into a
-// four-stage ring), 1 TMEM allocator and MMA issuer (one lane), 2-3 idle, 4-11 element-wise: warp w reads
-// TMEM lanes 32 (w mod 4) .. (its 32 keys), warpgroup 0 queries 0-31 of each step, warpgroup 1 queries
-// 32-63.  TMEM: buffer b of S^T at columns 128 b, of dP^T at 128 b + 64 (64 columns each), dV at 256, dK
-// at 384.  Every mbarrier wait is bounded (error word, abort flag; each role drains what it issued).
+// Warps: 0 item scheduler and TMA producer (K_j, V_j per item; Q_i, dO_i, lse_i, D_i per query block
+// into a two-stage ring), 1 TMEM allocator and MMA issuer (one lane), 2-3 idle, 4-19 element-wise: warp w
+// reads TMEM lanes 32 (w mod 4) .. (its 32 keys) and takes queries 64 h + 16 sub .. + 15 of half h
+// (sub = (w - 4) / 4); each warp writes its 32 x 16 pieces of dS^T, dK and dV through its own staging
+// tile with TMA stores.  TMEM: S^T at columns 0, dP^T at 128, dV at 256, dK at 384.  Every mbarrier wait
+// is bounded (error word, abort flag; each role drains what it issued).
 #include "attn_flash.cuh"
 #include "attn_kernels.cuh"
 
@@ -30,15 +32,44 @@ namespace lr {
 namespace flash {
 namespace bwd {
 
-constexpr int kQ = 64;                // queries per step (N of the S^T and dP^T MMAs)
-constexpr int kQTile = kQ * kDh * 2;  // 16 KB: 64 rows x 128 bf16
-constexpr int kQHalf = kQTile / 2;    // 8 KB: 64 rows x 64 columns
-constexpr int kStages = 4;
-constexpr int kSmem = 1024 + 2 * kTile + kStages * 2 * kQTile + kStages * 2 * kQ * 4 + 256;
+constexpr int kQ = kRows;             // queries per step (N of the S^T and dP^T MMAs)
+constexpr int kQTile = kTile;         // 32 KB: 128 rows x 128 bf16
+constexpr int kStages = 2;
+constexpr int kEw = 16;                          // element-wise warps (4 per TMEM lane quarter)
+constexpr int kThreadsB = 32 * (kSoftmax0 + kEw);  // 640
+constexpr int kStageDs = 32 * 16 * 2;  // one warp's 32 rows x 16 columns, staged for a TMA store (1 KB)
+constexpr int kSmem = 1024 + 2 * kTile + kStages * 2 * kQTile + kEw * kStageDs + kStages * 2 * kQ * 4 + 256;
+
+using umma::tmem_ld16;
 
 struct Maps {
-  CUtensorMap q, dout, k, v;  // q, dout: boxes of 64 columns x 64 rows; k, v: 64 x 128
+  CUtensorMap q, dout, k, v;  // boxes of 64 columns x 128 rows
+  CUtensorMap ds, dk, dv;     // outputs: boxes of 16 columns x 32 rows, 32-byte swizzle
 };
+
+// 32 lanes x 8 consecutive 32-bit columns from registers.
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// The sixteen element-wise warps' named barrier, returning the AND of `ok` over them.
+__device__ __forceinline__ bool ew_sync_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, 512, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(ok ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// Byte offset of 16-byte chunk u of row r in a staging tile of 32-byte rows with the 32-byte swizzle.
+__device__ __forceinline__ uint32_t sw32_off(int r, int u) { return r * 32 + ((u ^ ((r >> 2) & 1)) << 4); }
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -53,37 +84,63 @@ __device__ __forceinline__ void stg_zero64(bf16* p) {  // 64 bytes of zeros (16-
   for (int u = 0; u < 4; ++u) q[u] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// P^T and scale dS^T of 16 queries of one key row (the element-wise step), packed in bf16 pairs.
+template <bool MASK>
+__device__ __forceinline__ void pds16(const float* x, const float* y, const float* Ls, const float* Ds, float c,
+                                      float scale, int qrel, uint32_t* pk, uint32_t* dk2) {
+#pragma unroll
+  for (int u4 = 0; u4 < 4; ++u4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(Ls + 4 * u4);
+    const float4 d4 = *reinterpret_cast<const float4*>(Ds + 4 * u4);
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+    float p[4], d2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int u = 4 * u4 + e;
+      float pe = ex2_ftz(fmaf(x[u], c, -lv[e] * kLog2e));
+      if (MASK && qrel + u < 0) pe = 0.f;  // a query before this key (the diagonal block)
+      p[e] = pe;
+      d2[e] = scale * pe * (y[u] - dv[e]);
+    }
+    pk[2 * u4] = pack_bf16x2(p[0], p[1]);
+    pk[2 * u4 + 1] = pack_bf16x2(p[2], p[3]);
+    dk2[2 * u4] = pack_bf16x2(d2[0], d2[1]);
+    dk2[2 * u4 + 1] = pack_bf16x2(d2[2], d2[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsB, 1)
     attn_flash_bwd_kernel(const __grid_constant__ Maps maps, const float* lse, const float* Dr, bf16* dst, bf16* dk,
                           bf16* dv, int nheads, int H, int s, int group, float scale, unsigned* sched, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + kTile;
-  uint8_t* sQ = sV + kTile;                // [kStages]
-  uint8_t* sdO = sQ + kStages * kQTile;    // [kStages]
-  float* sL = reinterpret_cast<float*>(sdO + kStages * kQTile);  // [kStages][kQ] lse
+  uint8_t* sQ = sV + kTile;              // [kStages]
+  uint8_t* sdO = sQ + kStages * kQTile;  // [kStages]
+  uint8_t* sS = sdO + kStages * kQTile;  // [kEw] output staging, one tile per element-wise warp
+  float* sL = reinterpret_cast<float*>(sS + kEw * kStageDs);  // [kStages][kQ] lse
   float* sD = sL + kStages * kQ;                                   // [kStages][kQ] D
   uint64_t* bars = reinterpret_cast<uint64_t*>(sD + kStages * kQ);
   uint64_t* kv_full = bars;
   uint64_t* kv_free = bars + 1;     // the item's last S^T and dP^T MMAs have read K and V
   uint64_t* qd_full = bars + 2;     // [kStages]
-  uint64_t* qd_empty = bars + 6;    // [kStages] the step's dV and dK MMAs have read Q and dO
-  uint64_t* s_full = bars + 10;     // [2]
-  uint64_t* p_full = bars + 12;     // [2]
-  uint64_t* acc_full = bars + 14;   // the item's last dV and dK MMAs are complete
-  uint64_t* acc_free = bars + 15;   // the element-wise warps have read dV and dK
-  uint64_t* drain = bars + 16;
-  uint64_t* item_full = bars + 17;  // [2] the item ring
-  uint64_t* item_empty = bars + 19; // [2]
-  int* sitem = reinterpret_cast<int*>(bars + 21);  // [2]
+  uint64_t* qd_empty = bars + 4;    // [kStages] the step's dV and dK MMAs have read Q and dO
+  uint64_t* s_full = bars + 6;      // S^T and dP^T of the step are in TMEM
+  uint64_t* p_half = bars + 7;      // [2] P^T and dS^T of a half of the step's queries are in TMEM
+  uint64_t* acc_full = bars + 9;    // the item's last dV and dK MMAs are complete
+  uint64_t* acc_free = bars + 10;   // the element-wise warps have read dV and dK
+  uint64_t* drain = bars + 11;
+  uint64_t* item_full = bars + 12;  // [2] the item ring
+  uint64_t* item_empty = bars + 14; // [2]
+  int* sitem = reinterpret_cast<int*>(bars + 16);  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sitem + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = s / kRows, nqs = s / kQ;
+  const int nkb = s / kRows;
   const int items = nheads * nkb;
-  constexpr int kItemReaders = 1 + 8;  // MMA issuer, element-wise warps
+  constexpr int kItemReaders = 1 + kEw;  // MMA issuer, element-wise warps
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -92,14 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
     }
+    mbar_init(s_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
+      mbar_init(&p_half[i], kEw);
       mbar_init(&item_full[i], 1);
       mbar_init(&item_empty[i], kItemReaders);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_free, 8);
+    mbar_init(acc_free, kEw);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -129,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------ scheduler and TMA producer
       bool ok = true;
       int kv_issued = 0;
-      long long g = 0;  // query steps issued over all items
+      long long g = 0;  // query blocks issued over all items
       for (int it = 0;; ++it) {
         const int slot = it & 1;
         if (!mbar_wait(&item_empty[slot], static_cast<uint32_t>((it >> 1) & 1) ^ 1u, abort_flag, err,
@@ -143,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&item_full[slot]);
         if (t < 0) break;
         int j, n;
-        item_of(t, nheads, nkb, group, j, n);  // rank 0: key block 0 (the most query steps)
+        item_of(t, nheads, nkb, group, j, n);  // rank 0: key block 0 (the most query blocks)
         const int bi = n / H, h = n - bi * H;
         const int col0 = h * kDh;
         if (!mbar_wait(kv_free, static_cast<uint32_t>(it & 1) ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_PRODUCER)) {
@@ -157,9 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sV, &maps.v, kv_full, col0, key0);
         tma_load_2d(sV + kHalf, &maps.v, kv_full, col0 + 64, key0);
         ++kv_issued;
-        for (int i = 2 * j; i < nqs && ok; ++i, ++g) {
-          const int st = static_cast<int>(g & (kStages - 1));
-          const uint32_t ph = static_cast<uint32_t>((g / kStages) & 1);
+        for (int i = j; i < nkb && ok; ++i, ++g) {
+          const int st = static_cast<int>(g & 1);
+          const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
           if (!mbar_wait(&qd_empty[st], ph ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
@@ -167,9 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&qd_full[st], 2 * kQTile + 2 * kQ * 4);
           const int row = bi * s + i * kQ;
           tma_load_2d(sQ + st * kQTile, &maps.q, &qd_full[st], col0, row);
-          tma_load_2d(sQ + st * kQTile + kQHalf, &maps.q, &qd_full[st], col0 + 64, row);
+          tma_load_2d(sQ + st * kQTile + kHalf, &maps.q, &qd_full[st], col0 + 64, row);
           tma_load_2d(sdO + st * kQTile, &maps.dout, &qd_full[st], col0, row);
-          tma_load_2d(sdO + st * kQTile + kQHalf, &maps.dout, &qd_full[st], col0 + 64, row);
+          tma_load_2d(sdO + st * kQTile + kHalf, &maps.dout, &qd_full[st], col0 + 64, row);
           const long long r0 = 1LL * n * s + 1LL * i * kQ;  // head-major row of lse and D
           bulk_load(sL + st * kQ, lse + r0, kQ * 4, &qd_full[st]);
           bulk_load(sD + st * kQ, Dr + r0, kQ * 4, &qd_full[st]);
@@ -179,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {  // wait (bounded) for the copies still in flight before the CTA may exit
         for (long long k = (g > kStages ? g - kStages : 0); k < g; ++k) {
           const uint64_t t0 = global_timer_ns();
-          while (!mbar_test(&qd_full[k & (kStages - 1)], static_cast<uint32_t>((k / kStages) & 1)) &&
+          while (!mbar_test(&qd_full[k & 1], static_cast<uint32_t>((k >> 1) & 1)) &&
                  global_timer_ns() - t0 < umma::kWaitLimitNs) {
           }
         }
@@ -192,35 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdS = idesc_m128<false, kQ>();  // S^T, dP^T: keys x 64 queries, both K-major
+      constexpr uint32_t kIdS = idesc_m128<false, kQ>();  // S^T, dP^T: keys x 128 queries, both K-major
       constexpr uint32_t kIdG = idesc_m128<true, kDh>();  // dV, dK: A from TMEM, B (dO, Q) MN-major
       const uint32_t k_base = smem_addr(sK), v_base = smem_addr(sV);
       const uint32_t q_base = smem_addr(sQ), do_base = smem_addr(sdO);
       bool ok = true;
       long long g = 0;
-      // S^T and dP^T of step gg into TMEM buffer gg & 1 (last held the P^T and dS^T of step gg - 2, whose
-      // dV and dK MMAs were issued before this: the MMAs of a thread run in order).
-      auto issue_s = [&](long long gg, bool last) -> bool {
-        const int st = static_cast<int>(gg & (kStages - 1));
-        const uint32_t ph = static_cast<uint32_t>((gg / kStages) & 1);
-        if (!mbar_wait(&qd_full[st], ph, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(gg & 1) * 128;
-        const uint32_t qt = q_base + st * kQTile, dt = do_base + st * kQTile;
-#pragma unroll
-        for (int kk = 0; kk < kDh / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * kHalf + (kk & 3) * 32, bo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-          mma1(d, sdesc(k_base + ao, 16, 1024), sdesc(qt + bo, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < kDh / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * kHalf + (kk & 3) * 32, bo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-          mma1(d + 64, sdesc(v_base + ao, 16, 1024), sdesc(dt + bo, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-        }
-        commit1(&s_full[gg & 1]);
-        if (last) commit1(kv_free);  // K and V may be replaced once these are complete
-        return true;
-      };
       for (int it = 0; ok; ++it) {
         int t;
         if (!next_item(it, t)) {
@@ -231,39 +265,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         int j, n;
         item_of(t, nheads, nkb, group, j, n);
-        const int nsteps = nqs - 2 * j;
-        if (!mbar_wait(kv_full, static_cast<uint32_t>(it & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA) ||
-            !issue_s(g, nsteps == 1)) {
+        const int nsteps = nkb - j;
+        if (!mbar_wait(kv_full, static_cast<uint32_t>(it & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
           ok = false;
           break;
         }
         for (int k = 0; k < nsteps && ok; ++k, ++g) {
-          if (k + 1 < nsteps && !issue_s(g + 1, k + 2 == nsteps)) {
-            ok = false;
-            break;
-          }
-          const int b = static_cast<int>(g & 1);
-          const int st = static_cast<int>(g & (kStages - 1));
-          if (!mbar_wait(&p_full[b], static_cast<uint32_t>((g >> 1) & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
-            ok = false;
-            break;
-          }
-          // The item's first dV / dK MMAs overwrite the accumulators: the previous item's must have been read.
-          if (k == 0 && !mbar_wait(acc_free, static_cast<uint32_t>(it & 1) ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
+          const int st = static_cast<int>(g & 1);
+          if (!mbar_wait(&qd_full[st], static_cast<uint32_t>((g >> 1) & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t qt = q_base + st * kQTile, dt = do_base + st * kQTile;
+          // S^T and dP^T (their columns last held the previous step's P^T and dS^T, whose dV and dK MMAs
+          // were issued before these: the MMAs of a thread run in order)
 #pragma unroll
-          for (int kk = 0; kk < kQ / 16; ++kk) {
-            // K step kk = queries 16 kk .. 16 kk + 15: packed in columns 32 (kk / 2) + 8 (kk mod 2) of the
-            // buffer (each warpgroup wrote its 32 queries over the first half of the columns it read)
-            const uint32_t pc = static_cast<uint32_t>(b) * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
-            const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
-            mma1_ta(tmem + 256, tmem + pc, sdesc(dt + kk * 2048, kQHalf, 1024), kIdG, acc);
-            mma1_ta(tmem + 384, tmem + pc + 64, sdesc(qt + kk * 2048, kQHalf, 1024), kIdG, acc);
+          for (int kk = 0; kk < kDh / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma1(tmem, sdesc(k_base + o, 16, 1024), sdesc(qt + o, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
           }
+#pragma unroll
+          for (int kk = 0; kk < kDh / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma1(tmem + 128, sdesc(v_base + o, 16, 1024), sdesc(dt + o, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          }
+          commit1(s_full);
+          if (k + 1 == nsteps) commit1(kv_free);  // K and V may be replaced once these are complete
+          for (int hf = 0; hf < 2 && ok; ++hf) {
+            if (!mbar_wait(&p_half[hf], static_cast<uint32_t>(g & 1), abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            // The item's first dV / dK MMAs overwrite the accumulators: the previous item's must have been read.
+            if (k == 0 && hf == 0 &&
+                !mbar_wait(acc_free, static_cast<uint32_t>(it & 1) ^ 1u, abort_flag, err, DEV_ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+              // K step kk = queries 16 kk .. 16 kk + 15, packed by the warps of column group kk mod 4 of half
+              // kk / 4 in columns 64 (kk / 4) + 16 (kk mod 4) .. + 7: over the first half of what they read
+              const int kk = 4 * hf + kq;
+              const uint32_t pc = 64 * (kk >> 2) + 16 * (kk & 3);
+              const uint32_t acc = (k > 0 || kk > 0) ? 1u : 0u;
+              mma1_ta(tmem + 256, tmem + pc, sdesc(dt + kk * 2048, kHalf, 1024), kIdG, acc);
+              mma1_ta(tmem + 384, tmem + 128 + pc, sdesc(qt + kk * 2048, kHalf, 1024), kIdG, acc);
+            }
+          }
+          if (!ok) break;
           commit1(&qd_empty[st]);
           if (k + 1 == nsteps) commit1(acc_full);
         }
@@ -276,102 +328,107 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kSoftmax0) {
     // ------------------------------------------------ element-wise warps
     // `fail`: a wait of this warp gave up (its TMEM accesses and stores are skipped from then on); `ok`
-    // changes only at softmax_sync_and, so every warp leaves the item loop at the same barrier.
+    // changes only at ew_sync_and, so every warp leaves the item loop at the same barrier.
     const int q4 = warp & 3;
-    const int half = (warp - kSoftmax0) >> 2;  // queries 32 half .. 32 half + 31 of each step
-    const int row = q4 * 32 + lane;            // key within the block (TMEM lane)
+    const int sub = (warp - kSoftmax0) >> 2;  // column group: queries 64 h + 16 sub .. + 15 of half h
+    const int row = q4 * 32 + lane;           // key within the block (TMEM lane)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     const float c = scale * kLog2e;
-    const int HD = H * kDh;
+    const uint32_t tile = smem_addr(sS + (warp - kSoftmax0) * kStageDs);
+    uint8_t* tile_p = sS + (warp - kSoftmax0) * kStageDs;
     bool ok = true, fail = false;
     long long g = 0;
+    // 32 rows x 16 bf16 (this warp's 8 packed words per lane) through the staging tile to a TMA store.
+    auto store_tile = [&](const CUtensorMap* map, const uint32_t* w, int x, int y) {
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the tile is free
+      __syncwarp();
+      sts128(tile + sw32_off(lane, 0), w[0], w[1], w[2], w[3]);
+      sts128(tile + sw32_off(lane, 1), w[4], w[5], w[6], w[7]);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, tile_p, x, y);
+        bulk_commit();
+      }
+    };
     for (int it = 0;; ++it) {
       int t = -1;
       bool okw = next_item(it, t);
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[it & 1]);
-      ok = softmax_sync_and(okw && !fail);
+      ok = ew_sync_and(okw && !fail);
       if (!ok || t < 0) break;
       int j, n;
       item_of(t, nheads, nkb, group, j, n);
       const int bi = n / H, h = n - bi * H;
-      const int nsteps = nqs - 2 * j;
-      bf16* ds_row = dst + (1LL * n * s + 1LL * j * kRows + row) * s;  // this key's row of dS^T
-      if (j & 1) stg_zero64(ds_row + (j - 1) * kRows + 64 * half), stg_zero64(ds_row + (j - 1) * kRows + 64 * half + 32);
+      const int nsteps = nkb - j;
+      const int ds_key0 = n * s + j * kRows + q4 * 32;  // this warp's first key row of dS^T
+      if (j & 1) stg_zero64(dst + (1LL * n * s + 1LL * j * kRows + row) * s + (j - 1) * kRows + 32 * sub);
       for (int k = 0; k < nsteps; ++k, ++g) {
-        const int b = static_cast<int>(g & 1);
-        const int st = static_cast<int>(g & (kStages - 1));
-        okw = mbar_wait(&s_full[b], static_cast<uint32_t>((g >> 1) & 1), abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE) &&
-              mbar_wait(&qd_full[st], static_cast<uint32_t>((g / kStages) & 1), abort_flag, err,
+        const int st = static_cast<int>(g & 1);
+        okw = mbar_wait(s_full, static_cast<uint32_t>(g & 1), abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE) &&
+              mbar_wait(&qd_full[st], static_cast<uint32_t>((g >> 1) & 1), abort_flag, err,
                         DEV_ERR_TIMEOUT_EPILOGUE);  // complete already; orders the reads of lse and D
         okw = __all_sync(0xffffffffu, okw);
         fail = fail || !okw;
-        float x[32], y[32];
-        if (!fail) {
-          tc_fence_after();
-          tmem_ld32(t_lane + b * 128 + 32 * half, x);
-          tmem_ld32(t_lane + b * 128 + 64 + 32 * half, y);
-          tmem_ld_wait();
-        } else {
+        for (int hf = 0; hf < 2; ++hf) {
+          const int c0 = 64 * hf + 16 * sub;  // this warp's 16 queries of the block
+          float x[16], y[16];
+          if (!fail) {
+            tc_fence_after();
+            tmem_ld16(t_lane + c0, x);
+            tmem_ld16(t_lane + 128 + c0, y);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) x[u] = y[u] = 0.f;
-        }
-        const float* Ls = sL + st * kQ + 32 * half;
-        const float* Ds = sD + st * kQ + 32 * half;
-        const int qrel = 64 * k + 32 * half - row;  // query - key of column 0 (relative to the block)
-        uint32_t pk[16], dk2[16];
-#pragma unroll
-        for (int u = 0; u < 32; u += 2) {
-          float p[2], d2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float pe = ex2_ftz(fmaf(x[u + e], c, -Ls[u + e] * kLog2e));
-            if (qrel + u + e < 0) pe = 0.f;  // a query before this key (only on the diagonal steps)
-            p[e] = pe;
-            d2[e] = scale * pe * (y[u + e] - Ds[u + e]);
+            for (int u = 0; u < 16; ++u) x[u] = y[u] = 0.f;
           }
-          pk[u >> 1] = pack_bf16x2(p[0], p[1]);
-          dk2[u >> 1] = pack_bf16x2(d2[0], d2[1]);
+          const float* Ls = sL + st * kQ + c0;
+          const float* Ds = sD + st * kQ + c0;
+          uint32_t pk[8], dk2[8];
+          if (k == 0)
+            pds16<true>(x, y, Ls, Ds, c, scale, c0 - row, pk, dk2);
+          else
+            pds16<false>(x, y, Ls, Ds, c, scale, 0, pk, dk2);
+          if (!fail) {
+            tmem_st8u(t_lane + c0, pk);
+            tmem_st8u(t_lane + 128 + c0, dk2);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_half[hf]);
+          if (!fail) store_tile(&maps.ds, dk2, (j + k) * kQ + c0, ds_key0);
         }
-        if (!fail) {
-          tmem_st16u(t_lane + b * 128 + 32 * half, pk);
-          tmem_st16u(t_lane + b * 128 + 64 + 32 * half, dk2);
-          uint4* o = reinterpret_cast<uint4*>(ds_row + (2 * j + k) * kQ + 32 * half);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) o[u] = make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[b]);
       }
-      // dV_j and dK_j: this warp's 32 keys, dh columns 64 half .. 64 half + 63
+      // dV_j and dK_j: this warp's 32 keys, dh columns 32 sub .. 32 sub + 31 of each
       okw = mbar_wait(acc_full, static_cast<uint32_t>(it & 1), abort_flag, err, DEV_ERR_TIMEOUT_EPILOGUE);
       okw = __all_sync(0xffffffffu, okw);
       fail = fail || !okw;
-      if (!fail) {
-        tc_fence_after();
-        const long long orow = (1LL * bi * s + 1LL * j * kRows + row) * HD + 1LL * h * kDh + 64 * half;
+      if (!fail) tc_fence_after();
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          bf16* out = (which == 0 ? dv : dk) + orow;
+      for (int which = 0; which < 2; ++which)
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            float a[32];
-            tmem_ld32(t_lane + 256 + 128 * which + 64 * half + 32 * cc, a);
+        for (int hh = 0; hh < 2; ++hh) {
+          float a[16];
+          if (!fail) {
+            tmem_ld16(t_lane + 256 + 128 * which + 32 * sub + 16 * hh, a);
             tmem_ld_wait();
-            uint4* o = reinterpret_cast<uint4*>(out + 32 * cc);
+          }
+          if (which == 1 && hh == 1) {  // the accumulators are read; the last store below uses registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_free);
+          }
+          if (!fail) {
+            uint32_t w[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              o[u] = make_uint4(pack_bf16x2(a[8 * u], a[8 * u + 1]), pack_bf16x2(a[8 * u + 2], a[8 * u + 3]),
-                                pack_bf16x2(a[8 * u + 4], a[8 * u + 5]), pack_bf16x2(a[8 * u + 6], a[8 * u + 7]));
+            for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(a[2 * u], a[2 * u + 1]);
+            store_tile(which == 0 ? &maps.dv : &maps.dk, w, h * kDh + 32 * sub + 16 * hh, bi * s + j * kRows + q4 * 32);
           }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_free);
     }
+    if (lane == 0) bulk_wait_all();  // this warp's stores have completed
   }
 
   tc_fence_before();
@@ -380,6 +437,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
+}
+
+// bf16 [rows, cols] row-major (ld = cols) output map: boxes of 16 columns x 32 rows, 32-byte swizzle.
+inline bool encode_out16(CUtensorMap* m, const void* ptr, long long cols, long long rows) {
+  const long long dims[2] = {cols, rows}, strides[1] = {cols};
+  const int box[2] = {16, 32};
+  return umma::encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
 }  // namespace bwd
@@ -394,10 +458,12 @@ cudaError_t launch_attn_flash_bwd(const bf16* q, const bf16* k, const bf16* v, c
   bwd::Maps maps;
   memset(&maps, 0, sizeof(maps));
   const long long cols = 1LL * H * dh, rows = 1LL * b * s;
-  bool ok = umma::encode_operand(&maps.q, q, cols, rows, cols, 64, kQ) &&
-            umma::encode_operand(&maps.dout, dout, cols, rows, cols, 64, kQ) &&
+  bool ok = umma::encode_operand(&maps.q, q, cols, rows, cols, 64, kRows) &&
+            umma::encode_operand(&maps.dout, dout, cols, rows, cols, 64, kRows) &&
             umma::encode_operand(&maps.k, k, cols, rows, cols, 64, kRows) &&
-            umma::encode_operand(&maps.v, v, cols, rows, cols, 64, kRows);
+            umma::encode_operand(&maps.v, v, cols, rows, cols, 64, kRows) &&
+            encode_out16(&maps.ds, dst, s, 1LL * b * H * s) && encode_out16(&maps.dk, dk, cols, rows) &&
+            encode_out16(&maps.dv, dv, cols, rows);
   if (!ok) return cudaErrorInvalidValue;
   static int configured_mask = 0;
   int dev = 0;
@@ -415,7 +481,7 @@ cudaError_t launch_attn_flash_bwd(const bf16* q, const bf16* k, const bf16* v, c
   cudaError_t e = cudaMemsetAsync(sched, 0, sizeof(unsigned), st);  // the item counter of this launch
   if (e != cudaSuccess) return e;
   const long long grid = std::min<long long>(items, device_sm_count());
-  return launch_pdl(attn_flash_bwd_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmem, st, maps, lse,
+  return launch_pdl(attn_flash_bwd_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreadsB), kSmem, st, maps, lse,
                     D, dst, dk, dv, b * H, H, s, group, scale, sched, err);
 }
 
