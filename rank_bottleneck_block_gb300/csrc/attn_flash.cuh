@@ -150,10 +150,10 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
 // Work item t (in fetch order) of a walk over nheads heads x nb blocks -> (rank, head n).  Items come in
 // groups of `group` heads (whose operands stay in L2 while the group is worked on) and by rank inside a
 // group; the kernels map rank 0 to their heaviest block, so the last items fetched are light ones.
-__device__ __forceinline__ void item_of(int t, int nheads, int nb, int group, int& rank, int& n) {
+__host__ __device__ __forceinline__ void item_of(int t, int nheads, int nb, int group, int& rank, int& n) {
   const int per_group = group * nb;
   const int gi = t / per_group, r = t - gi * per_group;
-  const int gh = min(group, nheads - gi * group);
+  const int gh = group < nheads - gi * group ? group : nheads - gi * group;
   rank = r / gh;
   n = gi * group + (r - rank * gh);
 }
