@@ -165,6 +165,29 @@ struct Ctx {
   int chunk;  // row-partial chunk width of the engine
 };
 
+// A second stream for work that can run beside the caller's stream within one entry point, with the
+// events that fork it from and join it back to the caller's stream (under CUDA graph capture the
+// fork makes it part of the capture).  One per host thread and device, created on first use and kept.
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static lr_status side_stream(SideStream** out) {
+  thread_local SideStream per_dev[32];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 32) return fail(LR_ERR_CUDA, "no current device");
+  SideStream& s = per_dev[dev];
+  if (!s.st) {
+    if (cudaStreamCreateWithFlags(&s.st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
+      return fail(LR_ERR_CUDA, "side stream: %s", cudaGetErrorString(cudaGetLastError()));
+  }
+  *out = &s;
+  return LR_OK;
+}
+
 // Tile width of the SwiGLU dual GEMM (two accumulators: 256 fills TMEM with one buffer,
 // 128 keeps two buffers).
 static constexpr int kSwigluBn = 256;
@@ -669,7 +692,26 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
   const int ch = chunk_width(c.dt);
 
   StackSrc src = {{gate.A, up.A, nullptr}};
-  LR_TRY(fold(c, W.Af, src, 2, r, d, g));
+  void *z_gu, *z_d, *a, *b, *h;
+  z_gu = W.z_gu;
+  z_d = W.z_d;
+  // Checkpointed bf16: the gain fold and the re-forward of z from the saved u run on a second stream
+  // beside du_down's GEMM, whose last wave leaves SM pairs idle; joined before the re-forward GEMM.
+  const bool side = mode == LR_SAVE_CKPT && c.dt == LR_BF16 && !c.act;
+  SideStream* ss = nullptr;
+  if (side) {
+    LR_TRY(side_stream(&ss));
+    Ctx cs = c;
+    cs.st = ss->st;
+    if (cudaEventRecord(ss->fork, c.st) != cudaSuccess || cudaStreamWaitEvent(ss->st, ss->fork, 0) != cudaSuccess)
+      return fail(LR_ERR_CUDA, "fork: %s", cudaGetErrorString(cudaGetLastError()));
+    LR_TRY(fold(cs, W.Af, src, 2, r, d, g));
+    LR_TRY(silu_slabs(cs, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, r}, T));
+    if (cudaEventRecord(ss->join, ss->st) != cudaSuccess)
+      return fail(LR_ERR_CUDA, "join: %s", cudaGetErrorString(cudaGetLastError()));
+  } else {
+    LR_TRY(fold(c, W.Af, src, 2, r, d, g));
+  }
 
   // du_down = (G B_down) * SiLU'(u_down): needs only dout and the saved u_down, so it runs first
   // and the SwiGLU backward can follow the re-forward while a, b are still in L2
@@ -684,18 +726,18 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.ldo0 = r;
     LR_TRY(gemm(c, EPI_DSILU, k));
   }
-  void *z_gu, *z_d, *a, *b, *h;
   if (mode == LR_SAVE_CKPT) {
     // Low-rank activation checkpointing (technical summary §2.2): re-forward inside the block
     // from the saved [T, r] pre-activations; no other state is needed.
-    z_gu = W.z_gu;
-    z_d = W.z_d;
     a = W.a;
     b = W.b;
     h = W.h;
     if (c.act) {  // sigma = identity: z is u itself
       z_gu = S.u_gu;
       z_d = S.u_d;
+    } else if (side) {
+      if (cudaStreamWaitEvent(c.st, ss->join, 0) != cudaSuccess)
+        return fail(LR_ERR_CUDA, "join: %s", cudaGetErrorString(cudaGetLastError()));
     } else {
       LR_TRY(silu_slabs(c, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, r}, T));
     }
