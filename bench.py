@@ -42,9 +42,9 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 96.8e6 + 501.1e6,
-                                "sources_sha256": "a39158b9fa907833510e3bcbb8e142bba5df6c50a1e413d1bbf5a6387dbb287e",
-                                "profile": "profiles/gemm_kernels_mlp_block_T16384_ncu.md"},
+    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 87.3e6 + 501.1e6,
+                                "sources_sha256": "a8910df221e8ecbe3b4287abecef8928b04f84cdfbbdcbb1132274fa15b91386",
+                                "profile": "profiles/swiglu_rebwd_mlp_block_T16384_traffic.md"},
 }
 
 
