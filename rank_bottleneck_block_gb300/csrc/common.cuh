@@ -81,9 +81,15 @@ struct Num;
 template <>
 struct Num<bf16> {
   static __device__ __forceinline__ float round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
-  // logistic(u) = 1 / (1 + e^-u); the fast intrinsics are accurate far beyond bf16 storage
-  // precision.  For u below about -88 e^-u overflows to +inf and the quotient is exactly 0.
-  static __device__ __forceinline__ float logistic(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
+  // logistic(u) = 1 / (1 + e^-u) = (1 + tanh(u / 2)) / 2, with the hardware tanh approximation (one
+  // special-function op instead of an exponential and a reciprocal; its error, below 2^-10 absolute on
+  // the logistic, is far under bf16 storage precision).  tanh saturates to -1 / +1 for large |u|, so
+  // the logistic reaches exactly 0 / 1 there.
+  static __device__ __forceinline__ float logistic(float u) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * u));
+    return fmaf(0.5f, t, 0.5f);
+  }
 };
 
 template <>
