@@ -42,8 +42,8 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 87.3e6 + 501.1e6,
-                                "sources_sha256": "a8910df221e8ecbe3b4287abecef8928b04f84cdfbbdcbb1132274fa15b91386",
+    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 96.2e6 + 500.7e6,
+                                "sources_sha256": "be0729d203f16979d823212a15710547a9c3a16625649fec700ecffa208954d3",
                                 "profile": "profiles/swiglu_rebwd_mlp_block_T16384_traffic.md"},
 }
 
