@@ -18,14 +18,16 @@
 //
 // Warps: 0 item scheduler and TMA producer of Q (per item) and K_j (two-stage ring), 1 TMEM allocator and
 // MMA issuer (one lane), 2 TMA producer of V_j (its own two-stage ring: K_{j+2} loads once S_j is done,
-// V_{j+2} once P_j V_j is), 3 idle, 4-11 softmax and output in two warpgroups: warp w reads TMEM lanes 32 (w mod 4)
-// .. (its 32 query rows); warpgroup 0 takes keys 0-63 of each block and output columns 0-63, warpgroup 1
-// keys 64-127 and columns 64-127.  The two halves of a row agree on m through shared memory once per
-// block (a named barrier of the eight warps, which also orders every read of S before any write of P
-// over it).  Shared memory: Q, K[2], V[2] and the staged output O, each 128 x 128
-// bf16 in the 128-byte-swizzled UMMA layouts (K-major Q, K in two 64-column halves; V MN-major in two
-// 64-key halves of two 64-column chunks).  TMEM: S/P[2] at columns 0 and 128, O at 256.  Every mbarrier
-// wait is bounded (error word, abort flag; each role drains what it issued and TMEM is freed).
+// V_{j+2} once P_j V_j is), 3 idle, 4-11 softmax and output in two warpgroups: warp w reads TMEM lanes
+// 32 (w mod 4) .. (its 32 query rows); warpgroup 0 takes keys 0-63 of each block and output columns
+// 0-63, warpgroup 1 keys 64-127 and columns 64-127.  The two halves of a row agree on m through shared
+// memory once per block (a named barrier of the eight warps, which also orders every read of S before
+// any write of P over it).  The next item's Q is loaded once the last S MMA of the current one has read
+// Q, so its first S overlaps the current item's last softmax and output.  Shared memory: Q, K[2], V[2]
+// and the staged output O, each 128 x 128 bf16 in the 128-byte-swizzled UMMA layouts (K-major Q, K in
+// two 64-column halves; V MN-major in two 64-key halves of two 64-column chunks).  TMEM: S/P[2] at
+// columns 0 and 128, O at 256.  Every mbarrier wait is bounded (error word, abort flag; each role drains
+// what it issued and TMEM is freed).
 #include "attn_flash.cuh"
 #include "attn_kernels.cuh"
 
