@@ -371,6 +371,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                         DEV_ERR_TIMEOUT_EPILOGUE);  // complete already; orders the reads of lse and D
         okw = __all_sync(0xffffffffu, okw);
         fail = fail || !okw;
+        uint32_t dsk[2][8];  // this warp's scale dS^T of both halves, stored after the second (the warps
+                             // then wait for the next step's S^T anyway)
+#pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const int c0 = 64 * hf + 16 * sub;  // this warp's 16 queries of the block
           float x[16], y[16];
@@ -385,7 +388,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           }
           const float* Ls = sL + st * kQ + c0;
           const float* Ds = sD + st * kQ + c0;
-          uint32_t pk[8], dk2[8];
+          uint32_t pk[8];
+          uint32_t* dk2 = dsk[hf];
           if (k == 0)
             pds16<true>(x, y, Ls, Ds, c, scale, c0 - row, pk, dk2);
           else
@@ -398,7 +402,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&p_half[hf]);
-          if (!fail) store_tile(&maps.ds, dk2, (j + k) * kQ + c0, ds_key0);
+        }
+        if (!fail) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) store_tile(&maps.ds, dsk[hf], (j + k) * kQ + 64 * hf + 16 * sub, ds_key0);
         }
       }
       // dV_j and dK_j: this warp's 32 keys, dh columns 32 sub .. 32 sub + 31 of each
