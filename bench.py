@@ -42,8 +42,8 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 96.2e6 + 500.7e6,
-                                "sources_sha256": "be0729d203f16979d823212a15710547a9c3a16625649fec700ecffa208954d3",
+    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 99.8e6 + 500.8e6,
+                                "sources_sha256": "c1ebab91e9b9a2694e3d3a5e7876b11635d14666695d3cd089bea5565acc1455",
                                 "profile": "profiles/swiglu_rebwd_mlp_block_T16384_traffic.md"},
 }
 

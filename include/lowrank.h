@@ -214,10 +214,12 @@ lr_status lr_btp_finish(lr_dtype dt, lr_act act, int T, int d, int r, int group,
  * q, k, v, o, dout, dq, dk, dv: [b*s, H*dh] bf16, token-major as the projections write
  * them (head h of token t in columns h*dh .. h*dh + dh - 1 of row t = batch*s + position).
  * saved: lr_attn_saved_bytes (the row log-sum-exp of S, fp32 [b*H*s]); the backward
- * recomputes S from q and k.  ws: lr_attn_workspace_bytes (the head-major scores
- * [b*H*s, s]: S in fp32, whose first half holds dS in bf16 during the backward, P in bf16;
- * D in fp32 [b*H*s]: 6 b*H*s*s + 4 b*H*s bytes plus alignment; the forward uses one word of
- * it, the counter of its work items), owned by the caller.  The
+ * recomputes S from q and k.  ws: lr_attn_workspace_bytes, owned by the caller: for dh = 128
+ * (the kernels that keep the scores on chip) a work-item counter, scale dS^T in bf16
+ * [b*H*s keys, s queries] (written by the backward for its dQ GEMM) and D in fp32 [b*H*s]:
+ * 2 b*H*s*s + 4 b*H*s bytes plus alignment; for other dh the head-major scores [b*H*s, s]
+ * (S in fp32, whose first half holds dS in bf16 during the backward, P in bf16) and D:
+ * 6 b*H*s*s + 4 b*H*s bytes plus alignment.  The
  * kernels read q, k, v, o, dout and write o, dq, dk, dv in place.  bf16 only (LR_F32:
  * LR_ERR_UNSUPPORTED).  s a multiple of 256, dh a multiple of 128, b*H*s at most 2^30 and
  * b*H*s*s at most 2^40 (LR_ERR_SHAPE otherwise); pointers 16-byte aligned (LR_ERR_ALIGN).

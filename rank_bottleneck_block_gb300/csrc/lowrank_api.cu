@@ -1192,20 +1192,29 @@ static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
 // bi*s + s - 1, columns h*dh .. h*dh + dh - 1), read and written in place through per-head row
 // and column offsets.  The s x s score tensors (S, P, dS) are head-major ([b*H*s, s]: head n is
 // rows n*s .. n*s + s - 1), as are lse and D.
+// The head widths with kernels that keep the scores on chip (attn_flash*.cu) need only the work-item
+// counter, the stored scale dS^T (bf16 [b*H*s keys, s queries]) and D; the others S, P, dS and D.
 struct AttnWs {
   float *S, *D;
   bf16 *P, *dS;  // dS takes the first half of S's bytes (S is the forward's, dS the backward's)
+  unsigned* sched;  // flash kernels: the counter of work items
+  bf16* dST;        // flash backward: scale dS^T
 };
 
 static size_t attn_ws_layout(int b, int s, int H, int dh, void* base, AttnWs* W) {
-  (void)dh;
   Arena ar(base);
   AttnWs tmp;
   if (!W) W = &tmp;
+  memset(W, 0, sizeof(*W));
   const size_t R = static_cast<size_t>(b) * H * s;
-  W->S = static_cast<float*>(ar.take(R * s * sizeof(float)));
-  W->P = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
-  W->dS = reinterpret_cast<bf16*>(W->S);
+  if (attn_flash_fwd_supported(dh)) {
+    W->sched = static_cast<unsigned*>(ar.take(256));
+    W->dST = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
+  } else {
+    W->S = static_cast<float*>(ar.take(R * s * sizeof(float)));
+    W->P = static_cast<bf16*>(ar.take(R * s * sizeof(bf16)));
+    W->dS = reinterpret_cast<bf16*>(W->S);
+  }
   W->D = static_cast<float*>(ar.take(R * sizeof(float)));
   return ar.size();
 }
@@ -1260,13 +1269,13 @@ static lr_status attn_fwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   const int R = b * H * s, d = H * dh;
   if (attn_flash_fwd_supported(dh)) {
     // One persistent launch over the (head, 128 queries) items: S and O in TMEM, the softmax in the
-    // epilogue warps; no scores in memory (the first word of S's workspace counts the items taken).
+    // epilogue warps; no scores in memory (one word of the workspace counts the items taken).
     // Algorithmic FLOPs: Q K^T and P V over the causal half.
     const double causal = 2.0 * 2.0 * b * H * static_cast<double>(s) * s * dh * 0.5;
     LaunchScope scope("attn_flash_fwd", c.st, causal, 8.0 * b * s * d + 4.0 * R);
     cudaError_t e = launch_attn_flash_fwd(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
                                           static_cast<const bf16*>(v), static_cast<bf16*>(o), b, s, H, dh, scale,
-                                          lse, reinterpret_cast<unsigned*>(W.S), c.err, c.st);
+                                          lse, W.sched, c.err, c.st);
     if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention forward: %s", cudaGetErrorString(e));
     return LR_OK;
   }
@@ -1298,17 +1307,17 @@ static lr_status attn_bwd_impl(const Ctx& c, int b, int s, int H, int dh, float 
   }
   if (attn_flash_fwd_supported(dh)) {
     // dK and dV in one persistent launch over (head, 128 keys) items (S^T, dP^T, dV, dK in TMEM; P^T and
-    // dS^T as the TMEM A operands of dV and dK), which also stores scale dS^T (bf16, head-major, in P's
+    // dS^T as the TMEM A operands of dV and dK), which also stores scale dS^T (bf16, head-major, in the
     // workspace); then dQ = dS K as one GEMM that reads it MN-major.  Algorithmic FLOPs: four products
     // over the causal half; bytes: q, k, v, dO read, dk, dv and the causal half of dS^T written.
-    bf16* dst = W.P;
+    bf16* dst = W.dST;
     {
       const double causal4 = 4.0 * 2.0 * b * H * static_cast<double>(s) * s * dh * 0.5;
       LaunchScope scope("attn_flash_bwd", c.st, causal4, 12.0 * b * s * d + 1.0 * R * s + 8.0 * R);
       cudaError_t e = launch_attn_flash_bwd(
           static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
           static_cast<const bf16*>(dout), lse, W.D, dst, static_cast<bf16*>(dk), static_cast<bf16*>(dv), b, s, H, dh,
-          scale, reinterpret_cast<unsigned*>(W.S), c.err, c.st);
+          scale, W.sched, c.err, c.st);
       if (e != cudaSuccess) return fail(LR_ERR_CUDA, "attention backward: %s", cudaGetErrorString(e));
     }
     return attn_gemm(c, EPI_STORE, a, s, dh, s, {dst, s}, true, false, {k, d}, true, true, dq, d, true, 2);

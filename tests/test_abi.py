@@ -98,7 +98,10 @@ def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
 
 def test_attention_shape_rules(L):
     assert L.lr_attn_saved_bytes(2, 256, 3, 128) == 2 * 3 * 256 * 4
-    assert L.lr_attn_workspace_bytes(2, 256, 3, 128) > 6 * 2 * 3 * 256 * 256  # fp32 S and bf16 P
+    R = 2 * 3 * 256
+    assert L.lr_attn_workspace_bytes(2, 256, 3, 128) >= 2 * R * 256 + 4 * R  # dh 128: bf16 dS^T and D
+    assert L.lr_attn_workspace_bytes(2, 256, 3, 128) < 3 * R * 256
+    assert L.lr_attn_workspace_bytes(2, 256, 3, 256) > 6 * R * 256  # other dh: fp32 S and bf16 P
     assert L.lr_attn_saved_bytes(1, 200, 1, 128) == 0  # s not a multiple of 256
     assert L.lr_attn_workspace_bytes(1, 256, 1, 64) == 0  # dh not a multiple of 128
     assert L.lr_attn_saved_bytes(1 << 15, 256, 1 << 8, 128) == 0  # b*H*s = 2^31 score rows
