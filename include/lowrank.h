@@ -35,14 +35,20 @@
  *     device).  The library allocates and frees nothing and never synchronises,
  *     except lr_check_device_error.  Outputs must not alias inputs.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
- *     enqueued on it, asynchronously.
+ *     enqueued on it, asynchronously.  The checkpointed bf16 MLP backward also
+ *     runs two of its kernels on a second stream of the library's (one per host
+ *     thread and device, created on the first such call and kept), forked from
+ *     `stream` and joined back to it with events inside the call: to the caller
+ *     all work stays ordered on `stream`, and graph capture of `stream` takes it
+ *     in.
  *   - Errors: arguments are validated before any launch; on failure the call
  *     returns a non-zero lr_status, launches nothing and leaves a message in
  *     lr_last_error() (thread-local).  A failed launch returns LR_ERR_CUDA.
  *     Kernels never trap: a bounded wait that runs out sets a device error
  *     word, which lr_check_device_error reports as LR_ERR_TIMEOUT.
  *   - Results are deterministic: the same inputs give the same bits (no atomics
- *     in any reduction), so LR_SAVE_CKPT and LR_SAVE_FULL give bitwise-equal
+ *     in any reduction; the attention kernels take work items from an atomic
+ *     counter, but an item's result does not depend on who computes it), so LR_SAVE_CKPT and LR_SAVE_FULL give bitwise-equal
  *     gradients.
  */
 #ifndef LOWRANK_H_
