@@ -180,8 +180,12 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
 }
 
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+// Arrive on a barrier of another CTA of the cluster.  Its uses signal that TMEM columns are free:
+// the loads that read them have completed (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync)
+// and no memory write of the arriving thread is consumed through the barrier, so the release is
+// CTA-scoped (the default) rather than cluster-scoped.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -970,14 +974,19 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         tc_fence_after();
         if (leader) bulk_wait_read_all();  // the previous tile's h stores have read the a tiles
         __syncwarp();
+        static_assert(NC % 2 == 0, "phases 1 and 2 load two chunks per TMEM wait");
 #pragma unroll
-        for (int ci = 0; ci < NC; ++ci) {
-          float v[CW];
-          tmem_ld32(t_row + r0g * BN + (g + 2 * ci) * CW, v);
+        for (int ci = 0; ci < NC; ci += 2) {  // two chunks per wait: the load latency is paid half as often
+          float v[2][CW];
+          tmem_ld32(t_row + r0g * BN + (g + 2 * ci) * CW, v[0]);
+          tmem_ld32(t_row + r0g * BN + (g + 2 * ci + 2) * CW, v[1]);
           tmem_ld_wait();
-          const uint32_t base = smem_addr(abuf + ci * C::OUT_BUF);
 #pragma unroll
-          for (int j = 0; j < CW / 8; ++j) sts_bf16x8(base + stage_off<64>(lane, j), &v[8 * j]);
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t base = smem_addr(abuf + (ci + u) * C::OUT_BUF);
+#pragma unroll
+            for (int j = 0; j < CW / 8; ++j) sts_bf16x8(base + stage_off<64>(lane, j), &v[u][8 * j]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -987,12 +996,16 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         ++euse[r1g];
         tc_fence_after();
 #pragma unroll
-        for (int ci = 0; ci < NC; ++ci) {
-          float v[CW];
-          tmem_ld32(t_row + r1g * BN + (g + 2 * ci) * CW, v);
+        for (int ci = 0; ci < NC; ci += 2) {
+          float v[2][CW];
+          tmem_ld32(t_row + r1g * BN + (g + 2 * ci) * CW, v[0]);
+          tmem_ld32(t_row + r1g * BN + (g + 2 * ci + 2) * CW, v[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < CW / 2; ++j) bpk[ci][j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+          for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int j = 0; j < CW / 2; ++j) bpk[ci + u][j] = pack_bf16x2(v[u][2 * j], v[u][2 * j + 1]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -1000,25 +1013,29 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
         ok = mbar_wait(&tfull[r0g], euse[r0g] & 1u, abort_flag, sh.err, DEV_ERR_TIMEOUT_EPILOGUE) && ok;
         ++euse[r0g];
         tc_fence_after();
+        // dh is read 16 columns at a time (register pressure), each piece's load issued before the
+        // arithmetic on the previous one.
+        float dhb[2][CW / 2];
+        tmem_ld16(t_row + r0g * BN + g * CW, dhb[0]);
 #pragma unroll
         for (int ci = 0; ci < NC; ++ci) {
           const int c = g + 2 * ci;
-          wait_set_free();
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          const int b = qi % NO;
           const uint32_t abase = smem_addr(abuf + ci * C::OUT_BUF);
-          const uint32_t dbase = smem_addr(ostage(b));
+          // The chunk's h goes over its own a tile at once; da and db wait in registers (packed bf16)
+          // until the output set is free, so that wait overlaps this chunk's arithmetic.
+          uint32_t dap[CW / 8][4], dbp[CW / 8][4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {  // 16 columns of dh at a time (register pressure)
-            float dh[CW / 2];
-            tmem_ld16(t_row + r0g * BN + c * CW + hh * (CW / 2), dh);
+          for (int hh = 0; hh < 2; ++hh) {
             tmem_ld_wait();
             if (ci == NC - 1 && hh == 1) {  // every dh column of this warp is in registers: region free
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive_cluster(mapa(smem_addr(&tempty[r0g]), 0));
+            } else {
+              const int nc = hh == 1 ? c + 2 : c;  // the next piece: this chunk's second half or the next chunk's first
+              tmem_ld16(t_row + r0g * BN + nc * CW + (1 - hh) * (CW / 2), dhb[hh ^ 1]);
             }
+            const float* dh = dhb[hh];
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
               const int j = 2 * hh + jj;
@@ -1036,9 +1053,25 @@ __global__ void __launch_bounds__(Config<K, BN>::THREADS, 1)
                 dbv[t] = d * (a * l);
               }
               sts_bf16x8(abase + stage_off<64>(lane, j), hv);  // over this lane's own a values
-              sts_bf16x8(dbase + stage_off<64>(lane, j), dav);
-              sts_bf16x8(dbase + C::OUT_BUF + stage_off<64>(lane, j), dbv);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                dap[j][t] = pack_bf16x2(dav[2 * t], dav[2 * t + 1]);
+                dbp[j][t] = pack_bf16x2(dbv[2 * t], dbv[2 * t + 1]);
+              }
             }
+          }
+          wait_set_free();
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) {
+            tmem_ld_wait();  // the next piece's load may be in flight
+            break;
+          }
+          const int b = qi % NO;
+          const uint32_t dbase = smem_addr(ostage(b));
+#pragma unroll
+          for (int j = 0; j < CW / 8; ++j) {
+            sts128(dbase + stage_off<64>(lane, j), dap[j][0], dap[j][1], dap[j][2], dap[j][3]);
+            sts128(dbase + C::OUT_BUF + stage_off<64>(lane, j), dbp[j][0], dbp[j][1], dbp[j][2], dbp[j][3]);
           }
           fence_async_smem();
           __syncwarp();
