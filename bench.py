@@ -42,9 +42,12 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 99.8e6 + 500.8e6,
-                                "sources_sha256": "c1ebab91e9b9a2694e3d3a5e7876b11635d14666695d3cd089bea5565acc1455",
-                                "profile": "profiles/swiglu_rebwd_mlp_block_T16384_traffic.md"},
+    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 103.8e6 + 498.6e6,
+                                "sources_sha256": "d7e8fd93eb3aa7b3ae7a50572445ef2dbb836c6612751f6667439186b54654c5",
+                                "profile": "profiles/mlp_block_T16384_d2048_f5632_r512_launches.md"},
+    "umma_f32_bn256": {"bytes_per_launch": 402.7e6 + 10.1e6,
+                       "sources_sha256": "d7e8fd93eb3aa7b3ae7a50572445ef2dbb836c6612751f6667439186b54654c5",
+                       "profile": "profiles/mlp_block_T16384_d2048_f5632_r512_launches.md"},
 }
 
 
@@ -55,6 +58,11 @@ ALG_BYTES = {
     "umma_swiglu_bn256": lambda s: 2.0 * (2 * s.T * s.r + 2 * s.f * s.r),
     # three-accumulator re-forward + SwiGLU backward: z_g, z_u, du_down [T, r]; B_gate, B_up, A_down
     "umma_swiglu_rebwd_bn256": lambda s: 2.0 * (3 * s.T * s.r + 3 * s.f * s.r),
+    # weight gradients, the mean of the step's two launches: the grouped one reads da, db, h [T, f],
+    # z_g, z_u, du_down, z_down [T, r] and dout [T, d] and writes dB_gate, dB_up, dA_down, dB_down (fp32);
+    # the split-K one reads s du [T, 2r] and x [T, d] and writes dA'_gate;up [2r, d] (fp32)
+    "umma_f32_bn256": lambda s: 0.5 * (2.0 * (3 * s.T * s.f + 4 * s.T * s.r + s.T * s.d) + 4.0 * (3 * s.f * s.r + s.d * s.r)
+                                       + 2.0 * (2 * s.T * s.r + s.T * s.d) + 4.0 * (2 * s.r * s.d)),
 }
 
 
