@@ -46,7 +46,9 @@ enum EpiKind : int {
                             //   a = round(acc0), b = round(acc1), dh = acc2; h = SiLU(a) b -> out0,
                             //   da = dh b SiLU'(a) -> out1, db = dh SiLU(a) -> out2
   EPI_SWIGLU_H = 15,        // EPI_SWIGLU storing h only (the forward of the checkpointed block)
-  EPI_COUNT = 16
+  EPI_DSILU_Z = 16,         // EPI_DSILU that also writes z = SiLU(aux0) -> out1 (the checkpointed backward's
+                            //   re-forward of z_down from the saved u_down, which the epilogue reads anyway)
+  EPI_COUNT = 17
 };
 
 constexpr int kMaxBatch = 4;

@@ -135,6 +135,21 @@ struct EpiDef<EPI_DSILU> {  // du = acc sigma'(u)  (aux0 = u)
 };
 
 template <>
+struct EpiDef<EPI_DSILU_Z> {  // du = acc sigma'(u), z = sigma(u)  (aux0 = u)
+  static constexpr int NACC = 1, NAUX = 1, NOUT = 2;
+  static constexpr bool OUT_F32 = false, NEED_S = false, NEED_RHO = false, ROWPART = false;
+  template <typename ST, int W>
+  static __device__ __forceinline__ void run(const RowIn& ri, const float (&v)[1][W], const float (&a)[1][W],
+                                             float (&o)[2][W], float&) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      o[0][j] = v[0][j] * pair_act_grad<ST>(ri.act, a[0][j]);
+      o[1][j] = pair_act<ST>(ri.act, a[0][j]);
+    }
+  }
+};
+
+template <>
 struct EpiDef<EPI_DSILU_NORM> {  // du = acc sigma'(u); out = s du; row partial += du u  (aux0 = u)
   static constexpr int NACC = 1, NAUX = 1, NOUT = 1;
   static constexpr bool OUT_F32 = false, NEED_S = true, NEED_RHO = false, ROWPART = true;

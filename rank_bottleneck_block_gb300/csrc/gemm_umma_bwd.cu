@@ -8,6 +8,8 @@ namespace lr {
   template cudaError_t launch_umma<K, BN, AMN, BMN>(const GemmCall&, cudaStream_t);
 LR_INST(EPI_DSILU, 128, false, true)
 LR_INST(EPI_DSILU, 256, false, true)
+LR_INST(EPI_DSILU_Z, 128, false, true)
+LR_INST(EPI_DSILU_Z, 256, false, true)
 LR_INST(EPI_DSILU_NORM, 128, false, true)
 LR_INST(EPI_DSILU_NORM, 256, false, true)
 LR_INST(EPI_SWIGLU_BWD, 128, false, true)

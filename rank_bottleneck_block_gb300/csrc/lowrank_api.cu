@@ -252,6 +252,7 @@ static cudaError_t dispatch_bf16(EpiKind k, GemmCall& g, cudaStream_t st, int sm
     case EPI_SWIGLU_BWD_NORM: if (km) return umma_bn<EPI_SWIGLU_BWD_NORM, false, true>(g, st); break;
     case EPI_F32_SS: if (kk && g.ksplit == 1) return umma_bn<EPI_F32_SS, false, false>(g, st); break;
     case EPI_DSILU: if (km) return umma_bn<EPI_DSILU, false, true>(g, st); break;
+    case EPI_DSILU_Z: if (km) return umma_bn<EPI_DSILU_Z, false, true>(g, st); break;
     case EPI_DSILU_NORM: if (km) return umma_bn<EPI_DSILU_NORM, false, true>(g, st); break;
     case EPI_SWIGLU_BWD: if (km) return umma_bn<EPI_SWIGLU_BWD, false, true>(g, st); break;
     case EPI_SWIGLU_REBWD:
@@ -288,7 +289,7 @@ static cudaError_t dispatch_f32(EpiKind k, GemmCall& g, cudaStream_t st) {
 static const char* epi_name(EpiKind k) {
   static const char* names[] = {"norm_silu", "silu",       "store",  "resid",       "swiglu",        "dsilu",
                                 "dsilu_norm", "swiglu_bwd", "dx_norm", "f32", "norm_swiglu", "swiglu_bwd_norm",
-                                "f32_ss", "attn_bwd", "swiglu_rebwd", "swiglu"};
+                                "f32_ss", "attn_bwd", "swiglu_rebwd", "swiglu", "dsilu_z"};
   return (k >= 0 && k < EPI_COUNT) ? names[k] : "?";
 }
 
@@ -695,8 +696,10 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
   void *z_gu, *z_d, *a, *b, *h;
   z_gu = W.z_gu;
   z_d = W.z_d;
-  // Checkpointed bf16: the gain fold and the re-forward of z from the saved u run on a second stream
-  // beside du_down's GEMM, whose last wave leaves SM pairs idle; joined before the re-forward GEMM.
+  // Checkpointed bf16: the gain fold and the re-forward of z_gate;up from the saved u run on a second
+  // stream beside du_down's GEMM, which leaves SM pairs free (it fills them in fewer waves than it has
+  // pairs); joined before the re-forward GEMM.  z_down comes from du_down's own epilogue, which reads
+  // u_down anyway.
   const bool side = mode == LR_SAVE_CKPT && c.dt == LR_BF16 && !c.act;
   SideStream* ss = nullptr;
   if (side) {
@@ -706,7 +709,7 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     if (cudaEventRecord(ss->fork, c.st) != cudaSuccess || cudaStreamWaitEvent(ss->st, ss->fork, 0) != cudaSuccess)
       return fail(LR_ERR_CUDA, "fork: %s", cudaGetErrorString(cudaGetLastError()));
     LR_TRY(fold(cs, W.Af, src, 2, r, d, g));
-    LR_TRY(silu_slabs(cs, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, r}, T));
+    LR_TRY(silu_slabs(cs, {S.u_gu, 2LL * r, z_gu, 2LL * r, 2 * r}, {S.u_d, r, z_d, r, 0}, T));
     if (cudaEventRecord(ss->join, ss->st) != cudaSuccess)
       return fail(LR_ERR_CUDA, "join: %s", cudaGetErrorString(cudaGetLastError()));
   } else {
@@ -724,7 +727,11 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.lda0 = r;
     k.ep.out0[0] = W.du_d;
     k.ep.ldo0 = r;
-    LR_TRY(gemm(c, EPI_DSILU, k));
+    if (side) {  // z_down = SiLU(u_down) from the same operand tiles
+      k.ep.out1[0] = z_d;
+      k.ep.ldo1 = r;
+    }
+    LR_TRY(gemm(c, side ? EPI_DSILU_Z : EPI_DSILU, k));
   }
   if (mode == LR_SAVE_CKPT) {
     // Low-rank activation checkpointing (technical summary §2.2): re-forward inside the block

@@ -396,7 +396,8 @@ struct Config {
   // The three-accumulator kernel uses one set of da, db tiles: its shared memory goes to a fourth
   // operand stage, which is worth more (the MMA waits less for operands) than overlapping a chunk's
   // staging with the previous chunk's stores.
-  static constexpr int NO = TRIPLE ? 1 : (D::NAUX > 0 || SPLIT) ? 2 : 1;
+  // So does the dsilu epilogue that also writes z (two output tiles per set): one set keeps its five stages.
+  static constexpr int NO = (TRIPLE || K == EPI_DSILU_Z) ? 1 : (D::NAUX > 0 || SPLIT) ? 2 : 1;
   static constexpr int NA = D::NAUX > 0 ? aux_sets(K) : 0;
   static constexpr int WARP_BYTES = NO * OSET + NA * ASET + ABUF;
   static constexpr int EPI_BYTES = kEpiWarps * WARP_BYTES;

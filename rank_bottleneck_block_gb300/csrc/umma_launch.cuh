@@ -220,7 +220,15 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
     max_pairs[dev] = n;
     __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
-  const long long pairs = total < max_pairs[dev] ? total : max_pairs[dev];
+  // The fewest pairs that take the tiles in the same number of waves: the makespan of the static
+  // round-robin schedule is unchanged and the SMs left over stay free for concurrent work (a second
+  // stream's kernels; the next kernel's prologue).  Causal launches, whose tiles differ in length,
+  // keep every pair.
+  long long pairs = total < max_pairs[dev] ? total : max_pairs[dev];
+  if (g.causal == 0 && pairs > 0) {
+    const long long waves = (total + pairs - 1) / pairs;
+    pairs = (total + waves - 1) / waves;
+  }
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, sh, g.ep);
