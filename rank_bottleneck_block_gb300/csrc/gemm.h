@@ -55,6 +55,9 @@ struct GemmCall {
   // tiles on or below the diagonal are scheduled; 2 = rows are queries and K keys, K stops after the tile's last row;
   // 3 = rows are keys and K queries, K starts at the tile's first row.  0: none.
   int causal;
+  // At most this many SM pairs (0: as many as the tiles can use); the rest stay free for a kernel on
+  // another stream.
+  int max_pairs;
 };
 
 // Row-partial chunk width used by the epilogues of each engine.

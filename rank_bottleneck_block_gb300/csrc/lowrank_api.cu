@@ -400,16 +400,19 @@ static size_t wgrad_part_bytes(lr_dtype dt, int M, int N, int K) {
 // reduced over splits in a fixed order, times the optional column scale, and the
 // optional dg partial sums over row blocks.  Without a split, a scale or dg, the
 // GEMM writes the fp32 result straight into the single destination.
+// With `pairs` > 0 the GEMM runs without a split on 256-wide tiles and at most that many SM pairs (a
+// share of the GPU beside another stream's kernel).
 static lr_status wgrad(const Ctx& c, int M, int N, int K, Operand A, Operand B, WgradDst dst, int rows_each,
-                       const void* colscale, float* dgpart, float* wpart) {
+                       const void* colscale, float* dgpart, float* wpart, int pairs = 0) {
   const bool needs_pass = colscale != nullptr || dgpart != nullptr || rows_each != M;
-  const WgradPlan plan = wgrad_plan(c, M, N, K, needs_pass);
+  const WgradPlan plan = pairs > 0 ? WgradPlan{256, 1, 0.0} : wgrad_plan(c, M, N, K, needs_pass);
   GemmCall g = new_call(M, N, K);
   g.a_mn = g.b_mn = true;
   g.A[0] = A;
   g.B[0] = B;
   g.bn = plan.bn;
   g.ksplit = plan.ksplit;
+  g.max_pairs = pairs;
   const bool direct = !needs_pass && plan.ksplit == 1;
   g.ep.out0[0] = direct ? static_cast<void*>(dst.dst[0]) : static_cast<void*>(wpart);
   g.ep.ldo0 = N;
@@ -822,11 +825,28 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.rowpart_chunks = cdiv(r, ch);
     LR_TRY(gemm(c, EPI_DSILU_NORM, k));
   }
-  // dA'_{gate;up} = (s du)^T x; dA = dA' * g; dg_j = sum_i dA'_ij A_ij
+  // dA'_{gate;up} = (s du)^T x; dA = dA' * g; dg_j = sum_i dA'_ij A_ij.  dA' and dx below are independent:
+  // on the checkpointed bf16 path, when dA' (one 256 x 256 tile per SM pair, K = T, no split) needs at most
+  // half of the pairs, it runs with its pass and dg's final sum on the second stream on that many pairs,
+  // and dx on the others (the split-K alternative leaves pairs idle and adds the partials' reduction).
+  const int all_pairs = std::max(1, c.sms / 2);
+  const int wg_pairs = cdiv(2 * r, 256) * cdiv(d, 256);
+  const bool beside = side && T >= 8192 && 2 * wg_pairs <= all_pairs;
   {
     WgradDst dst = {{dgate.dA, dup.dA, nullptr}, {gate.A, up.A, nullptr}};
-    LR_TRY(wgrad(c, 2 * r, d, T, {W.du_s, 2LL * r}, {x, d}, dst, r, g, W.dgpart, W.wpart));
-    LR_TRY(dg_finalize(c, W.dgpart, cdiv(2 * r, kReduceRows), d, dg));
+    if (beside) {
+      Ctx cs = c;
+      cs.st = ss->st;
+      if (cudaEventRecord(ss->fork, c.st) != cudaSuccess || cudaStreamWaitEvent(ss->st, ss->fork, 0) != cudaSuccess)
+        return fail(LR_ERR_CUDA, "fork: %s", cudaGetErrorString(cudaGetLastError()));
+      LR_TRY(wgrad(cs, 2 * r, d, T, {W.du_s, 2LL * r}, {x, d}, dst, r, g, W.dgpart, W.wpart, wg_pairs));
+      LR_TRY(dg_finalize(cs, W.dgpart, cdiv(2 * r, kReduceRows), d, dg));
+      if (cudaEventRecord(ss->join, ss->st) != cudaSuccess)
+        return fail(LR_ERR_CUDA, "join: %s", cudaGetErrorString(cudaGetLastError()));
+    } else {
+      LR_TRY(wgrad(c, 2 * r, d, T, {W.du_s, 2LL * r}, {x, d}, dst, r, g, W.dgpart, W.wpart));
+      LR_TRY(dg_finalize(c, W.dgpart, cdiv(2 * r, kReduceRows), d, dg));
+    }
   }
   // dx = G + (s du) A' - (s^2 / d) rho x  (one GEMM with K = 2r: gate and up sum inside the MMA)
   {
@@ -843,8 +863,11 @@ static lr_status mlp_bwd_impl(const Ctx& c, lr_mode mode, int T, int d, int f, i
     k.ep.coef = 1.f / static_cast<float>(d);
     k.ep.out0[0] = dx;
     k.ep.ldo0 = d;
+    if (beside) k.max_pairs = all_pairs - wg_pairs;
     LR_TRY(gemm(c, EPI_DX_NORM, k));
   }
+  if (beside && cudaStreamWaitEvent(c.st, ss->join, 0) != cudaSuccess)
+    return fail(LR_ERR_CUDA, "join: %s", cudaGetErrorString(cudaGetLastError()));
   return LR_OK;
 }
 

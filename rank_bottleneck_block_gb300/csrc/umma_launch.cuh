@@ -225,6 +225,7 @@ cudaError_t launch_umma(const GemmCall& g, cudaStream_t st) {
   // stream's kernels; the next kernel's prologue).  Causal launches, whose tiles differ in length,
   // keep every pair.
   long long pairs = total < max_pairs[dev] ? total : max_pairs[dev];
+  if (g.max_pairs > 0 && pairs > g.max_pairs) pairs = g.max_pairs;
   if (g.causal == 0 && pairs > 0) {
     const long long waves = (total + pairs - 1) / pairs;
     pairs = (total + waves - 1) / waves;
