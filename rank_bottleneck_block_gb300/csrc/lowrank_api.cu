@@ -1115,9 +1115,22 @@ static lr_status proj_fwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
   proj_ws_layout(c.dt, false, T, d_in, d_out, r, group, norm, ws, &W);
   StackSrc src = {{nullptr, nullptr, nullptr}};
   for (int i = 0; i < group; ++i) src.src[i] = pairs[i].A;
-  LR_TRY(fold(c, W.Af, src, group, r, d_in, g));
-  if (norm && c.dt != LR_BF16) LR_TRY(rstd(c, x, T, d_in, eps, S.s));
-  {
+  if (!norm) {
+    // Without the norm there is no gain to fold: the A's are read where they are, one batch per pair
+    // writing its columns of u and z (the same tiles as one GEMM over the stacked A's).
+    GemmCall k = new_call(T, r, d_in);
+    k.batches = group;
+    for (int i = 0; i < group; ++i) {
+      k.A[i] = {x, d_in};
+      k.B[i] = {pairs[i].A, d_in};
+      k.ep.out0[i] = off(S.u, c.es * i * r);
+      k.ep.out1[i] = off(S.z, c.es * i * r);
+    }
+    k.ep.ldo0 = k.ep.ldo1 = 1LL * group * r;
+    LR_TRY(gemm(c, EPI_SILU, k));
+  } else {
+    LR_TRY(fold(c, W.Af, src, group, r, d_in, g));
+    if (c.dt != LR_BF16) LR_TRY(rstd(c, x, T, d_in, eps, S.s));
     GemmCall k = new_call(T, group * r, d_in);
     k.A[0] = {x, d_in};
     k.B[0] = {W.Af, d_in};
@@ -1128,7 +1141,7 @@ static lr_status proj_fwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
     k.ep.rowscale_out = S.s;
     k.ep.coef = 1.f / static_cast<float>(d_in);
     k.ep.eps = eps;
-    LR_TRY(gemm(c, norm ? EPI_NORM_SILU : EPI_SILU, k));
+    LR_TRY(gemm(c, EPI_NORM_SILU, k));
   }
   {
     // The B's have distinct inputs: one batched GEMM (technical summary §2.2).
@@ -1163,7 +1176,9 @@ static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
   const long long ldg = 1LL * group * r;
   StackSrc src = {{nullptr, nullptr, nullptr}};
   for (int i = 0; i < group; ++i) src.src[i] = pairs[i].A;
-  LR_TRY(fold(c, W.Af, src, group, r, d_in, g));
+  // dx reads the stacked (and, with the norm, gain-folded) A's; a single pair without the norm is read in place.
+  const bool stack = norm || group > 1;
+  if (stack) LR_TRY(fold(c, W.Af, src, group, r, d_in, g));
   for (int i = 0; i < group; ++i) {
     WgradDst dst = {{grads[i].dB, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
     LR_TRY(wgrad(c, d_out, r, T, {douts[i], d_out}, {off(S.z, c.es * i * r), ldg}, dst, d_out, nullptr, nullptr,
@@ -1198,7 +1213,7 @@ static lr_status proj_bwd_impl(const Ctx& c, int T, int d_in, int d_out, int r, 
     GemmCall k = new_call(T, d_in, group * r);
     k.b_mn = true;
     k.A[0] = {W.du, ldg};
-    k.B[0] = {W.Af, d_in};
+    k.B[0] = stack ? Operand{W.Af, d_in} : Operand{pairs[0].A, d_in};
     k.ep.out0[0] = dx;
     k.ep.ldo0 = d_in;
     if (norm) {
