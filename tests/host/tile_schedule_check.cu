@@ -93,6 +93,8 @@ int main() {
           Shape sk = plain(s, 128, BN, heads, 1, rev);
           sk.rowbatch = 1, sk.bh = heads, sk.causal = 2;
           if (!check<true>(sk, {}, BN)) return 1;
+          sk.causal = 3;
+          if (!check<true>(sk, {}, BN)) return 1;
         }
       // grouped batches of their own shapes
       const int gm[4] = {2048, 512, 300, 4096}, gn[4] = {512, 2048, 1000, 128};
