@@ -102,6 +102,21 @@ def test_mlp_bf16_medium(mode):
     check_mlp(I.MlpShape(T=2112, d=512, f=1376, r=128, dtype="bf16"), mode, seed=3)
 
 
+def test_mlp_wgrad_beside_dx():
+    """Checkpointed bf16 with T >= 8192: dA'_gate;up runs unsplit on its own share of the SM pairs on the
+    second stream while dx runs on the rest (ragged d, 2r under one tile); every tensor against the oracle,
+    and a second run bit for bit equal to the first."""
+    shape = I.MlpShape(T=8192, d=384, f=688, r=96, dtype="bf16")
+    _, blk = check_mlp(shape, 1, seed=9)
+    dx, dg, grads = blk.dx.clone(), blk.dg.clone(), {k: v.clone() for k, v in blk.grads.items()}
+    blk.forward()
+    blk.backward()
+    _sync_check()
+    assert torch.equal(dx, blk.dx) and torch.equal(dg, blk.dg)
+    for k in grads:
+        assert torch.equal(grads[k], blk.grads[k]), k
+
+
 def test_mlp_checkpoint_bitwise_equals_full():
     """Low-rank activation checkpointing: the re-forward reproduces the forward bit for bit,
     so every gradient equals the no-checkpoint run exactly."""
