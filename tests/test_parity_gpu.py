@@ -157,12 +157,14 @@ def test_mlp_split_k_weight_gradients_deterministic():
             assert torch.equal(grads[k], blk.grads[k]), k
 
 
-def test_graph_replay_matches_eager():
+@pytest.mark.parametrize("T", [520, 8192])
+def test_graph_replay_matches_eager(T):
     """A step captured once as a CUDA graph (programmatic-launch edges included) and replayed gives
-    bit-identical results to the same launches issued one by one."""
+    bit-identical results to the same launches issued one by one; at T 8192 the capture includes the
+    second stream's forks and joins and dA' beside dx."""
     from rank_bottleneck_block_gb300.runner import GraphStep
 
-    shape = I.MlpShape(T=520, d=256, f=688, r=64, dtype="bf16")
+    shape = I.MlpShape(T=T, d=256, f=688, r=64, dtype="bf16")
     _, blk = run_mlp(shape, 1, seed=14)
     ref = (blk.out.clone(), blk.dx.clone(), {k: v.clone() for k, v in blk.grads.items()})
     for t in (blk.out, blk.dx, *blk.grads.values()):
