@@ -42,11 +42,11 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 # taken on: TRAFFIC_SOURCES are hashed at run time and a mismatch reports traffic as null.
 TRAFFIC_SOURCES = ["common.cuh", "epilogues.cuh", "gemm.h", "umma_gemm.cuh", "umma_launch.cuh", "lowrank_api.cu"]
 NCU_TRAFFIC = {
-    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 104.7e6 + 498.5e6,
-                                "sources_sha256": "51a288e6830800b7ccb8103f82770b5f8b5805ca4477078f89f2d2f870486669",
+    "umma_swiglu_rebwd_bn256": {"bytes_per_launch": 105.1e6 + 498.5e6,
+                                "sources_sha256": "cb44c26bd0a709158dd92d7e717b74d34f2b6601324d51bc176e09e4c61851c5",
                                 "profile": "profiles/mlp_block_T16384_d2048_f5632_r512_launches.md"},
     "umma_f32_bn256": {"bytes_per_launch": 402.7e6 + 9.8e6,
-                       "sources_sha256": "51a288e6830800b7ccb8103f82770b5f8b5805ca4477078f89f2d2f870486669",
+                       "sources_sha256": "cb44c26bd0a709158dd92d7e717b74d34f2b6601324d51bc176e09e4c61851c5",
                        "profile": "profiles/mlp_block_T16384_d2048_f5632_r512_launches.md"},
 }
 

@@ -504,8 +504,16 @@ __host__ __device__ __forceinline__ void decode_tile(const Shape& sh, int tile, 
     mb = 2 * p + rank;
     return;
   }
-  const int mp = rem / sh.n_tiles;
+  int mp = rem / sh.n_tiles;
   nb = rem - mp * sh.n_tiles;
+  if (RB && (sh.causal == 2 || sh.causal == 3)) {
+    // Causal K ranges grow (mode 2) or shrink (mode 3) with the row block.  Within a batch the row
+    // blocks are taken as 0, 1, .., m/2 - 1, then m - 1, m - 2, .., m/2, so that tiles m/2 apart in the
+    // launch order (as a pair's round-robin share is when the pair count is an odd multiple of m/2) have
+    // complementary lengths; a batch's tiles stay together (its K operand in L2).
+    const int h = sh.m_pairs >> 1;
+    if (mp >= h) mp = sh.m_pairs - 1 - (mp - h);
+  }
   mb = 2 * mp + rank;
 }
 
